@@ -1,0 +1,226 @@
+"""Float64 CPU oracle for one Medusa decoding step -- TEST INFRASTRUCTURE.
+
+Only ``tests/``, ``__graft_entry__.smoke()`` and the CPU-baseline leg of
+``bench.py`` may import this package.  The CUDA library never loads it and
+has no fallback to it.  The arithmetic lives in ``oracle.c`` (plain loops in
+IEEE double, compiled with ``-ffp-contract=off``); this module only compiles
+it and marshals numpy arrays through ctypes.
+
+bf16 arrays travel as ``uint16`` bit patterns, float32 arrays as ``float32``.
+"""
+from __future__ import annotations
+
+import ctypes
+import os
+import subprocess
+import threading
+
+import numpy as np
+
+_HERE = os.path.dirname(os.path.abspath(__file__))
+_SRC = os.path.join(_HERE, "oracle.c")
+_LIB = os.path.join(_HERE, "liboracle.so")
+_lock = threading.Lock()
+_lib = None
+
+F32, BF16 = 0, 1
+GREEDY, TYPICAL = 0, 1
+
+
+def build(force: bool = False) -> str:
+    """Compile oracle.c into liboracle.so next to it (plain gcc, no BLAS)."""
+    if force or not os.path.exists(_LIB) or os.path.getmtime(_LIB) < os.path.getmtime(_SRC):
+        tmp = _LIB + f".{os.getpid()}.tmp"
+        subprocess.run(
+            ["gcc", "-O2", "-std=c11", "-ffp-contract=off", "-fno-fast-math",
+             "-Wall", "-shared", "-fPIC", "-o", tmp, _SRC, "-lm"],
+            check=True,
+        )
+        os.replace(tmp, _LIB)
+    return _LIB
+
+
+def _load():
+    global _lib
+    with _lock:
+        if _lib is None:
+            build()
+            lib = ctypes.CDLL(_LIB)
+            P = ctypes.c_void_p
+            I = ctypes.c_int
+            D = ctypes.c_double
+            lib.oracle_heads.argtypes = [I, P, P, P, P, I, I, I, I, I, P, P, P, P]
+            lib.oracle_heads.restype = I
+            lib.oracle_build_tree.argtypes = [P, P, P, I, I, P, I, I, P, P, P, P, P, P, P, P, P]
+            lib.oracle_build_tree.restype = I
+            lib.oracle_tree_attention.argtypes = [I, P, P, P, P, P, I, I, I, I, D, P]
+            lib.oracle_tree_attention.restype = I
+            lib.oracle_softmax_entropy.argtypes = [P, I, D]
+            lib.oracle_softmax_entropy.restype = D
+            lib.oracle_posterior.argtypes = [I, P, P, P, P, I, I, I, I, I, D, D, D, P, P, P, P, P, P, P]
+            lib.oracle_posterior.restype = I
+            lib.oracle_commit_kv.argtypes = [P, P, P, P, P, I, I, ctypes.c_size_t, P]
+            lib.oracle_commit_kv.restype = I
+            _lib = lib
+    return _lib
+
+
+def _ptr(a):
+    return None if a is None else ctypes.c_void_p(a.ctypes.data)
+
+
+def _c(a, dtype=None):
+    a = np.asarray(a) if dtype is None else np.asarray(a, dtype=dtype)
+    return np.ascontiguousarray(a)
+
+
+def _dt(a) -> int:
+    if a.dtype == np.float32:
+        return F32
+    if a.dtype == np.uint16:
+        return BF16
+    raise TypeError(f"oracle takes float32 or bf16-bits (uint16) arrays, got {a.dtype}")
+
+
+def _check(rc: int, what: str):
+    if rc != 0:
+        raise RuntimeError(f"oracle {what} failed with code {rc}")
+
+
+def heads(h, W1, b1, W2, top_s: int, want_logits: bool = False):
+    """Medusa heads: top-s ids and log-probs per (sequence, head).
+
+    h [B,d], W1 [K,d,d], b1 [K,d] or None, W2 [K,V,d], all float32 or all bf16 bits.
+    Returns (ids int32 [B,K,s], logp float64 [B,K,s], logits [B,K,V] or None,
+    logz [B,K]).
+    """
+    lib = _load()
+    h, W1, W2 = _c(h), _c(W1), _c(W2)
+    b1 = None if b1 is None else _c(b1)
+    dt = _dt(h)
+    for a in (W1, W2) + (() if b1 is None else (b1,)):
+        if _dt(a) != dt:
+            raise TypeError("mixed dtypes")
+    B, d = h.shape
+    K, V = W2.shape[0], W2.shape[1]
+    ids = np.zeros((B, K, top_s), np.int32)
+    logp = np.zeros((B, K, top_s), np.float64)
+    logits = np.zeros((B, K, V), np.float64) if want_logits else None
+    logz = np.zeros((B, K), np.float64)
+    rc = lib.oracle_heads(dt, _ptr(h), _ptr(W1), _ptr(b1), _ptr(W2), B, d, V, K, top_s,
+                          _ptr(ids), _ptr(logp), _ptr(logits), _ptr(logz))
+    _check(rc, "heads")
+    return ids, logp, logits, logz
+
+
+def build_tree(root, topk_ids, topk_logp, s, n: int, prefix_len=None):
+    """Greedy budgeted candidate tree in canonical order (see oracle.c, O2).
+
+    Returns a dict of numpy arrays: tokens, parent, depth, pos_id [B,R],
+    anc_mask uint64 [B,R,W], paths [B,n,K+1], n_leaf [B], cut_gap [B].
+    """
+    lib = _load()
+    root = _c(root, np.int32)
+    topk_ids = _c(topk_ids, np.int32)
+    topk_logp = _c(topk_logp, np.float64)
+    s = _c(s, np.int32)
+    B, K, s_stride = topk_ids.shape
+    R = n + 1
+    W = (R + 63) // 64
+    pl = _c(np.zeros(B) if prefix_len is None else prefix_len, np.int32)
+    out = dict(
+        tokens=np.zeros((B, R), np.int32), parent=np.zeros((B, R), np.int32),
+        depth=np.zeros((B, R), np.int32), pos_id=np.zeros((B, R), np.int32),
+        anc_mask=np.zeros((B, R, W), np.uint64), paths=np.zeros((B, n, K + 1), np.int32),
+        n_leaf=np.zeros(B, np.int32), cut_gap=np.zeros(B, np.float64),
+    )
+    rc = lib.oracle_build_tree(_ptr(root), _ptr(topk_ids), _ptr(topk_logp), B, K, _ptr(s),
+                               s_stride, n, _ptr(pl), _ptr(out["tokens"]), _ptr(out["parent"]),
+                               _ptr(out["depth"]), _ptr(out["pos_id"]), _ptr(out["anc_mask"]),
+                               _ptr(out["paths"]), _ptr(out["n_leaf"]), _ptr(out["cut_gap"]))
+    _check(rc, "build_tree")
+    return out
+
+
+def tree_attention(q, k_caches, v_caches, prefix_len, anc_mask, scale: float):
+    """Tree-masked attention, direct definition.  q [B,R,H,dh]; k/v caches: lists
+    of B arrays [P_b+R,H,dh].  Returns float64 [B,R,H,dh]."""
+    lib = _load()
+    q = _c(q)
+    dt = _dt(q)
+    B, R, H, dh = q.shape
+    ks = [_c(k) for k in k_caches]
+    vs = [_c(v) for v in v_caches]
+    for a in ks + vs:
+        if _dt(a) != dt:
+            raise TypeError("mixed dtypes")
+    pl = _c(prefix_len, np.int32)
+    for b in range(B):
+        need = (int(pl[b]) + R) * H * dh
+        if ks[b].size < need or vs[b].size < need:
+            raise ValueError("cache too small")
+    kp = (ctypes.c_void_p * B)(*[k.ctypes.data for k in ks])
+    vp = (ctypes.c_void_p * B)(*[v.ctypes.data for v in vs])
+    am = _c(anc_mask, np.uint64)
+    out = np.zeros((B, R, H, dh), np.float64)
+    rc = lib.oracle_tree_attention(dt, _ptr(q), ctypes.cast(kp, ctypes.c_void_p),
+                                   ctypes.cast(vp, ctypes.c_void_p), _ptr(pl), _ptr(am),
+                                   B, R, H, dh, float(scale), _ptr(out))
+    _check(rc, "tree_attention")
+    return out
+
+
+def softmax_entropy(x, T: float = 1.0) -> float:
+    """Natural-log entropy of softmax(x / T) for one float64 row."""
+    lib = _load()
+    x = _c(x, np.float64)
+    return float(lib.oracle_softmax_entropy(_ptr(x), x.size, float(T)))
+
+
+def posterior(logits, tokens, parent, depth, K: int, mode: int, eps=0.09, delta=0.3,
+              temperature=1.0, forced_accept=None):
+    """Acceptance + longest accepted path.  logits [B,R,V] float32 or bf16 bits.
+    Returns dict: accept_len [B], path/path_tokens [B,K+1], next_token [B],
+    accept [B,R], margin [B,R]."""
+    lib = _load()
+    logits = _c(logits)
+    dt = _dt(logits)
+    B, R, V = logits.shape
+    tokens = _c(tokens, np.int32)
+    parent = _c(parent, np.int32)
+    depth = _c(depth, np.int32)
+    fa = None if forced_accept is None else _c(forced_accept, np.int32)
+    out = dict(
+        accept_len=np.zeros(B, np.int32), path=np.zeros((B, K + 1), np.int32),
+        path_tokens=np.zeros((B, K + 1), np.int32), next_token=np.zeros(B, np.int32),
+        accept=np.zeros((B, R), np.int32), margin=np.zeros((B, R), np.float64),
+    )
+    rc = lib.oracle_posterior(dt, _ptr(logits), _ptr(tokens), _ptr(parent), _ptr(depth),
+                              B, R, V, K, int(mode), float(eps), float(delta), float(temperature),
+                              _ptr(fa), _ptr(out["accept_len"]), _ptr(out["path"]),
+                              _ptr(out["path_tokens"]), _ptr(out["next_token"]),
+                              _ptr(out["accept"]), _ptr(out["margin"]))
+    _check(rc, "posterior")
+    return out
+
+
+def commit_kv(k_caches, v_caches, prefix_len, path, accept_len):
+    """Gather the accepted path's K/V rows into contiguous slots (in place on the
+    given numpy caches).  Returns the new prefix lengths."""
+    lib = _load()
+    B = len(k_caches)
+    path = _c(path, np.int32)
+    K = path.shape[1] - 1
+    pl = _c(prefix_len, np.int32)
+    al = _c(accept_len, np.int32)
+    for a in list(k_caches) + list(v_caches):
+        if not a.flags["C_CONTIGUOUS"]:
+            raise ValueError("caches must be contiguous")
+    row_bytes = k_caches[0][0].nbytes
+    kp = (ctypes.c_void_p * B)(*[k.ctypes.data for k in k_caches])
+    vp = (ctypes.c_void_p * B)(*[v.ctypes.data for v in v_caches])
+    new_pl = np.zeros(B, np.int32)
+    rc = lib.oracle_commit_kv(ctypes.cast(kp, ctypes.c_void_p), ctypes.cast(vp, ctypes.c_void_p),
+                              _ptr(pl), _ptr(path), _ptr(al), B, K, row_bytes, _ptr(new_pl))
+    _check(rc, "commit_kv")
+    return new_pl

@@ -1,0 +1,428 @@
+"""Pins for the float64 oracle: checks against what the pages and mathematics
+fix, independent of the oracle's own code (CPU only)."""
+import itertools
+import json
+import math
+import os
+
+import numpy as np
+import pytest
+import torch
+from scipy.special import expit, logsumexp
+
+import oracle
+import synth
+
+GOLDEN = os.path.join(os.path.dirname(__file__), "golden")
+
+
+# ---------------------------------------------------------------- tree ----
+
+def _rank_tables(a):
+    """Per-level tables where token id encodes (level, rank): 100*(k+1) + r."""
+    K = len(a)
+    s = max(len(x) for x in a)
+    ids = np.full((1, K, s), -1, np.int32)
+    logp = np.full((1, K, s), -np.inf)
+    for k, row in enumerate(a):
+        for r, w in enumerate(row):
+            ids[0, k, r] = 100 * (k + 1) + r
+            logp[0, k, r] = math.log(w)
+    return ids, logp
+
+
+def _rank_path(t, i):
+    """Rank path (0-based) of node i from the token encoding."""
+    out = []
+    while i > 0:
+        out.append(int(t["tokens"][0, i]) % 100)
+        i = int(t["parent"][0, i])
+    return tuple(reversed(out))
+
+
+def test_worked_example_sparse_tree():
+    """[P2] §6.2 worked example: exact picks in order and E[L_cover] = 1.9325."""
+    g = json.load(open(os.path.join(GOLDEN, "sparse_tree_worked_example.json")))
+    a = g["a"]
+    ids, logp = _rank_tables(a)
+    s = [len(x) for x in a]
+    picks = [tuple(r - 1 for r in p) for p in g["picks_in_order"]]
+    prev = set()
+    for n in range(1, g["budget"] + 1):
+        t = oracle.build_tree([7], ids, logp, s, n)
+        got = {_rank_path(t, i) for i in range(1, n + 1)}
+        assert len(got) == n
+        added = got - prev
+        assert added == {picks[n - 1]}, (n, added)
+        prev = got
+    weights = [math.prod(a[k][r] for k, r in enumerate(p)) for p in sorted(prev)]
+    assert sum(weights) == pytest.approx(g["expected_cover_depth"], abs=1e-12)
+    for p, w in zip(picks, g["weights_in_order"]):
+        assert math.prod(a[k][r] for k, r in enumerate(p)) == pytest.approx(w, abs=1e-15)
+
+
+@pytest.mark.parametrize("s,count,seqs", [((2, 3), 8, 6), ((2, 2, 2), 14, 8),
+                                          ((4, 3, 2, 2, 1), 136, 48),
+                                          ((8, 4, 4, 2, 2), 936, 512)])
+def test_full_cartesian_tree_node_count(s, count, seqs):
+    """[P2] §6.1: new nodes = sum_k prod_{j<=k} s_j; candidate sequences =
+    prod s_k (one leaf per sequence when the whole Cartesian tree is kept)."""
+    rng = np.random.default_rng(5)
+    a = [sorted(rng.uniform(0.01, 1.0, size=sk), reverse=True) for sk in s]
+    ids, logp = _rank_tables(a)
+    t = oracle.build_tree([1], ids, logp, list(s), count)
+    assert t["tokens"].shape[1] == count + 1
+    assert int(t["n_leaf"][0]) == seqs
+    per_depth = np.bincount(t["depth"][0], minlength=len(s) + 1)
+    assert list(per_depth[1:]) == list(np.cumprod(s))
+    with pytest.raises(RuntimeError):
+        oracle.build_tree([1], ids, logp, list(s), count + 1)
+
+
+def _all_nodes(s):
+    nodes = []
+    for k in range(1, len(s) + 1):
+        nodes += list(itertools.product(*[range(x) for x in s[:k]]))
+    return nodes
+
+
+@pytest.mark.parametrize("s,n,seed", [((2, 2), 3, 0), ((2, 2, 2), 5, 1), ((3, 2), 4, 2),
+                                      ((2, 3, 2), 6, 3), ((3, 3), 7, 4)])
+def test_greedy_tree_maximises_cover(s, n, seed):
+    """[P2] §6.2: E[L_cover] = sum of node weights over the tree; the greedy
+    tree attains the maximum over every prefix-closed tree of n nodes
+    (brute force)."""
+    rng = np.random.default_rng(seed)
+    a = [sorted(rng.dirichlet(np.ones(x + 1))[:x], reverse=True) for x in s]
+    ids, logp = _rank_tables(a)
+    t = oracle.build_tree([0], ids, logp, list(s), n)
+    w = lambda p: math.prod(a[k][r] for k, r in enumerate(p))
+    greedy = sum(w(_rank_path(t, i)) for i in range(1, n + 1))
+    best = 0.0
+    for sub in itertools.combinations(_all_nodes(s), n):
+        ss = set(sub)
+        if all(len(p) == 1 or p[:-1] in ss for p in sub):
+            best = max(best, sum(w(p) for p in sub))
+    assert greedy == pytest.approx(best, abs=1e-12)
+
+
+def test_tree_structure_invariants():
+    """[P2] §6.1: a node sees the root and its own ancestors; nodes of one depth
+    share one position index; canonical order puts parents first."""
+    cfg = synth.sweep(128, 512)
+    rng = np.random.default_rng(11)
+    B = 3
+    ids = rng.integers(0, 32000, size=(B, cfg.K, cfg.top_s)).astype(np.int32)
+    logp = np.log(np.sort(rng.dirichlet(np.ones(cfg.top_s + 1), size=(B, cfg.K))[..., :cfg.top_s], -1)[..., ::-1])
+    P = np.array([5, 100, 0], np.int32)
+    t = oracle.build_tree([3, 4, 5], ids, logp, cfg.s, cfg.n, prefix_len=P)
+    R = cfg.R
+    for b in range(B):
+        par, de = t["parent"][b], t["depth"][b]
+        assert par[0] == -1 and de[0] == 0
+        assert t["tokens"][b, 0] == [3, 4, 5][b]
+        for i in range(1, R):
+            assert 0 <= par[i] < i
+            assert de[i] == de[par[i]] + 1
+        assert np.all(np.diff(de) >= 0)
+        assert np.all(t["pos_id"][b] == P[b] + de)
+        for i in range(R):
+            anc = set()
+            a = i
+            while a >= 0:
+                anc.add(a)
+                a = par[a]
+            bits = {j for j in range(R) if (int(t["anc_mask"][b, i, j // 64]) >> (j % 64)) & 1}
+            assert bits == anc
+        nl = int(t["n_leaf"][b])
+        leaves = [i for i in range(R) if i not in set(par[1:].tolist())]
+        assert nl == len(leaves)
+        for li, leaf in enumerate(leaves):
+            row = t["paths"][b, li]
+            assert row[de[leaf]] == leaf and row[0] == 0
+            assert np.all(row[de[leaf] + 1:] == -1)
+        assert np.all(t["paths"][b, nl:] == -1)
+
+
+# --------------------------------------------------------------- heads ----
+
+def _ref_topk(logits, s):
+    order = sorted(range(len(logits)), key=lambda v: (-logits[v], v))
+    return order[:s]
+
+
+def test_heads_identity_init_reproduces_lm_head():
+    """[P2] §3.1 initialisation: W1 = 0 (and b1 = 0) makes the residual branch
+    the identity; with W2 = the LM head every head reproduces the LM-head
+    distribution softmax(W_lm h)."""
+    cfg = synth.tiny().replace(lm_head_variant=True)
+    hi = synth.heads_inputs(cfg)
+    ids, logp, logits, logz = oracle.heads(hi.h, hi.W1, hi.b1, hi.W2, 4, want_logits=True)
+    w_lm = hi.W2[0].astype(np.float64)
+    ref = w_lm @ hi.h[0].astype(np.float64)
+    ref_lp = ref - logsumexp(ref)
+    for k in range(cfg.K):
+        np.testing.assert_allclose(logits[0, k], ref, rtol=0, atol=1e-12)
+        assert list(ids[0, k]) == _ref_topk(ref, 4)
+        np.testing.assert_allclose(logp[0, k], ref_lp[ids[0, k]], atol=1e-12)
+        assert list(ids[0, k]) == list(ids[0, 0])
+
+
+def test_heads_residual_silu_and_orientation():
+    """[P3] Part 3 residual block z = h + SiLU(W1 h + b1), vocab projection
+    W2 z without bias.  W1 = a permutation and W2 = scaled one-hot rows turn
+    both products into index gathers, so the expected logits have a closed
+    form; transposed operands, a dropped residual, bias or SiLU term all
+    change them."""
+    rng = np.random.default_rng(3)
+    d, V, K, B = 16, 40, 2, 2
+    h = rng.standard_normal((B, d)).astype(np.float32)
+    perm = np.stack([rng.permutation(d) for _ in range(K)])
+    W1 = np.zeros((K, d, d), np.float32)
+    for k in range(K):
+        W1[k, np.arange(d), perm[k]] = 1.0
+    b1 = rng.standard_normal((K, d)).astype(np.float32)
+    col = rng.integers(0, d, size=(K, V))
+    scale = rng.uniform(0.5, 2.0, size=(K, V)).astype(np.float32)
+    W2 = np.zeros((K, V, d), np.float32)
+    for k in range(K):
+        W2[k, np.arange(V), col[k]] = scale[k]
+    ids, logp, logits, logz = oracle.heads(h, W1, b1, W2, 5, want_logits=True)
+    for b in range(B):
+        for k in range(K):
+            u = h[b, perm[k]].astype(np.float64) + b1[k]
+            z = h[b].astype(np.float64) + u * expit(u)
+            ref = scale[k].astype(np.float64) * z[col[k]]
+            np.testing.assert_allclose(logits[b, k], ref, atol=1e-12)
+            assert logz[b, k] == pytest.approx(logsumexp(ref), abs=1e-12)
+            assert list(ids[b, k]) == _ref_topk(ref, 5)
+
+
+def test_heads_tie_rule_lowest_id():
+    """Equal logits rank the smaller token id first (convention)."""
+    d, V = 4, 10
+    h = np.ones((1, d), np.float32)
+    W1 = np.zeros((1, d, d), np.float32)
+    W2 = np.zeros((1, V, d), np.float32)
+    W2[0, [7, 2, 5], 0] = 1.0
+    ids, _, _, _ = oracle.heads(h, W1, None, W2, 4)
+    assert list(ids[0, 0]) == [2, 5, 7, 0]
+
+
+def test_heads_bf16_widening_exact():
+    """bf16 inputs are widened exactly: bf16 data gives the same result as the
+    same values passed as float32."""
+    cfg = synth.tiny()
+    hi = synth.heads_inputs(cfg)
+    to16 = synth.f32_to_bf16_bits
+    to32 = synth.bf16_bits_to_f32
+    a = oracle.heads(to16(hi.h), to16(hi.W1), to16(hi.b1), to16(hi.W2), 3, want_logits=True)
+    b = oracle.heads(to32(to16(hi.h)), to32(to16(hi.W1)), to32(to16(hi.b1)), to32(to16(hi.W2)), 3,
+                     want_logits=True)
+    assert np.array_equal(a[0], b[0]) and np.array_equal(a[2], b[2])
+
+
+# ----------------------------------------------------------- attention ----
+
+def _sdpa_path(q_rows, k_rows, v_rows, P, scale):
+    """Textbook causal attention (torch float64) of the path queries over
+    [prefix ; path]: query t sits at position P+t and sees positions <= P+t."""
+    L = q_rows.shape[0]
+    qt = torch.from_numpy(q_rows).permute(1, 0, 2)[None]      # [1,H,L,dh]
+    kt = torch.from_numpy(k_rows).permute(1, 0, 2)[None]      # [1,H,P+L,dh]
+    vt = torch.from_numpy(v_rows).permute(1, 0, 2)[None]
+    pos_q = P + torch.arange(L)[:, None]
+    pos_k = torch.arange(P + L)[None, :]
+    mask = pos_k <= pos_q
+    o = torch.nn.functional.scaled_dot_product_attention(qt, kt, vt, attn_mask=mask, scale=scale)
+    return o[0].permute(1, 0, 2).numpy()
+
+
+@pytest.mark.parametrize("s,n,P,H,dh", [((2, 2, 2), 14, 32, 1, 64), ((3, 2, 2), 10, 7, 2, 16),
+                                        ((4, 3, 2, 2, 1), 40, 0, 3, 8), ((1, 1, 1, 1), 4, 12, 2, 8)])
+def test_tree_attention_equals_per_path_causal(s, n, P, H, dh):
+    """[P2] §6.1: with the tree mask every root-to-leaf path is exactly an
+    independent causal sequence over [prefix ; path]."""
+    rng = np.random.default_rng(n + P)
+    K = len(s)
+    ids = rng.integers(0, 1000, size=(1, K, max(s))).astype(np.int32)
+    logp = np.log(np.sort(rng.dirichlet(np.ones(max(s) + 1), size=(1, K))[..., :max(s)], -1)[..., ::-1])
+    t = oracle.build_tree([9], ids, logp, list(s), n, prefix_len=[P])
+    R = n + 1
+    q = rng.standard_normal((1, R, H, dh)).astype(np.float32)
+    kc = rng.standard_normal((P + R, H, dh)).astype(np.float32)
+    vc = rng.standard_normal((P + R, H, dh)).astype(np.float32)
+    scale = 1.0 / math.sqrt(dh)
+    out = oracle.tree_attention(q, [kc], [vc], [P], t["anc_mask"], scale)
+    for li in range(int(t["n_leaf"][0])):
+        path = [int(x) for x in t["paths"][0, li] if x >= 0]
+        rows = np.array(path)
+        kk = np.concatenate([kc[:P], kc[P + rows]]).astype(np.float64)
+        vv = np.concatenate([vc[:P], vc[P + rows]]).astype(np.float64)
+        ref = _sdpa_path(q[0, rows].astype(np.float64), kk, vv, P, scale)
+        np.testing.assert_allclose(out[0, rows], ref, atol=1e-12, rtol=0)
+
+
+# ----------------------------------------------------------- posterior ----
+
+def _chain_tree(L, root=0):
+    """Chain tree root -> 1 -> ... -> L with tokens 10+i."""
+    R = L + 1
+    tokens = np.array([[root] + [10 + i for i in range(1, R)]], np.int32)
+    parent = np.array([[-1] + list(range(R - 1))], np.int32)
+    depth = np.array([list(range(R))], np.int32)
+    return tokens, parent, depth
+
+
+@pytest.mark.parametrize("L_true", [0, 1, 3, 5])
+def test_greedy_stops_at_first_mismatch(L_true):
+    """[P3] Part 2: greedy verification accepts while the candidate equals the
+    target argmax; the first mismatch ends the prefix, even if later
+    candidates would match."""
+    K, V = 5, 50
+    tokens, parent, depth = _chain_tree(K)
+    logits = np.zeros((1, K + 1, V), np.float32)
+    for i in range(1, K + 1):
+        p = parent[0, i]
+        if i != L_true + 1:
+            logits[0, p, tokens[0, i]] = 5.0          # match
+        else:
+            logits[0, p, 3] = 5.0                     # mismatch
+    logits[0, K, 42] = 9.0
+    o = oracle.posterior(logits, tokens, parent, depth, K, oracle.GREEDY)
+    assert int(o["accept_len"][0]) == L_true
+    assert list(o["path"][0, :L_true + 1]) == list(range(L_true + 1))
+    assert np.all(o["path"][0, L_true + 1:] == -1)
+    assert list(o["path_tokens"][0, :L_true + 1]) == list(tokens[0, :L_true + 1])
+    exp_next = 42 if L_true == K else 0
+    if L_true < K:
+        exp_next = int(np.argmax(logits[0, L_true]))
+    assert int(o["next_token"][0]) == exp_next
+
+
+def test_progress_guarantee_all_rejected():
+    """[P3] Part 2 / [P2] §5: with every candidate wrong the step still commits
+    the root and yields the next greedy token (L = 0, path = [root])."""
+    cfg = synth.tiny()
+    rng = np.random.default_rng(2)
+    ids = rng.integers(0, cfg.V, size=(1, cfg.K, 2)).astype(np.int32)
+    logp = np.log(np.full((1, cfg.K, 2), 0.4))
+    t = oracle.build_tree([17], ids, logp, cfg.s, cfg.n)
+    logits = rng.standard_normal((1, cfg.R, cfg.V)).astype(np.float32)
+    for i in range(1, cfg.R):
+        logits[0, t["parent"][0, i], t["tokens"][0, i]] = -50.0
+    for mode in (oracle.GREEDY, oracle.TYPICAL):
+        o = oracle.posterior(logits, t["tokens"], t["parent"], t["depth"], cfg.K, mode)
+        assert int(o["accept_len"][0]) == 0
+        assert list(o["path"][0]) == [0] + [-1] * cfg.K
+        assert list(o["path_tokens"][0]) == [17] + [-1] * cfg.K
+        assert int(o["next_token"][0]) == int(np.argmax(logits[0, 0]))
+
+
+def test_entropy_closed_forms():
+    """H of a uniform row is ln V; H of a two-level row has a closed form."""
+    V = 1000
+    assert oracle.softmax_entropy(np.zeros(V)) == pytest.approx(math.log(V), abs=1e-12)
+    m, a = 7, 3.0
+    x = np.zeros(V)
+    x[:m] = a
+    Z = m * math.exp(a) + (V - m)
+    ph, pl = math.exp(a) / Z, 1.0 / Z
+    Href = -m * ph * math.log(ph) - (V - m) * pl * math.log(pl)
+    assert oracle.softmax_entropy(x) == pytest.approx(Href, abs=1e-12)
+    # temperature: softmax(x/T) equals softmax of the pre-divided row
+    assert oracle.softmax_entropy(x, 2.5) == pytest.approx(oracle.softmax_entropy(x / 2.5), abs=1e-12)
+
+
+@pytest.mark.parametrize("m,a", [(1, 12.0), (2, 6.0), (20, 4.0), (300, 1.0), (900, 2.0)])
+def test_typical_threshold_closed_form(m, a):
+    """[P2] §5: accept x iff p(x) > min(eps, delta * exp(-H)).  Rows with two
+    probability levels give p and H in closed form; the oracle's margin is
+    log p - log threshold for tokens of both levels."""
+    V, eps, delta = 1000, 0.09, 0.3
+    x = np.zeros(V, np.float32)
+    x[:m] = a
+    Z = m * math.exp(a) + (V - m)
+    ph, pl = math.exp(a) / Z, 1.0 / Z
+    H = -m * ph * math.log(ph) - (V - m) * pl * math.log(pl)
+    thr = min(eps, delta * math.exp(-H))
+    tokens = np.array([[0, 0, V - 1]], np.int32)
+    parent = np.array([[-1, 0, 0]], np.int32)
+    depth = np.array([[0, 1, 1]], np.int32)
+    logits = np.stack([x, x, x])[None]
+    o = oracle.posterior(logits, tokens, parent, depth, 1, oracle.TYPICAL, eps, delta)
+    assert o["margin"][0, 1] == pytest.approx(math.log(ph) - math.log(thr), abs=1e-9)
+    assert o["margin"][0, 2] == pytest.approx(math.log(pl) - math.log(thr), abs=1e-9)
+    assert o["accept"][0, 1] == int(ph > thr) and o["accept"][0, 2] == int(pl > thr)
+
+
+def test_typical_threshold_values_and_monotone():
+    """min(eps, delta e^{-H}) with eps=.09, delta=.3: switch-over at
+    H* = ln(delta/eps); values at H = 1, 3, 6 nats; non-increasing in H."""
+    eps, delta = 0.09, 0.3
+    thr = lambda H: min(eps, delta * math.exp(-H))
+    assert math.log(delta / eps) == pytest.approx(1.2039728, abs=1e-6)
+    assert thr(1.0) == pytest.approx(0.09, abs=1e-12)
+    assert thr(3.0) == pytest.approx(0.0149361, abs=1e-7)
+    assert thr(6.0) == pytest.approx(7.43626e-4, abs=1e-9)
+    # the oracle's decision flips exactly where p crosses the threshold:
+    # build rows of rising entropy (larger uniform support) with one token at
+    # fixed probability 0.05 and check accept <-> 0.05 > thr(H)
+    V = 2000
+    for m in (1, 3, 10, 100, 1000):
+        x = np.full(V, -1e4)
+        x[1:m + 1] = 0.0
+        # token 0 gets probability 0.05 exactly: e^{x0} / (e^{x0} + m) = 0.05
+        x[0] = math.log(0.05 * m / 0.95)
+        p = np.exp(x - x.max())
+        p /= p.sum()
+        H = float(-(p[p > 0] * np.log(p[p > 0])).sum())
+        tokens = np.array([[0, 0]], np.int32)
+        parent = np.array([[-1, 0]], np.int32)
+        depth = np.array([[0, 1]], np.int32)
+        o = oracle.posterior(np.stack([x, x]).astype(np.float32)[None], tokens, parent, depth, 1,
+                             oracle.TYPICAL, eps, delta)
+        assert o["accept"][0, 1] == int(0.05 > thr(H)), (m, H)
+
+
+def test_longest_path_tie_lowest_index():
+    """Two fully accepted branches of the same depth: the lower canonical index
+    wins (convention); a deeper accepted branch beats both."""
+    # root -> 1, 2 ; 1 -> 3 ; 2 -> 4 ; 4 -> 5
+    tokens = np.array([[0, 11, 12, 13, 14, 15]], np.int32)
+    parent = np.array([[-1, 0, 0, 1, 2, 4]], np.int32)
+    depth = np.array([[0, 1, 1, 2, 2, 3]], np.int32)
+    forced = np.array([[1, 1, 1, 1, 1, 0]], np.int32)
+    logits = np.zeros((1, 6, 20), np.float32)
+    o = oracle.posterior(logits, tokens, parent, depth, 3, oracle.GREEDY, forced_accept=forced)
+    assert int(o["accept_len"][0]) == 2 and list(o["path"][0]) == [0, 1, 3, -1]
+    forced[0, 5] = 1
+    o = oracle.posterior(logits, tokens, parent, depth, 3, oracle.GREEDY, forced_accept=forced)
+    assert int(o["accept_len"][0]) == 3 and list(o["path"][0]) == [0, 2, 4, 5]
+
+
+def test_argmax_tie_lowest_id():
+    V = 10
+    x = np.zeros(V, np.float32)
+    x[[6, 3, 8]] = 2.0
+    tokens = np.array([[0, 6]], np.int32)
+    parent = np.array([[-1, 0]], np.int32)
+    depth = np.array([[0, 1]], np.int32)
+    o = oracle.posterior(np.stack([x, x])[None], tokens, parent, depth, 1, oracle.GREEDY)
+    assert int(o["accept_len"][0]) == 0 and int(o["next_token"][0]) == 3
+
+
+# -------------------------------------------------------------- commit ----
+
+def test_commit_kv_gathers_path():
+    """The accepted path's rows move to slots P..P+L; new prefix = P+L+1."""
+    P, R, H, dh = 4, 6, 2, 3
+    kc = np.arange((P + R) * H * dh, dtype=np.float32).reshape(P + R, H, dh)
+    vc = -kc.copy()
+    k0, v0 = kc.copy(), vc.copy()
+    path = np.array([[0, 2, 5, -1]], np.int32)
+    new = oracle.commit_kv([kc], [vc], [P], path, [2])
+    assert int(new[0]) == P + 3
+    assert np.array_equal(kc[:P], k0[:P])
+    for q, node in enumerate([0, 2, 5]):
+        assert np.array_equal(kc[P + q], k0[P + node]) and np.array_equal(vc[P + q], v0[P + node])
