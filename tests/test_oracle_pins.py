@@ -426,3 +426,44 @@ def test_commit_kv_gathers_path():
     assert np.array_equal(kc[:P], k0[:P])
     for q, node in enumerate([0, 2, 5]):
         assert np.array_equal(kc[P + q], k0[P + node]) and np.array_equal(vc[P + q], v0[P + node])
+
+
+def test_typical_decision_at_the_crossing():
+    """[P2] §5 strict rule p(x) > min(eps, delta e^{-H}).  In a two-level row
+    (m tokens at logit a, the rest at 0) the low-level token's margin
+    log p_low + H - log delta falls through zero as a grows; the float32
+    logits just before and just after the closed-form crossing must be
+    accepted and rejected respectively."""
+    V, m, eps, delta = 1000, 5, 0.09, 0.3
+
+    def f(a):
+        Z = m * math.exp(a) + (V - m)
+        ph, pl = math.exp(a) / Z, 1.0 / Z
+        H = -m * ph * math.log(ph) - (V - m) * pl * math.log(pl)
+        thr = min(eps, delta * math.exp(-H))
+        return math.log(pl) - math.log(thr), H
+
+    lo, hi = 0.0, 30.0
+    assert f(lo)[0] > 0 > f(hi)[0]
+    for _ in range(200):
+        mid = 0.5 * (lo + hi)
+        if f(mid)[0] > 0:
+            lo = mid
+        else:
+            hi = mid
+    assert f(lo)[1] > math.log(delta / eps)        # entropy branch of the min
+    a_below = np.float32(lo)
+    while f(float(a_below))[0] <= 0:
+        a_below = np.nextafter(a_below, np.float32(-np.inf))
+    a_above = np.nextafter(a_below, np.float32(np.inf))
+    while f(float(a_above))[0] > 0:
+        a_above = np.nextafter(a_above, np.float32(np.inf))
+    for a, want in ((a_below, 1), (a_above, 0)):
+        x = np.zeros(V, np.float32)
+        x[:m] = a
+        tokens = np.array([[0, V - 1]], np.int32)
+        parent = np.array([[-1, 0]], np.int32)
+        depth = np.array([[0, 1]], np.int32)
+        o = oracle.posterior(np.stack([x, x])[None], tokens, parent, depth, 1, oracle.TYPICAL,
+                             eps, delta)
+        assert int(o["accept"][0, 1]) == want, (a, f(float(a)))
