@@ -1,0 +1,254 @@
+/*
+ * medusa.h -- C ABI of libmedusa_gb300.so: the data-parallel hot path of one
+ * Medusa decoding step on one GB300 GPU (sm_103a).
+ *
+ * The step, as the pages define it:
+ *   1. medusa_heads               K Medusa heads read the last hidden state and
+ *                                 keep their top-s tokens.
+ *   2. medusa_build_tree          the proposals become a budgeted candidate tree.
+ *   3. medusa_tree_attention      every tree node attends to the prefix and to
+ *                                 its own ancestors.
+ *   4. medusa_evaluate_posterior  greedy or typical acceptance; the longest
+ *                                 accepted path is returned.
+ * Page citations are by title and section:
+ *   [P1] "Medusa: Faster LLM text generation" (nazmi.tech)
+ *   [P2] "Medusa 深读：解码慢不是算力问题，是搬运问题" (jokeuncle.pages.dev)
+ *   [P3] "Medusa Part I: Architecture, Training, and Shifted Loss"
+ *        (sudhirpol522.github.io)
+ *
+ * Conventions shared by every call
+ *   - All tensor pointers are DEVICE pointers unless the name ends in _host.
+ *     The caller allocates and owns every buffer; the library allocates
+ *     nothing and keeps no per-call state between calls.
+ *   - Every call is asynchronous on `stream` (a cudaStream_t passed as void*;
+ *     NULL = legacy default stream).  No call synchronises the host, except
+ *     medusa_read_device_status.
+ *   - Arguments are validated on the host before any launch.  A bad argument
+ *     returns MEDUSA_ERR_INVALID_ARG (or MEDUSA_ERR_UNSUPPORTED for a legal
+ *     but unimplemented shape) and launches nothing; medusa_last_error()
+ *     then describes it.  A failed launch returns MEDUSA_ERR_CUDA.
+ *   - Problems only the device can see (a token id out of range, a prefix
+ *     longer than the stated maximum, a non-log-probability score) set the
+ *     device status word that sits in the first bytes of the workspace
+ *     (first error wins; it stays set until medusa_clear_device_status).
+ *     Read it with medusa_read_device_status.
+ *   - Workspace: `ws` is a caller-owned device buffer of at least the bytes
+ *     the matching *_workspace_size function returns, 256-byte aligned.  One
+ *     buffer sized for the largest call may serve every call on one stream.
+ *     Zero it once before first use (the status word must start at 0).
+ *   - Row-major layouts; "[A,B,C]" lists dimensions outermost first.  Every
+ *     tensor pointer must be 16-byte aligned and every innermost dimension a
+ *     multiple of 16 bytes where stated.
+ *   - bf16 tensors hold IEEE bfloat16; accumulation is fp32 everywhere.
+ */
+#ifndef MEDUSA_GB300_H
+#define MEDUSA_GB300_H
+
+#include <stddef.h>
+#include <stdint.h>
+
+#if defined(__GNUC__)
+#define MEDUSA_API __attribute__((visibility("default")))
+#else
+#define MEDUSA_API
+#endif
+
+#ifdef __cplusplus
+extern "C" {
+#endif
+
+typedef enum medusa_status {
+    MEDUSA_OK = 0,
+    MEDUSA_ERR_INVALID_ARG = 1,   /* bad pointer, size or alignment          */
+    MEDUSA_ERR_UNSUPPORTED = 2,   /* legal but not implemented               */
+    MEDUSA_ERR_WORKSPACE = 3,     /* workspace missing or too small          */
+    MEDUSA_ERR_CUDA = 4,          /* a CUDA runtime call or launch failed    */
+    MEDUSA_ERR_TIMEOUT = 5,       /* a bounded device wait ran out           */
+    MEDUSA_ERR_DEVICE_CHECK = 6   /* the device found invalid data           */
+} medusa_status;
+
+typedef enum medusa_dtype {
+    MEDUSA_F32 = 0,
+    MEDUSA_BF16 = 1
+} medusa_dtype;
+
+typedef enum medusa_accept_mode {
+    MEDUSA_GREEDY = 0,
+    MEDUSA_TYPICAL = 1
+} medusa_accept_mode;
+
+/* Device status codes written into the workspace status word. */
+enum {
+    MEDUSA_DEV_OK = 0,
+    MEDUSA_DEV_BAD_TOKEN = 1,      /* a token id outside [0, V)               */
+    MEDUSA_DEV_BAD_PARENT = 2,     /* parent[i] not in [0, i)                 */
+    MEDUSA_DEV_BAD_PREFIX = 3,     /* prefix_len[b] < 0 or > P_max            */
+    MEDUSA_DEV_BAD_SCORE = 4,      /* a tree score > 0 or NaN                 */
+    MEDUSA_DEV_BAD_DEPTH = 5,      /* depth[i] > K or depth[i] != depth[parent]+1 */
+    MEDUSA_DEV_TIMEOUT = 6         /* a bounded wait gave up                  */
+};
+
+/* Limits. */
+#define MEDUSA_MAX_HEADS 8        /* K                                         */
+#define MEDUSA_MAX_TOP_S 16       /* s_k, and the top-s kept per head          */
+#define MEDUSA_MAX_TREE_ROWS 256  /* R = n + 1                                 */
+#define MEDUSA_MAX_BATCH 8        /* B for medusa_heads                        */
+#define MEDUSA_WS_HEADER 256      /* bytes of workspace before any scratch     */
+
+typedef void *medusa_stream;      /* cudaStream_t */
+
+/* Human-readable name of a status code (static string). */
+MEDUSA_API const char *medusa_status_string(medusa_status s);
+
+/* Message of the last failing call on this host thread ("" if none). */
+MEDUSA_API const char *medusa_last_error(void);
+
+/* Number of kernels this library has launched in this process. */
+MEDUSA_API uint64_t medusa_launch_count(void);
+
+/* Copy the workspace status word to *status_host.  Synchronises `stream`. */
+MEDUSA_API medusa_status medusa_read_device_status(const void *ws, int32_t *status_host,
+                                        medusa_stream stream);
+
+/* Reset the workspace status word to 0 (asynchronous on `stream`). */
+MEDUSA_API medusa_status medusa_clear_device_status(void *ws, medusa_stream stream);
+
+/* ------------------------------------------------------------------------
+ * 1. Medusa heads.
+ *
+ * [P2] §3.1 (definition of p_t^(k)) and [P3] Part 3 (ResidualBlock,
+ * vocabulary projection without bias): for every sequence b and head k
+ *     u = W1[k] h[b] + b1[k],   z = h[b] + SiLU(u),   logits = W2[k] z,
+ *     p^(k) = softmax(logits)
+ * and each head keeps its `top_s` most probable tokens ([P2] §6.1).  The
+ * vocabulary logits are never written to memory.
+ *
+ *   h      [B,d]      dtype
+ *   W1     [K,d,d]    dtype; row j holds the weights of output unit j
+ *   b1     [K,d]      dtype, or NULL for no bias
+ *   W2     [K,V,d]    dtype; row v holds token v's projection
+ *   topk_ids  [B,K,top_s] int32  out: token ids, most probable first;
+ *                               equal logits rank the smaller id first
+ *   topk_logp [B,K,top_s] fp32   out: log p^(k)(token)
+ * Requirements: 1 <= B <= 8, 1 <= K <= 8, d % 8 == 0, 1 <= top_s <= 16,
+ * top_s <= V, B'*d*4 <= 160 KiB where B' is B rounded up to 1, 2, 4 or 8.
+ * Pointers 16-byte aligned.
+ * ---------------------------------------------------------------------- */
+MEDUSA_API size_t medusa_heads_workspace_size(int B, int K, int d, int V, int top_s);
+
+MEDUSA_API medusa_status medusa_heads(medusa_dtype dtype, const void *h, const void *W1,
+                           const void *b1, const void *W2, int B, int d, int V,
+                           int K, int top_s, int32_t *topk_ids,
+                           float *topk_logp, void *ws, size_t ws_bytes,
+                           medusa_stream stream);
+
+/* ------------------------------------------------------------------------
+ * 2. Candidate tree under a node budget.
+ *
+ * [P2] §6.2 (greedy construction within a budget: repeatedly take the
+ * frontier node of largest path weight, then add its children) with the
+ * heads' own probabilities as the per-level weights, so a rank path
+ * (i_1..i_k) scores sum_j topk_logp[b][j-1][i_j] (summed from depth 1 down,
+ * in fp64).  [P2] §6.1 (tree mask and shared position index).
+ * Ties: equal scores go to the smaller depth, then to the lexicographically
+ * smaller rank path.  Output order is canonical: root first, then by depth,
+ * then by rank path, so parent[i] < i and each depth is contiguous.
+ *
+ *   root       [B]              int32  the LM head's greedy token per sequence
+ *   topk_ids   [B,K,top_s]      int32  from medusa_heads
+ *   topk_logp  [B,K,top_s]      fp32   log-probabilities (must be <= 0)
+ *   s_host     [K]   HOST       int32  candidates used at depth k+1, 1..top_s
+ *   n                                  tree nodes besides the root; R = n+1
+ *   prefix_len [B] or NULL      int32  P_b, for pos_id (NULL = 0)
+ * Outputs (R = n+1, W = ceil(R/64)):
+ *   tokens [B,R], parent [B,R] (-1 at root), depth [B,R], pos_id [B,R] =
+ *   P_b + depth, anc_mask [B,R,W] uint64 (bit j of row i set iff node j is
+ *   node i or one of its ancestors), paths [B,n,K+1] (node indices root ->
+ *   leaf for each leaf in canonical order, -1 padded), n_leaf [B].
+ * Requirements: K <= 8, R <= 256, n <= sum_k prod_{j<=k} s_j.
+ * ---------------------------------------------------------------------- */
+MEDUSA_API size_t medusa_build_tree_workspace_size(int B, int K, int top_s, int n);
+
+MEDUSA_API medusa_status medusa_build_tree(const int32_t *root, const int32_t *topk_ids,
+                                const float *topk_logp, int B, int K,
+                                const int32_t *s_host, int top_s, int n,
+                                const int32_t *prefix_len, int32_t *tokens,
+                                int32_t *parent, int32_t *depth,
+                                int32_t *pos_id, uint64_t *anc_mask,
+                                int32_t *paths, int32_t *n_leaf, void *ws,
+                                size_t ws_bytes, medusa_stream stream);
+
+/* ------------------------------------------------------------------------
+ * 3. Tree attention.
+ *
+ * [P1] "Tree attention" and [P2] §6.1: node i of sequence b attends to every
+ * prefix slot and to the tree slots of its own ancestors (itself included),
+ * never to another branch:
+ *     out[b,i,h] = softmax_j( scale * q[b,i,h] . K_b[j,h] + M_i(j) ) V_b[j,h]
+ * with M_i(j) = 0 for j < P_b or for tree slot j = P_b + t where bit t of
+ * anc_mask[b,i] is set, -inf otherwise.
+ *
+ *   q         [B,R,H,dh]                 dtype (RoPE, if any, already applied)
+ *   k_cache   [B] device array of device pointers; sequence b's cache is
+ *             [>= P_b+R, H, dh] dtype: prefix in slots 0..P_b-1, the tree
+ *             nodes (canonical order) in slots P_b..P_b+R-1
+ *   v_cache   same layout as k_cache
+ *   prefix_len [B] int32 (device), 0 <= P_b <= P_max
+ *   anc_mask  [B,R,W] uint64 from medusa_build_tree
+ *   out       [B,R,H,dh] dtype
+ * Requirements: dh in {64,128}; R <= 256; bf16: any P_max; f32: P_max + R
+ * <= 16384.
+ * ---------------------------------------------------------------------- */
+MEDUSA_API size_t medusa_tree_attention_workspace_size(medusa_dtype dtype, int B, int R,
+                                            int H, int dh, int P_max);
+
+MEDUSA_API medusa_status medusa_tree_attention(medusa_dtype dtype, const void *q,
+                                    const void *const *k_cache,
+                                    const void *const *v_cache,
+                                    const int32_t *prefix_len, int P_max,
+                                    const uint64_t *anc_mask, int B, int R,
+                                    int H, int dh, float scale, void *out,
+                                    void *ws, size_t ws_bytes,
+                                    medusa_stream stream);
+
+/* ------------------------------------------------------------------------
+ * 4. Posterior: acceptance and the longest accepted path.
+ *
+ * Node i's token is judged by the verification logits of its parent's row.
+ *   MEDUSA_GREEDY  ([P3] Part 2): accept iff the token is that row's argmax.
+ *   MEDUSA_TYPICAL ([P2] §5):  accept iff p(x) > min(eps, delta*exp(-H(p))),
+ *                  p = softmax(logits / temperature), H in nats.
+ * The root (the LM head's greedy token) is accepted unconditionally ([P2] §5);
+ * a node counts only if all its ancestors are accepted ([P3] Part 2); the
+ * deepest such node wins, the smallest canonical index among equals.
+ *
+ *   logits [B,R,V] dtype; tokens/parent/depth [B,R] int32 from
+ *   medusa_build_tree (parent[i] < i).
+ * Outputs:
+ *   accept_len [B]         accepted nodes beyond the root, 0..K
+ *   path [B,K+1]           node indices root -> best (-1 padded)
+ *   path_tokens [B,K+1]    their tokens (-1 padded)
+ *   next_token [B]         argmax of the best node's row (ties -> smaller id)
+ *   accept [B,R] or NULL   per-node decision (root = 1)
+ * Requirements: R <= 256, K <= 8, V % 8 == 0 (bf16) or V % 4 == 0 (f32),
+ * temperature > 0, eps > 0, delta > 0.
+ * ---------------------------------------------------------------------- */
+MEDUSA_API size_t medusa_posterior_workspace_size(int B, int R);
+
+MEDUSA_API medusa_status medusa_evaluate_posterior(medusa_dtype dtype, const void *logits,
+                                        const int32_t *tokens,
+                                        const int32_t *parent,
+                                        const int32_t *depth, int B, int R,
+                                        int V, int K, medusa_accept_mode mode,
+                                        float eps, float delta,
+                                        float temperature, int32_t *accept_len,
+                                        int32_t *path, int32_t *path_tokens,
+                                        int32_t *next_token, int32_t *accept,
+                                        void *ws, size_t ws_bytes,
+                                        medusa_stream stream);
+
+#ifdef __cplusplus
+}
+#endif
+
+#endif /* MEDUSA_GB300_H */

@@ -1,0 +1,277 @@
+"""Thin Python binding over libmedusa_gb300.so (ctypes).
+
+Every step of the Medusa decoding step runs in the library's CUDA kernels;
+this module only turns torch tensors into device pointers, sizes and the
+current CUDA stream, allocates outputs and workspaces with torch, and raises
+``MedusaError`` on a non-OK status.  There is no CPU or PyTorch fallback: if
+the compiled library is missing, importing the calls fails loudly.
+
+Public calls (same names as the C ABI in include/medusa.h):
+    heads, build_tree, tree_attention, evaluate_posterior
+plus workspace-size queries, device-status helpers, launch_count, and the
+``MedusaStep`` object that chains the four calls for one decoding step.
+"""
+from __future__ import annotations
+
+import ctypes
+import math
+import os
+from dataclasses import dataclass
+from typing import Optional, Sequence
+
+import torch
+
+_HERE = os.path.dirname(os.path.abspath(__file__))
+LIB_PATH = os.path.join(_HERE, "libmedusa_gb300.so")
+
+F32, BF16 = 0, 1
+GREEDY, TYPICAL = 0, 1
+WS_HEADER = 256
+MAX_TOP_S = 16
+MAX_TREE_ROWS = 256
+
+STATUS = {0: "MEDUSA_OK", 1: "MEDUSA_ERR_INVALID_ARG", 2: "MEDUSA_ERR_UNSUPPORTED",
+          3: "MEDUSA_ERR_WORKSPACE", 4: "MEDUSA_ERR_CUDA", 5: "MEDUSA_ERR_TIMEOUT",
+          6: "MEDUSA_ERR_DEVICE_CHECK"}
+DEVICE_STATUS = {0: "ok", 1: "bad token", 2: "bad parent", 3: "bad prefix", 4: "bad score",
+                 5: "bad depth", 6: "timeout"}
+
+EXPORTS = ("medusa_status_string", "medusa_last_error", "medusa_launch_count",
+           "medusa_read_device_status", "medusa_clear_device_status",
+           "medusa_heads_workspace_size", "medusa_heads",
+           "medusa_build_tree_workspace_size", "medusa_build_tree",
+           "medusa_tree_attention_workspace_size", "medusa_tree_attention",
+           "medusa_posterior_workspace_size", "medusa_evaluate_posterior")
+
+
+class MedusaError(RuntimeError):
+    def __init__(self, status: int, msg: str):
+        super().__init__(f"{STATUS.get(status, status)}: {msg}")
+        self.status = status
+
+
+_lib = None
+
+
+def lib() -> ctypes.CDLL:
+    """Load libmedusa_gb300.so (built by ``build.build()``); raise if absent."""
+    global _lib
+    if _lib is not None:
+        return _lib
+    if not os.path.exists(LIB_PATH):
+        raise ImportError(
+            f"{LIB_PATH} is missing: build it with "
+            "`python -c 'import __graft_entry__ as g; g.build()'` (needs nvcc, sm_103a)")
+    L = ctypes.CDLL(LIB_PATH)
+    P, I, F, S = ctypes.c_void_p, ctypes.c_int, ctypes.c_float, ctypes.c_size_t
+    sig = {
+        "medusa_status_string": ([I], ctypes.c_char_p),
+        "medusa_last_error": ([], ctypes.c_char_p),
+        "medusa_launch_count": ([], ctypes.c_uint64),
+        "medusa_read_device_status": ([P, P, P], I),
+        "medusa_clear_device_status": ([P, P], I),
+        "medusa_heads_workspace_size": ([I, I, I, I, I], S),
+        "medusa_heads": ([I, P, P, P, P, I, I, I, I, I, P, P, P, S, P], I),
+        "medusa_build_tree_workspace_size": ([I, I, I, I], S),
+        "medusa_build_tree": ([P, P, P, I, I, P, I, I, P, P, P, P, P, P, P, P, P, S, P], I),
+        "medusa_tree_attention_workspace_size": ([I, I, I, I, I, I], S),
+        "medusa_tree_attention": ([I, P, P, P, P, I, P, I, I, I, I, F, P, P, S, P], I),
+        "medusa_posterior_workspace_size": ([I, I], S),
+        "medusa_evaluate_posterior": ([I, P, P, P, P, I, I, I, I, I, F, F, F, P, P, P, P, P, P, S, P], I),
+    }
+    for name, (args, res) in sig.items():
+        fn = getattr(L, name)
+        fn.argtypes = args
+        fn.restype = res
+    _lib = L
+    return L
+
+
+def _check(rc: int):
+    if rc != 0:
+        msg = lib().medusa_last_error().decode(errors="replace")
+        raise MedusaError(rc, msg)
+
+
+def _ptr(t: Optional[torch.Tensor]):
+    return None if t is None else ctypes.c_void_p(t.data_ptr())
+
+
+def _stream(stream=None):
+    s = torch.cuda.current_stream() if stream is None else stream
+    return ctypes.c_void_p(s.cuda_stream)
+
+
+def _dtype(t: torch.Tensor) -> int:
+    if t.dtype == torch.bfloat16:
+        return BF16
+    if t.dtype == torch.float32:
+        return F32
+    raise TypeError(f"unsupported dtype {t.dtype} (bf16 or fp32)")
+
+
+def _need(t: torch.Tensor, name: str):
+    if not t.is_cuda:
+        raise ValueError(f"{name} must be a CUDA tensor")
+    if not t.is_contiguous():
+        raise ValueError(f"{name} must be contiguous")
+
+
+def launch_count() -> int:
+    return int(lib().medusa_launch_count())
+
+
+def new_workspace(nbytes: int, device=None) -> torch.Tensor:
+    """Zeroed device workspace (the status word must start at 0)."""
+    n = (max(int(nbytes), WS_HEADER) + 255) // 256 * 256
+    return torch.zeros(n, dtype=torch.uint8, device=device or "cuda")
+
+
+def read_device_status(ws: torch.Tensor, stream=None) -> int:
+    out = ctypes.c_int32(0)
+    _check(lib().medusa_read_device_status(_ptr(ws), ctypes.byref(out), _stream(stream)))
+    return int(out.value)
+
+
+def clear_device_status(ws: torch.Tensor, stream=None):
+    _check(lib().medusa_clear_device_status(_ptr(ws), _stream(stream)))
+
+
+# ------------------------------------------------------------------ heads ---
+
+def heads_workspace_size(B: int, K: int, d: int, V: int, top_s: int) -> int:
+    return int(lib().medusa_heads_workspace_size(B, K, d, V, top_s))
+
+
+def heads(h, W1, b1, W2, top_s: int, ws=None, out=None, stream=None):
+    """Top-s token ids [B,K,s] (int32) and log-probs (fp32) of the K heads."""
+    for t, n in ((h, "h"), (W1, "W1"), (W2, "W2")):
+        _need(t, n)
+    if b1 is not None:
+        _need(b1, "b1")
+    B, d = h.shape
+    K, V = W2.shape[0], W2.shape[1]
+    if ws is None:
+        ws = new_workspace(heads_workspace_size(B, K, d, V, top_s), h.device)
+    if out is None:
+        out = (torch.empty((B, K, top_s), dtype=torch.int32, device=h.device),
+               torch.empty((B, K, top_s), dtype=torch.float32, device=h.device))
+    ids, logp = out
+    _check(lib().medusa_heads(_dtype(h), _ptr(h), _ptr(W1), _ptr(b1), _ptr(W2), B, d, V, K, top_s,
+                              _ptr(ids), _ptr(logp), _ptr(ws), ws.numel(), _stream(stream)))
+    return ids, logp
+
+
+# ------------------------------------------------------------------- tree ---
+
+@dataclass
+class Tree:
+    tokens: torch.Tensor
+    parent: torch.Tensor
+    depth: torch.Tensor
+    pos_id: torch.Tensor
+    anc_mask: torch.Tensor
+    paths: torch.Tensor
+    n_leaf: torch.Tensor
+
+    @staticmethod
+    def empty(B: int, n: int, K: int, device) -> "Tree":
+        R = n + 1
+        W = (R + 63) // 64
+        i32 = dict(dtype=torch.int32, device=device)
+        return Tree(torch.empty((B, R), **i32), torch.empty((B, R), **i32),
+                    torch.empty((B, R), **i32), torch.empty((B, R), **i32),
+                    torch.empty((B, R, W), dtype=torch.int64, device=device),
+                    torch.empty((B, n, K + 1), **i32), torch.empty((B,), **i32))
+
+
+def build_tree_workspace_size(B: int, K: int, top_s: int, n: int) -> int:
+    return int(lib().medusa_build_tree_workspace_size(B, K, top_s, n))
+
+
+def build_tree(root, topk_ids, topk_logp, s: Sequence[int], n: int, prefix_len=None, ws=None,
+               out: Optional[Tree] = None, stream=None) -> Tree:
+    """Budgeted candidate tree (canonical order) from the heads' top-s lists."""
+    for t, nm in ((root, "root"), (topk_ids, "topk_ids"), (topk_logp, "topk_logp")):
+        _need(t, nm)
+    B, K, S = topk_ids.shape
+    s_host = (ctypes.c_int32 * K)(*[int(x) for x in s])
+    if ws is None:
+        ws = new_workspace(build_tree_workspace_size(B, K, S, n), root.device)
+    t = out or Tree.empty(B, n, K, root.device)
+    _check(lib().medusa_build_tree(_ptr(root), _ptr(topk_ids), _ptr(topk_logp), B, K, s_host, S, n,
+                                   _ptr(prefix_len), _ptr(t.tokens), _ptr(t.parent), _ptr(t.depth),
+                                   _ptr(t.pos_id), _ptr(t.anc_mask), _ptr(t.paths), _ptr(t.n_leaf),
+                                   _ptr(ws), ws.numel(), _stream(stream)))
+    return t
+
+
+# -------------------------------------------------------------- attention ---
+
+def tree_attention_workspace_size(dtype: int, B: int, R: int, H: int, dh: int, P_max: int) -> int:
+    return int(lib().medusa_tree_attention_workspace_size(dtype, B, R, H, dh, P_max))
+
+
+def cache_pointers(caches: Sequence[torch.Tensor], device) -> torch.Tensor:
+    """Device array of the per-sequence cache base pointers."""
+    for c in caches:
+        _need(c, "cache")
+    return torch.tensor([c.data_ptr() for c in caches], dtype=torch.int64, device=device)
+
+
+def tree_attention(q, k_ptrs, v_ptrs, prefix_len, P_max: int, anc_mask, scale=None, out=None,
+                   ws=None, stream=None):
+    """Tree-masked attention.  q [B,R,H,dh]; k_ptrs/v_ptrs: int64 device arrays of
+    per-sequence cache pointers (see cache_pointers); prefix_len int32 [B]."""
+    _need(q, "q")
+    B, R, H, dh = q.shape
+    dt = _dtype(q)
+    if scale is None:
+        scale = 1.0 / math.sqrt(dh)
+    if ws is None:
+        ws = new_workspace(tree_attention_workspace_size(dt, B, R, H, dh, P_max), q.device)
+    if out is None:
+        out = torch.empty_like(q)
+    _check(lib().medusa_tree_attention(dt, _ptr(q), _ptr(k_ptrs), _ptr(v_ptrs), _ptr(prefix_len),
+                                       int(P_max), _ptr(anc_mask), B, R, H, dh, float(scale),
+                                       _ptr(out), _ptr(ws), ws.numel(), _stream(stream)))
+    return out
+
+
+# -------------------------------------------------------------- posterior ---
+
+@dataclass
+class Posterior:
+    accept_len: torch.Tensor
+    path: torch.Tensor
+    path_tokens: torch.Tensor
+    next_token: torch.Tensor
+    accept: Optional[torch.Tensor]
+
+    @staticmethod
+    def empty(B: int, R: int, K: int, device, with_accept: bool = True) -> "Posterior":
+        i32 = dict(dtype=torch.int32, device=device)
+        return Posterior(torch.empty((B,), **i32), torch.empty((B, K + 1), **i32),
+                         torch.empty((B, K + 1), **i32), torch.empty((B,), **i32),
+                         torch.empty((B, R), **i32) if with_accept else None)
+
+
+def posterior_workspace_size(B: int, R: int) -> int:
+    return int(lib().medusa_posterior_workspace_size(B, R))
+
+
+def evaluate_posterior(logits, tokens, parent, depth, K: int, mode: int = GREEDY, eps=0.09,
+                       delta=0.3, temperature=1.0, ws=None, out: Optional[Posterior] = None,
+                       with_accept: bool = True, stream=None) -> Posterior:
+    """Acceptance + longest accepted path.  logits [B,R,V] bf16 or fp32."""
+    _need(logits, "logits")
+    B, R, V = logits.shape
+    if ws is None:
+        ws = new_workspace(posterior_workspace_size(B, R), logits.device)
+    o = out or Posterior.empty(B, R, K, logits.device, with_accept)
+    _check(lib().medusa_evaluate_posterior(_dtype(logits), _ptr(logits), _ptr(tokens), _ptr(parent),
+                                           _ptr(depth), B, R, V, K, int(mode), float(eps),
+                                           float(delta), float(temperature), _ptr(o.accept_len),
+                                           _ptr(o.path), _ptr(o.path_tokens), _ptr(o.next_token),
+                                           _ptr(o.accept), _ptr(ws), ws.numel(), _stream(stream)))
+    return o

@@ -1,0 +1,267 @@
+// api.cu -- the extern "C" boundary of libmedusa_gb300.so.
+//
+// Every entry point validates its arguments on the host, launches nothing on
+// a bad argument, and maps CUDA failures to MEDUSA_ERR_CUDA.  The message of
+// the last failure on the calling thread is kept for medusa_last_error().
+#include <atomic>
+#include <cstdarg>
+#include <cstdio>
+#include <cstring>
+#include <mutex>
+
+#include "launch.h"
+
+namespace medusa {
+
+namespace {
+
+thread_local char g_err[512] = "";
+std::atomic<uint64_t> g_launches{0};
+
+medusa_status fail(medusa_status s, const char *fmt, ...) {
+    va_list ap;
+    va_start(ap, fmt);
+    vsnprintf(g_err, sizeof g_err, fmt, ap);
+    va_end(ap);
+    return s;
+}
+
+medusa_status cuda_fail(cudaError_t e, const char *where) {
+    return fail(MEDUSA_ERR_CUDA, "%s: %s", where, cudaGetErrorString(e));
+}
+
+bool aligned16(const void *p) { return (reinterpret_cast<uintptr_t>(p) & 15u) == 0; }
+bool aligned256(const void *p) { return (reinterpret_cast<uintptr_t>(p) & 255u) == 0; }
+
+medusa_status check_ws(const void *ws, size_t have, size_t need, const char *who) {
+    if (!ws) return fail(MEDUSA_ERR_WORKSPACE, "%s: workspace is NULL", who);
+    if (!aligned256(ws)) return fail(MEDUSA_ERR_WORKSPACE, "%s: workspace not 256-byte aligned", who);
+    if (have < need)
+        return fail(MEDUSA_ERR_WORKSPACE, "%s: workspace has %zu bytes, needs %zu", who, have, need);
+    return MEDUSA_OK;
+}
+
+}  // namespace
+
+int device_sm_count() {
+    static std::mutex mu;
+    static int cache[64] = {0};
+    int dev = 0;
+    if (cudaGetDevice(&dev) != cudaSuccess || dev < 0 || dev >= 64) return 152;
+    std::lock_guard<std::mutex> lk(mu);
+    if (!cache[dev]) {
+        int n = 0;
+        if (cudaDeviceGetAttribute(&n, cudaDevAttrMultiProcessorCount, dev) != cudaSuccess || n <= 0)
+            n = 152;
+        cache[dev] = n;
+    }
+    return cache[dev];
+}
+
+void note_launch() { g_launches.fetch_add(1, std::memory_order_relaxed); }
+
+}  // namespace medusa
+
+using namespace medusa;
+
+extern "C" {
+
+const char *medusa_status_string(medusa_status s) {
+    switch (s) {
+    case MEDUSA_OK: return "MEDUSA_OK";
+    case MEDUSA_ERR_INVALID_ARG: return "MEDUSA_ERR_INVALID_ARG";
+    case MEDUSA_ERR_UNSUPPORTED: return "MEDUSA_ERR_UNSUPPORTED";
+    case MEDUSA_ERR_WORKSPACE: return "MEDUSA_ERR_WORKSPACE";
+    case MEDUSA_ERR_CUDA: return "MEDUSA_ERR_CUDA";
+    case MEDUSA_ERR_TIMEOUT: return "MEDUSA_ERR_TIMEOUT";
+    case MEDUSA_ERR_DEVICE_CHECK: return "MEDUSA_ERR_DEVICE_CHECK";
+    }
+    return "MEDUSA_ERR_UNKNOWN";
+}
+
+const char *medusa_last_error(void) { return g_err; }
+
+uint64_t medusa_launch_count(void) { return g_launches.load(std::memory_order_relaxed); }
+
+medusa_status medusa_read_device_status(const void *ws, int32_t *status_host, medusa_stream stream) {
+    if (!ws || !status_host) return fail(MEDUSA_ERR_INVALID_ARG, "read_device_status: NULL pointer");
+    cudaStream_t st = static_cast<cudaStream_t>(stream);
+    cudaError_t e = cudaMemcpyAsync(status_host, ws, sizeof(int32_t), cudaMemcpyDeviceToHost, st);
+    if (e) return cuda_fail(e, "read_device_status");
+    e = cudaStreamSynchronize(st);
+    if (e) return cuda_fail(e, "read_device_status");
+    return MEDUSA_OK;
+}
+
+medusa_status medusa_clear_device_status(void *ws, medusa_stream stream) {
+    if (!ws) return fail(MEDUSA_ERR_INVALID_ARG, "clear_device_status: NULL workspace");
+    cudaError_t e = cudaMemsetAsync(ws, 0, sizeof(int32_t), static_cast<cudaStream_t>(stream));
+    if (e) return cuda_fail(e, "clear_device_status");
+    return MEDUSA_OK;
+}
+
+// ----------------------------------------------------------------- heads ---
+
+size_t medusa_heads_workspace_size(int B, int K, int d, int V, int top_s) {
+    if (B < 1 || K < 1 || d < 1 || V < 1 || top_s < 1) return 0;
+    return heads_workspace_bytes(B, K, d, V, top_s);
+}
+
+medusa_status medusa_heads(medusa_dtype dtype, const void *h, const void *W1, const void *b1,
+                           const void *W2, int B, int d, int V, int K, int top_s,
+                           int32_t *topk_ids, float *topk_logp, void *ws, size_t ws_bytes,
+                           medusa_stream stream) {
+    const char *who = "medusa_heads";
+    if (dtype != MEDUSA_F32 && dtype != MEDUSA_BF16)
+        return fail(MEDUSA_ERR_INVALID_ARG, "%s: unknown dtype %d", who, (int)dtype);
+    if (!h || !W1 || !W2 || !topk_ids || !topk_logp)
+        return fail(MEDUSA_ERR_INVALID_ARG, "%s: NULL tensor pointer", who);
+    if (B < 1 || B > MEDUSA_MAX_BATCH)
+        return fail(MEDUSA_ERR_UNSUPPORTED, "%s: B=%d outside 1..%d", who, B, MEDUSA_MAX_BATCH);
+    if (K < 1 || K > MEDUSA_MAX_HEADS)
+        return fail(MEDUSA_ERR_INVALID_ARG, "%s: K=%d outside 1..%d", who, K, MEDUSA_MAX_HEADS);
+    if (d < 8 || d % 8)
+        return fail(MEDUSA_ERR_INVALID_ARG, "%s: d=%d must be a positive multiple of 8", who, d);
+    if (top_s < 1 || top_s > MEDUSA_MAX_TOP_S || top_s > V)
+        return fail(MEDUSA_ERR_INVALID_ARG, "%s: top_s=%d outside 1..min(16, V)", who, top_s);
+    const int nb = B <= 1 ? 1 : B <= 2 ? 2 : B <= 4 ? 4 : 8;  // batch bucket held in smem
+    if ((size_t)nb * d * sizeof(float) > 160 * 1024)
+        return fail(MEDUSA_ERR_UNSUPPORTED, "%s: %d x d x 4 = %zu bytes exceeds 160 KiB", who, nb,
+                    (size_t)nb * d * sizeof(float));
+    if (!aligned16(h) || !aligned16(W1) || !aligned16(W2) || (b1 && !aligned16(b1)))
+        return fail(MEDUSA_ERR_INVALID_ARG, "%s: tensor pointers must be 16-byte aligned", who);
+    if (medusa_status s = check_ws(ws, ws_bytes, heads_workspace_bytes(B, K, d, V, top_s), who))
+        return s;
+    cudaError_t e = launch_heads(dtype, h, W1, b1, W2, B, d, V, K, top_s, topk_ids, topk_logp, ws,
+                                 static_cast<cudaStream_t>(stream));
+    if (e) return cuda_fail(e, who);
+    return MEDUSA_OK;
+}
+
+// ------------------------------------------------------------------ tree ---
+
+size_t medusa_build_tree_workspace_size(int B, int K, int top_s, int n) {
+    return tree_workspace_bytes(B, K, top_s, n);
+}
+
+medusa_status medusa_build_tree(const int32_t *root, const int32_t *topk_ids,
+                                const float *topk_logp, int B, int K, const int32_t *s_host,
+                                int top_s, int n, const int32_t *prefix_len, int32_t *tokens,
+                                int32_t *parent, int32_t *depth, int32_t *pos_id,
+                                uint64_t *anc_mask, int32_t *paths, int32_t *n_leaf, void *ws,
+                                size_t ws_bytes, medusa_stream stream) {
+    const char *who = "medusa_build_tree";
+    if (!root || !topk_ids || !topk_logp || !s_host || !tokens || !parent || !depth || !pos_id ||
+        !anc_mask || !paths || !n_leaf)
+        return fail(MEDUSA_ERR_INVALID_ARG, "%s: NULL pointer", who);
+    if (B < 1) return fail(MEDUSA_ERR_INVALID_ARG, "%s: B=%d", who, B);
+    if (K < 1 || K > MEDUSA_MAX_HEADS)
+        return fail(MEDUSA_ERR_INVALID_ARG, "%s: K=%d outside 1..%d", who, K, MEDUSA_MAX_HEADS);
+    if (top_s < 1 || top_s > MEDUSA_MAX_TOP_S)
+        return fail(MEDUSA_ERR_INVALID_ARG, "%s: top_s=%d outside 1..16", who, top_s);
+    long long total = 0, level = 1;
+    for (int k = 0; k < K; ++k) {
+        if (s_host[k] < 1 || s_host[k] > top_s)
+            return fail(MEDUSA_ERR_INVALID_ARG, "%s: s[%d]=%d outside 1..top_s", who, k, s_host[k]);
+        level *= s_host[k];
+        total += level;
+        if (total > (1 << 20)) break;
+    }
+    if (n < 1 || n + 1 > MEDUSA_MAX_TREE_ROWS)
+        return fail(MEDUSA_ERR_INVALID_ARG, "%s: n=%d outside 1..%d", who, n,
+                    MEDUSA_MAX_TREE_ROWS - 1);
+    if (n > total)
+        return fail(MEDUSA_ERR_INVALID_ARG, "%s: n=%d exceeds the %lld nodes of the full tree",
+                    who, n, total);
+    if (medusa_status s = check_ws(ws, ws_bytes, tree_workspace_bytes(B, K, top_s, n), who))
+        return s;
+    cudaError_t e = launch_build_tree(root, topk_ids, topk_logp, B, K, s_host, top_s, n,
+                                      prefix_len, tokens, parent, depth, pos_id, anc_mask, paths,
+                                      n_leaf, ws, static_cast<cudaStream_t>(stream));
+    if (e) return cuda_fail(e, who);
+    return MEDUSA_OK;
+}
+
+// ------------------------------------------------------------- attention ---
+
+size_t medusa_tree_attention_workspace_size(medusa_dtype dtype, int B, int R, int H, int dh,
+                                            int P_max) {
+    if (B < 1 || R < 1 || H < 1 || dh < 1 || P_max < 0) return 0;
+    return attention_workspace_bytes(dtype, B, R, H, dh, P_max);
+}
+
+medusa_status medusa_tree_attention(medusa_dtype dtype, const void *q, const void *const *k_cache,
+                                    const void *const *v_cache, const int32_t *prefix_len,
+                                    int P_max, const uint64_t *anc_mask, int B, int R, int H,
+                                    int dh, float scale, void *out, void *ws, size_t ws_bytes,
+                                    medusa_stream stream) {
+    const char *who = "medusa_tree_attention";
+    if (dtype != MEDUSA_F32 && dtype != MEDUSA_BF16)
+        return fail(MEDUSA_ERR_INVALID_ARG, "%s: unknown dtype %d", who, (int)dtype);
+    if (!q || !k_cache || !v_cache || !prefix_len || !anc_mask || !out)
+        return fail(MEDUSA_ERR_INVALID_ARG, "%s: NULL pointer", who);
+    if (B < 1 || H < 1) return fail(MEDUSA_ERR_INVALID_ARG, "%s: B=%d H=%d", who, B, H);
+    if (R < 1 || R > MEDUSA_MAX_TREE_ROWS)
+        return fail(MEDUSA_ERR_INVALID_ARG, "%s: R=%d outside 1..%d", who, R, MEDUSA_MAX_TREE_ROWS);
+    if (dh != 64 && dh != 128)
+        return fail(MEDUSA_ERR_UNSUPPORTED, "%s: dh=%d (supported: 64, 128)", who, dh);
+    if (P_max < 0) return fail(MEDUSA_ERR_INVALID_ARG, "%s: P_max=%d", who, P_max);
+    if (dtype == MEDUSA_F32 && (long long)P_max + R > 16384)
+        return fail(MEDUSA_ERR_UNSUPPORTED, "%s: f32 path needs P_max + R <= 16384", who);
+    if (!(scale > 0.f)) return fail(MEDUSA_ERR_INVALID_ARG, "%s: scale must be > 0", who);
+    if (!aligned16(q) || !aligned16(out) || !aligned16(anc_mask) || !aligned16(k_cache) ||
+        !aligned16(v_cache))
+        return fail(MEDUSA_ERR_INVALID_ARG, "%s: pointers must be 16-byte aligned", who);
+    if (medusa_status s = check_ws(ws, ws_bytes, attention_workspace_bytes(dtype, B, R, H, dh, P_max), who))
+        return s;
+    cudaError_t e = launch_tree_attention(dtype, q, k_cache, v_cache, prefix_len, P_max, anc_mask,
+                                          B, R, H, dh, scale, out, ws,
+                                          static_cast<cudaStream_t>(stream));
+    if (e) return cuda_fail(e, who);
+    return MEDUSA_OK;
+}
+
+// ------------------------------------------------------------- posterior ---
+
+size_t medusa_posterior_workspace_size(int B, int R) {
+    if (B < 1 || R < 1) return 0;
+    return posterior_workspace_bytes(B, R);
+}
+
+medusa_status medusa_evaluate_posterior(medusa_dtype dtype, const void *logits,
+                                        const int32_t *tokens, const int32_t *parent,
+                                        const int32_t *depth, int B, int R, int V, int K,
+                                        medusa_accept_mode mode, float eps, float delta,
+                                        float temperature, int32_t *accept_len, int32_t *path,
+                                        int32_t *path_tokens, int32_t *next_token,
+                                        int32_t *accept, void *ws, size_t ws_bytes,
+                                        medusa_stream stream) {
+    const char *who = "medusa_evaluate_posterior";
+    if (dtype != MEDUSA_F32 && dtype != MEDUSA_BF16)
+        return fail(MEDUSA_ERR_INVALID_ARG, "%s: unknown dtype %d", who, (int)dtype);
+    if (mode != MEDUSA_GREEDY && mode != MEDUSA_TYPICAL)
+        return fail(MEDUSA_ERR_INVALID_ARG, "%s: unknown mode %d", who, (int)mode);
+    if (!logits || !tokens || !parent || !depth || !accept_len || !path || !path_tokens ||
+        !next_token)
+        return fail(MEDUSA_ERR_INVALID_ARG, "%s: NULL pointer", who);
+    if (B < 1) return fail(MEDUSA_ERR_INVALID_ARG, "%s: B=%d", who, B);
+    if (R < 1 || R > MEDUSA_MAX_TREE_ROWS)
+        return fail(MEDUSA_ERR_INVALID_ARG, "%s: R=%d outside 1..%d", who, R, MEDUSA_MAX_TREE_ROWS);
+    if (K < 0 || K > MEDUSA_MAX_HEADS)
+        return fail(MEDUSA_ERR_INVALID_ARG, "%s: K=%d outside 0..%d", who, K, MEDUSA_MAX_HEADS);
+    const int vn = dtype == MEDUSA_BF16 ? 8 : 4;
+    if (V < 1 || V % vn)
+        return fail(MEDUSA_ERR_INVALID_ARG, "%s: V=%d must be a positive multiple of %d", who, V, vn);
+    if (!(temperature > 0.f) || !(eps > 0.f) || !(delta > 0.f))
+        return fail(MEDUSA_ERR_INVALID_ARG, "%s: eps, delta and temperature must be > 0", who);
+    if (!aligned16(logits))
+        return fail(MEDUSA_ERR_INVALID_ARG, "%s: logits must be 16-byte aligned", who);
+    if (medusa_status s = check_ws(ws, ws_bytes, posterior_workspace_bytes(B, R), who)) return s;
+    cudaError_t e = launch_posterior(dtype, logits, tokens, parent, depth, B, R, V, K, mode, eps,
+                                     delta, temperature, accept_len, path, path_tokens, next_token,
+                                     accept, ws, static_cast<cudaStream_t>(stream));
+    if (e) return cuda_fail(e, who);
+    return MEDUSA_OK;
+}
+
+}  // extern "C"

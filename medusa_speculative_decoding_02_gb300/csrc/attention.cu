@@ -1,0 +1,493 @@
+// attention.cu -- tree-masked attention over the KV cache.
+//
+// "Medusa: Faster LLM text generation" (Tree attention) and "Medusa 深读"
+// §6.1: every tree node attends to the whole prefix and to its own branch
+// ancestors (itself included), never to another branch.  Sequence b's cache
+// holds the prefix in slots 0..P_b-1 and the R tree nodes (canonical order)
+// in slots P_b..P_b+R-1; node i may see tree slot t iff bit t of its
+// ancestor-mask row is set.
+//
+// bf16 path (tensor cores, split-KV):
+//   tree_attn_split_kernel  grid (prefix splits + 1, H, B).  One CTA owns one
+//       head of one sequence and one key range; its warps own 16 query rows
+//       each, so all R tree rows share every K/V tile, which is staged into
+//       shared memory with cp.async (double-buffered, XOR-swizzled rows).
+//       S = Q K^T and O += P V run as m16n8k16 bf16 MMAs with fp32
+//       accumulation; the softmax is online in the log2 domain.  The last
+//       split covers the R tree slots and applies the ancestor bitmask; the
+//       prefix splits need no mask.  Each CTA writes unnormalised partial
+//       (O, m, l) rows.
+//   tree_attn_combine_kernel  merges the splits of each (b, row, head) with a
+//       log-sum-exp rescale and writes the bf16 output.
+// f32 path (small problems): tree_attn_f32_kernel, one CTA per
+// (row, head, sequence) on CUDA cores, exact softmax.
+#include <algorithm>
+
+#include "common.cuh"
+#include "launch.h"
+
+namespace medusa {
+
+namespace {
+
+constexpr int kTile = 64;        // keys per shared-memory stage
+constexpr int kSub = 32;         // keys per softmax/MMA sub-step
+constexpr int kTargetCtas = 304; // split-KV aim: two CTAs per SM on 152 SMs
+constexpr float kLog2e = 1.4426950408889634f;
+
+__device__ __forceinline__ unsigned smem_u32(const void *p) {
+    return static_cast<unsigned>(__cvta_generic_to_shared(p));
+}
+
+__device__ __forceinline__ void cp_async16(unsigned dst, const void *src, int src_bytes) {
+    asm volatile("cp.async.cg.shared.global [%0], [%1], 16, %2;\n" ::"r"(dst), "l"(src),
+                 "r"(src_bytes));
+}
+__device__ __forceinline__ void cp_async_commit() { asm volatile("cp.async.commit_group;\n"); }
+template <int N>
+__device__ __forceinline__ void cp_async_wait() {
+    asm volatile("cp.async.wait_group %0;\n" ::"n"(N));
+}
+
+__device__ __forceinline__ void ldsm_x4(unsigned addr, uint32_t &r0, uint32_t &r1, uint32_t &r2,
+                                        uint32_t &r3) {
+    asm volatile("ldmatrix.sync.aligned.m8n8.x4.shared.b16 {%0,%1,%2,%3}, [%4];\n"
+                 : "=r"(r0), "=r"(r1), "=r"(r2), "=r"(r3)
+                 : "r"(addr));
+}
+__device__ __forceinline__ void ldsm_x4_t(unsigned addr, uint32_t &r0, uint32_t &r1, uint32_t &r2,
+                                          uint32_t &r3) {
+    asm volatile("ldmatrix.sync.aligned.m8n8.x4.trans.shared.b16 {%0,%1,%2,%3}, [%4];\n"
+                 : "=r"(r0), "=r"(r1), "=r"(r2), "=r"(r3)
+                 : "r"(addr));
+}
+
+__device__ __forceinline__ void mma_bf16(float (&c)[4], const uint32_t (&a)[4], uint32_t b0,
+                                         uint32_t b1) {
+    asm volatile(
+        "mma.sync.aligned.m16n8k16.row.col.f32.bf16.bf16.f32 {%0,%1,%2,%3}, {%4,%5,%6,%7}, "
+        "{%8,%9}, {%0,%1,%2,%3};\n"
+        : "+f"(c[0]), "+f"(c[1]), "+f"(c[2]), "+f"(c[3])
+        : "r"(a[0]), "r"(a[1]), "r"(a[2]), "r"(a[3]), "r"(b0), "r"(b1));
+}
+
+__device__ __forceinline__ uint32_t pack_bf16(float lo, float hi) {
+    __nv_bfloat162 v = __floats2bfloat162_rn(lo, hi);
+    return *reinterpret_cast<uint32_t *>(&v);
+}
+
+// byte offset of 16-byte chunk `ch` of row `row` in a tile of DH bf16 per row
+template <int DH>
+__device__ __forceinline__ unsigned swz(int row, int ch) {
+    return row * (DH * 2) + ((ch ^ (row & 7)) << 4);
+}
+
+struct AttnArgs {
+    const bf16 *q;
+    const bf16 *const *kc;
+    const bf16 *const *vc;
+    const int32_t *prefix_len;
+    const uint64_t *anc_mask;
+    int B, R, H, P_max;
+    int chunk, nps;
+    float scale_log2;
+    float *part_o;
+    float2 *part_ml;
+    int *status;
+};
+
+template <int DH, int MAXW>
+__global__ void __launch_bounds__(MAXW * 32, 1) tree_attn_split_kernel(AttnArgs a) {
+    extern __shared__ __align__(128) unsigned char asmem[];
+    constexpr int CPR = DH / 8;  // 16-byte chunks per row
+    const int NW = blockDim.x >> 5;
+    const int QROWS = NW * 16;
+    unsigned char *q_s = asmem;
+    unsigned char *k_s = q_s + QROWS * DH * 2;
+    unsigned char *v_s = k_s + 2 * kTile * DH * 2;
+    uint64_t *mask_s = reinterpret_cast<uint64_t *>(v_s + 2 * kTile * DH * 2);  // [QROWS][4]
+    const int sp = blockIdx.x, h = blockIdx.y, b = blockIdx.z;
+    const int NS = a.nps + 1;
+    const int R = a.R, H = a.H;
+    const int tid = threadIdx.x, lane = tid & 31, warp = tid >> 5;
+    const int g = lane >> 2, t4 = lane & 3;
+
+    int P = a.prefix_len[b];
+    if (P < 0 || P > a.P_max) {
+        set_status(a.status, MEDUSA_DEV_BAD_PREFIX);
+        P = 0;
+    }
+    const bool tree_split = (sp == a.nps);
+    const int kbeg = tree_split ? P : sp * a.chunk;
+    const int kend = tree_split ? P + R : min((sp + 1) * a.chunk, P);
+    const size_t pbase = ((size_t)(b * H + h) * NS + sp) * R;
+
+    if (kend <= kbeg) {
+        for (int r = tid; r < R; r += blockDim.x)
+            a.part_ml[pbase + r] = make_float2(-INFINITY, 0.f);
+        return;
+    }
+
+    const bf16 *kc = a.kc[b];
+    const bf16 *vc = a.vc[b];
+
+    // stage Q (rows >= R zero-filled)
+    for (int i = tid; i < QROWS * CPR; i += blockDim.x) {
+        const int row = i / CPR, ch = i - row * CPR;
+        const bool ok = row < R;
+        const bf16 *src = a.q + (((size_t)b * R + (ok ? row : 0)) * H + h) * DH + ch * 8;
+        cp_async16(smem_u32(q_s + swz<DH>(row, ch)), src, ok ? 16 : 0);
+    }
+    auto load_tile = [&](int tile, int stage) {
+        const int base = kbeg + tile * kTile;
+        unsigned char *ks = k_s + stage * kTile * DH * 2;
+        unsigned char *vs = v_s + stage * kTile * DH * 2;
+        for (int i = tid; i < kTile * CPR; i += blockDim.x) {
+            const int row = i / CPR, ch = i - row * CPR;
+            const int key = base + row;
+            const bool ok = key < kend;
+            const size_t off = ((size_t)(ok ? key : kbeg) * H + h) * DH + ch * 8;
+            cp_async16(smem_u32(ks + swz<DH>(row, ch)), kc + off, ok ? 16 : 0);
+            cp_async16(smem_u32(vs + swz<DH>(row, ch)), vc + off, ok ? 16 : 0);
+        }
+    };
+    const int ntiles = (kend - kbeg + kTile - 1) / kTile;
+    load_tile(0, 0);
+    cp_async_commit();
+
+    // tree-split ancestor masks of every query row (rows >= R see nothing)
+    const int row0 = warp * 16 + g, row1 = row0 + 8;
+    if (tree_split) {
+        const int W = (R + 63) / 64;
+        for (int i = tid; i < QROWS * 4; i += blockDim.x) {
+            const int row = i >> 2, w = i & 3;
+            mask_s[i] = (row < R && w < W) ? a.anc_mask[((size_t)b * R + row) * W + w] : 0ull;
+        }
+    }
+
+    float o[DH / 8][4];
+#pragma unroll
+    for (int i = 0; i < DH / 8; ++i) o[i][0] = o[i][1] = o[i][2] = o[i][3] = 0.f;
+    float mrow[2] = {-INFINITY, -INFINITY}, lrow[2] = {0.f, 0.f};
+
+    for (int tile = 0; tile < ntiles; ++tile) {
+        if (tile + 1 < ntiles) {
+            load_tile(tile + 1, (tile + 1) & 1);
+            cp_async_commit();
+            cp_async_wait<1>();
+        } else {
+            cp_async_wait<0>();
+        }
+        __syncthreads();
+        const unsigned char *ks_ = k_s + (tile & 1) * kTile * DH * 2;
+        const unsigned char *vs_ = v_s + (tile & 1) * kTile * DH * 2;
+        const int tbase = kbeg + tile * kTile;
+#pragma unroll
+        for (int sub = 0; sub < kTile / kSub; ++sub) {
+            float s[kSub / 8][4];
+#pragma unroll
+            for (int nt = 0; nt < kSub / 8; ++nt) s[nt][0] = s[nt][1] = s[nt][2] = s[nt][3] = 0.f;
+#pragma unroll
+            for (int ks = 0; ks < DH / 16; ks += 2) {
+                const int i = lane >> 3, r8 = lane & 7;
+                uint32_t qa[2][4];
+#pragma unroll
+                for (int j = 0; j < 2; ++j) {
+                    const int row = warp * 16 + (i & 1) * 8 + r8;
+                    const int ch = (ks + j) * 2 + (i >> 1);
+                    ldsm_x4(smem_u32(q_s + swz<DH>(row, ch)), qa[j][0], qa[j][1], qa[j][2],
+                            qa[j][3]);
+                }
+#pragma unroll
+                for (int nt = 0; nt < kSub / 8; ++nt) {
+                    const int key = sub * kSub + nt * 8 + r8;
+                    const int ch = (ks + (i >> 1)) * 2 + (i & 1);
+                    uint32_t b0, b1, b2, b3;
+                    ldsm_x4(smem_u32(ks_ + swz<DH>(key, ch)), b0, b1, b2, b3);
+                    mma_bf16(s[nt], qa[0], b0, b1);
+                    mma_bf16(s[nt], qa[1], b2, b3);
+                }
+            }
+            // scale, mask, running max
+            float mx[2] = {-INFINITY, -INFINITY};
+#pragma unroll
+            for (int nt = 0; nt < kSub / 8; ++nt) {
+#pragma unroll
+                for (int e = 0; e < 4; ++e) {
+                    const int key = tbase + sub * kSub + nt * 8 + 2 * t4 + (e & 1);
+                    bool ok = key < kend;
+                    if (tree_split && ok) {
+                        const int tslot = key - P;
+                        const int row = (e < 2) ? row0 : row1;
+                        ok = (mask_s[row * 4 + (tslot >> 6)] >> (tslot & 63)) & 1u;
+                    }
+                    const float v = ok ? s[nt][e] * a.scale_log2 : -INFINITY;
+                    s[nt][e] = v;
+                    mx[e >> 1] = fmaxf(mx[e >> 1], v);
+                }
+            }
+            float corr[2], muse[2];
+#pragma unroll
+            for (int r = 0; r < 2; ++r) {
+                mx[r] = fmaxf(mx[r], __shfl_xor_sync(0xffffffffu, mx[r], 1));
+                mx[r] = fmaxf(mx[r], __shfl_xor_sync(0xffffffffu, mx[r], 2));
+                const float mn = fmaxf(mrow[r], mx[r]);
+                muse[r] = (mn == -INFINITY) ? 0.f : mn;
+                corr[r] = exp2f(mrow[r] - muse[r]);
+                mrow[r] = mn;
+                lrow[r] *= corr[r];
+            }
+#pragma unroll
+            for (int nt = 0; nt < kSub / 8; ++nt) {
+#pragma unroll
+                for (int e = 0; e < 4; ++e) {
+                    const float p = exp2f(s[nt][e] - muse[e >> 1]);
+                    s[nt][e] = p;
+                    lrow[e >> 1] += p;
+                }
+            }
+#pragma unroll
+            for (int dn = 0; dn < DH / 8; ++dn) {
+                o[dn][0] *= corr[0];
+                o[dn][1] *= corr[0];
+                o[dn][2] *= corr[1];
+                o[dn][3] *= corr[1];
+            }
+            // O += P V
+#pragma unroll
+            for (int kk = 0; kk < kSub / 16; ++kk) {
+                uint32_t pa[4];
+                pa[0] = pack_bf16(s[2 * kk][0], s[2 * kk][1]);
+                pa[1] = pack_bf16(s[2 * kk][2], s[2 * kk][3]);
+                pa[2] = pack_bf16(s[2 * kk + 1][0], s[2 * kk + 1][1]);
+                pa[3] = pack_bf16(s[2 * kk + 1][2], s[2 * kk + 1][3]);
+#pragma unroll
+                for (int dn = 0; dn < DH / 16; ++dn) {
+                    const int i = lane >> 3, r8 = lane & 7;
+                    const int key = sub * kSub + kk * 16 + (i & 1) * 8 + r8;
+                    const int ch = dn * 2 + (i >> 1);
+                    uint32_t b0, b1, b2, b3;
+                    ldsm_x4_t(smem_u32(vs_ + swz<DH>(key, ch)), b0, b1, b2, b3);
+                    mma_bf16(o[2 * dn], pa, b0, b1);
+                    mma_bf16(o[2 * dn + 1], pa, b2, b3);
+                }
+            }
+        }
+        __syncthreads();
+    }
+
+    // finish the row sums across the quad and write the partials
+#pragma unroll
+    for (int r = 0; r < 2; ++r) {
+        lrow[r] += __shfl_xor_sync(0xffffffffu, lrow[r], 1);
+        lrow[r] += __shfl_xor_sync(0xffffffffu, lrow[r], 2);
+    }
+#pragma unroll
+    for (int r = 0; r < 2; ++r) {
+        const int row = r == 0 ? row0 : row1;
+        if (row < R) {
+            float *dst = a.part_o + (pbase + row) * DH;
+#pragma unroll
+            for (int dn = 0; dn < DH / 8; ++dn)
+                *reinterpret_cast<float2 *>(dst + dn * 8 + 2 * t4) =
+                    make_float2(o[dn][2 * r], o[dn][2 * r + 1]);
+            if (t4 == 0) a.part_ml[pbase + row] = make_float2(mrow[r], lrow[r]);
+        }
+    }
+}
+
+template <int DH>
+__global__ void __launch_bounds__(256)
+tree_attn_combine_kernel(const float *__restrict__ part_o, const float2 *__restrict__ part_ml,
+                         int B, int R, int H, int NS, bf16 *__restrict__ out) {
+    constexpr int PER = DH / 32;
+    const int lane = threadIdx.x & 31;
+    const long long item = (long long)blockIdx.x * (blockDim.x >> 5) + (threadIdx.x >> 5);
+    if (item >= (long long)B * R * H) return;
+    const int h = (int)(item % H);
+    const int row = (int)((item / H) % R);
+    const int b = (int)(item / ((long long)H * R));
+    const size_t base = (size_t)(b * H + h) * NS;
+    float M = -INFINITY;
+    for (int s = 0; s < NS; ++s) {
+        const float2 ml = part_ml[(base + s) * R + row];
+        if (ml.y > 0.f) M = fmaxf(M, ml.x);
+    }
+    float L = 0.f;
+    float acc[PER];
+#pragma unroll
+    for (int j = 0; j < PER; ++j) acc[j] = 0.f;
+    for (int s = 0; s < NS; ++s) {
+        const float2 ml = part_ml[(base + s) * R + row];
+        if (!(ml.y > 0.f)) continue;
+        const float w = exp2f(ml.x - M);
+        L += w * ml.y;
+        const float *src = part_o + ((base + s) * R + row) * DH;
+#pragma unroll
+        for (int j = 0; j < PER; ++j) acc[j] = fmaf(w, src[lane + 32 * j], acc[j]);
+    }
+    const float inv = L > 0.f ? 1.f / L : 0.f;
+    bf16 *dst = out + (((size_t)b * R + row) * H + h) * DH;
+#pragma unroll
+    for (int j = 0; j < PER; ++j) dst[lane + 32 * j] = __float2bfloat16_rn(acc[j] * inv);
+}
+
+// ------------------------------------------------------------ f32 path ---
+
+__global__ void __launch_bounds__(128)
+tree_attn_f32_kernel(const float *__restrict__ q, const float *const *kcs, const float *const *vcs,
+                     const int32_t *__restrict__ prefix_len, const uint64_t *__restrict__ anc_mask,
+                     int R, int H, int dh, int P_max, float scale, float *__restrict__ out,
+                     int *status) {
+    extern __shared__ float fsm[];
+    __shared__ float red[128 / kWarp];
+    const int i = blockIdx.x, h = blockIdx.y, b = blockIdx.z;
+    int P = prefix_len[b];
+    if (P < 0 || P > P_max) {
+        set_status(status, MEDUSA_DEV_BAD_PREFIX);
+        P = 0;
+    }
+    const int n = P + R;
+    float *qs = fsm;
+    float *sc = fsm + dh;
+    const float *kc = kcs[b];
+    const float *vc = vcs[b];
+    const int W = (R + 63) / 64;
+    const uint64_t *mrow = anc_mask + ((size_t)b * R + i) * W;
+    for (int c = threadIdx.x; c < dh; c += blockDim.x) qs[c] = q[(((size_t)b * R + i) * H + h) * dh + c];
+    __syncthreads();
+    float lmax = -INFINITY;
+    for (int j = threadIdx.x; j < n; j += blockDim.x) {
+        bool vis = j < P;
+        if (!vis) {
+            const int t = j - P;
+            vis = (mrow[t >> 6] >> (t & 63)) & 1u;
+        }
+        float s = -INFINITY;
+        if (vis) {
+            const float *kr = kc + ((size_t)j * H + h) * dh;
+            float acc = 0.f;
+            for (int c = 0; c < dh; ++c) acc = fmaf(qs[c], kr[c], acc);
+            s = acc * scale;
+        }
+        sc[j] = s;
+        lmax = fmaxf(lmax, s);
+    }
+    for (int o = 16; o > 0; o >>= 1) lmax = fmaxf(lmax, __shfl_xor_sync(0xffffffffu, lmax, o));
+    if ((threadIdx.x & 31) == 0) red[threadIdx.x >> 5] = lmax;
+    __syncthreads();
+    float m = red[0];
+    for (int w = 1; w < (int)(blockDim.x >> 5); ++w) m = fmaxf(m, red[w]);
+    __syncthreads();
+    float lsum = 0.f;
+    for (int j = threadIdx.x; j < n; j += blockDim.x) {
+        const float p = (sc[j] == -INFINITY) ? 0.f : expf(sc[j] - m);
+        sc[j] = p;
+        lsum += p;
+    }
+    lsum = warp_sum(lsum);
+    if ((threadIdx.x & 31) == 0) red[threadIdx.x >> 5] = lsum;
+    __syncthreads();
+    float L = 0.f;
+    for (int w = 0; w < (int)(blockDim.x >> 5); ++w) L += red[w];
+    for (int c = threadIdx.x; c < dh; c += blockDim.x) {
+        float acc = 0.f;
+        for (int j = 0; j < n; ++j)
+            if (sc[j] != 0.f) acc = fmaf(sc[j], vc[((size_t)j * H + h) * dh + c], acc);
+        out[(((size_t)b * R + i) * H + h) * dh + c] = acc / L;
+    }
+}
+
+// ---------------------------------------------------------------- host ---
+
+void split_plan(int B, int H, int P_max, int *nps, int *chunk) {
+    const int per_head = std::max(1, (kTargetCtas + B * H - 1) / (B * H));
+    int n = std::max(1, per_head - 1);
+    const int max_n = std::max(1, (P_max + kTile - 1) / kTile);
+    n = std::min(n, max_n);
+    int c = (P_max + n - 1) / n;
+    c = std::max(kTile, (c + kTile - 1) / kTile * kTile);
+    *chunk = c;
+    *nps = std::max(1, (P_max + c - 1) / c);
+}
+
+size_t align256(size_t x) { return (x + 255) & ~size_t(255); }
+
+}  // namespace
+
+size_t attention_workspace_bytes(medusa_dtype dtype, int B, int R, int H, int dh, int P_max) {
+    if (dtype == MEDUSA_F32) return MEDUSA_WS_HEADER;
+    int nps, chunk;
+    split_plan(B, H, P_max, &nps, &chunk);
+    const size_t rows = (size_t)B * H * (nps + 1) * R;
+    return MEDUSA_WS_HEADER + align256(rows * dh * sizeof(float)) + align256(rows * sizeof(float2));
+}
+
+cudaError_t launch_tree_attention(medusa_dtype dtype, const void *q, const void *const *k_cache,
+                                  const void *const *v_cache, const int32_t *prefix_len,
+                                  int P_max, const uint64_t *anc_mask, int B, int R, int H,
+                                  int dh, float scale, void *out, void *ws, cudaStream_t stream) {
+    int *status = static_cast<int *>(ws);
+    cudaError_t e;
+    if (dtype == MEDUSA_F32) {
+        const size_t smem = (size_t)(dh + P_max + R) * sizeof(float);
+        if ((e = cudaFuncSetAttribute(tree_attn_f32_kernel,
+                                      cudaFuncAttributeMaxDynamicSharedMemorySize, (int)smem)))
+            return e;
+        tree_attn_f32_kernel<<<dim3(R, H, B), 128, smem, stream>>>(
+            static_cast<const float *>(q), reinterpret_cast<const float *const *>(k_cache),
+            reinterpret_cast<const float *const *>(v_cache), prefix_len, anc_mask, R, H, dh, P_max,
+            scale, static_cast<float *>(out), status);
+        note_launch();
+        return cudaGetLastError();
+    }
+    int nps, chunk;
+    split_plan(B, H, P_max, &nps, &chunk);
+    const int NS = nps + 1;
+    const size_t rows = (size_t)B * H * NS * R;
+    char *w = static_cast<char *>(ws) + MEDUSA_WS_HEADER;
+    float *part_o = reinterpret_cast<float *>(w);
+    float2 *part_ml = reinterpret_cast<float2 *>(w + align256(rows * dh * sizeof(float)));
+    AttnArgs a;
+    a.q = static_cast<const bf16 *>(q);
+    a.kc = reinterpret_cast<const bf16 *const *>(k_cache);
+    a.vc = reinterpret_cast<const bf16 *const *>(v_cache);
+    a.prefix_len = prefix_len;
+    a.anc_mask = anc_mask;
+    a.B = B;
+    a.R = R;
+    a.H = H;
+    a.P_max = P_max;
+    a.chunk = chunk;
+    a.nps = nps;
+    a.scale_log2 = scale * kLog2e;
+    a.part_o = part_o;
+    a.part_ml = part_ml;
+    a.status = status;
+    const int NW = (R + 15) / 16;
+    const int threads = NW * 32;
+    const size_t smem = (size_t)(NW * 16 + 4 * kTile) * dh * 2 + (size_t)NW * 16 * 4 * sizeof(uint64_t);
+    dim3 grid(NS, H, B);
+    auto kern = tree_attn_split_kernel<128, 8>;
+    if (dh == 128)
+        kern = NW <= 8 ? tree_attn_split_kernel<128, 8> : tree_attn_split_kernel<128, 16>;
+    else
+        kern = NW <= 8 ? tree_attn_split_kernel<64, 8> : tree_attn_split_kernel<64, 16>;
+    if ((e = cudaFuncSetAttribute(kern, cudaFuncAttributeMaxDynamicSharedMemorySize, (int)smem)))
+        return e;
+    kern<<<grid, threads, smem, stream>>>(a);
+    note_launch();
+    if ((e = cudaGetLastError())) return e;
+    const long long items = (long long)B * R * H;
+    const int cblocks = (int)((items + 7) / 8);
+    if (dh == 128)
+        tree_attn_combine_kernel<128><<<cblocks, 256, 0, stream>>>(part_o, part_ml, B, R, H, NS,
+                                                                   static_cast<bf16 *>(out));
+    else
+        tree_attn_combine_kernel<64><<<cblocks, 256, 0, stream>>>(part_o, part_ml, B, R, H, NS,
+                                                                  static_cast<bf16 *>(out));
+    note_launch();
+    return cudaGetLastError();
+}
+
+}  // namespace medusa

@@ -1,0 +1,84 @@
+// common.cuh -- device helpers shared by the Medusa step kernels (sm_103a).
+#pragma once
+
+#include <cuda_bf16.h>
+#include <cuda_runtime.h>
+#include <stdint.h>
+
+#include "medusa.h"
+
+namespace medusa {
+
+constexpr int kWarp = 32;
+
+using bf16 = __nv_bfloat16;
+
+// ---------------------------------------------------------------- loads ---
+
+// 16-byte streaming load: read-only path, no L1 allocation (weights and
+// logits are touched once per step).
+__device__ __forceinline__ uint4 ld_stream16(const void *p) {
+    uint4 r;
+    asm("ld.global.nc.L1::no_allocate.v4.u32 {%0,%1,%2,%3}, [%4];"
+        : "=r"(r.x), "=r"(r.y), "=r"(r.z), "=r"(r.w)
+        : "l"(p));
+    return r;
+}
+
+// bf16 pair packed in a 32-bit word -> two floats (exact widening).
+__device__ __forceinline__ float bf_lo(uint32_t w) { return __uint_as_float(w << 16); }
+__device__ __forceinline__ float bf_hi(uint32_t w) { return __uint_as_float(w & 0xffff0000u); }
+
+__device__ __forceinline__ float bf16_to_f(uint16_t b) {
+    return __uint_as_float(static_cast<uint32_t>(b) << 16);
+}
+
+// Element type traits: how many elements one 16-byte vector holds and how to
+// widen them to fp32.
+template <typename T> struct Vec16;
+
+template <> struct Vec16<float> {
+    static constexpr int N = 4;
+    __device__ __forceinline__ static void widen(const uint4 &v, float (&f)[4]) {
+        f[0] = __uint_as_float(v.x);
+        f[1] = __uint_as_float(v.y);
+        f[2] = __uint_as_float(v.z);
+        f[3] = __uint_as_float(v.w);
+    }
+    __device__ __forceinline__ static float load1(const float *p) { return __ldg(p); }
+};
+
+template <> struct Vec16<bf16> {
+    static constexpr int N = 8;
+    __device__ __forceinline__ static void widen(const uint4 &v, float (&f)[8]) {
+        f[0] = bf_lo(v.x); f[1] = bf_hi(v.x);
+        f[2] = bf_lo(v.y); f[3] = bf_hi(v.y);
+        f[4] = bf_lo(v.z); f[5] = bf_hi(v.z);
+        f[6] = bf_lo(v.w); f[7] = bf_hi(v.w);
+    }
+    __device__ __forceinline__ static float load1(const bf16 *p) {
+        return bf16_to_f(__ldg(reinterpret_cast<const unsigned short *>(p)));
+    }
+};
+
+// ----------------------------------------------------------- reductions ---
+
+__device__ __forceinline__ float warp_sum(float v) {
+#pragma unroll
+    for (int o = 16; o > 0; o >>= 1) v += __shfl_xor_sync(0xffffffffu, v, o);
+    return v;
+}
+
+// (value, id) ordering used for every top-k and argmax: larger value first,
+// equal values -> smaller id first.
+__device__ __forceinline__ bool better(float va, int ia, float vb, int ib) {
+    return va > vb || (va == vb && ia < ib);
+}
+
+// ------------------------------------------------------- device status ---
+
+__device__ __forceinline__ void set_status(int *status, int code) {
+    if (status) atomicCAS(status, 0, code);
+}
+
+}  // namespace medusa

@@ -1,0 +1,43 @@
+// launch.h -- internal interface between the C ABI layer (api.cu) and the
+// kernel files.  Each launch_* enqueues its kernels on `stream` and returns
+// the first CUDA error; arguments were validated by the caller.
+#pragma once
+
+#include <cuda_runtime.h>
+#include <stddef.h>
+#include <stdint.h>
+
+#include "medusa.h"
+
+namespace medusa {
+
+int device_sm_count();   // SMs of the current device (cached per device)
+void note_launch();      // count one kernel launch
+
+size_t heads_workspace_bytes(int B, int K, int d, int V, int S);
+cudaError_t launch_heads(medusa_dtype dtype, const void *h, const void *W1, const void *b1,
+                         const void *W2, int B, int d, int V, int K, int S, int32_t *ids,
+                         float *logp, void *ws, cudaStream_t stream);
+
+size_t tree_workspace_bytes(int B, int K, int S, int n);
+cudaError_t launch_build_tree(const int32_t *root, const int32_t *ids, const float *logp, int B,
+                              int K, const int32_t *s_host, int S, int n,
+                              const int32_t *prefix_len, int32_t *tokens, int32_t *parent,
+                              int32_t *depth, int32_t *pos_id, uint64_t *anc_mask, int32_t *paths,
+                              int32_t *n_leaf, void *ws, cudaStream_t stream);
+
+size_t attention_workspace_bytes(medusa_dtype dtype, int B, int R, int H, int dh, int P_max);
+cudaError_t launch_tree_attention(medusa_dtype dtype, const void *q, const void *const *k_cache,
+                                  const void *const *v_cache, const int32_t *prefix_len,
+                                  int P_max, const uint64_t *anc_mask, int B, int R, int H,
+                                  int dh, float scale, void *out, void *ws, cudaStream_t stream);
+
+size_t posterior_workspace_bytes(int B, int R);
+cudaError_t launch_posterior(medusa_dtype dtype, const void *logits, const int32_t *tokens,
+                             const int32_t *parent, const int32_t *depth, int B, int R, int V,
+                             int K, medusa_accept_mode mode, float eps, float delta,
+                             float temperature, int32_t *accept_len, int32_t *path,
+                             int32_t *path_tokens, int32_t *next_token, int32_t *accept,
+                             void *ws, cudaStream_t stream);
+
+}  // namespace medusa

@@ -1,0 +1,310 @@
+// posterior.cu -- acceptance and the longest accepted path.
+//
+// A tree node's token is judged by the verification logits of its parent's
+// row (that row is the target model's distribution for the next position).
+//   greedy  ("Medusa Part I" Part 2): accept iff the token is the row argmax.
+//   typical ("Medusa 深读" §5): accept iff p(x) > min(eps, delta*exp(-H(p))),
+//           p = softmax(logits / T), H in nats.
+// The root is accepted unconditionally ("Medusa 深读" §5); a node counts only
+// if its whole branch is accepted ("Medusa Part I" Part 2: a rejection ends
+// the prefix); the deepest counted node wins and its row's argmax is the next
+// token.
+//
+// Two kernels:
+//   posterior_rows_kernel    one CTA per logits row: a single streaming pass
+//                            with 16-byte loads computes the argmax and, for
+//                            typical acceptance, the shifted sums
+//                            S = sum 2^(y-m), A = sum 2^(y-m) (y-m) in the
+//                            log2 domain (y = logit * log2(e) / T), from which
+//                            H = ln S - ln2 * A / S.  Row stats go to scratch.
+//   posterior_select_kernel  one CTA per sequence, one thread per node:
+//                            per-node decision, prefix-AND down the tree
+//                            level by level, longest path, next token.
+#include <climits>
+
+#include "common.cuh"
+#include "launch.h"
+
+namespace medusa {
+
+namespace {
+
+constexpr int kRowThreads = 256;
+constexpr int kSelectThreads = 256;
+constexpr float kLog2e = 1.4426950408889634f;
+constexpr float kLn2 = 0.6931471805599453f;
+
+struct RowStats {
+    int argmax;
+    float m2;     // max of y = logit * log2(e) / T
+    float log2s;  // log2 sum 2^(y - m2)
+    float H;      // entropy in nats
+};
+
+// (m, S, A) triple of shifted sums in the log2 domain
+struct Moments {
+    float m, S, A;
+    __device__ __forceinline__ void merge(float m2, float S2, float A2) {
+        if (S2 == 0.f) return;
+        if (S == 0.f) {
+            m = m2; S = S2; A = A2;
+            return;
+        }
+        const float mn = fmaxf(m, m2);
+        const float f1 = exp2f(m - mn), f2 = exp2f(m2 - mn);
+        A = f1 * (A + S * (m - mn)) + f2 * (A2 + S2 * (m2 - mn));
+        S = S * f1 + S2 * f2;
+        m = mn;
+    }
+};
+
+template <typename T, bool TYPICAL>
+__global__ void __launch_bounds__(kRowThreads)
+posterior_rows_kernel(const T *__restrict__ logits, int R, int V, float y_scale,
+                      RowStats *__restrict__ stats) {
+    constexpr int VN = Vec16<T>::N;
+    constexpr int U = 4;
+    __shared__ float s_val[kRowThreads / kWarp];
+    __shared__ int s_id[kRowThreads / kWarp];
+    __shared__ float s_m[kRowThreads / kWarp], s_S[kRowThreads / kWarp], s_A[kRowThreads / kWarp];
+    const int row = blockIdx.x, b = blockIdx.y;
+    const uint4 *x = reinterpret_cast<const uint4 *>(logits + ((size_t)b * R + row) * V);
+    const int nvec = V / VN;
+    float bv = -INFINITY;
+    int bi = INT_MAX;
+    Moments mo{-INFINITY, 0.f, 0.f};
+    for (int base = threadIdx.x; base < nvec; base += kRowThreads * U) {
+        uint4 v[U];
+#pragma unroll
+        for (int u = 0; u < U; ++u) {
+            const int idx = base + u * kRowThreads;
+            if (idx < nvec) v[u] = ld_stream16(x + idx);
+        }
+        float f[U][VN];
+        float bm = -INFINITY;
+#pragma unroll
+        for (int u = 0; u < U; ++u) {
+            const int idx = base + u * kRowThreads;
+            if (idx < nvec) {
+                Vec16<T>::widen(v[u], f[u]);
+#pragma unroll
+                for (int e = 0; e < VN; ++e) {
+                    const float val = f[u][e];
+                    const int id = idx * VN + e;
+                    if (better(val, id, bv, bi)) {
+                        bv = val;
+                        bi = id;
+                    }
+                    bm = fmaxf(bm, val);
+                }
+            }
+        }
+        if (TYPICAL) {
+            // fold this batch into the shifted sums with the batch max
+            const float m_new = fmaxf(mo.m, bm * y_scale);
+            if (mo.S != 0.f && m_new > mo.m) {
+                const float f1 = exp2f(mo.m - m_new);
+                mo.A = f1 * (mo.A + mo.S * (mo.m - m_new));
+                mo.S *= f1;
+            }
+            mo.m = m_new;
+#pragma unroll
+            for (int u = 0; u < U; ++u) {
+                const int idx = base + u * kRowThreads;
+                if (idx < nvec) {
+#pragma unroll
+                    for (int e = 0; e < VN; ++e) {
+                        const float t = fmaf(f[u][e], y_scale, -mo.m);
+                        const float p = exp2f(t);
+                        mo.S += p;
+                        mo.A = fmaf(p, t, mo.A);
+                    }
+                }
+            }
+        }
+    }
+    // warp reductions
+    const int lane = threadIdx.x & 31, warp = threadIdx.x >> 5;
+#pragma unroll
+    for (int o = 16; o > 0; o >>= 1) {
+        const float ov = __shfl_xor_sync(0xffffffffu, bv, o);
+        const int oi = __shfl_xor_sync(0xffffffffu, bi, o);
+        if (better(ov, oi, bv, bi)) {
+            bv = ov;
+            bi = oi;
+        }
+        if (TYPICAL) {
+            const float om = __shfl_xor_sync(0xffffffffu, mo.m, o);
+            const float oS = __shfl_xor_sync(0xffffffffu, mo.S, o);
+            const float oA = __shfl_xor_sync(0xffffffffu, mo.A, o);
+            mo.merge(om, oS, oA);
+        }
+    }
+    if (lane == 0) {
+        s_val[warp] = bv;
+        s_id[warp] = bi;
+        s_m[warp] = mo.m;
+        s_S[warp] = mo.S;
+        s_A[warp] = mo.A;
+    }
+    __syncthreads();
+    if (threadIdx.x == 0) {
+        for (int w = 1; w < kRowThreads / kWarp; ++w) {
+            if (better(s_val[w], s_id[w], bv, bi)) {
+                bv = s_val[w];
+                bi = s_id[w];
+            }
+            if (TYPICAL) mo.merge(s_m[w], s_S[w], s_A[w]);
+        }
+        RowStats st;
+        st.argmax = bi;
+        st.m2 = mo.m;
+        st.log2s = TYPICAL ? log2f(mo.S) : 0.f;
+        st.H = TYPICAL ? logf(mo.S) - kLn2 * mo.A / mo.S : 0.f;
+        stats[(size_t)b * R + row] = st;
+    }
+}
+
+template <typename T>
+__global__ void __launch_bounds__(kSelectThreads)
+posterior_select_kernel(const T *__restrict__ logits, const int32_t *__restrict__ tokens,
+                        const int32_t *__restrict__ parent, const int32_t *__restrict__ depth,
+                        const RowStats *__restrict__ stats, int R, int V, int K, int typical,
+                        float y_scale, float log2_eps, float log2_delta,
+                        int32_t *__restrict__ accept_len, int32_t *__restrict__ path,
+                        int32_t *__restrict__ path_tokens, int32_t *__restrict__ next_token,
+                        int32_t *__restrict__ accept_out, int *status) {
+    __shared__ int s_acc[MEDUSA_MAX_TREE_ROWS];
+    __shared__ int s_chain[MEDUSA_MAX_TREE_ROWS];
+    __shared__ int s_par[MEDUSA_MAX_TREE_ROWS];
+    __shared__ int s_dep[MEDUSA_MAX_TREE_ROWS];
+    __shared__ int s_tok[MEDUSA_MAX_TREE_ROWS];
+    __shared__ int s_L, s_best;
+    const int b = blockIdx.x;
+    const int i = threadIdx.x;
+    if (i == 0) {
+        s_L = 0;
+        s_best = INT_MAX;
+    }
+    if (i < R) {
+        const size_t o = (size_t)b * R + i;
+        s_par[i] = parent[o];
+        s_dep[i] = depth[o];
+        s_tok[i] = tokens[o];
+        s_chain[i] = (i == 0);
+        if (i == 0 && (s_dep[0] != 0 || s_par[0] != -1)) {
+            set_status(status, MEDUSA_DEV_BAD_DEPTH);
+            s_dep[0] = 0;
+            s_par[0] = -1;
+        }
+    }
+    __syncthreads();
+    if (i < R) {
+        int acc = 1;
+        if (i > 0) {
+            const int p = s_par[i], tok = s_tok[i], D = s_dep[i];
+            bool ok = true;
+            if (p < 0 || p >= i) {
+                set_status(status, MEDUSA_DEV_BAD_PARENT);
+                ok = false;
+            } else if (D < 1 || D > K || D != s_dep[p] + 1) {
+                set_status(status, MEDUSA_DEV_BAD_DEPTH);
+                ok = false;
+            } else if (tok < 0 || tok >= V) {
+                set_status(status, MEDUSA_DEV_BAD_TOKEN);
+                ok = false;
+            }
+            if (!ok) {
+                acc = 0;
+            } else {
+                const RowStats st = stats[(size_t)b * R + p];
+                if (!typical) {
+                    acc = (tok == st.argmax);
+                } else {
+                    const float y = Vec16<T>::load1(logits + ((size_t)b * R + p) * V + tok) * y_scale;
+                    const float lp2 = y - st.m2 - st.log2s;
+                    const float thr2 = fminf(log2_eps, log2_delta - st.H * kLog2e);
+                    acc = lp2 > thr2;
+                }
+            }
+        }
+        s_acc[i] = acc;
+        if (accept_out) accept_out[(size_t)b * R + i] = acc;
+    }
+    __syncthreads();
+    for (int D = 1; D <= K; ++D) {
+        if (i < R && i > 0 && s_dep[i] == D && s_acc[i]) {
+            const int p = s_par[i];
+            if (p >= 0 && p < i) s_chain[i] = s_chain[p];
+        }
+        __syncthreads();
+    }
+    if (i < R && s_chain[i]) atomicMax(&s_L, s_dep[i]);
+    __syncthreads();
+    if (i < R && s_chain[i] && s_dep[i] == s_L) atomicMin(&s_best, i);
+    if (i <= K) {
+        path[(size_t)b * (K + 1) + i] = -1;
+        path_tokens[(size_t)b * (K + 1) + i] = -1;
+    }
+    __syncthreads();
+    if (i == 0) {
+        const int best = s_best < R ? s_best : 0;
+        const int L = s_best < R ? s_L : 0;
+        for (int x = best, q = L; x >= 0 && q >= 0; x = s_par[x], --q) {
+            path[(size_t)b * (K + 1) + q] = x;
+            path_tokens[(size_t)b * (K + 1) + q] = s_tok[x];
+            if (x == 0) break;
+        }
+        accept_len[b] = L;
+        next_token[b] = stats[(size_t)b * R + best].argmax;
+    }
+}
+
+template <typename T>
+cudaError_t run_posterior(const void *logits, const int32_t *tokens, const int32_t *parent,
+                          const int32_t *depth, int B, int R, int V, int K, bool typical,
+                          float eps, float delta, float temperature, int32_t *accept_len,
+                          int32_t *path, int32_t *path_tokens, int32_t *next_token,
+                          int32_t *accept, void *ws, cudaStream_t stream) {
+    int *status = static_cast<int *>(ws);
+    RowStats *stats = reinterpret_cast<RowStats *>(static_cast<char *>(ws) + MEDUSA_WS_HEADER);
+    const T *lg = static_cast<const T *>(logits);
+    const float y_scale = kLog2e / temperature;
+    dim3 grid(R, B);
+    if (typical)
+        posterior_rows_kernel<T, true><<<grid, kRowThreads, 0, stream>>>(lg, R, V, y_scale, stats);
+    else
+        posterior_rows_kernel<T, false><<<grid, kRowThreads, 0, stream>>>(lg, R, V, y_scale, stats);
+    note_launch();
+    cudaError_t e = cudaGetLastError();
+    if (e) return e;
+    posterior_select_kernel<T><<<B, kSelectThreads, 0, stream>>>(
+        lg, tokens, parent, depth, stats, R, V, K, typical ? 1 : 0, y_scale, log2f(eps),
+        log2f(delta), accept_len, path, path_tokens, next_token, accept, status);
+    note_launch();
+    return cudaGetLastError();
+}
+
+}  // namespace
+
+size_t posterior_workspace_bytes(int B, int R) {
+    return MEDUSA_WS_HEADER + (size_t)B * R * sizeof(RowStats);
+}
+
+cudaError_t launch_posterior(medusa_dtype dtype, const void *logits, const int32_t *tokens,
+                             const int32_t *parent, const int32_t *depth, int B, int R, int V,
+                             int K, medusa_accept_mode mode, float eps, float delta,
+                             float temperature, int32_t *accept_len, int32_t *path,
+                             int32_t *path_tokens, int32_t *next_token, int32_t *accept,
+                             void *ws, cudaStream_t stream) {
+    const bool typical = mode == MEDUSA_TYPICAL;
+    if (dtype == MEDUSA_BF16)
+        return run_posterior<bf16>(logits, tokens, parent, depth, B, R, V, K, typical, eps, delta,
+                                   temperature, accept_len, path, path_tokens, next_token, accept,
+                                   ws, stream);
+    return run_posterior<float>(logits, tokens, parent, depth, B, R, V, K, typical, eps, delta,
+                                temperature, accept_len, path, path_tokens, next_token, accept, ws,
+                                stream);
+}
+
+}  // namespace medusa

@@ -15,9 +15,11 @@ five heads, tree sizes, attention heads, context lengths), random values.
 """
 from __future__ import annotations
 
+import concurrent.futures as cf
 import dataclasses
-from dataclasses import dataclass, field
-from typing import Callable, Optional, Sequence
+import os
+from dataclasses import dataclass
+from typing import Callable
 
 import numpy as np
 
@@ -143,11 +145,38 @@ def rng_for(cfg: StepConfig, part: str, rep: int = 0) -> np.random.Generator:
     return np.random.Generator(np.random.PCG64(np.random.SeedSequence([cfg.seed, _STREAMS[part], rep])))
 
 
-def _normal(rng, shape, std, dtype) -> np.ndarray:
-    x = rng.standard_normal(size=shape, dtype=np.float32)
-    if std != 1.0:
-        x *= np.float32(std)
-    return f32_to_bf16_bits(x) if dtype == "bf16" else x
+_CHUNK = 1 << 22
+_POOL = None
+
+
+def _pool():
+    global _POOL
+    if _POOL is None:
+        _POOL = cf.ThreadPoolExecutor(max_workers=max(1, min(16, os.cpu_count() or 1)))
+    return _POOL
+
+
+def _normal_keyed(key: tuple, shape, std: float, dtype: str) -> np.ndarray:
+    """N(0, std) array drawn in fixed chunks of 2^22 elements; chunk c comes from
+    its own PCG64 stream seeded by (key, c), so the values do not depend on how
+    many threads fill the chunks."""
+    size = int(np.prod(shape))
+    out = np.empty(size, np.uint16 if dtype == "bf16" else np.float32)
+
+    def fill(c):
+        lo, hi = c * _CHUNK, min(size, (c + 1) * _CHUNK)
+        g = np.random.Generator(np.random.PCG64(np.random.SeedSequence([*key, c])))
+        x = g.standard_normal(size=hi - lo, dtype=np.float32)
+        if std != 1.0:
+            x *= np.float32(std)
+        out[lo:hi] = f32_to_bf16_bits(x) if dtype == "bf16" else x
+
+    list(_pool().map(fill, range((size + _CHUNK - 1) // _CHUNK)))
+    return out.reshape(shape)
+
+
+def _normal(cfg: StepConfig, part: str, rep: int, shape, std, dtype, *sub) -> np.ndarray:
+    return _normal_keyed((cfg.seed, _STREAMS[part], rep, *sub), shape, std, dtype)
 
 
 def _zeros(shape, dtype) -> np.ndarray:
@@ -166,22 +195,16 @@ def heads_inputs(cfg: StepConfig, rep: int = 0) -> HeadsInputs:
     """h ~ N(0, h_std); W1 ~ N(0, w1_std); b1 = 0; W2 ~ N(0, w2_std).  The
     LM-head variant sets W1 = 0, b1 = 0 and every head's W2 to one shared
     LM-head matrix W_lm ~ N(0, w2_std)."""
-    h = _normal(rng_for(cfg, "h", rep), (cfg.B, cfg.d), cfg.h_std, cfg.dtype)
+    h = _normal(cfg, "h", rep, (cfg.B, cfg.d), cfg.h_std, cfg.dtype)
     b1 = _zeros((cfg.K, cfg.d), cfg.dtype)
     if cfg.lm_head_variant:
         W1 = _zeros((cfg.K, cfg.d, cfg.d), cfg.dtype)
-        w_lm = _normal(rng_for(cfg, "w2", rep), (cfg.V, cfg.d), cfg.w2_std, cfg.dtype)
+        w_lm = _normal(cfg, "w2", rep, (cfg.V, cfg.d), cfg.w2_std, cfg.dtype, 1)
         W2 = np.empty((cfg.K, cfg.V, cfg.d), w_lm.dtype)
         W2[:] = w_lm[None]
     else:
-        r1 = rng_for(cfg, "w1", rep)
-        W1 = np.empty((cfg.K, cfg.d, cfg.d), np.uint16 if cfg.dtype == "bf16" else np.float32)
-        for k in range(cfg.K):
-            W1[k] = _normal(r1, (cfg.d, cfg.d), cfg.w1_std, cfg.dtype)
-        r2 = rng_for(cfg, "w2", rep)
-        W2 = np.empty((cfg.K, cfg.V, cfg.d), W1.dtype)
-        for k in range(cfg.K):
-            W2[k] = _normal(r2, (cfg.V, cfg.d), cfg.w2_std, cfg.dtype)
+        W1 = _normal(cfg, "w1", rep, (cfg.K, cfg.d, cfg.d), cfg.w1_std, cfg.dtype)
+        W2 = _normal(cfg, "w2", rep, (cfg.K, cfg.V, cfg.d), cfg.w2_std, cfg.dtype)
     return HeadsInputs(h=h, W1=W1, b1=b1, W2=W2)
 
 
@@ -201,24 +224,19 @@ class AttentionInputs:
 def attention_inputs(cfg: StepConfig, rep: int = 0, extra_slots: int = 0) -> AttentionInputs:
     """q and every K/V slot ~ N(0,1).  Sequence b's cache holds P_b prefix slots
     followed by R tree slots (plus ``extra_slots`` spare rows)."""
-    rq = rng_for(cfg, "q", rep)
-    q = _normal(rq, (cfg.B, cfg.R, cfg.H, cfg.dh), 1.0, cfg.dtype)
-    rk = rng_for(cfg, "kv", rep)
+    q = _normal(cfg, "q", rep, (cfg.B, cfg.R, cfg.H, cfg.dh), 1.0, cfg.dtype)
     ks, vs = [], []
     for b in range(cfg.B):
         rows = cfg.prefix[b] + cfg.R + extra_slots
-        ks.append(_normal(rk, (rows, cfg.H, cfg.dh), 1.0, cfg.dtype))
-        vs.append(_normal(rk, (rows, cfg.H, cfg.dh), 1.0, cfg.dtype))
+        ks.append(_normal(cfg, "kv", rep, (rows, cfg.H, cfg.dh), 1.0, cfg.dtype, b, 0))
+        vs.append(_normal(cfg, "kv", rep, (rows, cfg.H, cfg.dh), 1.0, cfg.dtype, b, 1))
     return AttentionInputs(q=q, k_cache=ks, v_cache=vs,
                            prefix_len=np.asarray(cfg.prefix, np.int32))
 
 
 def base_logits(cfg: StepConfig, rep: int = 0) -> np.ndarray:
     """Verification logits [B,R,V] ~ N(0, logit_std) as float32 (not yet cast)."""
-    r = rng_for(cfg, "logits", rep)
-    x = r.standard_normal(size=(cfg.B, cfg.R, cfg.V), dtype=np.float32)
-    x *= np.float32(cfg.logit_std)
-    return x
+    return _normal(cfg, "logits", rep, (cfg.B, cfg.R, cfg.V), cfg.logit_std, "f32")
 
 
 def plant_bernoulli(logits: np.ndarray, tokens: np.ndarray, parent: np.ndarray,

@@ -1,0 +1,147 @@
+"""C-ABI checks that need no GPU: the library loads, exports every symbol the
+header declares, and rejects bad arguments before launching anything."""
+import ctypes
+import os
+import re
+
+import pytest
+
+import medusa_speculative_decoding_02_gb300 as m
+from medusa_speculative_decoding_02_gb300 import build as mbuild
+
+ROOT = os.path.dirname(os.path.dirname(os.path.abspath(__file__)))
+P = ctypes.c_void_p
+A = P(4096)          # fake, 16-byte aligned device address: never dereferenced
+MISALIGNED = P(4100)
+WS = P(1 << 20)      # fake 256-byte aligned workspace
+
+
+@pytest.fixture(scope="module")
+def L():
+    mbuild.build()
+    return m.lib()
+
+
+def declared_symbols():
+    names = set()
+    for fn in os.listdir(os.path.join(ROOT, "include")):
+        if fn.endswith(".h"):
+            txt = open(os.path.join(ROOT, "include", fn)).read()
+            names |= set(re.findall(r"MEDUSA_API[^;(]*?\b(medusa_\w+)\s*\(", txt, flags=re.S))
+    return names
+
+
+def test_exports_every_declared_symbol(L):
+    names = declared_symbols()
+    assert len(names) >= 13
+    for n in names:
+        assert hasattr(L, n), n
+    assert set(m.EXPORTS) <= names
+
+
+def test_status_strings(L):
+    for code, name in m.STATUS.items():
+        assert L.medusa_status_string(code).decode() == name
+
+
+def _heads(L, **kw):
+    a = dict(dtype=m.BF16, h=A, W1=A, b1=None, W2=A, B=1, d=4096, V=32000, K=5, s=4, ids=A,
+             logp=A, ws=WS, ws_bytes=1 << 30)
+    a.update(kw)
+    return L.medusa_heads(a["dtype"], a["h"], a["W1"], a["b1"], a["W2"], a["B"], a["d"], a["V"],
+                          a["K"], a["s"], a["ids"], a["logp"], a["ws"], a["ws_bytes"], None)
+
+
+@pytest.mark.parametrize("kw,code", [
+    (dict(h=None), 1), (dict(W2=None), 1), (dict(dtype=7), 1), (dict(B=0), 2), (dict(B=9), 2),
+    (dict(K=0), 1), (dict(K=9), 1), (dict(d=12), 1), (dict(s=0), 1), (dict(s=17), 1),
+    (dict(V=3, s=4), 1), (dict(B=8, d=8192), 2), (dict(W1=MISALIGNED), 1), (dict(ws=None), 3),
+    (dict(ws=P((1 << 20) + 16)), 3), (dict(ws_bytes=100), 3)])
+def test_heads_rejects(L, kw, code):
+    before = L.medusa_launch_count()
+    assert _heads(L, **kw) == code
+    assert L.medusa_launch_count() == before
+    assert L.medusa_last_error().decode()
+
+
+def _tree(L, s=(4, 3, 2, 2, 1), n=64, **kw):
+    a = dict(root=A, ids=A, logp=A, B=1, K=len(s), S=max(s), ws=WS, ws_bytes=1 << 20)
+    a.update(kw)
+    sh = (ctypes.c_int32 * len(s))(*s)
+    return L.medusa_build_tree(a["root"], a["ids"], a["logp"], a["B"], a["K"], sh, a["S"], n, None,
+                               A, A, A, A, A, A, A, a["ws"], a["ws_bytes"], None)
+
+
+@pytest.mark.parametrize("args,code", [
+    (dict(n=137), 1), (dict(n=0), 1), (dict(n=256, s=(16, 16)), 1), (dict(s=(4, 3, 2, 2, 1), S=3), 1),
+    (dict(K=9, s=(1,) * 9), 1), (dict(root=None), 1), (dict(ws=None), 3), (dict(B=0), 1)])
+def test_tree_rejects(L, args, code):
+    before = L.medusa_launch_count()
+    assert _tree(L, **args) == code
+    assert L.medusa_launch_count() == before
+
+
+def test_tree_full_cartesian_budget_accepted_by_validation(L):
+    # n equal to the full node count passes validation; with a NULL output the
+    # call must still be rejected before any launch.
+    sh = (ctypes.c_int32 * 5)(4, 3, 2, 2, 1)
+    rc = L.medusa_build_tree(A, A, A, 1, 5, sh, 4, 136, None, None, A, A, A, A, A, A, WS, 1 << 20,
+                             None)
+    assert rc == 1
+
+
+def _attn(L, **kw):
+    a = dict(dtype=m.BF16, q=A, k=A, v=A, pl=A, P_max=1024, mask=A, B=1, R=65, H=32, dh=128,
+             scale=0.088, out=A, ws=WS, ws_bytes=1 << 30)
+    a.update(kw)
+    return L.medusa_tree_attention(a["dtype"], a["q"], a["k"], a["v"], a["pl"], a["P_max"],
+                                   a["mask"], a["B"], a["R"], a["H"], a["dh"],
+                                   ctypes.c_float(a["scale"]), a["out"], a["ws"], a["ws_bytes"],
+                                   None)
+
+
+@pytest.mark.parametrize("kw,code", [
+    (dict(dh=96), 2), (dict(R=0), 1), (dict(R=257), 1), (dict(P_max=-1), 1), (dict(q=None), 1),
+    (dict(scale=0.0), 1), (dict(out=MISALIGNED), 1), (dict(dtype=m.F32, P_max=16384), 2),
+    (dict(ws_bytes=1000), 3)])
+def test_attention_rejects(L, kw, code):
+    before = L.medusa_launch_count()
+    assert _attn(L, **kw) == code
+    assert L.medusa_launch_count() == before
+
+
+def _post(L, **kw):
+    a = dict(dtype=m.BF16, logits=A, B=1, R=65, V=32000, K=5, mode=m.TYPICAL, eps=0.09, delta=0.3,
+             T=1.0, ws=WS, ws_bytes=1 << 20)
+    a.update(kw)
+    f = ctypes.c_float
+    return L.medusa_evaluate_posterior(a["dtype"], a["logits"], A, A, A, a["B"], a["R"], a["V"],
+                                       a["K"], a["mode"], f(a["eps"]), f(a["delta"]), f(a["T"]), A, A,
+                                       A, A, None, a["ws"], a["ws_bytes"], None)
+
+
+@pytest.mark.parametrize("kw,code", [
+    (dict(V=32001), 1), (dict(dtype=m.F32, V=1002), 1), (dict(R=257), 1), (dict(K=9), 1),
+    (dict(mode=2), 1), (dict(T=0.0), 1), (dict(eps=-1.0), 1), (dict(delta=0.0), 1),
+    (dict(logits=MISALIGNED), 1), (dict(ws_bytes=64), 3)])
+def test_posterior_rejects(L, kw, code):
+    before = L.medusa_launch_count()
+    assert _post(L, **kw) == code
+    assert L.medusa_launch_count() == before
+
+
+def test_workspace_sizes(L):
+    hs = m.heads_workspace_size(1, 5, 4096, 32000, 4)
+    assert hs >= 256 + 5 * 4096 * 4
+    assert m.heads_workspace_size(8, 5, 4096, 32000, 4) > hs
+    assert m.build_tree_workspace_size(1, 5, 4, 64) >= 256
+    a1 = m.tree_attention_workspace_size(m.BF16, 1, 65, 32, 128, 1024)
+    assert a1 > 65 * 32 * 128 * 4
+    assert m.tree_attention_workspace_size(m.F32, 1, 15, 1, 64, 32) >= 256
+    assert m.posterior_workspace_size(8, 65) >= 256 + 8 * 65 * 16
+    assert L.medusa_heads_workspace_size(0, 5, 4096, 32000, 4) == 0
+
+
+def test_device_status_helpers_reject_null(L):
+    assert L.medusa_read_device_status(None, None, None) == 1
+    assert L.medusa_clear_device_status(None, None) == 1
