@@ -1,0 +1,457 @@
+"""Benchmark one Medusa decoding step on synthetic Vicuna-7B-shaped inputs.
+
+    python bench.py [--gpus N] [--steps K] [--warmup W] [--impl ours|reference]
+
+A step is one pass of the whole hot path on one batch of input:
+    medusa_heads -> medusa_build_tree -> medusa_tree_attention -> medusa_evaluate_posterior
+at the 7B shape, batch 1 (d=4096, V=32000, K=5 heads, s=(4,3,2,2,1) cut to 64
+nodes, 32 x 128 attention heads, prefix 1024, typical acceptance eps=0.09,
+delta=0.3).  Inputs are seeded random values of those shapes.
+
+The metric is the step's achieved HBM bandwidth: algorithmic bytes of the step
+(every weight, cache and logits byte the method must read once, plus its
+outputs) divided by the device time of the step; the step time in microseconds
+is reported beside it.  One JSON line goes to stdout.
+
+Multi-GPU: the step does not shard (one sequence, one GPU); with N > 1 every
+rank runs an independent replica and rank 0 reports the aggregate.
+
+--impl reference times the float64 CPU oracle (the only other implementation
+of this method here) on a bounded sample of the same workload.
+"""
+from __future__ import annotations
+
+import argparse
+import json
+import math
+import os
+import subprocess
+import sys
+import time
+
+import numpy as np
+
+ROOT = os.path.dirname(os.path.abspath(__file__))
+if ROOT not in sys.path:
+    sys.path.insert(0, ROOT)
+
+import synth  # noqa: E402
+
+METRIC = "Medusa step µs and achieved HBM GB/s (heads+tree attn+posterior), 7B shape, bs1"
+UNIT = "GB/s"
+
+
+# ------------------------------------------------------------ accounting ---
+
+def step_bytes(cfg: synth.StepConfig, heads_frac: float = 1.0, attn_heads=None) -> dict:
+    """Algorithmic bytes per step, by stage (every byte the method must move
+    once).  heads_frac / attn_heads describe a sample of the workload."""
+    e = 2 if cfg.dtype == "bf16" else 4
+    B, K, d, V, S = cfg.B, cfg.K, cfg.d, cfg.V, cfg.top_s
+    R, n = cfg.R, cfg.n
+    W = (R + 63) // 64
+    H = cfg.H if attn_heads is None else attn_heads
+    heads = (K * (d * d + d + V * d) * e) * heads_frac + B * d * e + B * K * S * 8
+    tree = B * K * S * 8 + B * 4 + B * 4 + B * R * (4 * 4 + 8 * W) + B * n * (K + 1) * 4 + B * 4
+    prefix_kv = sum(2 * p * H * cfg.dh * e for p in cfg.prefix)
+    attn = prefix_kv + B * R * H * cfg.dh * e * 4 + B * R * W * 8 + B * 4
+    post = B * R * V * e + B * R * 12 + B * (2 + 2 * (K + 1)) * 4
+    return dict(heads=heads, tree=tree, attention=attn, posterior=post,
+                total=heads + tree + attn + post)
+
+
+def measured_peaks() -> tuple[dict, str]:
+    p = os.path.join(ROOT, "MEASURED_PEAKS.json")
+    if os.path.exists(p):
+        try:
+            return json.load(open(p)), "measured"
+        except Exception:
+            pass
+    return {"hbm_gbs": 6800.0, "bf16_tflops": 1900.0, "bf16_tflops_sustained": 1700.0}, "fallback"
+
+
+# ---------------------------------------------------------------- clocks ---
+
+class ClockSampler:
+    """nvidia-smi sampling of SM clocks and throttle reasons while running."""
+    Q = ("index,clocks.sm,clocks.max.sm,power.draw,clocks_event_reasons.active,"
+         "clocks_event_reasons.hw_slowdown,clocks_event_reasons.hw_thermal_slowdown,"
+         "clocks_event_reasons.sw_thermal_slowdown,clocks_event_reasons.sw_power_cap")
+
+    def __init__(self, index: int):
+        self.index = index
+        self.proc = None
+        self.path = None
+
+    def __enter__(self):
+        try:
+            os.makedirs(os.path.join(ROOT, "gpurun_out"), exist_ok=True)
+            self.path = os.path.join(ROOT, "gpurun_out", f"clocks_{os.getpid()}.csv")
+            self.f = open(self.path, "w")
+            self.proc = subprocess.Popen(
+                ["nvidia-smi", f"--id={self.index}", f"--query-gpu={self.Q}", "--format=csv,noheader,nounits",
+                 "-lms", "200"], stdout=self.f, stderr=subprocess.DEVNULL)
+            time.sleep(0.3)
+        except Exception:
+            self.proc = None
+        return self
+
+    def __exit__(self, *exc):
+        if self.proc is not None:
+            self.proc.terminate()
+            try:
+                self.proc.wait(timeout=5)
+            except Exception:
+                self.proc.kill()
+            self.f.close()
+
+    def summary(self):
+        if self.proc is None or not self.path or not os.path.exists(self.path):
+            return None
+        sm, mx, reasons = [], [], set()
+        names = ["hw_slowdown", "hw_thermal_slowdown", "sw_thermal_slowdown", "sw_power_cap"]
+        for line in open(self.path):
+            parts = [x.strip() for x in line.split(",")]
+            if len(parts) < 9:
+                continue
+            try:
+                sm.append(float(parts[1]))
+                mx.append(float(parts[2]))
+            except ValueError:
+                continue
+            for nm, v in zip(names, parts[5:9]):
+                if v.lower().startswith("active"):
+                    reasons.add(nm)
+        if not sm:
+            return None
+        return {"sm_mhz": float(np.median(sm)), "sm_max_mhz": float(max(mx)),
+                "reasons": sorted(reasons), "samples": len(sm)}
+
+
+# ------------------------------------------------------------ CPU oracle ---
+
+def oracle_step(cfg, inp, heads_sample=None, attn_heads=None):
+    """One oracle pass over (a sample of) the step; returns seconds."""
+    import oracle
+    hi = inp["heads"]
+    t0 = time.perf_counter()
+    if heads_sample is None:
+        ids, logp, _, _ = oracle.heads(hi.h, hi.W1, hi.b1, hi.W2, cfg.top_s)
+    else:
+        k = heads_sample
+        ids1, logp1, _, _ = oracle.heads(hi.h, hi.W1[k:k + 1], hi.b1[k:k + 1], hi.W2[k:k + 1],
+                                         cfg.top_s)
+        ids = np.repeat(ids1, cfg.K, axis=1)
+        logp = np.repeat(logp1, cfg.K, axis=1)
+    t = oracle.build_tree(inp["root"], ids, logp, cfg.s, cfg.n, prefix_len=np.asarray(cfg.prefix))
+    ai = inp["attn"]
+    if attn_heads is None:
+        oracle.tree_attention(ai.q, ai.k_cache, ai.v_cache, ai.prefix_len, t["anc_mask"],
+                              1.0 / math.sqrt(cfg.dh))
+    else:
+        sl = lambda x: np.ascontiguousarray(x[..., :attn_heads, :])
+        oracle.tree_attention(sl(ai.q), [sl(k) for k in ai.k_cache], [sl(v) for v in ai.v_cache],
+                              ai.prefix_len, t["anc_mask"], 1.0 / math.sqrt(cfg.dh))
+    oracle.posterior(inp["logits"], t["tokens"], t["parent"], t["depth"], cfg.K, oracle.TYPICAL,
+                     cfg.eps, cfg.delta, cfg.temperature)
+    return time.perf_counter() - t0
+
+
+def make_inputs(cfg):
+    hi = synth.heads_inputs(cfg)
+    root = synth.root_tokens(cfg)
+    ai = synth.attention_inputs(cfg)
+    logits = synth.base_logits(cfg)
+    return dict(heads=hi, root=root, attn=ai, logits_f32=logits)
+
+
+def plant_on(inp, cfg, tree_np):
+    lg = inp["logits_f32"].copy()
+    synth.plant_chain(lg, tree_np["tokens"], tree_np["parent"], tree_np["depth"], 3,
+                      synth.rng_for(cfg, "plant"))
+    inp["logits"] = synth.cast(lg, cfg.dtype)
+
+
+# ------------------------------------------------------------ distributed ---
+
+def dist_env():
+    world = int(os.environ.get("WORLD_SIZE", "1"))
+    rank = int(os.environ.get("RANK", "0"))
+    local = int(os.environ.get("LOCAL_RANK", "0"))
+    return world, rank, local
+
+
+# -------------------------------------------------------------- reference ---
+
+def run_reference(args, cfg):
+    world, rank, _ = dist_env()
+    if rank != 0:
+        return 0
+    import oracle
+    oracle.build()
+    inp = make_inputs(cfg)
+    ids, logp, _, _ = oracle.heads(inp["heads"].h, inp["heads"].W1[:1], inp["heads"].b1[:1],
+                                   inp["heads"].W2[:1], cfg.top_s)
+    t = oracle.build_tree(inp["root"], np.repeat(ids, cfg.K, 1), np.repeat(logp, cfg.K, 1), cfg.s,
+                          cfg.n, prefix_len=np.asarray(cfg.prefix))
+    plant_on(inp, cfg, t)
+    attn_heads = 4
+    sample_bytes = step_bytes(cfg, heads_frac=1.0 / cfg.K, attn_heads=attn_heads)["total"]
+    for _ in range(args.warmup):
+        oracle_step(cfg, inp, heads_sample=0, attn_heads=attn_heads)
+    secs = [oracle_step(cfg, inp, heads_sample=0, attn_heads=attn_heads) for _ in range(args.steps)]
+    per = float(np.mean(secs))
+    value = sample_bytes / per / 1e9
+    sample = (f"per step: 1 of {cfg.K} heads (W1+W2 of head 0), the full tree, {attn_heads} of "
+              f"{cfg.H} attention heads, the full posterior; {sample_bytes / 1e6:.1f} MB of the "
+              f"step's {step_bytes(cfg)['total'] / 1e6:.1f} MB")
+    line = {
+        "impl": "reference", "metric": METRIC, "value": round(value, 4), "unit": UNIT,
+        "n_gpus": args.gpus, "steps": args.steps, "warmup": args.warmup,
+        "ms_per_step": round(per * 1e3, 3), "higher_is_better": True, "scaling": "weak",
+        "vs_baseline": None, "dtype": "f64", "data": "synthetic (seeded, Vicuna-7B shapes)",
+        "config": {"workload": cfg.name + "_bs1_step", "sample": sample},
+        "cpu_baseline": {"value": round(value, 4), "unit": UNIT, "cores": 1, "kind": "oracle",
+                         "sample": sample},
+        "e2e": {"value": round(value, 4), "unit": UNIT, "h2d_bytes_per_step": 0,
+                "d2h_bytes_per_step": 0},
+    }
+    print(json.dumps(line), flush=True)
+    return 0
+
+
+# -------------------------------------------------------------------- ours ---
+
+def run_ours(args, cfg):
+    import torch
+    world, rank, local = dist_env()
+    if world > 1:
+        import torch.distributed as dist
+        torch.cuda.set_device(local)
+        dist.init_process_group("nccl")
+    dev = torch.device("cuda", local if world > 1 else 0)
+    torch.cuda.set_device(dev)
+    import medusa_speculative_decoding_02_gb300 as m
+    m.lib()
+
+    def T(a):
+        a = np.ascontiguousarray(a)
+        if a.dtype == np.uint16:
+            return torch.from_numpy(a.view(np.int16)).view(torch.bfloat16).to(dev)
+        return torch.from_numpy(a).to(dev)
+
+    inp = make_inputs(cfg)
+    hi = inp["heads"]
+    h, W1, b1, W2 = T(hi.h), T(hi.W1), T(hi.b1), T(hi.W2)
+    root = T(inp["root"])
+    ai = inp["attn"]
+    q = T(ai.q)
+    kc = [T(x) for x in ai.k_cache]
+    vc = [T(x) for x in ai.v_cache]
+    kptr, vptr = m.cache_pointers(kc, dev), m.cache_pointers(vc, dev)
+    prefix = T(ai.prefix_len)
+    B, K, S, R, n = cfg.B, cfg.K, cfg.top_s, cfg.R, cfg.n
+    ws_bytes = max(m.heads_workspace_size(B, K, cfg.d, cfg.V, S),
+                   m.build_tree_workspace_size(B, K, S, n),
+                   m.tree_attention_workspace_size(m.BF16, B, R, cfg.H, cfg.dh, cfg.P_max),
+                   m.posterior_workspace_size(B, R))
+    ws = m.new_workspace(ws_bytes, dev)
+    ids = torch.empty((B, K, S), dtype=torch.int32, device=dev)
+    logp = torch.empty((B, K, S), dtype=torch.float32, device=dev)
+    tree = m.Tree.empty(B, n, K, dev)
+    out = torch.empty_like(q)
+    post = m.Posterior.empty(B, R, K, dev, with_accept=False)
+    stream = torch.cuda.current_stream(dev)
+
+    # the verification logits carry one planted chain on this step's tree
+    m.heads(h, W1, b1, W2, S, ws=ws, out=(ids, logp))
+    m.build_tree(root, ids, logp, cfg.s, n, prefix_len=prefix, ws=ws, out=tree)
+    tnp = {k: getattr(tree, k).cpu().numpy() for k in ("tokens", "parent", "depth")}
+    plant_on(inp, cfg, tnp)
+    logits = T(inp["logits"])
+    mode = m.TYPICAL if cfg.mode == "typical" else m.GREEDY
+
+    ev = [torch.cuda.Event(enable_timing=True) for _ in range(5)]
+
+    def step(record=None):
+        if record is not None:
+            record[0].record(stream)
+        m.heads(h, W1, b1, W2, S, ws=ws, out=(ids, logp))
+        if record is not None:
+            record[1].record(stream)
+        m.build_tree(root, ids, logp, cfg.s, n, prefix_len=prefix, ws=ws, out=tree)
+        if record is not None:
+            record[2].record(stream)
+        m.tree_attention(q, kptr, vptr, prefix, cfg.P_max, tree.anc_mask, out=out, ws=ws)
+        if record is not None:
+            record[3].record(stream)
+        m.evaluate_posterior(logits, tree.tokens, tree.parent, tree.depth, K, mode, cfg.eps,
+                             cfg.delta, cfg.temperature, ws=ws, out=post)
+        if record is not None:
+            record[4].record(stream)
+
+    def barrier():
+        if world > 1:
+            import torch.distributed as dist
+            dist.barrier()
+
+    for _ in range(args.warmup):
+        step()
+    torch.cuda.synchronize(dev)
+    if m.read_device_status(ws) != 0:
+        raise RuntimeError("device status set during warm-up")
+
+    per_call = {k: [] for k in ("heads", "tree", "attention", "posterior")}
+    recs = [[torch.cuda.Event(enable_timing=True) for _ in range(5)] for _ in range(args.steps)]
+    t_start = torch.cuda.Event(enable_timing=True)
+    t_end = torch.cuda.Event(enable_timing=True)
+    launches0 = m.launch_count()
+    with ClockSampler(dev.index) as clk:
+        barrier()
+        torch.cuda.synchronize(dev)
+        t_start.record(stream)
+        for i in range(args.steps):
+            step(recs[i])
+        t_end.record(stream)
+        torch.cuda.synchronize(dev)
+        barrier()
+    launches = m.launch_count() - launches0
+    total_ms = t_start.elapsed_time(t_end)
+    for r in recs:
+        per_call["heads"].append(r[0].elapsed_time(r[1]))
+        per_call["tree"].append(r[1].elapsed_time(r[2]))
+        per_call["attention"].append(r[2].elapsed_time(r[3]))
+        per_call["posterior"].append(r[3].elapsed_time(r[4]))
+    ms_step = total_ms / args.steps
+    if world > 1:
+        import torch.distributed as dist
+        tt = torch.tensor([ms_step], device=dev)
+        dist.all_reduce(tt, op=dist.ReduceOp.MAX)
+        ms_step = float(tt.item())
+    nb = step_bytes(cfg)
+    value = world * nb["total"] / (ms_step * 1e-3) / 1e9
+
+    # ---- end to end through the public API with pinned host buffers
+    host_in = {
+        "h": torch.from_numpy(np.ascontiguousarray(hi.h).view(np.int16)).view(torch.bfloat16).pin_memory(),
+        "root": torch.from_numpy(inp["root"]).pin_memory(),
+        "q": torch.from_numpy(np.ascontiguousarray(ai.q).view(np.int16)).view(torch.bfloat16).pin_memory(),
+        "k_tree": torch.from_numpy(ai.k_cache[0][cfg.prefix[0]:].view(np.int16)).view(torch.bfloat16).pin_memory(),
+        "v_tree": torch.from_numpy(ai.v_cache[0][cfg.prefix[0]:].view(np.int16)).view(torch.bfloat16).pin_memory(),
+        "logits": torch.from_numpy(inp["logits"].view(np.int16)).view(torch.bfloat16).pin_memory(),
+    }
+    host_out = {k: torch.empty(v.shape, dtype=v.dtype).pin_memory()
+                for k, v in (("accept_len", post.accept_len), ("path", post.path),
+                             ("path_tokens", post.path_tokens), ("next_token", post.next_token))}
+    h2d = sum(v.numel() * v.element_size() for v in host_in.values())
+    d2h = sum(v.numel() * v.element_size() for v in host_out.values())
+    P0 = cfg.prefix[0]
+
+    def e2e_step():
+        h.copy_(host_in["h"], non_blocking=True)
+        root.copy_(host_in["root"], non_blocking=True)
+        q.copy_(host_in["q"], non_blocking=True)
+        kc[0][P0:].copy_(host_in["k_tree"], non_blocking=True)
+        vc[0][P0:].copy_(host_in["v_tree"], non_blocking=True)
+        logits.copy_(host_in["logits"], non_blocking=True)
+        step()
+        for k, v in host_out.items():
+            v.copy_(getattr(post, k), non_blocking=True)
+        stream.synchronize()
+
+    e2e_steps = max(3, min(args.steps, 50))
+    for _ in range(2):
+        e2e_step()
+    barrier()
+    t0 = time.perf_counter()
+    for _ in range(e2e_steps):
+        e2e_step()
+    e2e_s = (time.perf_counter() - t0) / e2e_steps
+    if world > 1:
+        import torch.distributed as dist
+        tt = torch.tensor([e2e_s], device=dev)
+        dist.all_reduce(tt, op=dist.ReduceOp.MAX)
+        e2e_s = float(tt.item())
+    e2e_value = world * nb["total"] / e2e_s / 1e9
+
+    if world > 1:
+        import torch.distributed as dist
+        dist.barrier()
+        dist.destroy_process_group()
+    if rank != 0:
+        return 0
+
+    peaks, peak_src = measured_peaks()
+    heads_ms = float(np.mean(per_call["heads"]))
+    achieved = nb["heads"] / (heads_ms * 1e-3) / 1e9
+    traffic = None
+    tp = os.path.join(ROOT, "profiles", "heads_v7b_bs1_traffic.json")
+    if os.path.exists(tp):
+        try:
+            traffic = json.load(open(tp)).get("bytes_per_launch")
+        except Exception:
+            traffic = None
+    roofline = {"bound": "hbm", "achieved": round(achieved, 1), "peak": peaks["hbm_gbs"],
+                "unit": "GB/s", "frac": round(achieved / peaks["hbm_gbs"], 4), "traffic": traffic,
+                "kernel": "medusa_heads (heads_w1 + heads_w2 + heads_reduce)",
+                "peak_source": f"hbm_gbs of {peak_src}"}
+
+    # ---- CPU baseline: the oracle on the full step, ~10 s of host work
+    import oracle
+    oracle.build()
+    cpu_secs = []
+    tb = time.perf_counter()
+    while True:
+        cpu_secs.append(oracle_step(cfg, inp))
+        if time.perf_counter() - tb > 10.0 or len(cpu_secs) >= 5:
+            break
+    cpu_value = nb["total"] / float(np.mean(cpu_secs)) / 1e9
+
+    stages = {k: {"us": round(float(np.mean(v)) * 1e3, 2),
+                  "GB/s": round(nb[k] / (float(np.mean(v)) * 1e-3) / 1e9, 1),
+                  "frac_hbm": round(nb[k] / (float(np.mean(v)) * 1e-3) / 1e9 / peaks["hbm_gbs"], 4)}
+              for k, v in per_call.items()}
+    line = {
+        "metric": METRIC, "value": round(value, 2), "unit": UNIT, "n_gpus": world,
+        "steps": args.steps, "warmup": args.warmup, "ms_per_step": round(ms_step, 5),
+        "step_us": round(ms_step * 1e3, 2), "higher_is_better": True,
+        "scaling": "weak", "vs_baseline": None, "dtype": "bf16",
+        "data": "synthetic (seeded, Vicuna-7B shapes: random weights, KV and logits)",
+        "config": {"workload": "v7b_bs1_step", "d": cfg.d, "V": cfg.V, "K": cfg.K,
+                   "s": list(cfg.s), "tree_nodes": cfg.n, "attn_heads": cfg.H, "head_dim": cfg.dh,
+                   "prefix": cfg.P_max, "batch": cfg.B, "accept": cfg.mode,
+                   "bytes_per_step": int(nb["total"]), "parallelism": f"replicas{world}",
+                   "l2": "inputs larger than L2: 1.50 GB of weights, KV and logits per step"},
+        "stages": stages,
+        "roofline": roofline,
+        "cpu_baseline": {"value": round(cpu_value, 4), "unit": UNIT, "cores": 1, "kind": "oracle",
+                         "sample": f"{len(cpu_secs)} full oracle steps of the same workload "
+                                   f"(single-threaded float64 C), mean "
+                                   f"{float(np.mean(cpu_secs)):.2f} s per step"},
+        "e2e": {"value": round(e2e_value, 2), "unit": UNIT, "h2d_bytes_per_step": int(h2d),
+                "d2h_bytes_per_step": int(d2h), "us_per_step": round(e2e_s * 1e6, 2),
+                "steps": e2e_steps},
+        "gpu_launches": int(launches),
+        "clocks": clk.summary(),
+    }
+    print(json.dumps(line), flush=True)
+    return 0
+
+
+def main():
+    ap = argparse.ArgumentParser()
+    ap.add_argument("--gpus", type=int, default=1)
+    ap.add_argument("--steps", type=int, default=50)
+    ap.add_argument("--warmup", type=int, default=5)
+    ap.add_argument("--impl", default="ours", choices=["ours", "reference"])
+    args = ap.parse_args()
+    if args.warmup < 3 and args.impl == "ours":
+        args.warmup = 3
+    cfg = synth.v7b().replace(mode="typical")
+    if args.impl == "reference":
+        return run_reference(args, cfg)
+    return run_ours(args, cfg)
+
+
+if __name__ == "__main__":
+    sys.exit(main())

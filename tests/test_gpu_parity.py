@@ -122,8 +122,8 @@ def random_topk(rng, B, K, S, V=32000):
     return ids, logp
 
 
-def oracle_tree_for(rng, s, n, B, prefix):
-    ids, logp = random_topk(rng, B, len(s), max(s))
+def oracle_tree_for(rng, s, n, B, prefix, V=32000):
+    ids, logp = random_topk(rng, B, len(s), max(s), V)
     return oracle.build_tree(np.arange(B, dtype=np.int32) + 7, ids, logp.astype(np.float64), s, n,
                              prefix_len=np.asarray(prefix, np.int32))
 
@@ -343,7 +343,7 @@ def run_posterior(dev, logits_np, ot, K, mode, eps=0.09, delta=0.3, temp=1.0):
 @pytest.mark.parametrize("mode", [m.GREEDY, m.TYPICAL])
 def test_posterior_tiny(dev, mode):
     cfg = synth.tiny()
-    ot = oracle_tree_for(np.random.default_rng(1), cfg.s, cfg.n, 1, cfg.prefix)
+    ot = oracle_tree_for(np.random.default_rng(1), cfg.s, cfg.n, 1, cfg.prefix, cfg.V)
     logits = synth.base_logits(cfg)
     synth.plant_bernoulli(logits, ot["tokens"], ot["parent"], synth.rng_for(cfg, "plant"))
     gp = run_posterior(dev, logits, ot, cfg.K, mode, cfg.eps, cfg.delta)
@@ -457,7 +457,7 @@ def test_device_status_reports_bad_data(dev):
     """Data only the device can see is reported in the workspace status word
     (first error wins) and cleared on request; nothing faults."""
     cfg = synth.tiny()
-    ot = oracle_tree_for(np.random.default_rng(3), cfg.s, cfg.n, 1, cfg.prefix)
+    ot = oracle_tree_for(np.random.default_rng(3), cfg.s, cfg.n, 1, cfg.prefix, cfg.V)
     logits = synth.base_logits(cfg)
     ws = m.new_workspace(m.posterior_workspace_size(1, cfg.R), dev)
     bad = ot["tokens"].copy()
