@@ -143,6 +143,31 @@ MEDUSA_API medusa_status medusa_heads(medusa_dtype dtype, const void *h, const v
                            medusa_stream stream);
 
 /* ------------------------------------------------------------------------
+ * 1b. Medusa heads with library-held scratch (no workspace argument).
+ *
+ * The pages have no counterpart: this is a calling convention, not part of
+ * the method.  It is for callers that cannot allocate device memory at the
+ * time they run the heads -- a serving runtime that gives all free HBM to its
+ * KV-cache pool at start-up, or a decode loop that cannot afford the
+ * device-wide synchronisation of cudaMalloc/cudaFree.  Same arguments and
+ * results as medusa_heads, minus the workspace: the scratch is a 4 MiB
+ * device array inside the library, reserved on every GPU that loads the
+ * library until the process exits.  Shapes whose scratch
+ * (medusa_heads_workspace_size) exceeds 4 MiB return MEDUSA_ERR_UNSUPPORTED
+ * and launch nothing.  The call allocates nothing.  The first call on a
+ * device looks up the array's device address (cudaGetSymbolAddress) with that
+ * device current; make that first call before any stream capture.  All calls
+ * share the one array: calls that overlap on the GPU race and must be
+ * serialised by the caller.
+ * ---------------------------------------------------------------------- */
+MEDUSA_API medusa_status medusa_heads_noalloc(medusa_dtype dtype, const void *h,
+                                              const void *W1, const void *b1,
+                                              const void *W2, int B, int d, int V,
+                                              int K, int top_s, int32_t *topk_ids,
+                                              float *topk_logp,
+                                              medusa_stream stream);
+
+/* ------------------------------------------------------------------------
  * 2. Candidate tree under a node budget.
  *
  * [P2] §6.2 (greedy construction within a budget: repeatedly take the

@@ -162,6 +162,27 @@ def heads(h, W1, b1, W2, top_s: int, ws=None, out=None, stream=None):
     return ids, logp
 
 
+def heads_noalloc(h, W1, b1, W2, top_s: int, out=None, stream=None):
+    """medusa_heads with the library's own 4 MiB device scratch: for callers
+    that cannot allocate device memory when they run the heads.  Calls that
+    overlap on the GPU share the scratch and must be serialised."""
+    for t, n in ((h, "h"), (W1, "W1"), (W2, "W2")):
+        _need(t, n)
+    fn = lib().medusa_heads_noalloc
+    P, I = ctypes.c_void_p, ctypes.c_int
+    fn.argtypes = [I, P, P, P, P, I, I, I, I, I, P, P, P]
+    fn.restype = I
+    B, d = h.shape
+    K, V = W2.shape[0], W2.shape[1]
+    if out is None:
+        out = (torch.empty((B, K, top_s), dtype=torch.int32, device=h.device),
+               torch.empty((B, K, top_s), dtype=torch.float32, device=h.device))
+    ids, logp = out
+    _check(fn(_dtype(h), _ptr(h), _ptr(W1), _ptr(b1), _ptr(W2), B, d, V, K, top_s, _ptr(ids),
+              _ptr(logp), _stream(stream)))
+    return ids, logp
+
+
 # ------------------------------------------------------------------- tree ---
 
 @dataclass

@@ -60,6 +60,13 @@ int device_sm_count() {
 
 void note_launch() { g_launches.fetch_add(1, std::memory_order_relaxed); }
 
+void set_last_error(const char *fmt, ...) {
+    va_list ap;
+    va_start(ap, fmt);
+    vsnprintf(g_err, sizeof g_err, fmt, ap);
+    va_end(ap);
+}
+
 }  // namespace medusa
 
 using namespace medusa;

@@ -13,6 +13,7 @@ namespace medusa {
 
 int device_sm_count();   // SMs of the current device (cached per device)
 void note_launch();      // count one kernel launch
+void set_last_error(const char *fmt, ...);  // message for medusa_last_error()
 
 size_t heads_workspace_bytes(int B, int K, int d, int V, int S);
 cudaError_t launch_heads(medusa_dtype dtype, const void *h, const void *W1, const void *b1,
