@@ -98,6 +98,7 @@ struct AttnArgs {
 
 template <int DH, int MAXW>
 __global__ void __launch_bounds__(MAXW * 32, 1) tree_attn_split_kernel(AttnArgs a) {
+    pdl_enter();
     extern __shared__ __align__(128) unsigned char asmem[];
     constexpr int CPR = DH / 8;  // 16-byte chunks per row
     const int NW = blockDim.x >> 5;
@@ -296,10 +297,15 @@ __global__ void __launch_bounds__(MAXW * 32, 1) tree_attn_split_kernel(AttnArgs 
     }
 }
 
+// One warp per (sequence, row, head).  Lane s reads split s's (m, l), so the
+// weights come from one round of independent loads; the O partials of all
+// splits are then read with independent loads as well (no load waits on
+// another).
 template <int DH>
 __global__ void __launch_bounds__(256)
 tree_attn_combine_kernel(const float *__restrict__ part_o, const float2 *__restrict__ part_ml,
                          int B, int R, int H, int NS, bf16 *__restrict__ out) {
+    pdl_enter();
     constexpr int PER = DH / 32;
     const int lane = threadIdx.x & 31;
     const long long item = (long long)blockIdx.x * (blockDim.x >> 5) + (threadIdx.x >> 5);
@@ -309,27 +315,41 @@ tree_attn_combine_kernel(const float *__restrict__ part_o, const float2 *__restr
     const int b = (int)(item / ((long long)H * R));
     const size_t base = (size_t)(b * H + h) * NS;
     float M = -INFINITY;
-    for (int s = 0; s < NS; ++s) {
+    for (int s = lane; s < NS; s += 32) {
         const float2 ml = part_ml[(base + s) * R + row];
         if (ml.y > 0.f) M = fmaxf(M, ml.x);
     }
+#pragma unroll
+    for (int o = 16; o > 0; o >>= 1) M = fmaxf(M, __shfl_xor_sync(0xffffffffu, M, o));
     float L = 0.f;
     float acc[PER];
 #pragma unroll
     for (int j = 0; j < PER; ++j) acc[j] = 0.f;
-    for (int s = 0; s < NS; ++s) {
-        const float2 ml = part_ml[(base + s) * R + row];
-        if (!(ml.y > 0.f)) continue;
-        const float w = exp2f(ml.x - M);
-        L += w * ml.y;
-        const float *src = part_o + ((base + s) * R + row) * DH;
+    for (int s0 = 0; s0 < NS; s0 += 32) {
+        float w_l = 0.f;
+        if (s0 + lane < NS) {
+            const float2 ml = part_ml[(base + s0 + lane) * R + row];
+            if (ml.y > 0.f) {
+                w_l = exp2f(ml.x - M);
+                L = fmaf(w_l, ml.y, L);
+            }
+        }
+        const int cnt = min(32, NS - s0);
+#pragma unroll 4
+        for (int j = 0; j < cnt; ++j) {
+            const float w = __shfl_sync(0xffffffffu, w_l, j);
+            const float *src = part_o + ((base + s0 + j) * R + row) * DH;
+            if (w != 0.f) {
 #pragma unroll
-        for (int j = 0; j < PER; ++j) acc[j] = fmaf(w, src[lane + 32 * j], acc[j]);
+                for (int p = 0; p < PER; ++p) acc[p] = fmaf(w, src[lane + 32 * p], acc[p]);
+            }
+        }
     }
+    L = warp_sum(L);
     const float inv = L > 0.f ? 1.f / L : 0.f;
     bf16 *dst = out + (((size_t)b * R + row) * H + h) * DH;
 #pragma unroll
-    for (int j = 0; j < PER; ++j) dst[lane + 32 * j] = __float2bfloat16_rn(acc[j] * inv);
+    for (int p = 0; p < PER; ++p) dst[lane + 32 * p] = __float2bfloat16_rn(acc[p] * inv);
 }
 
 // ------------------------------------------------------------ f32 path ---
@@ -339,6 +359,7 @@ tree_attn_f32_kernel(const float *__restrict__ q, const float *const *kcs, const
                      const int32_t *__restrict__ prefix_len, const uint64_t *__restrict__ anc_mask,
                      int R, int H, int dh, int P_max, float scale, float *__restrict__ out,
                      int *status) {
+    pdl_enter();
     extern __shared__ float fsm[];
     __shared__ float red[128 / kWarp];
     const int i = blockIdx.x, h = blockIdx.y, b = blockIdx.z;
@@ -434,12 +455,13 @@ cudaError_t launch_tree_attention(medusa_dtype dtype, const void *q, const void 
         if ((e = cudaFuncSetAttribute(tree_attn_f32_kernel,
                                       cudaFuncAttributeMaxDynamicSharedMemorySize, (int)smem)))
             return e;
-        tree_attn_f32_kernel<<<dim3(R, H, B), 128, smem, stream>>>(
-            static_cast<const float *>(q), reinterpret_cast<const float *const *>(k_cache),
-            reinterpret_cast<const float *const *>(v_cache), prefix_len, anc_mask, R, H, dh, P_max,
-            scale, static_cast<float *>(out), status);
+        e = launch_pdl(tree_attn_f32_kernel, dim3(R, H, B), dim3(128), smem, stream,
+                       static_cast<const float *>(q),
+                       reinterpret_cast<const float *const *>(k_cache),
+                       reinterpret_cast<const float *const *>(v_cache), prefix_len, anc_mask, R, H,
+                       dh, P_max, scale, static_cast<float *>(out), status);
         note_launch();
-        return cudaGetLastError();
+        return e;
     }
     int nps, chunk;
     split_plan(B, H, P_max, &nps, &chunk);
@@ -475,19 +497,16 @@ cudaError_t launch_tree_attention(medusa_dtype dtype, const void *q, const void 
         kern = NW <= 8 ? tree_attn_split_kernel<64, 8> : tree_attn_split_kernel<64, 16>;
     if ((e = cudaFuncSetAttribute(kern, cudaFuncAttributeMaxDynamicSharedMemorySize, (int)smem)))
         return e;
-    kern<<<grid, threads, smem, stream>>>(a);
+    e = launch_pdl(kern, grid, dim3(threads), smem, stream, a);
     note_launch();
-    if ((e = cudaGetLastError())) return e;
+    if (e) return e;
     const long long items = (long long)B * R * H;
     const int cblocks = (int)((items + 7) / 8);
-    if (dh == 128)
-        tree_attn_combine_kernel<128><<<cblocks, 256, 0, stream>>>(part_o, part_ml, B, R, H, NS,
-                                                                   static_cast<bf16 *>(out));
-    else
-        tree_attn_combine_kernel<64><<<cblocks, 256, 0, stream>>>(part_o, part_ml, B, R, H, NS,
-                                                                  static_cast<bf16 *>(out));
+    e = launch_pdl(dh == 128 ? tree_attn_combine_kernel<128> : tree_attn_combine_kernel<64>,
+                   dim3(cblocks), dim3(256), 0, stream, static_cast<const float *>(part_o),
+                   static_cast<const float2 *>(part_ml), B, R, H, NS, static_cast<bf16 *>(out));
     note_launch();
-    return cudaGetLastError();
+    return e;
 }
 
 }  // namespace medusa

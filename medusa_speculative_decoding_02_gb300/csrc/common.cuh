@@ -25,6 +25,11 @@ __device__ __forceinline__ uint4 ld_stream16(const void *p) {
     return r;
 }
 
+// Bulk prefetch of `bytes` (multiple of 16, 16-byte aligned) into L2.
+__device__ __forceinline__ void prefetch_l2_bulk(const void *p, unsigned bytes) {
+    asm volatile("cp.async.bulk.prefetch.L2.global [%0], %1;\n" ::"l"(p), "r"(bytes) : "memory");
+}
+
 // bf16 pair packed in a 32-bit word -> two floats (exact widening).
 __device__ __forceinline__ float bf_lo(uint32_t w) { return __uint_as_float(w << 16); }
 __device__ __forceinline__ float bf_hi(uint32_t w) { return __uint_as_float(w & 0xffff0000u); }
@@ -73,6 +78,22 @@ __device__ __forceinline__ float warp_sum(float v) {
 // equal values -> smaller id first.
 __device__ __forceinline__ bool better(float va, int ia, float vb, int ib) {
     return va > vb || (va == vb && ia < ib);
+}
+
+// ---------------------------------------------- programmatic dependent launch
+//
+// Every kernel of the step is launched with programmatic stream serialization
+// (see launch_pdl).  At its start a kernel waits for the grid before it in the
+// stream to complete and flush (griddepcontrol.wait) and then lets the next
+// grid begin launching (griddepcontrol.launch_dependents), so the next
+// kernel's launch overlaps this one's execution instead of following its
+// completion.  The next grid cannot start before every CTA of this grid has
+// started and passed the trigger, and it waits for this grid's completion
+// before touching memory; both instructions are no-ops for a kernel launched
+// without the attribute.
+__device__ __forceinline__ void pdl_enter() {
+    asm volatile("griddepcontrol.wait;\n" ::: "memory");
+    asm volatile("griddepcontrol.launch_dependents;\n" ::: "memory");
 }
 
 // ------------------------------------------------------- device status ---

@@ -36,7 +36,7 @@ namespace {
 constexpr int kW1Threads = 256;
 constexpr int kW2Threads = 512;
 constexpr int kW2Warps = kW2Threads / kWarp;
-constexpr int kReduceThreads = 256;
+constexpr int kReduceThreads = 512;
 
 // Index (in floats) of element c of vector row b in the split-plane layout.
 template <int VN>
@@ -96,9 +96,10 @@ __device__ __forceinline__ void row_dot(const uint4 *__restrict__ w, const float
 // ------------------------------------------------------------- phase 1 ---
 
 template <typename T, int NB, int U>
-__global__ void __launch_bounds__(kW1Threads)
+__global__ void __launch_bounds__(kW1Threads, NB <= 2 ? 4 : 1)
 heads_w1_kernel(const T *__restrict__ h, const T *__restrict__ W1, const T *__restrict__ b1,
-                float *__restrict__ z, int B, int d, int K) {
+                float *__restrict__ z, int B, int d, int K, int rows_per_warp) {
+    pdl_enter();
     extern __shared__ float4 smem4[];
     float *hs = reinterpret_cast<float *>(smem4);
     constexpr int VN = Vec16<T>::N;
@@ -112,7 +113,12 @@ heads_w1_kernel(const T *__restrict__ h, const T *__restrict__ W1, const T *__re
     const int warp = threadIdx.x >> 5;
     const int nwarps = blockDim.x >> 5;
     const int rows = K * d;
-    for (int row = blockIdx.x * nwarps + warp; row < rows; row += gridDim.x * nwarps) {
+    // every warp owns rows_per_warp consecutive rows (the host sizes the grid
+    // so that the warps' shares are equal)
+    const int gw = blockIdx.x * nwarps + warp;
+    const int r_begin = gw * rows_per_warp;
+    const int r_end = min(rows, r_begin + rows_per_warp);
+    for (int row = r_begin; row < r_end; ++row) {
         float acc[NB];
         row_dot<T, NB, U>(reinterpret_cast<const uint4 *>(W1 + (size_t)row * d), smem4, nvec, lane,
                           acc);
@@ -201,19 +207,54 @@ __device__ __forceinline__ void flush_slot(TopSlot &slot, const WarpTop &st, int
     }
 }
 
-// merge a sorted list (best first) into the warp state; stops at the first
-// entry that cannot enter
-__device__ __forceinline__ void merge_list(WarpTop &st, const float *val, const int *id, int S,
-                                           int lane) {
-    for (int j = 0; j < S; ++j) {
-        const float cv = val[j];
-        const int ci = id[j];
-        if (ci == INT_MAX) break;
-        const float wv = __shfl_sync(0xffffffffu, st.val, S - 1);
-        const int wi = __shfl_sync(0xffffffffu, st.id, S - 1);
-        if (!better(cv, ci, wv, wi)) break;
-        st.insert(cv, ci, S, lane);
+// Number of entries of a best-first list that rank before (cv, ci); empty
+// entries (id INT_MAX) sit at the tail and rank after everything.
+__device__ __forceinline__ int count_better(const TopSlot &sl, float cv, int ci, int S) {
+    int lo = 0, hi = S;
+    while (lo < hi) {
+        const int mid = (lo + hi) >> 1;
+        const int id = sl.id[mid];
+        if (id != INT_MAX && better(sl.val[mid], id, cv, ci))
+            lo = mid + 1;
+        else
+            hi = mid;
     }
+    return lo;
+}
+
+// Merge nslot best-first lists (slot w at slots[w * stride]) by ranking every
+// entry against the other lists (binary search each); the entry of rank r < S
+// goes to out_val[r] / out_id[r].  One thread per entry, no serial chain.
+__device__ __forceinline__ void rank_merge_entry(const TopSlot *slots, int stride, int nslot,
+                                                 int S, int w, int j, float *out_val,
+                                                 int *out_id) {
+    const TopSlot &me = slots[w * stride];
+    const int ci = me.id[j];
+    if (ci == INT_MAX) return;
+    const float cv = me.val[j];
+    int rank = j;
+    for (int o = 0; o < nslot; ++o)
+        if (o != w) rank += count_better(slots[o * stride], cv, ci, S);
+    if (rank < S) {
+        out_val[rank] = cv;
+        out_id[rank] = ci;
+    }
+}
+
+// (max, sum-exp) of nslot slots, merged by one warp; valid in every lane.
+__device__ __forceinline__ void warp_merge_ms(const TopSlot *slots, int stride, int nslot,
+                                              int lane, float &m, float &s) {
+    WarpTop t;
+    t.reset();
+    for (int w = lane; w < nslot; w += kWarp) t.merge_ms(slots[w * stride].m, slots[w * stride].s);
+#pragma unroll
+    for (int o = 16; o > 0; o >>= 1) {
+        const float om = __shfl_xor_sync(0xffffffffu, t.m, o);
+        const float os = __shfl_xor_sync(0xffffffffu, t.s, o);
+        t.merge_ms(om, os);
+    }
+    m = t.m;
+    s = t.s;
 }
 
 template <typename T, int NB, int U>
@@ -234,6 +275,11 @@ heads_w2_kernel(const float *__restrict__ z, const T *__restrict__ W2, int B, in
     const int r0 = (int)(((long long)g * V) / G);
     const int r1 = (int)(((long long)(g + 1) * V) / G);
     const int nrows = r1 - r0;
+    // The weights are never written by any kernel, so this warp's first row
+    // can be pulled into L2 before the wait for phase 1's z.
+    if (lane == 0 && warp < nrows)
+        prefetch_l2_bulk(W2 + (size_t)(r0 + warp) * d, (unsigned)(d * sizeof(T)));
+    pdl_enter();
 
     for (int k0 = 0; k0 < K; k0 += hpg) {
         const int hk = min(hpg, K - k0);
@@ -281,22 +327,31 @@ heads_w2_kernel(const float *__restrict__ z, const T *__restrict__ W2, int B, in
         }
         __syncthreads();
 
-        // merge the warps' states: one warp per (head, sequence)
-        for (int pair = warp; pair < hk * B; pair += kW2Warps) {
+        // merge the warps' states per (head, sequence): empty defaults first,
+        // then every warp entry is ranked against the other warps' lists
+        const int pairs = hk * B;
+        for (int t = threadIdx.x; t < pairs * S; t += blockDim.x) {
+            const int pair = t / S, j = t - pair * S;
             const int kk = pair / B, b = pair - kk * B;
-            WarpTop acc;
-            acc.reset();
-            for (int w = 0; w < kW2Warps; ++w) {
-                const TopSlot &sl = slots[(w * hpg + kk) * NB + b];
-                acc.merge_ms(sl.m, sl.s);
-                merge_list(acc, sl.val, sl.id, S, lane);
-            }
             const size_t o = ((size_t)(k0 + kk) * B + b) * G + g;
-            if (lane == 0) part_ms[o] = make_float2(acc.m, acc.s);
-            if (lane < S) {
-                part_val[o * S + lane] = acc.val;
-                part_id[o * S + lane] = acc.id;
-            }
+            part_val[o * S + j] = -INFINITY;
+            part_id[o * S + j] = INT_MAX;
+        }
+        for (int pair = warp; pair < pairs; pair += kW2Warps) {
+            const int kk = pair / B, b = pair - kk * B;
+            float m, sum;
+            warp_merge_ms(slots + kk * NB + b, hpg * NB, kW2Warps, lane, m, sum);
+            if (lane == 0) part_ms[((size_t)(k0 + kk) * B + b) * G + g] = make_float2(m, sum);
+        }
+        __syncthreads();
+        for (int t = threadIdx.x; t < pairs * kW2Warps * S; t += blockDim.x) {
+            const int pair = t / (kW2Warps * S);
+            const int rem = t - pair * kW2Warps * S;
+            const int w = rem / S, j = rem - w * S;
+            const int kk = pair / B, b = pair - kk * B;
+            const size_t o = ((size_t)(k0 + kk) * B + b) * G + g;
+            rank_merge_entry(slots + kk * NB + b, hpg * NB, kW2Warps, S, w, j, part_val + o * S,
+                             part_id + o * S);
         }
         __syncthreads();
     }
@@ -304,39 +359,127 @@ heads_w2_kernel(const float *__restrict__ z, const T *__restrict__ W2, int B, in
 
 // ------------------------------------------------------------- phase 3 ---
 
+// compare-exchange so that (va, ia) ends up the better of the two
+__device__ __forceinline__ void cx(float &va, int &ia, float &vb, int &ib) {
+    if (better(vb, ib, va, ia)) {
+        const float tv = va; va = vb; vb = tv;
+        const int ti = ia; ia = ib; ib = ti;
+    }
+}
+
+// Warp top-S selection over up to 32*U candidates plus the warp's running
+// list (lanes < S): every lane sorts its own few candidates in registers, then
+// S rounds each take the best lane head by a five-step shuffle argmax and pop
+// it.  The result is left sorted best-first in lanes 0..S-1 (val, id).
+template <int U>
+__device__ __forceinline__ void warp_select_top(float (&cv)[U + 1], int (&ci)[U + 1], int S,
+                                                int lane, float &val, int &id) {
+    // sort the lane's U+1 entries best-first (odd-even transposition)
+#pragma unroll
+    for (int r = 0; r < U + 1; ++r)
+#pragma unroll
+        for (int e = (r & 1); e + 1 < U + 1; e += 2) cx(cv[e], ci[e], cv[e + 1], ci[e + 1]);
+    float nv = -INFINITY;
+    int ni = INT_MAX;
+    for (int k = 0; k < S; ++k) {
+        float bv = cv[0];
+        int bi = ci[0];
+#pragma unroll
+        for (int o = 16; o > 0; o >>= 1) {
+            const float ov = __shfl_xor_sync(0xffffffffu, bv, o);
+            const int oi = __shfl_xor_sync(0xffffffffu, bi, o);
+            if (better(ov, oi, bv, bi)) {
+                bv = ov;
+                bi = oi;
+            }
+        }
+        if (lane == k) {
+            nv = bv;
+            ni = bi;
+        }
+        if (bi != INT_MAX && ci[0] == bi) {  // this lane's head won: pop it
+#pragma unroll
+            for (int e = 0; e < U; ++e) {
+                cv[e] = cv[e + 1];
+                ci[e] = ci[e + 1];
+            }
+            cv[U] = -INFINITY;
+            ci[U] = INT_MAX;
+        }
+    }
+    val = nv;
+    id = ni;
+}
+
+// One CTA per (head, sequence).  The G partial top-s lists sit contiguously
+// (G*S candidates); each warp selects the top-s of its share with
+// warp_select_top (loads issued together, no load waits on another), then the
+// warps' lists are merged by parallel ranking.  Partial (max, sum) pairs merge
+// in parallel.
 __global__ void __launch_bounds__(kReduceThreads)
 heads_reduce_kernel(const float2 *__restrict__ part_ms, const float *__restrict__ part_val,
                     const int *__restrict__ part_id, int G, int B, int K, int S,
                     int32_t *__restrict__ topk_ids, float *__restrict__ topk_logp) {
-    __shared__ TopSlot slots[kReduceThreads / kWarp];
+    constexpr int U = 4;
+    constexpr int NW = kReduceThreads / kWarp;
+    pdl_enter();
+    __shared__ TopSlot slots[NW];
+    __shared__ float s_logz;
+    __shared__ float r_val[MEDUSA_MAX_TOP_S];
+    __shared__ int r_id[MEDUSA_MAX_TOP_S];
     const int kb = blockIdx.x;  // k * B + b
     const int k = kb / B, b = kb - k * B;
     const int lane = threadIdx.x & 31;
     const int warp = threadIdx.x >> 5;
-    const int nwarps = blockDim.x >> 5;
+    const int C = G * S;
+    const float *pv = part_val + (size_t)kb * C;
+    const int *pi = part_id + (size_t)kb * C;
+    // this warp's contiguous share of the candidates
+    const int c_lo = (int)(((long long)warp * C) / NW);
+    const int c_hi = (int)(((long long)(warp + 1) * C) / NW);
+    float val = -INFINITY;
+    int id = INT_MAX;
+    for (int c0 = c_lo; c0 < c_hi; c0 += kWarp * U) {
+        float cv[U + 1];
+        int ci[U + 1];
+#pragma unroll
+        for (int u = 0; u < U; ++u) {
+            const int idx = c0 + u * kWarp + lane;
+            cv[u] = idx < c_hi ? pv[idx] : -INFINITY;
+            ci[u] = idx < c_hi ? pi[idx] : INT_MAX;
+        }
+        cv[U] = lane < S ? val : -INFINITY;  // the running list joins the pool
+        ci[U] = lane < S ? id : INT_MAX;
+        warp_select_top<U>(cv, ci, S, lane, val, id);
+    }
     WarpTop st;
     st.reset();
-    for (int g = warp; g < G; g += nwarps) {
-        const size_t o = (size_t)kb * G + g;
-        const float2 ms = part_ms[o];
+    for (int g = threadIdx.x; g < G; g += kReduceThreads) {
+        const float2 ms = part_ms[(size_t)kb * G + g];
         st.merge_ms(ms.x, ms.y);
-        merge_list(st, part_val + o * S, part_id + o * S, S, lane);
     }
+#pragma unroll
+    for (int o = 16; o > 0; o >>= 1) {
+        const float om = __shfl_xor_sync(0xffffffffu, st.m, o);
+        const float os = __shfl_xor_sync(0xffffffffu, st.s, o);
+        st.merge_ms(om, os);
+    }
+    st.val = val;
+    st.id = id;
     flush_slot(slots[warp], st, S, lane);
     __syncthreads();
     if (warp == 0) {
-        WarpTop acc;
-        acc.reset();
-        for (int w = 0; w < nwarps; ++w) {
-            acc.merge_ms(slots[w].m, slots[w].s);
-            merge_list(acc, slots[w].val, slots[w].id, S, lane);
-        }
-        const float logz = acc.m + logf(acc.s);
-        if (lane < S) {
-            const size_t o = ((size_t)b * K + k) * S + lane;
-            topk_ids[o] = acc.id;
-            topk_logp[o] = acc.val - logz;
-        }
+        float m, sum;
+        warp_merge_ms(slots, 1, NW, lane, m, sum);
+        if (lane == 0) s_logz = m + logf(sum);
+    }
+    for (int t = threadIdx.x; t < NW * S; t += kReduceThreads)
+        rank_merge_entry(slots, 1, NW, S, t / S, t % S, r_val, r_id);
+    __syncthreads();
+    if (threadIdx.x < S) {
+        const size_t o = ((size_t)b * K + k) * S + threadIdx.x;
+        topk_ids[o] = r_id[threadIdx.x];
+        topk_logp[o] = r_val[threadIdx.x] - s_logz;
     }
 }
 
@@ -390,11 +533,14 @@ cudaError_t run_heads(const void *h, const void *W1, const void *b1, const void 
     int occ1 = 0;
     if ((e = cudaOccupancyMaxActiveBlocksPerMultiprocessor(&occ1, k1, kW1Threads, smem1))) return e;
     const int rows1 = K * d;
-    const int grid1 = std::max(1, std::min(sms * std::max(occ1, 1), (rows1 + 7) / 8));
-    k1<<<grid1, kW1Threads, smem1, stream>>>(static_cast<const T *>(h), static_cast<const T *>(W1),
-                                             static_cast<const T *>(b1), z, B, d, K);
+    const int warps1 = kW1Threads / kWarp;
+    const int slots1 = sms * std::max(occ1, 1) * warps1;
+    const int rpw = std::max(1, (rows1 + slots1 - 1) / slots1);
+    const int grid1 = std::max(1, (((rows1 + rpw - 1) / rpw) + warps1 - 1) / warps1);
+    e = launch_pdl(k1, dim3(grid1), dim3(kW1Threads), smem1, stream, static_cast<const T *>(h),
+                   static_cast<const T *>(W1), static_cast<const T *>(b1), z, B, d, K, rpw);
     note_launch();
-    if ((e = cudaGetLastError())) return e;
+    if (e) return e;
 
     // phase 2
     const size_t per_head = (size_t)NB * d * sizeof(float);
@@ -407,15 +553,17 @@ cudaError_t run_heads(const void *h, const void *W1, const void *b1, const void 
     int occ2 = 0;
     if ((e = cudaOccupancyMaxActiveBlocksPerMultiprocessor(&occ2, k2, kW2Threads, smem2))) return e;
     const int G = std::max(1, std::min(kMaxW2Ctas, sms * std::max(occ2, 1)));
-    k2<<<G, kW2Threads, smem2, stream>>>(z, static_cast<const T *>(W2), B, d, V, K, S, hpg, pms,
-                                         pval, pid);
+    e = launch_pdl(k2, dim3(G), dim3(kW2Threads), smem2, stream, static_cast<const float *>(z),
+                   static_cast<const T *>(W2), B, d, V, K, S, hpg, pms, pval, pid);
     note_launch();
-    if ((e = cudaGetLastError())) return e;
+    if (e) return e;
 
     // phase 3
-    heads_reduce_kernel<<<K * B, kReduceThreads, 0, stream>>>(pms, pval, pid, G, B, K, S, ids, logp);
+    e = launch_pdl(heads_reduce_kernel, dim3(K * B), dim3(kReduceThreads), 0, stream,
+                   static_cast<const float2 *>(pms), static_cast<const float *>(pval),
+                   static_cast<const int *>(pid), G, B, K, S, ids, logp);
     note_launch();
-    return cudaGetLastError();
+    return e;
 }
 
 }  // namespace

@@ -11,6 +11,25 @@
 
 namespace medusa {
 
+// Launch `kernel` on `stream` with programmatic stream serialization, so that
+// its launch may overlap the tail of the previous kernel in the stream (the
+// kernel itself calls pdl_enter() before touching global memory).
+template <typename... KArgs, typename... Args>
+cudaError_t launch_pdl(void (*kernel)(KArgs...), dim3 grid, dim3 block, size_t smem,
+                       cudaStream_t stream, Args... args) {
+    cudaLaunchConfig_t cfg = {};
+    cfg.gridDim = grid;
+    cfg.blockDim = block;
+    cfg.dynamicSmemBytes = smem;
+    cfg.stream = stream;
+    cudaLaunchAttribute attr[1];
+    attr[0].id = cudaLaunchAttributeProgrammaticStreamSerialization;
+    attr[0].val.programmaticStreamSerializationAllowed = 1;
+    cfg.attrs = attr;
+    cfg.numAttrs = 1;
+    return cudaLaunchKernelEx(&cfg, kernel, static_cast<KArgs>(args)...);
+}
+
 int device_sm_count();   // SMs of the current device (cached per device)
 void note_launch();      // count one kernel launch
 void set_last_error(const char *fmt, ...);  // message for medusa_last_error()

@@ -11,15 +11,17 @@
 // token.
 //
 // Two kernels:
-//   posterior_rows_kernel    one CTA per logits row: a single streaming pass
-//                            with 16-byte loads computes the argmax and, for
-//                            typical acceptance, the shifted sums
-//                            S = sum 2^(y-m), A = sum 2^(y-m) (y-m) in the
-//                            log2 domain (y = logit * log2(e) / T), from which
-//                            H = ln S - ln2 * A / S.  Row stats go to scratch.
+//   posterior_rows_kernel    each logits row split over a few CTAs (enough for
+//                            every SM): one streaming pass with 16-byte loads
+//                            computes the slice's argmax and, for typical
+//                            acceptance, the shifted sums S = sum 2^(y-m),
+//                            A = sum 2^(y-m) (y-m) in the log2 domain
+//                            (y = logit * log2(e) / T).  Slices go to scratch;
+//                            merged, they give H = ln S - ln2 * A / S.
 //   posterior_select_kernel  one CTA per sequence, one thread per node:
 //                            per-node decision, prefix-AND down the tree
 //                            level by level, longest path, next token.
+#include <algorithm>
 #include <climits>
 
 #include "common.cuh"
@@ -30,15 +32,18 @@ namespace medusa {
 namespace {
 
 constexpr int kRowThreads = 256;
+constexpr int kMaxSplits = 8;
 constexpr int kSelectThreads = 256;
 constexpr float kLog2e = 1.4426950408889634f;
 constexpr float kLn2 = 0.6931471805599453f;
 
-struct RowStats {
-    int argmax;
-    float m2;     // max of y = logit * log2(e) / T
-    float log2s;  // log2 sum 2^(y - m2)
-    float H;      // entropy in nats
+// Statistics of one slice of a logits row (a row is split over several CTAs).
+struct RowPart {
+    float amax;   // largest logit of the slice
+    int arg;      // its token id (smallest id among equal values)
+    float m2;     // max of y = logit * log2(e) / T over the slice
+    float S;      // sum 2^(y - m2)
+    float A;      // sum 2^(y - m2) (y - m2)
 };
 
 // (m, S, A) triple of shifted sums in the log2 domain
@@ -60,61 +65,60 @@ struct Moments {
 
 template <typename T, bool TYPICAL>
 __global__ void __launch_bounds__(kRowThreads)
-posterior_rows_kernel(const T *__restrict__ logits, int R, int V, float y_scale,
-                      RowStats *__restrict__ stats) {
+posterior_rows_kernel(const T *__restrict__ logits, int R, int V, int splits, float y_scale,
+                      RowPart *__restrict__ parts) {
+    pdl_enter();
     constexpr int VN = Vec16<T>::N;
     constexpr int U = 4;
     __shared__ float s_val[kRowThreads / kWarp];
     __shared__ int s_id[kRowThreads / kWarp];
     __shared__ float s_m[kRowThreads / kWarp], s_S[kRowThreads / kWarp], s_A[kRowThreads / kWarp];
-    const int row = blockIdx.x, b = blockIdx.y;
+    const int sp = blockIdx.x, row = blockIdx.y, b = blockIdx.z;
     const uint4 *x = reinterpret_cast<const uint4 *>(logits + ((size_t)b * R + row) * V);
     const int nvec = V / VN;
+    const int v_lo = (int)(((long long)sp * nvec) / splits);
+    const int v_hi = (int)(((long long)(sp + 1) * nvec) / splits);
     float bv = -INFINITY;
     int bi = INT_MAX;
     Moments mo{-INFINITY, 0.f, 0.f};
-    for (int base = threadIdx.x; base < nvec; base += kRowThreads * U) {
+    for (int base = v_lo + threadIdx.x; base < v_hi; base += kRowThreads * U) {
         uint4 v[U];
 #pragma unroll
         for (int u = 0; u < U; ++u) {
             const int idx = base + u * kRowThreads;
-            if (idx < nvec) v[u] = ld_stream16(x + idx);
+            if (idx < v_hi) v[u] = ld_stream16(x + idx);
         }
-        float f[U][VN];
-        float bm = -INFINITY;
 #pragma unroll
         for (int u = 0; u < U; ++u) {
             const int idx = base + u * kRowThreads;
-            if (idx < nvec) {
-                Vec16<T>::widen(v[u], f[u]);
+            if (idx < v_hi) {
+                float f[VN];
+                Vec16<T>::widen(v[u], f);
+                float vm = f[0];
+                // ids rise within a thread, so a strict > keeps the smallest
+                // id among equal values (the first element always enters, so a
+                // row of -inf still yields its first id)
 #pragma unroll
                 for (int e = 0; e < VN; ++e) {
-                    const float val = f[u][e];
-                    const int id = idx * VN + e;
-                    if (better(val, id, bv, bi)) {
-                        bv = val;
-                        bi = id;
+                    if (f[e] > bv || bi == INT_MAX) {
+                        bv = f[e];
+                        bi = idx * VN + e;
                     }
-                    bm = fmaxf(bm, val);
+                    vm = fmaxf(vm, f[e]);
                 }
-            }
-        }
-        if (TYPICAL) {
-            // fold this batch into the shifted sums with the batch max
-            const float m_new = fmaxf(mo.m, bm * y_scale);
-            if (mo.S != 0.f && m_new > mo.m) {
-                const float f1 = exp2f(mo.m - m_new);
-                mo.A = f1 * (mo.A + mo.S * (mo.m - m_new));
-                mo.S *= f1;
-            }
-            mo.m = m_new;
-#pragma unroll
-            for (int u = 0; u < U; ++u) {
-                const int idx = base + u * kRowThreads;
-                if (idx < nvec) {
+                if (TYPICAL) {
+                    const float m_new = fmaxf(mo.m, vm * y_scale);
+                    if (m_new > mo.m) {
+                        if (mo.S != 0.f) {
+                            const float f1 = exp2f(mo.m - m_new);
+                            mo.A = f1 * (mo.A + mo.S * (mo.m - m_new));
+                            mo.S *= f1;
+                        }
+                        mo.m = m_new;
+                    }
 #pragma unroll
                     for (int e = 0; e < VN; ++e) {
-                        const float t = fmaf(f[u][e], y_scale, -mo.m);
+                        const float t = fmaf(f[e], y_scale, -mo.m);
                         const float p = exp2f(t);
                         mo.S += p;
                         mo.A = fmaf(p, t, mo.A);
@@ -156,24 +160,48 @@ posterior_rows_kernel(const T *__restrict__ logits, int R, int V, float y_scale,
             }
             if (TYPICAL) mo.merge(s_m[w], s_S[w], s_A[w]);
         }
-        RowStats st;
-        st.argmax = bi;
-        st.m2 = mo.m;
-        st.log2s = TYPICAL ? log2f(mo.S) : 0.f;
-        st.H = TYPICAL ? logf(mo.S) - kLn2 * mo.A / mo.S : 0.f;
-        stats[(size_t)b * R + row] = st;
+        RowPart pt;
+        pt.amax = bv;
+        pt.arg = bi;
+        pt.m2 = mo.m;
+        pt.S = mo.S;
+        pt.A = mo.A;
+        parts[((size_t)b * R + row) * splits + sp] = pt;
     }
+}
+
+// Merge the slices of one row: argmax, and log2 S, H (nats) when typical.
+__device__ __forceinline__ void row_stats(const RowPart *__restrict__ parts, int splits,
+                                          bool typical, int &arg, float &m2, float &log2s,
+                                          float &H) {
+    float bv = -INFINITY;
+    int bi = INT_MAX;
+    Moments mo{-INFINITY, 0.f, 0.f};
+    for (int k = 0; k < splits; ++k) {
+        const RowPart pt = parts[k];
+        if (better(pt.amax, pt.arg, bv, bi)) {
+            bv = pt.amax;
+            bi = pt.arg;
+        }
+        if (typical) mo.merge(pt.m2, pt.S, pt.A);
+    }
+    arg = bi;
+    m2 = mo.m;
+    log2s = typical ? log2f(mo.S) : 0.f;
+    H = typical ? logf(mo.S) - kLn2 * mo.A / mo.S : 0.f;
 }
 
 template <typename T>
 __global__ void __launch_bounds__(kSelectThreads)
 posterior_select_kernel(const T *__restrict__ logits, const int32_t *__restrict__ tokens,
                         const int32_t *__restrict__ parent, const int32_t *__restrict__ depth,
-                        const RowStats *__restrict__ stats, int R, int V, int K, int typical,
+                        const RowPart *__restrict__ parts, int splits, int R, int V, int K,
+                        int typical,
                         float y_scale, float log2_eps, float log2_delta,
                         int32_t *__restrict__ accept_len, int32_t *__restrict__ path,
                         int32_t *__restrict__ path_tokens, int32_t *__restrict__ next_token,
                         int32_t *__restrict__ accept_out, int *status) {
+    pdl_enter();
     __shared__ int s_acc[MEDUSA_MAX_TREE_ROWS];
     __shared__ int s_chain[MEDUSA_MAX_TREE_ROWS];
     __shared__ int s_par[MEDUSA_MAX_TREE_ROWS];
@@ -217,13 +245,15 @@ posterior_select_kernel(const T *__restrict__ logits, const int32_t *__restrict_
             if (!ok) {
                 acc = 0;
             } else {
-                const RowStats st = stats[(size_t)b * R + p];
+                int arg;
+                float m2, log2s, H;
+                row_stats(parts + ((size_t)b * R + p) * splits, splits, typical, arg, m2, log2s, H);
                 if (!typical) {
-                    acc = (tok == st.argmax);
+                    acc = (tok == arg);
                 } else {
                     const float y = Vec16<T>::load1(logits + ((size_t)b * R + p) * V + tok) * y_scale;
-                    const float lp2 = y - st.m2 - st.log2s;
-                    const float thr2 = fminf(log2_eps, log2_delta - st.H * kLog2e);
+                    const float lp2 = y - m2 - log2s;
+                    const float thr2 = fminf(log2_eps, log2_delta - H * kLog2e);
                     acc = lp2 > thr2;
                 }
             }
@@ -256,8 +286,17 @@ posterior_select_kernel(const T *__restrict__ logits, const int32_t *__restrict_
             if (x == 0) break;
         }
         accept_len[b] = L;
-        next_token[b] = stats[(size_t)b * R + best].argmax;
+        int arg;
+        float m2, log2s, H;
+        row_stats(parts + ((size_t)b * R + best) * splits, splits, false, arg, m2, log2s, H);
+        next_token[b] = arg;
     }
+}
+
+// Slices per logits row: enough CTAs for two per SM on 152 SMs, at most 8.
+int row_splits(int B, int R) {
+    const int rows = B * R;
+    return std::max(1, std::min(kMaxSplits, (2 * 152 + rows - 1) / rows));
 }
 
 template <typename T>
@@ -267,28 +306,27 @@ cudaError_t run_posterior(const void *logits, const int32_t *tokens, const int32
                           int32_t *path, int32_t *path_tokens, int32_t *next_token,
                           int32_t *accept, void *ws, cudaStream_t stream) {
     int *status = static_cast<int *>(ws);
-    RowStats *stats = reinterpret_cast<RowStats *>(static_cast<char *>(ws) + MEDUSA_WS_HEADER);
+    RowPart *parts = reinterpret_cast<RowPart *>(static_cast<char *>(ws) + MEDUSA_WS_HEADER);
     const T *lg = static_cast<const T *>(logits);
     const float y_scale = kLog2e / temperature;
-    dim3 grid(R, B);
-    if (typical)
-        posterior_rows_kernel<T, true><<<grid, kRowThreads, 0, stream>>>(lg, R, V, y_scale, stats);
-    else
-        posterior_rows_kernel<T, false><<<grid, kRowThreads, 0, stream>>>(lg, R, V, y_scale, stats);
+    const int splits = row_splits(B, R);
+    cudaError_t e = launch_pdl(typical ? posterior_rows_kernel<T, true> : posterior_rows_kernel<T, false>,
+                               dim3(splits, R, B), dim3(kRowThreads), 0, stream, lg, R, V, splits,
+                               y_scale, parts);
     note_launch();
-    cudaError_t e = cudaGetLastError();
     if (e) return e;
-    posterior_select_kernel<T><<<B, kSelectThreads, 0, stream>>>(
-        lg, tokens, parent, depth, stats, R, V, K, typical ? 1 : 0, y_scale, log2f(eps),
-        log2f(delta), accept_len, path, path_tokens, next_token, accept, status);
+    e = launch_pdl(posterior_select_kernel<T>, dim3(B), dim3(kSelectThreads), 0, stream, lg, tokens,
+                   parent, depth, static_cast<const RowPart *>(parts), splits, R, V, K,
+                   typical ? 1 : 0, y_scale, log2f(eps), log2f(delta), accept_len, path,
+                   path_tokens, next_token, accept, status);
     note_launch();
-    return cudaGetLastError();
+    return e;
 }
 
 }  // namespace
 
 size_t posterior_workspace_bytes(int B, int R) {
-    return MEDUSA_WS_HEADER + (size_t)B * R * sizeof(RowStats);
+    return MEDUSA_WS_HEADER + (size_t)B * R * kMaxSplits * sizeof(RowPart);
 }
 
 cudaError_t launch_posterior(medusa_dtype dtype, const void *logits, const int32_t *tokens,

@@ -35,27 +35,37 @@ namespace medusa {
 
 namespace {
 
-constexpr int kTreeThreads = 256;
+constexpr int kTreeThreads = 1024;
 
 __device__ __forceinline__ int nib_shift(int depth) { return 28 - 4 * (depth - 1); }
 
-__device__ __forceinline__ bool precedes(double sa, int da, uint32_t pa, double sb, int db,
-                                         uint32_t pb) {
-    if (sa != sb) return sa > sb;
-    if (da != db) return da < db;
-    return pa < pb;
+// Order-preserving integer image of an fp64 score (no NaN; -0 folded into
+// +0), so every comparison below is integer work: GB300's fp64 rate is a
+// small fraction of its integer rate.
+__device__ __forceinline__ uint64_t score_key(double s) {
+    const uint64_t u = static_cast<uint64_t>(__double_as_longlong(s + 0.0));
+    return (u >> 63) ? ~u : (u | 0x8000000000000000ull);
 }
+
+// node a is taken before node b: larger score, then smaller depth, then the
+// smaller rank path; lo = depth << 32 | path
+__device__ __forceinline__ bool precedes(uint64_t ka, uint64_t la, uint64_t kb, uint64_t lb) {
+    return ka > kb || (ka == kb && la < lb);
+}
+
+// Full Cartesian trees up to this many nodes are ranked in one pass over all
+// their nodes; larger ones go level by level.
+constexpr int kDirectMax = 512;
 
 struct TreeSmem {
     double *cand_score;
-    uint32_t *cand_path;
+    uint64_t *cand_key;
+    uint64_t *cand_lo;     // depth << 32 | rank path
     double *kept_score;
-    uint32_t *kept_path;
-    unsigned char *kept_depth;
-    int *sel_depth;
-    uint32_t *sel_path;
-    int *c_depth;
-    uint32_t *c_path;
+    uint64_t *kept_key;
+    uint64_t *kept_lo;
+    uint64_t *sel_lo;      // the n picks, any order
+    uint64_t *c_lo;        // canonical order: c_lo[0] = root, ascending
     int *c_parent;
     int *has_child;
     int *leaf_of;
@@ -68,36 +78,40 @@ __host__ __device__ inline size_t take_bytes(size_t &o, size_t bytes, size_t ali
     return at;
 }
 
-__host__ __device__ inline size_t tree_smem_layout(int K, int S, int n, TreeSmem *p, char *base) {
-    const int cand_cap = n * S > S ? n * S : S;
-    const int kept_cap = K * n;
+__host__ __device__ inline int tree_cand_cap(int S, int n, long long full) {
+    if (full <= kDirectMax) return (int)full;
+    return n * S > S ? n * S : S;
+}
+
+__host__ __device__ inline size_t tree_smem_layout(int K, int S, int n, long long full, TreeSmem *p,
+                                                   char *base) {
+    const int cand_cap = tree_cand_cap(S, n, full);
+    const int kept_cap = full <= kDirectMax ? 1 : K * n;
     const int R = n + 1;
     size_t o = 0;
     const size_t a0 = take_bytes(o, sizeof(double) * cand_cap, 8);
-    const size_t a1 = take_bytes(o, sizeof(double) * kept_cap, 8);
-    const size_t a2 = take_bytes(o, sizeof(uint32_t) * cand_cap, 4);
-    const size_t a3 = take_bytes(o, sizeof(uint32_t) * kept_cap, 4);
-    const size_t a4 = take_bytes(o, sizeof(int) * n, 4);
-    const size_t a5 = take_bytes(o, sizeof(uint32_t) * n, 4);
-    const size_t a6 = take_bytes(o, sizeof(int) * R, 4);
-    const size_t a7 = take_bytes(o, sizeof(uint32_t) * R, 4);
+    const size_t a1 = take_bytes(o, sizeof(uint64_t) * cand_cap, 8);
+    const size_t a2 = take_bytes(o, sizeof(uint64_t) * cand_cap, 8);
+    const size_t a3 = take_bytes(o, sizeof(double) * kept_cap, 8);
+    const size_t a4 = take_bytes(o, sizeof(uint64_t) * kept_cap, 8);
+    const size_t a5 = take_bytes(o, sizeof(uint64_t) * kept_cap, 8);
+    const size_t a6 = take_bytes(o, sizeof(uint64_t) * n, 8);
+    const size_t a7 = take_bytes(o, sizeof(uint64_t) * R, 8);
     const size_t a8 = take_bytes(o, sizeof(int) * R, 4);
     const size_t a9 = take_bytes(o, sizeof(int) * R, 4);
-    const size_t a10 = take_bytes(o, sizeof(int) * n, 4);
-    const size_t a11 = take_bytes(o, kept_cap, 1);
+    const size_t a10 = take_bytes(o, sizeof(int) * R, 4);
     if (p) {
         p->cand_score = reinterpret_cast<double *>(base + a0);
-        p->kept_score = reinterpret_cast<double *>(base + a1);
-        p->cand_path = reinterpret_cast<uint32_t *>(base + a2);
-        p->kept_path = reinterpret_cast<uint32_t *>(base + a3);
-        p->sel_depth = reinterpret_cast<int *>(base + a4);
-        p->sel_path = reinterpret_cast<uint32_t *>(base + a5);
-        p->c_depth = reinterpret_cast<int *>(base + a6);
-        p->c_path = reinterpret_cast<uint32_t *>(base + a7);
+        p->cand_key = reinterpret_cast<uint64_t *>(base + a1);
+        p->cand_lo = reinterpret_cast<uint64_t *>(base + a2);
+        p->kept_score = reinterpret_cast<double *>(base + a3);
+        p->kept_key = reinterpret_cast<uint64_t *>(base + a4);
+        p->kept_lo = reinterpret_cast<uint64_t *>(base + a5);
+        p->sel_lo = reinterpret_cast<uint64_t *>(base + a6);
+        p->c_lo = reinterpret_cast<uint64_t *>(base + a7);
         p->c_parent = reinterpret_cast<int *>(base + a8);
         p->has_child = reinterpret_cast<int *>(base + a9);
         p->leaf_of = reinterpret_cast<int *>(base + a10);
-        p->kept_depth = reinterpret_cast<unsigned char *>(base + a11);
     }
     return (o + 15) / 16 * 16;
 }
@@ -107,6 +121,7 @@ struct TreeArgs {
     const int32_t *ids;
     const float *logp;
     int K, S, n;
+    long long full;  // nodes of the full Cartesian tree (capped)
     int s[MEDUSA_MAX_HEADS];
     const int32_t *prefix_len;
     int32_t *tokens, *parent, *depth, *pos_id;
@@ -115,17 +130,36 @@ struct TreeArgs {
     int *status;
 };
 
+__device__ __forceinline__ int warp_sum_int(int v) {
+#pragma unroll
+    for (int o = 16; o > 0; o >>= 1) v += __shfl_xor_sync(0xffffffffu, v, o);
+    return v;
+}
+
+// Number of entries of (key, lo)[0..c) that are taken before (ki, li):
+// computed by one warp, lanes splitting the entries.
+__device__ __forceinline__ int count_before(const uint64_t *key, const uint64_t *lo, int c,
+                                            uint64_t ki, uint64_t li, int lane) {
+    int cnt = 0;
+#pragma unroll 4
+    for (int j = lane; j < c; j += kWarp) cnt += precedes(key[j], lo[j], ki, li);
+    return warp_sum_int(cnt);
+}
+
+// Every counting pass gives one warp per item and splits the comparisons over
+// its lanes, so the longest dependent chain is ~c/32 shared loads plus a
+// five-step shuffle.
 __global__ void __launch_bounds__(kTreeThreads) build_tree_kernel(TreeArgs a) {
+    pdl_enter();
     extern __shared__ __align__(16) char tsm[];
     __shared__ double lp[MEDUSA_MAX_HEADS][MEDUSA_MAX_TOP_S];
     __shared__ int tid_tok[MEDUSA_MAX_HEADS][MEDUSA_MAX_TOP_S];
-    __shared__ int level_off[MEDUSA_MAX_HEADS + 1];
-    __shared__ int n_leaf_s;
+    __shared__ int warp_leaves[kTreeThreads / kWarp];
     TreeSmem sm;
-    tree_smem_layout(a.K, a.S, a.n, &sm, tsm);
+    tree_smem_layout(a.K, a.S, a.n, a.full, &sm, tsm);
     const int b = blockIdx.x;
-    const int tid = threadIdx.x;
-    const int nt = blockDim.x;
+    const int tid = threadIdx.x, lane = tid & 31, warp = tid >> 5;
+    const int nt = blockDim.x, nw = nt >> 5;
     const int K = a.K, S = a.S, n = a.n, R = n + 1;
     const int W = (R + 63) / 64;
 
@@ -136,130 +170,158 @@ __global__ void __launch_bounds__(kTreeThreads) build_tree_kernel(TreeArgs a) {
         lp[k][r] = (double)v;
         tid_tok[k][r] = a.ids[((size_t)b * K + k) * S + r];
     }
-    if (tid == 0) {
-        level_off[0] = 0;
-        n_leaf_s = 0;
+    __syncthreads();
+
+    if (a.full <= kDirectMax) {
+        // ---- small tree: every node of the full tree, ranked once
+        const int full = (int)a.full;
+        for (int t = tid; t < full; t += nt) {
+            int D = 1, base = 0, width = a.s[0];
+            while (t >= base + width) {
+                base += width;
+                width *= a.s[D];
+                ++D;
+            }
+            // mixed-radix digits of the index within its depth, depth 1 first;
+            // the score is summed from depth 1 down, as the frontier does
+            const int l = t - base;
+            int div = width / a.s[0];
+            uint32_t path = 0;
+            double sc = 0.0;
+            for (int j = 0; j < D; ++j) {
+                const int r = (l / div) % a.s[j];
+                sc = (j == 0) ? lp[0][r] : sc + lp[j][r];
+                path |= (uint32_t)r << nib_shift(j + 1);
+                if (j + 1 < D) div /= a.s[j + 1];
+            }
+            sm.cand_key[t] = score_key(sc);
+            sm.cand_lo[t] = ((uint64_t)D << 32) | path;
+        }
+        __syncthreads();
+        for (int i = warp; i < full; i += nw) {
+            const int cnt = count_before(sm.cand_key, sm.cand_lo, full, sm.cand_key[i],
+                                         sm.cand_lo[i], lane);
+            if (lane == 0 && cnt < n) sm.sel_lo[cnt] = sm.cand_lo[i];
+        }
+    } else {
+        // ---- large tree: level D keeps its best n candidates (a node
+        // outside them cannot be among the first n overall)
+        int prev_count = 0, prev_off = 0;
+        for (int D = 1; D <= K; ++D) {
+            const int sD = a.s[D - 1];
+            const int c = (D == 1) ? sD : prev_count * sD;
+            const int sh = nib_shift(D);
+            for (int i = tid; i < c; i += nt) {
+                double sc;
+                uint32_t pa;
+                if (D == 1) {
+                    sc = lp[0][i];
+                    pa = (uint32_t)i << sh;
+                } else {
+                    const int p = i / sD, r = i - p * sD;
+                    sc = sm.kept_score[prev_off + p] + lp[D - 1][r];
+                    pa = (uint32_t)sm.kept_lo[prev_off + p] | ((uint32_t)r << sh);
+                }
+                sm.cand_score[i] = sc;
+                sm.cand_key[i] = score_key(sc);
+                sm.cand_lo[i] = ((uint64_t)D << 32) | pa;
+            }
+            __syncthreads();
+            const int off = (D == 1) ? 0 : prev_off + prev_count;
+            for (int i = warp; i < c; i += nw) {
+                const int cnt = count_before(sm.cand_key, sm.cand_lo, c, sm.cand_key[i],
+                                             sm.cand_lo[i], lane);
+                if (lane == 0 && cnt < n) {
+                    sm.kept_score[off + cnt] = sm.cand_score[i];
+                    sm.kept_key[off + cnt] = sm.cand_key[i];
+                    sm.kept_lo[off + cnt] = sm.cand_lo[i];
+                }
+            }
+            prev_off = off;
+            prev_count = c < n ? c : n;
+            __syncthreads();
+        }
+        const int total = prev_off + prev_count;
+        for (int i = warp; i < total; i += nw) {
+            const int cnt = count_before(sm.kept_key, sm.kept_lo, total, sm.kept_key[i],
+                                         sm.kept_lo[i], lane);
+            if (lane == 0 && cnt < n) sm.sel_lo[cnt] = sm.kept_lo[i];
+        }
     }
     __syncthreads();
 
-    // ---- level-wise survivors
-    int prev_count = 0, prev_off = 0;
-    for (int D = 1; D <= K; ++D) {
-        const int sD = a.s[D - 1];
-        const int c = (D == 1) ? sD : prev_count * sD;
-        const int sh = nib_shift(D);
-        for (int i = tid; i < c; i += nt) {
-            if (D == 1) {
-                sm.cand_score[i] = lp[0][i];
-                sm.cand_path[i] = (uint32_t)i << sh;
-            } else {
-                const int p = i / sD, r = i - p * sD;
-                sm.cand_score[i] = sm.kept_score[prev_off + p] + lp[D - 1][r];
-                sm.cand_path[i] = sm.kept_path[prev_off + p] | ((uint32_t)r << sh);
-            }
-        }
-        __syncthreads();
-        const int off = (D == 1) ? 0 : prev_off + prev_count;
-        for (int i = tid; i < c; i += nt) {
-            const double si = sm.cand_score[i];
-            const uint32_t pi = sm.cand_path[i];
-            int rank = 0;
-            for (int j = 0; j < c; ++j) {
-                const double sj = sm.cand_score[j];
-                rank += (sj > si) || (sj == si && sm.cand_path[j] < pi);
-            }
-            if (rank < n) {
-                sm.kept_score[off + rank] = si;
-                sm.kept_path[off + rank] = pi;
-                sm.kept_depth[off + rank] = (unsigned char)D;
-            }
-        }
-        prev_off = off;
-        prev_count = c < n ? c : n;
-        if (tid == 0) level_off[D] = off + prev_count;
-        __syncthreads();
+    // ---- canonical order: root, then (depth, rank path) ascending
+    for (int i = warp; i < n; i += nw) {
+        const uint64_t li = sm.sel_lo[i];
+        int cnt = 0;
+#pragma unroll 4
+        for (int j = lane; j < n; j += kWarp) cnt += sm.sel_lo[j] < li;
+        cnt = warp_sum_int(cnt);
+        if (lane == 0) sm.c_lo[1 + cnt] = li;
     }
-    const int total = level_off[K];
-
-    // ---- global first n among all survivors
-    for (int i = tid; i < total; i += nt) {
-        const double si = sm.kept_score[i];
-        const int di = sm.kept_depth[i];
-        const uint32_t pi = sm.kept_path[i];
-        int rank = 0;
-        for (int j = 0; j < total; ++j)
-            rank += precedes(sm.kept_score[j], sm.kept_depth[j], sm.kept_path[j], si, di, pi);
-        if (rank < n) {
-            sm.sel_depth[rank] = di;
-            sm.sel_path[rank] = pi;
-        }
-    }
-    __syncthreads();
-
-    // ---- canonical order: root, then (depth, rank path)
-    if (tid == 0) {
-        sm.c_depth[0] = 0;
-        sm.c_path[0] = 0;
-        sm.c_parent[0] = -1;
-    }
-    for (int i = tid; i < n; i += nt) {
-        const int di = sm.sel_depth[i];
-        const uint32_t pi = sm.sel_path[i];
-        int ci = 1;
-        for (int j = 0; j < n; ++j) {
-            const int dj = sm.sel_depth[j];
-            ci += (dj < di) || (dj == di && sm.sel_path[j] < pi);
-        }
-        sm.c_depth[ci] = di;
-        sm.c_path[ci] = pi;
-    }
+    if (tid == 0) sm.c_lo[0] = 0;
     for (int i = tid; i < R; i += nt) sm.has_child[i] = 0;
     __syncthreads();
-    for (int i = 1 + tid; i < R; i += nt) {
-        const int D = sm.c_depth[i];
-        int p = 0;
-        if (D > 1) {
-            const uint32_t pp = sm.c_path[i] & ~((uint32_t)0xF << nib_shift(D));
-            p = -1;
-            for (int j = 1; j < i; ++j)
-                if (sm.c_depth[j] == D - 1 && sm.c_path[j] == pp) {
-                    p = j;
-                    break;
+    // parent = the node one level up with this node's rank path minus its
+    // last rank; c_lo is sorted, so binary search finds its index
+    for (int i = tid; i < R; i += nt) {
+        int p = -1;
+        if (i > 0) {
+            const uint64_t li = sm.c_lo[i];
+            const int D = (int)(li >> 32);
+            p = 0;
+            if (D > 1) {
+                const uint64_t want = ((uint64_t)(D - 1) << 32) |
+                                      ((uint32_t)li & ~((uint32_t)0xF << nib_shift(D)));
+                int lo = 1, hi = i;
+                while (lo < hi) {
+                    const int mid = (lo + hi) >> 1;
+                    if (sm.c_lo[mid] < want) lo = mid + 1; else hi = mid;
                 }
+                p = lo;
+            }
+            sm.has_child[p] = 1;
         }
         sm.c_parent[i] = p;
-        if (p >= 0) sm.has_child[p] = 1;
     }
     __syncthreads();
 
-    // ---- per-node outputs
+    // ---- per-node outputs; leaves numbered by a ballot scan
     const int P = a.prefix_len ? a.prefix_len[b] : 0;
-    for (int i = tid; i < R; i += nt) {
-        const int D = sm.c_depth[i];
+    const bool leaf = tid < R && !sm.has_child[tid];
+    const unsigned bal = __ballot_sync(0xffffffffu, leaf);
+    if (lane == 0) warp_leaves[warp] = __popc(bal);
+    __syncthreads();
+    int before = 0, nl = 0;
+    for (int w = 0; w < nw; ++w) {
+        if (w < warp) before += warp_leaves[w];
+        nl += warp_leaves[w];
+    }
+    if (leaf) sm.leaf_of[before + __popc(bal & ((1u << lane) - 1u))] = tid;
+    if (tid < R) {
+        const int i = tid;
+        const uint64_t li = sm.c_lo[i];
+        const int D = (int)(li >> 32);
         const size_t o = (size_t)b * R + i;
         int tok;
         if (i == 0) {
             tok = a.root[b];
         } else {
-            const int r = (int)((sm.c_path[i] >> nib_shift(D)) & 0xF);
+            const int r = (int)(((uint32_t)li >> nib_shift(D)) & 0xF);
             tok = tid_tok[D - 1][r];
         }
         a.tokens[o] = tok;
         a.parent[o] = sm.c_parent[i];
         a.depth[o] = D;
         a.pos_id[o] = P + D;
-        uint64_t m[4] = {0, 0, 0, 0};
-        for (int x = i; x >= 0; x = sm.c_parent[x]) m[x >> 6] |= (uint64_t)1 << (x & 63);
-        for (int w = 0; w < W; ++w) a.anc_mask[o * W + w] = m[w];
-        if (!sm.has_child[i]) {
-            int li = 0;
-            for (int j = 0; j < i; ++j) li += !sm.has_child[j];
-            sm.leaf_of[li] = i;
-            atomicAdd(&n_leaf_s, 1);
+        for (int w = 0; w < W; ++w) {
+            uint64_t m = 0;
+            for (int x = i; x >= 0; x = sm.c_parent[x])
+                if ((x >> 6) == w) m |= (uint64_t)1 << (x & 63);
+            a.anc_mask[o * W + w] = m;
         }
     }
     __syncthreads();
-    const int nl = n_leaf_s;
     if (tid == 0) a.n_leaf[b] = nl;
     const int cols = K + 1;
     for (int e = tid; e < n * cols; e += nt) {
@@ -267,7 +329,7 @@ __global__ void __launch_bounds__(kTreeThreads) build_tree_kernel(TreeArgs a) {
         int v = -1;
         if (li < nl) {
             int x = sm.leaf_of[li];
-            const int D = sm.c_depth[x];
+            const int D = (int)(sm.c_lo[x] >> 32);
             if (q <= D) {
                 for (int up = D - q; up > 0; --up) x = sm.c_parent[x];
                 v = x;
@@ -294,6 +356,15 @@ cudaError_t launch_build_tree(const int32_t *root, const int32_t *ids, const flo
     a.ids = ids;
     a.logp = logp;
     a.K = K;
+    {
+        long long full = 0, level = 1;
+        for (int k = 0; k < K; ++k) {
+            level *= s_host[k];
+            full += level;
+            if (full > (1 << 20)) break;
+        }
+        a.full = full;
+    }
     a.S = S;
     a.n = n;
     for (int k = 0; k < MEDUSA_MAX_HEADS; ++k) a.s[k] = k < K ? s_host[k] : 0;
@@ -306,13 +377,13 @@ cudaError_t launch_build_tree(const int32_t *root, const int32_t *ids, const flo
     a.paths = paths;
     a.n_leaf = n_leaf;
     a.status = static_cast<int *>(ws);
-    const size_t smem = tree_smem_layout(K, S, n, nullptr, nullptr);
+    const size_t smem = tree_smem_layout(K, S, n, a.full, nullptr, nullptr);
     cudaError_t e = cudaFuncSetAttribute(build_tree_kernel,
                                          cudaFuncAttributeMaxDynamicSharedMemorySize, (int)smem);
     if (e) return e;
-    build_tree_kernel<<<B, kTreeThreads, smem, stream>>>(a);
+    e = launch_pdl(build_tree_kernel, dim3(B), dim3(kTreeThreads), smem, stream, a);
     note_launch();
-    return cudaGetLastError();
+    return e;
 }
 
 }  // namespace medusa
