@@ -25,6 +25,7 @@
 
 #include "common.cuh"
 #include "launch.h"
+#include "tcgen05.cuh"
 
 namespace medusa {
 
@@ -297,6 +298,258 @@ __global__ void __launch_bounds__(MAXW * 32, 1) tree_attn_split_kernel(AttnArgs 
     }
 }
 
+// ------------------------------------------------------- tensor-core path ---
+//
+// tree_attn_tc_kernel: one CTA per (key chunk, head, sequence); a chunk is
+// 128 consecutive slots of the cache, prefix and tree slots alike (they are
+// contiguous).  256 threads: threads t and t+128 own query row t (rows >= R
+// are zero), each handling half of the chunk's keys and of the output columns.  Q, K and V are staged by cp.async into 128-byte-swizzled shared
+// memory; one thread issues the MMAs:
+//     S[128 x 128] = Q K^T      (TMEM columns 0..127)
+//     O[128 x DH]  = P V        (TMEM columns 128..)
+// Between them every thread reads its S row from TMEM, masks it (slots past
+// the chunk; tree slots that are not ancestors-or-self of the row), takes the
+// row max m and writes P = 2^(s*scale*log2e - m) as bf16 into shared memory
+// (the K buffer, which the first MMA no longer needs).  The CTA writes the
+// unnormalised partial (O, m, l) rows; tree_attn_combine_kernel merges them.
+// Every mbarrier wait is bounded; on a timeout the CTA records
+// MEDUSA_DEV_TIMEOUT, waits once more (bounded) for its MMAs and frees its
+// tensor memory before returning.
+constexpr int kChunk = 128;
+constexpr uint32_t kWaitPolls = 1u << 16;
+
+template <int DH>
+struct TcSmem {
+    static constexpr int NB = DH / 64;                 // 64-element column blocks of dh
+    static constexpr int Q_BYTES = NB * 128 * 128;      // [NB][128 rows][128 B]
+    static constexpr int K_BYTES = NB * kChunk * 128;   // [NB][128 keys][128 B]; P reuses it
+    static constexpr int P_BYTES = 2 * 128 * 128;       // [2][128 rows][64 keys]
+    static constexpr int KP_BYTES = K_BYTES > P_BYTES ? K_BYTES : P_BYTES;
+    static constexpr int V_BYTES = NB * kChunk * 128;   // [NB][128 keys][128 B]
+    static constexpr int Q_OFF = 0;
+    static constexpr int KP_OFF = Q_OFF + Q_BYTES;
+    static constexpr int V_OFF = KP_OFF + KP_BYTES;
+    // two CTAs per SM stay within the same shared-memory carveout as the heads
+    // kernels (2 x 96 KB): a larger carveout would shrink L1 under them
+    static constexpr int BAR_OFF = V_OFF + V_BYTES;  // two mbarriers, TMEM holder, flag
+    // 2 x (TOTAL + 1 KB reserved per CTA) must stay within a 196 KB carveout
+    static constexpr int TOTAL = BAR_OFF + 64;
+};
+
+template <int DH>
+__global__ void __launch_bounds__(256, 2) tree_attn_tc_kernel(AttnArgs a) {
+    pdl_enter();
+    using L = TcSmem<DH>;
+    constexpr int NB = L::NB;
+    constexpr int HALF = kChunk / 2;  // keys per thread: two threads share a row
+    // operand tiles need 1024-byte alignment (swizzle atoms)
+    extern __shared__ __align__(1024) unsigned char tc_raw[];
+    unsigned char *q_s = tc_raw + L::Q_OFF;
+    unsigned char *kp_s = tc_raw + L::KP_OFF;
+    unsigned char *v_s = tc_raw + L::V_OFF;
+    uint64_t &bar_s = *reinterpret_cast<uint64_t *>(tc_raw + L::BAR_OFF);
+    uint64_t &bar_o = *reinterpret_cast<uint64_t *>(tc_raw + L::BAR_OFF + 8);
+    uint32_t &tmem_holder = *reinterpret_cast<uint32_t *>(tc_raw + L::BAR_OFF + 16);
+    int &failed = *reinterpret_cast<int *>(tc_raw + L::BAR_OFF + 20);
+    // [2][128] row max / sum exchange, in the Q tile (dead once S is computed)
+    float *xch = reinterpret_cast<float *>(q_s);
+
+    const int chunk = blockIdx.x, h = blockIdx.y, b = blockIdx.z;
+    const int R = a.R, H = a.H;
+    const int tid = threadIdx.x, warp = tid >> 5;
+    // warp w reads TMEM lanes 32*(w%4)..: row = tid % 128; half = column half
+    const int row = tid & 127, half = tid >> 7;
+    int P = a.prefix_len[b];
+    if (P < 0 || P > a.P_max) {
+        set_status(a.status, MEDUSA_DEV_BAD_PREFIX);
+        P = 0;
+    }
+    const int NS = a.nps;  // chunks per (sequence, head)
+    const size_t pbase = ((size_t)(b * H + h) * NS + chunk) * R;
+    const int kbeg = chunk * kChunk;
+    const int kend = min(kbeg + kChunk, P + R);
+    if (kend <= kbeg) {
+        for (int r = tid; r < R; r += blockDim.x) a.part_ml[pbase + r] = make_float2(-INFINITY, 0.f);
+        return;
+    }
+    const bf16 *kc = a.kc[b];
+    const bf16 *vc = a.vc[b];
+
+    // ---- stage Q and K (group 0), V (group 1); 16-byte chunk c of row r
+    constexpr int CPR = NB * 8;
+    for (int i = tid; i < 128 * CPR; i += 256) {
+        const int r = i / CPR, c16 = i - r * CPR;
+        const bool ok = r < R;
+        const bf16 *src = a.q + (((size_t)b * R + (ok ? r : 0)) * H + h) * DH + c16 * 8;
+        cp_async16(tc::smem_addr(q_s + (c16 >> 3) * 128 * 128 + tc::sw128(r, c16 & 7)), src,
+                   ok ? 16 : 0);
+    }
+    for (int i = tid; i < kChunk * CPR; i += 256) {
+        const int r = i / CPR, c16 = i - r * CPR;
+        const int key = kbeg + r;
+        const bool ok = key < kend;
+        const size_t off = ((size_t)(ok ? key : kbeg) * H + h) * DH + c16 * 8;
+        cp_async16(tc::smem_addr(kp_s + (c16 >> 3) * kChunk * 128 + tc::sw128(r, c16 & 7)),
+                   kc + off, ok ? 16 : 0);
+    }
+    cp_async_commit();
+    for (int i = tid; i < kChunk * CPR; i += 256) {
+        const int r = i / CPR, c16 = i - r * CPR;
+        const int key = kbeg + r;
+        const bool ok = key < kend;
+        const size_t off = ((size_t)(ok ? key : kbeg) * H + h) * DH + c16 * 8;
+        cp_async16(tc::smem_addr(v_s + (c16 >> 3) * kChunk * 128 + tc::sw128(r, c16 & 7)),
+                   vc + off, ok ? 16 : 0);
+    }
+    cp_async_commit();
+    // this row's ancestor-mask words (only chunks that reach the tree)
+    const bool masked = kend > P || kend - kbeg < kChunk;
+    uint64_t am0 = 0, am1 = 0, am2 = 0, am3 = 0;
+    if (kend > P && row < R) {
+        const int W = (R + 63) / 64;
+        const uint64_t *mr = a.anc_mask + ((size_t)b * R + row) * W;
+        am0 = mr[0];
+        if (W > 1) am1 = mr[1];
+        if (W > 2) am2 = mr[2];
+        if (W > 3) am3 = mr[3];
+    }
+    if (tid == 0) {
+        tc::mbar_init(&bar_s, 1);
+        tc::mbar_init(&bar_o, 1);
+        failed = 0;
+    }
+    if (warp == 0) tc::tmem_alloc(&tmem_holder, 256);
+    cp_async_wait<1>();
+    tc::fence_proxy_async_smem();
+    tc::fence_before_sync();
+    __syncthreads();
+    tc::fence_after_sync();
+    const uint32_t tmem = tmem_holder;
+    const uint32_t t_s = tmem, t_o = tmem + 128;
+
+    // ---- S = Q K^T
+    if (tid == 0) {
+        constexpr uint32_t idesc = tc::idesc_bf16(128, kChunk, 0);
+        for (int ks = 0; ks < DH / 16; ++ks) {
+            const uint32_t off = (ks >> 2) * 128 * 128 + (ks & 3) * 32;
+            const uint64_t ad = tc::sdesc_sw128(tc::smem_addr(q_s) + off, 16, 1024);
+            const uint32_t koff = (ks >> 2) * kChunk * 128 + (ks & 3) * 32;
+            const uint64_t bd = tc::sdesc_sw128(tc::smem_addr(kp_s) + koff, 16, 1024);
+            tc::mma_bf16_ss(t_s, ad, bd, idesc, ks > 0);
+        }
+        tc::mma_commit(&bar_s);
+    }
+    __syncwarp();
+    if (!tc::mbar_wait_bounded(&bar_s, 0, kWaitPolls)) {
+        failed = 1;
+        set_status(a.status, MEDUSA_DEV_TIMEOUT);
+    }
+    tc::fence_after_sync();
+    __syncthreads();
+    const bool ok_s = !failed;
+
+    // ---- softmax over this thread's 64 columns of its row
+    const uint32_t lane_base = (uint32_t)((warp & 3) * 32) << 16;
+    const int c0 = half * HALF;
+    float x[HALF];
+    if (ok_s) {
+        tc::tmem_ld32(t_s + lane_base + c0, *reinterpret_cast<float(*)[32]>(&x[0]));
+        tc::tmem_ld32(t_s + lane_base + c0 + 32, *reinterpret_cast<float(*)[32]>(&x[32]));
+    }
+    float mx[4] = {-INFINITY, -INFINITY, -INFINITY, -INFINITY};
+    if (!masked) {
+#pragma unroll
+        for (int j = 0; j < HALF; ++j) {
+            x[j] *= a.scale_log2;
+            mx[j & 3] = fmaxf(mx[j & 3], x[j]);
+        }
+    } else {
+#pragma unroll
+        for (int j = 0; j < HALF; ++j) {
+            const int key = kbeg + c0 + j;
+            bool vis = key < kend;
+            if (vis && key >= P) {
+                const int t = key - P;
+                const uint64_t mw = (t < 64) ? am0 : (t < 128) ? am1 : (t < 192) ? am2 : am3;
+                vis = (mw >> (t & 63)) & 1u;
+            }
+            x[j] = vis ? x[j] * a.scale_log2 : -INFINITY;
+            mx[j & 3] = fmaxf(mx[j & 3], x[j]);
+        }
+    }
+    xch[half * 128 + row] = fmaxf(fmaxf(mx[0], mx[1]), fmaxf(mx[2], mx[3]));
+    __syncthreads();
+    const float m = fmaxf(xch[row], xch[128 + row]);
+    const float mu = (m == -INFINITY) ? 0.f : m;
+    float ls[4] = {0.f, 0.f, 0.f, 0.f};
+#pragma unroll
+    for (int q8 = 0; q8 < HALF / 8; ++q8) {
+        float p[8];
+#pragma unroll
+        for (int e = 0; e < 8; ++e) {
+            p[e] = exp2f(x[q8 * 8 + e] - mu);
+            ls[e & 3] += p[e];
+        }
+        uint4 w;
+        w.x = pack_bf16(p[0], p[1]);
+        w.y = pack_bf16(p[2], p[3]);
+        w.z = pack_bf16(p[4], p[5]);
+        w.w = pack_bf16(p[6], p[7]);
+        // keys c0 + 8*q8 .. +7: column block `half`, 16-byte chunk q8
+        *reinterpret_cast<uint4 *>(kp_s + half * 128 * 128 + tc::sw128(row, q8)) = w;
+    }
+    const float lpart = (ls[0] + ls[1]) + (ls[2] + ls[3]);
+    cp_async_wait<0>();
+    tc::fence_proxy_async_smem();
+    tc::fence_before_sync();
+    __syncthreads();  // every read of xch (max) is done before it is reused for sums
+    xch[half * 128 + row] = lpart;
+    tc::fence_after_sync();
+
+    // ---- O = P V
+    if (ok_s && tid == 0) {
+        constexpr uint32_t idesc = tc::idesc_bf16(128, DH, 1);
+        for (int ks = 0; ks < kChunk / 16; ++ks) {
+            const uint32_t poff = (ks >> 2) * 128 * 128 + (ks & 3) * 32;
+            const uint64_t ad = tc::sdesc_sw128(tc::smem_addr(kp_s) + poff, 16, 1024);
+            const uint64_t bd =
+                tc::sdesc_sw128(tc::smem_addr(v_s) + ks * 16 * 128, kChunk * 128, 1024);
+            tc::mma_bf16_ss(t_o, ad, bd, idesc, ks > 0);
+        }
+        tc::mma_commit(&bar_o);
+    }
+    __syncwarp();
+    if (ok_s && !tc::mbar_wait_bounded(&bar_o, 0, kWaitPolls)) {
+        failed = 1;
+        set_status(a.status, MEDUSA_DEV_TIMEOUT);
+        tc::mbar_wait_bounded(&bar_o, 0, kWaitPolls);  // let the MMAs drain before freeing TMEM
+    }
+    tc::fence_after_sync();
+    __syncthreads();
+    const bool ok_o = !failed;  // uniform over the CTA: tcgen05.ld is warp-collective
+    if (ok_o) {
+        // this thread's half of the row's DH output columns
+        float ov[32];
+        float *dst = a.part_o + (pbase + row) * DH;
+        for (int c = half * (DH / 2); c < (half + 1) * (DH / 2); c += 32) {
+            tc::tmem_ld32(t_o + lane_base + c, ov);
+            if (row < R) {
+#pragma unroll
+                for (int j = 0; j < 32; j += 4)
+                    *reinterpret_cast<float4 *>(dst + c + j) =
+                        make_float4(ov[j], ov[j + 1], ov[j + 2], ov[j + 3]);
+            }
+        }
+    }
+    if (half == 0 && row < R) {
+        const float l = xch[row] + xch[128 + row];
+        a.part_ml[pbase + row] = ok_o ? make_float2(m, l) : make_float2(-INFINITY, 0.f);
+    }
+    tc::fence_before_sync();
+    __syncthreads();
+    if (warp == 0) tc::tmem_dealloc(tmem, 256);
+}
+
 // One warp per (sequence, row, head).  Lane s reads split s's (m, l), so the
 // weights come from one round of independent loads; the O partials of all
 // splits are then read with independent loads as well (no load waits on
@@ -440,7 +693,8 @@ size_t attention_workspace_bytes(medusa_dtype dtype, int B, int R, int H, int dh
     if (dtype == MEDUSA_F32) return MEDUSA_WS_HEADER;
     int nps, chunk;
     split_plan(B, H, P_max, &nps, &chunk);
-    const size_t rows = (size_t)B * H * (nps + 1) * R;
+    const int NS = R <= 128 ? (P_max + R + kChunk - 1) / kChunk : nps + 1;
+    const size_t rows = (size_t)B * H * NS * R;
     return MEDUSA_WS_HEADER + align256(rows * dh * sizeof(float)) + align256(rows * sizeof(float2));
 }
 
@@ -463,9 +717,11 @@ cudaError_t launch_tree_attention(medusa_dtype dtype, const void *q, const void 
         note_launch();
         return e;
     }
+    const bool use_tc = R <= 128;
     int nps, chunk;
     split_plan(B, H, P_max, &nps, &chunk);
-    const int NS = nps + 1;
+    if (use_tc) nps = (P_max + R + kChunk - 1) / kChunk;  // chunks per head
+    const int NS = use_tc ? nps : nps + 1;
     const size_t rows = (size_t)B * H * NS * R;
     char *w = static_cast<char *>(ws) + MEDUSA_WS_HEADER;
     float *part_o = reinterpret_cast<float *>(w);
@@ -486,20 +742,30 @@ cudaError_t launch_tree_attention(medusa_dtype dtype, const void *q, const void 
     a.part_o = part_o;
     a.part_ml = part_ml;
     a.status = status;
-    const int NW = (R + 15) / 16;
-    const int threads = NW * 32;
-    const size_t smem = (size_t)(NW * 16 + 4 * kTile) * dh * 2 + (size_t)NW * 16 * 4 * sizeof(uint64_t);
-    dim3 grid(NS, H, B);
-    auto kern = tree_attn_split_kernel<128, 8>;
-    if (dh == 128)
-        kern = NW <= 8 ? tree_attn_split_kernel<128, 8> : tree_attn_split_kernel<128, 16>;
-    else
-        kern = NW <= 8 ? tree_attn_split_kernel<64, 8> : tree_attn_split_kernel<64, 16>;
-    if ((e = cudaFuncSetAttribute(kern, cudaFuncAttributeMaxDynamicSharedMemorySize, (int)smem)))
-        return e;
-    e = launch_pdl(kern, grid, dim3(threads), smem, stream, a);
-    note_launch();
-    if (e) return e;
+    if (use_tc) {
+        auto kern = dh == 128 ? tree_attn_tc_kernel<128> : tree_attn_tc_kernel<64>;
+        const int smem = dh == 128 ? TcSmem<128>::TOTAL : TcSmem<64>::TOTAL;
+        if ((e = cudaFuncSetAttribute(kern, cudaFuncAttributeMaxDynamicSharedMemorySize, smem)))
+            return e;
+        e = launch_pdl(kern, dim3(NS, H, B), dim3(256), (size_t)smem, stream, a);
+        note_launch();
+        if (e) return e;
+    } else {
+        const int NW = (R + 15) / 16;
+        const int threads = NW * 32;
+        const size_t smem = (size_t)(NW * 16 + 4 * kTile) * dh * 2 + (size_t)NW * 16 * 4 * sizeof(uint64_t);
+        dim3 grid(NS, H, B);
+        auto kern = tree_attn_split_kernel<128, 8>;
+        if (dh == 128)
+            kern = NW <= 8 ? tree_attn_split_kernel<128, 8> : tree_attn_split_kernel<128, 16>;
+        else
+            kern = NW <= 8 ? tree_attn_split_kernel<64, 8> : tree_attn_split_kernel<64, 16>;
+        if ((e = cudaFuncSetAttribute(kern, cudaFuncAttributeMaxDynamicSharedMemorySize, (int)smem)))
+            return e;
+        e = launch_pdl(kern, grid, dim3(threads), smem, stream, a);
+        note_launch();
+        if (e) return e;
+    }
     const long long items = (long long)B * R * H;
     const int cblocks = (int)((items + 7) / 8);
     e = launch_pdl(dh == 128 ? tree_attn_combine_kernel<128> : tree_attn_combine_kernel<64>,
