@@ -181,6 +181,27 @@ def dist_env():
     return world, rank, local
 
 
+def max_over_ranks(x: float, device=None) -> float:
+    """Largest value of x over all ranks (x itself without a process group)."""
+    import torch
+    import torch.distributed as dist
+    if not (dist.is_available() and dist.is_initialized()) or dist.get_world_size() == 1:
+        return float(x)
+    t = torch.tensor([float(x)], dtype=torch.float64, device=device or "cpu")
+    dist.all_reduce(t, op=dist.ReduceOp.MAX)
+    return float(t.item())
+
+
+def replica_throughput(seconds_per_step: float, bytes_per_step: float, device=None):
+    """Replicas: every rank runs the same step on its own GPU.  The job's time
+    per step is the slowest rank's; the job's throughput counts every rank's
+    bytes.  Returns (slowest seconds per step, aggregate GB/s)."""
+    import torch.distributed as dist
+    world = dist.get_world_size() if dist.is_available() and dist.is_initialized() else 1
+    slowest = max_over_ranks(seconds_per_step, device)
+    return slowest, world * bytes_per_step / slowest / 1e9
+
+
 # -------------------------------------------------------------- reference ---
 
 def run_reference(args, cfg):
@@ -329,14 +350,9 @@ def run_ours(args, cfg):
         per_call["tree"].append(r[1].elapsed_time(r[2]))
         per_call["attention"].append(r[2].elapsed_time(r[3]))
         per_call["posterior"].append(r[3].elapsed_time(r[4]))
-    ms_step = total_ms / args.steps
-    if world > 1:
-        import torch.distributed as dist
-        tt = torch.tensor([ms_step], device=dev)
-        dist.all_reduce(tt, op=dist.ReduceOp.MAX)
-        ms_step = float(tt.item())
     nb = step_bytes(cfg)
-    value = world * nb["total"] / (ms_step * 1e-3) / 1e9
+    s_step, value = replica_throughput(total_ms / args.steps * 1e-3, nb["total"], dev)
+    ms_step = s_step * 1e3
 
     # ---- end to end through the public API with pinned host buffers
     host_in = {
@@ -373,13 +389,7 @@ def run_ours(args, cfg):
     t0 = time.perf_counter()
     for _ in range(e2e_steps):
         e2e_step()
-    e2e_s = (time.perf_counter() - t0) / e2e_steps
-    if world > 1:
-        import torch.distributed as dist
-        tt = torch.tensor([e2e_s], device=dev)
-        dist.all_reduce(tt, op=dist.ReduceOp.MAX)
-        e2e_s = float(tt.item())
-    e2e_value = world * nb["total"] / e2e_s / 1e9
+    e2e_s, e2e_value = replica_throughput((time.perf_counter() - t0) / e2e_steps, nb["total"], dev)
 
     if world > 1:
         import torch.distributed as dist
