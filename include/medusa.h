@@ -10,6 +10,10 @@
  *                                 its own ancestors.
  *   4. medusa_evaluate_posterior  greedy or typical acceptance; the longest
  *                                 accepted path is returned.
+ *   5. medusa_commit_kv           the accepted path's K/V rows move into
+ *                                 consecutive cache slots and the prefix
+ *                                 grows (also fused into the posterior as
+ *                                 medusa_evaluate_posterior_commit).
  * Page citations are by title and section:
  *   [P1] "Medusa: Faster LLM text generation" (nazmi.tech)
  *   [P2] "Medusa 深读：解码慢不是算力问题，是搬运问题" (jokeuncle.pages.dev)
@@ -85,7 +89,11 @@ enum {
     MEDUSA_DEV_BAD_PREFIX = 3,     /* prefix_len[b] < 0 or > P_max            */
     MEDUSA_DEV_BAD_SCORE = 4,      /* a tree score > 0 or NaN                 */
     MEDUSA_DEV_BAD_DEPTH = 5,      /* depth[i] > K or depth[i] != depth[parent]+1 */
-    MEDUSA_DEV_TIMEOUT = 6         /* a bounded wait gave up                  */
+    MEDUSA_DEV_TIMEOUT = 6,        /* a bounded wait gave up                  */
+    MEDUSA_DEV_BAD_PATH = 7,       /* accept_len outside 0..min(K,R-1), or a
+                                      path entry outside [0, R)              */
+    MEDUSA_DEV_BAD_CACHE = 8       /* a cache pointer NULL or not 16-byte
+                                      aligned                                 */
 };
 
 /* Limits. */
@@ -271,6 +279,55 @@ MEDUSA_API medusa_status medusa_evaluate_posterior(medusa_dtype dtype, const voi
                                         int32_t *next_token, int32_t *accept,
                                         void *ws, size_t ws_bytes,
                                         medusa_stream stream);
+
+/* ------------------------------------------------------------------------
+ * 5. Commit of the accepted path into the KV cache.
+ *
+ * [P1] Introduction and [P2] §5: the accepted tokens become part of the
+ * context for the next step, so the K/V the verification pass computed for
+ * them is kept and the rest of the tree is dropped.  With the tree nodes in
+ * cache slots P_b .. P_b+R-1 (canonical order, as medusa_tree_attention
+ * reads them) and the accepted path root -> best of accept_len[b]+1 nodes,
+ * slot P_b + q receives the K and V rows of node path[b][q] for
+ * q = 0 .. accept_len[b], and new_prefix_len[b] = P_b + accept_len[b] + 1.
+ * The next step's root is the posterior's next_token.  Rows are copied as
+ * raw bytes; every source row is read before any target row is written, so
+ * overlapping sources and targets are handled.  Slots past the new prefix
+ * keep stale data.
+ *
+ *   k_cache, v_cache  [B] device arrays of device pointers, each to a
+ *                     sequence's [>= P_b+R, H, dh] dtype cache (16-byte
+ *                     aligned; checked on the device: MEDUSA_DEV_BAD_CACHE)
+ *   prefix_len [B]    int32 P_b >= 0 (device; MEDUSA_DEV_BAD_PREFIX)
+ *   path [B,K+1]      int32 node indices from medusa_evaluate_posterior
+ *   accept_len [B]    int32 0 .. min(K, R-1) (MEDUSA_DEV_BAD_PATH)
+ *   new_prefix_len [B] int32 out; must not alias prefix_len
+ * A sequence that fails a device check is left untouched and gets
+ * new_prefix_len = prefix_len.  Requirements: K <= 8, R <= 256,
+ * H*dh*sizeof(dtype) a multiple of 16.  Needs a workspace of
+ * MEDUSA_WS_HEADER bytes (the status word).
+ * ---------------------------------------------------------------------- */
+MEDUSA_API medusa_status medusa_commit_kv(medusa_dtype dtype, void *const *k_cache,
+                                          void *const *v_cache, const int32_t *prefix_len,
+                                          const int32_t *path, const int32_t *accept_len,
+                                          int B, int K, int R, int H, int dh,
+                                          int32_t *new_prefix_len, void *ws, size_t ws_bytes,
+                                          medusa_stream stream);
+
+/* ------------------------------------------------------------------------
+ * 4+5. Posterior and commit in one call: medusa_evaluate_posterior's
+ * results, then the commit of medusa_commit_kv done by the same kernel that
+ * picks the path (no extra launch).  `dtype` is that of the logits and of
+ * the caches.  Arguments and requirements are the union of the two calls;
+ * the workspace is medusa_posterior_workspace_size(B, R).
+ * ---------------------------------------------------------------------- */
+MEDUSA_API medusa_status medusa_evaluate_posterior_commit(
+    medusa_dtype dtype, const void *logits, const int32_t *tokens, const int32_t *parent,
+    const int32_t *depth, int B, int R, int V, int K, medusa_accept_mode mode, float eps,
+    float delta, float temperature, int32_t *accept_len, int32_t *path, int32_t *path_tokens,
+    int32_t *next_token, int32_t *accept, void *const *k_cache, void *const *v_cache,
+    const int32_t *prefix_len, int H, int dh, int32_t *new_prefix_len, void *ws,
+    size_t ws_bytes, medusa_stream stream);
 
 #ifdef __cplusplus
 }

@@ -7,9 +7,9 @@ current CUDA stream, allocates outputs and workspaces with torch, and raises
 the compiled library is missing, importing the calls fails loudly.
 
 Public calls (same names as the C ABI in include/medusa.h):
-    heads, build_tree, tree_attention, evaluate_posterior
-plus workspace-size queries, device-status helpers, launch_count, and the
-``MedusaStep`` object that chains the four calls for one decoding step.
+    heads, heads_noalloc, build_tree, tree_attention, evaluate_posterior,
+    commit_kv, evaluate_posterior_commit
+plus workspace-size queries, device-status helpers and launch_count.
 """
 from __future__ import annotations
 
@@ -34,14 +34,15 @@ STATUS = {0: "MEDUSA_OK", 1: "MEDUSA_ERR_INVALID_ARG", 2: "MEDUSA_ERR_UNSUPPORTE
           3: "MEDUSA_ERR_WORKSPACE", 4: "MEDUSA_ERR_CUDA", 5: "MEDUSA_ERR_TIMEOUT",
           6: "MEDUSA_ERR_DEVICE_CHECK"}
 DEVICE_STATUS = {0: "ok", 1: "bad token", 2: "bad parent", 3: "bad prefix", 4: "bad score",
-                 5: "bad depth", 6: "timeout"}
+                 5: "bad depth", 6: "timeout", 7: "bad path", 8: "bad cache"}
 
 EXPORTS = ("medusa_status_string", "medusa_last_error", "medusa_launch_count",
            "medusa_read_device_status", "medusa_clear_device_status",
            "medusa_heads_workspace_size", "medusa_heads",
            "medusa_build_tree_workspace_size", "medusa_build_tree",
            "medusa_tree_attention_workspace_size", "medusa_tree_attention",
-           "medusa_posterior_workspace_size", "medusa_evaluate_posterior")
+           "medusa_posterior_workspace_size", "medusa_evaluate_posterior",
+           "medusa_evaluate_posterior_commit", "medusa_commit_kv")
 
 
 class MedusaError(RuntimeError):
@@ -78,6 +79,9 @@ def lib() -> ctypes.CDLL:
         "medusa_tree_attention": ([I, P, P, P, P, I, P, I, I, I, I, F, P, P, S, P], I),
         "medusa_posterior_workspace_size": ([I, I], S),
         "medusa_evaluate_posterior": ([I, P, P, P, P, I, I, I, I, I, F, F, F, P, P, P, P, P, P, S, P], I),
+        "medusa_evaluate_posterior_commit": ([I, P, P, P, P, I, I, I, I, I, F, F, F, P, P, P, P, P,
+                                              P, P, P, I, I, P, P, S, P], I),
+        "medusa_commit_kv": ([I, P, P, P, P, P, I, I, I, I, I, P, P, S, P], I),
     }
     for name, (args, res) in sig.items():
         fn = getattr(L, name)
@@ -296,3 +300,44 @@ def evaluate_posterior(logits, tokens, parent, depth, K: int, mode: int = GREEDY
                                            _ptr(o.path), _ptr(o.path_tokens), _ptr(o.next_token),
                                            _ptr(o.accept), _ptr(ws), ws.numel(), _stream(stream)))
     return o
+
+
+def evaluate_posterior_commit(logits, tokens, parent, depth, K: int, k_ptrs, v_ptrs, prefix_len,
+                              H: int, dh: int, new_prefix_len=None, mode: int = GREEDY, eps=0.09,
+                              delta=0.3, temperature=1.0, ws=None,
+                              out: Optional[Posterior] = None, with_accept: bool = True,
+                              stream=None):
+    """evaluate_posterior, then the commit of commit_kv in the same kernel.
+    The caches hold logits.dtype elements.  Returns (Posterior, new_prefix_len)."""
+    _need(logits, "logits")
+    B, R, V = logits.shape
+    if ws is None:
+        ws = new_workspace(posterior_workspace_size(B, R), logits.device)
+    o = out or Posterior.empty(B, R, K, logits.device, with_accept)
+    if new_prefix_len is None:
+        new_prefix_len = torch.empty((B,), dtype=torch.int32, device=logits.device)
+    _check(lib().medusa_evaluate_posterior_commit(
+        _dtype(logits), _ptr(logits), _ptr(tokens), _ptr(parent), _ptr(depth), B, R, V, K,
+        int(mode), float(eps), float(delta), float(temperature), _ptr(o.accept_len), _ptr(o.path),
+        _ptr(o.path_tokens), _ptr(o.next_token), _ptr(o.accept), _ptr(k_ptrs), _ptr(v_ptrs),
+        _ptr(prefix_len), int(H), int(dh), _ptr(new_prefix_len), _ptr(ws), ws.numel(),
+        _stream(stream)))
+    return o, new_prefix_len
+
+
+# ----------------------------------------------------------------- commit ---
+
+def commit_kv(dtype: int, k_ptrs, v_ptrs, prefix_len, path, accept_len, R: int, H: int, dh: int,
+              new_prefix_len=None, ws=None, stream=None):
+    """Move the accepted path's K/V rows into slots P_b..P_b+L (in place in the
+    caches behind k_ptrs/v_ptrs); return new_prefix_len = P_b + L + 1."""
+    B, K1 = path.shape
+    dev = path.device
+    if ws is None:
+        ws = new_workspace(WS_HEADER, dev)
+    if new_prefix_len is None:
+        new_prefix_len = torch.empty((B,), dtype=torch.int32, device=dev)
+    _check(lib().medusa_commit_kv(int(dtype), _ptr(k_ptrs), _ptr(v_ptrs), _ptr(prefix_len),
+                                  _ptr(path), _ptr(accept_len), B, K1 - 1, int(R), int(H), int(dh),
+                                  _ptr(new_prefix_len), _ptr(ws), ws.numel(), _stream(stream)))
+    return new_prefix_len

@@ -235,15 +235,16 @@ size_t medusa_posterior_workspace_size(int B, int R) {
     return posterior_workspace_bytes(B, R);
 }
 
-medusa_status medusa_evaluate_posterior(medusa_dtype dtype, const void *logits,
-                                        const int32_t *tokens, const int32_t *parent,
-                                        const int32_t *depth, int B, int R, int V, int K,
-                                        medusa_accept_mode mode, float eps, float delta,
-                                        float temperature, int32_t *accept_len, int32_t *path,
-                                        int32_t *path_tokens, int32_t *next_token,
-                                        int32_t *accept, void *ws, size_t ws_bytes,
-                                        medusa_stream stream) {
-    const char *who = "medusa_evaluate_posterior";
+}  // extern "C"
+
+namespace {
+
+medusa_status check_posterior(const char *who, medusa_dtype dtype, const void *logits,
+                              const int32_t *tokens, const int32_t *parent, const int32_t *depth,
+                              int B, int R, int V, int K, medusa_accept_mode mode, float eps,
+                              float delta, float temperature, const int32_t *accept_len,
+                              const int32_t *path, const int32_t *path_tokens,
+                              const int32_t *next_token, const void *ws, size_t ws_bytes) {
     if (dtype != MEDUSA_F32 && dtype != MEDUSA_BF16)
         return fail(MEDUSA_ERR_INVALID_ARG, "%s: unknown dtype %d", who, (int)dtype);
     if (mode != MEDUSA_GREEDY && mode != MEDUSA_TYPICAL)
@@ -263,10 +264,99 @@ medusa_status medusa_evaluate_posterior(medusa_dtype dtype, const void *logits,
         return fail(MEDUSA_ERR_INVALID_ARG, "%s: eps, delta and temperature must be > 0", who);
     if (!aligned16(logits))
         return fail(MEDUSA_ERR_INVALID_ARG, "%s: logits must be 16-byte aligned", who);
-    if (medusa_status s = check_ws(ws, ws_bytes, posterior_workspace_bytes(B, R), who)) return s;
+    return check_ws(ws, ws_bytes, posterior_workspace_bytes(B, R), who);
+}
+
+// Host checks of the commit arguments shared by both commit entry points.
+medusa_status check_commit(const char *who, medusa_dtype dtype, const void *const *k_cache,
+                           const void *const *v_cache, const int32_t *prefix_len,
+                           const int32_t *new_prefix_len, int H, int dh) {
+    if (dtype != MEDUSA_F32 && dtype != MEDUSA_BF16)
+        return fail(MEDUSA_ERR_INVALID_ARG, "%s: unknown dtype %d", who, (int)dtype);
+    if (!k_cache || !v_cache || !prefix_len || !new_prefix_len)
+        return fail(MEDUSA_ERR_INVALID_ARG, "%s: NULL pointer", who);
+    if (static_cast<const void *>(new_prefix_len) == static_cast<const void *>(prefix_len))
+        return fail(MEDUSA_ERR_INVALID_ARG, "%s: new_prefix_len must not alias prefix_len", who);
+    if (!aligned16(k_cache) || !aligned16(v_cache))
+        return fail(MEDUSA_ERR_INVALID_ARG, "%s: cache pointer arrays must be 16-byte aligned", who);
+    const size_t elt = dtype == MEDUSA_BF16 ? 2 : 4;
+    if (H < 1 || dh < 1 || (long long)H * dh > (1LL << 26))
+        return fail(MEDUSA_ERR_INVALID_ARG, "%s: H=%d dh=%d", who, H, dh);
+    if (((size_t)H * dh * elt) % 16)
+        return fail(MEDUSA_ERR_INVALID_ARG, "%s: a cache row (H*dh elements) must be a multiple of 16 bytes",
+                    who);
+    return MEDUSA_OK;
+}
+
+}  // namespace
+
+extern "C" {
+
+medusa_status medusa_evaluate_posterior(medusa_dtype dtype, const void *logits,
+                                        const int32_t *tokens, const int32_t *parent,
+                                        const int32_t *depth, int B, int R, int V, int K,
+                                        medusa_accept_mode mode, float eps, float delta,
+                                        float temperature, int32_t *accept_len, int32_t *path,
+                                        int32_t *path_tokens, int32_t *next_token,
+                                        int32_t *accept, void *ws, size_t ws_bytes,
+                                        medusa_stream stream) {
+    const char *who = "medusa_evaluate_posterior";
+    if (medusa_status s = check_posterior(who, dtype, logits, tokens, parent, depth, B, R, V, K,
+                                          mode, eps, delta, temperature, accept_len, path,
+                                          path_tokens, next_token, ws, ws_bytes))
+        return s;
     cudaError_t e = launch_posterior(dtype, logits, tokens, parent, depth, B, R, V, K, mode, eps,
                                      delta, temperature, accept_len, path, path_tokens, next_token,
-                                     accept, ws, static_cast<cudaStream_t>(stream));
+                                     accept, nullptr, nullptr, nullptr, 0, 0, nullptr, ws,
+                                     static_cast<cudaStream_t>(stream));
+    if (e) return cuda_fail(e, who);
+    return MEDUSA_OK;
+}
+
+medusa_status medusa_evaluate_posterior_commit(
+    medusa_dtype dtype, const void *logits, const int32_t *tokens, const int32_t *parent,
+    const int32_t *depth, int B, int R, int V, int K, medusa_accept_mode mode, float eps,
+    float delta, float temperature, int32_t *accept_len, int32_t *path, int32_t *path_tokens,
+    int32_t *next_token, int32_t *accept, void *const *k_cache, void *const *v_cache,
+    const int32_t *prefix_len, int H, int dh, int32_t *new_prefix_len, void *ws,
+    size_t ws_bytes, medusa_stream stream) {
+    const char *who = "medusa_evaluate_posterior_commit";
+    if (medusa_status s = check_posterior(who, dtype, logits, tokens, parent, depth, B, R, V, K,
+                                          mode, eps, delta, temperature, accept_len, path,
+                                          path_tokens, next_token, ws, ws_bytes))
+        return s;
+    if (medusa_status s = check_commit(who, dtype, k_cache, v_cache, prefix_len, new_prefix_len,
+                                       H, dh))
+        return s;
+    cudaError_t e = launch_posterior(dtype, logits, tokens, parent, depth, B, R, V, K, mode, eps,
+                                     delta, temperature, accept_len, path, path_tokens, next_token,
+                                     accept, k_cache, v_cache, prefix_len, H, dh, new_prefix_len,
+                                     ws, static_cast<cudaStream_t>(stream));
+    if (e) return cuda_fail(e, who);
+    return MEDUSA_OK;
+}
+
+// ---------------------------------------------------------------- commit ---
+
+medusa_status medusa_commit_kv(medusa_dtype dtype, void *const *k_cache, void *const *v_cache,
+                               const int32_t *prefix_len, const int32_t *path,
+                               const int32_t *accept_len, int B, int K, int R, int H, int dh,
+                               int32_t *new_prefix_len, void *ws, size_t ws_bytes,
+                               medusa_stream stream) {
+    const char *who = "medusa_commit_kv";
+    if (medusa_status s = check_commit(who, dtype, k_cache, v_cache, prefix_len, new_prefix_len,
+                                       H, dh))
+        return s;
+    if (!path || !accept_len) return fail(MEDUSA_ERR_INVALID_ARG, "%s: NULL pointer", who);
+    if (B < 1) return fail(MEDUSA_ERR_INVALID_ARG, "%s: B=%d", who, B);
+    if (K < 0 || K > MEDUSA_MAX_HEADS)
+        return fail(MEDUSA_ERR_INVALID_ARG, "%s: K=%d outside 0..%d", who, K, MEDUSA_MAX_HEADS);
+    if (R < 1 || R > MEDUSA_MAX_TREE_ROWS)
+        return fail(MEDUSA_ERR_INVALID_ARG, "%s: R=%d outside 1..%d", who, R, MEDUSA_MAX_TREE_ROWS);
+    if (medusa_status s = check_ws(ws, ws_bytes, MEDUSA_WS_HEADER, who)) return s;
+    cudaError_t e = launch_commit_kv(dtype == MEDUSA_BF16 ? 2 : 4, k_cache, v_cache, prefix_len,
+                                     path, accept_len, B, K, R, H, dh, new_prefix_len, ws,
+                                     static_cast<cudaStream_t>(stream));
     if (e) return cuda_fail(e, who);
     return MEDUSA_OK;
 }

@@ -83,6 +83,14 @@ __device__ __forceinline__ unsigned swz(int row, int ch) {
     return row * (DH * 2) + ((ch ^ (row & 7)) << 4);
 }
 
+// A sequence's cache pointers are read on the device, so their checks run
+// there: NULL or not 16-byte aligned -> MEDUSA_DEV_BAD_CACHE, and the
+// sequence's output is zero.
+__device__ __forceinline__ bool cache_pointers_bad(const void *kc, const void *vc) {
+    return !kc || !vc ||
+           ((reinterpret_cast<uintptr_t>(kc) | reinterpret_cast<uintptr_t>(vc)) & 15u) != 0;
+}
+
 struct AttnArgs {
     const bf16 *q;
     const bf16 *const *kc;
@@ -123,15 +131,16 @@ __global__ void __launch_bounds__(MAXW * 32, 1) tree_attn_split_kernel(AttnArgs 
     const int kbeg = tree_split ? P : sp * a.chunk;
     const int kend = tree_split ? P + R : min((sp + 1) * a.chunk, P);
     const size_t pbase = ((size_t)(b * H + h) * NS + sp) * R;
+    const bf16 *kc = a.kc[b];
+    const bf16 *vc = a.vc[b];
+    const bool bad_cache = cache_pointers_bad(kc, vc);
+    if (bad_cache) set_status(a.status, MEDUSA_DEV_BAD_CACHE);
 
-    if (kend <= kbeg) {
+    if (kend <= kbeg || bad_cache) {
         for (int r = tid; r < R; r += blockDim.x)
             a.part_ml[pbase + r] = make_float2(-INFINITY, 0.f);
         return;
     }
-
-    const bf16 *kc = a.kc[b];
-    const bf16 *vc = a.vc[b];
 
     // stage Q (rows >= R zero-filled)
     for (int i = tid; i < QROWS * CPR; i += blockDim.x) {
@@ -368,12 +377,14 @@ __global__ void __launch_bounds__(256, 2) tree_attn_tc_kernel(AttnArgs a) {
     const size_t pbase = ((size_t)(b * H + h) * NS + chunk) * R;
     const int kbeg = chunk * kChunk;
     const int kend = min(kbeg + kChunk, P + R);
-    if (kend <= kbeg) {
+    const bf16 *kc = a.kc[b];
+    const bf16 *vc = a.vc[b];
+    const bool bad_cache = cache_pointers_bad(kc, vc);
+    if (bad_cache) set_status(a.status, MEDUSA_DEV_BAD_CACHE);
+    if (kend <= kbeg || bad_cache) {
         for (int r = tid; r < R; r += blockDim.x) a.part_ml[pbase + r] = make_float2(-INFINITY, 0.f);
         return;
     }
-    const bf16 *kc = a.kc[b];
-    const bf16 *vc = a.vc[b];
 
     // ---- stage Q and K (group 0), V (group 1); 16-byte chunk c of row r
     constexpr int CPR = NB * 8;
@@ -626,6 +637,12 @@ tree_attn_f32_kernel(const float *__restrict__ q, const float *const *kcs, const
     float *sc = fsm + dh;
     const float *kc = kcs[b];
     const float *vc = vcs[b];
+    if (cache_pointers_bad(kc, vc)) {  // uniform over the CTA
+        set_status(status, MEDUSA_DEV_BAD_CACHE);
+        for (int c = threadIdx.x; c < dh; c += blockDim.x)
+            out[(((size_t)b * R + i) * H + h) * dh + c] = 0.f;
+        return;
+    }
     const int W = (R + 63) / 64;
     const uint64_t *mrow = anc_mask + ((size_t)b * R + i) * W;
     for (int c = threadIdx.x; c < dh; c += blockDim.x) qs[c] = q[(((size_t)b * R + i) * H + h) * dh + c];

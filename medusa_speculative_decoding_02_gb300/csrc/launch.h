@@ -58,6 +58,14 @@ cudaError_t launch_posterior(medusa_dtype dtype, const void *logits, const int32
                              int K, medusa_accept_mode mode, float eps, float delta,
                              float temperature, int32_t *accept_len, int32_t *path,
                              int32_t *path_tokens, int32_t *next_token, int32_t *accept,
+                             void *const *k_cache, void *const *v_cache,
+                             const int32_t *prefix_len, int H, int dh, int32_t *new_prefix_len,
                              void *ws, cudaStream_t stream);
+
+// k_cache == nullptr in launch_posterior: no commit.  elt = bytes per element.
+cudaError_t launch_commit_kv(size_t elt, void *const *k_cache, void *const *v_cache,
+                             const int32_t *prefix_len, const int32_t *path,
+                             const int32_t *accept_len, int B, int K, int R, int H, int dh,
+                             int32_t *new_prefix_len, void *ws, cudaStream_t stream);
 
 }  // namespace medusa

@@ -24,6 +24,7 @@
 #include <algorithm>
 #include <climits>
 
+#include "commit.cuh"
 #include "common.cuh"
 #include "launch.h"
 
@@ -200,7 +201,7 @@ posterior_select_kernel(const T *__restrict__ logits, const int32_t *__restrict_
                         float y_scale, float log2_eps, float log2_delta,
                         int32_t *__restrict__ accept_len, int32_t *__restrict__ path,
                         int32_t *__restrict__ path_tokens, int32_t *__restrict__ next_token,
-                        int32_t *__restrict__ accept_out, int *status) {
+                        int32_t *__restrict__ accept_out, CommitArgs ca, int *status) {
     pdl_enter();
     __shared__ int s_acc[MEDUSA_MAX_TREE_ROWS];
     __shared__ int s_chain[MEDUSA_MAX_TREE_ROWS];
@@ -208,6 +209,8 @@ posterior_select_kernel(const T *__restrict__ logits, const int32_t *__restrict_
     __shared__ int s_dep[MEDUSA_MAX_TREE_ROWS];
     __shared__ int s_tok[MEDUSA_MAX_TREE_ROWS];
     __shared__ int s_L, s_best;
+    __shared__ int s_path[MEDUSA_MAX_HEADS + 1];
+    __shared__ int s_code;
     const int b = blockIdx.x;
     const int i = threadIdx.x;
     if (i == 0) {
@@ -275,6 +278,7 @@ posterior_select_kernel(const T *__restrict__ logits, const int32_t *__restrict_
     if (i <= K) {
         path[(size_t)b * (K + 1) + i] = -1;
         path_tokens[(size_t)b * (K + 1) + i] = -1;
+        s_path[i] = -1;
     }
     __syncthreads();
     if (i == 0) {
@@ -283,14 +287,30 @@ posterior_select_kernel(const T *__restrict__ logits, const int32_t *__restrict_
         for (int x = best, q = L; x >= 0 && q >= 0; x = s_par[x], --q) {
             path[(size_t)b * (K + 1) + q] = x;
             path_tokens[(size_t)b * (K + 1) + q] = s_tok[x];
+            s_path[q] = x;
             if (x == 0) break;
         }
+        s_L = L;
         accept_len[b] = L;
         int arg;
         float m2, log2s, H;
         row_stats(parts + ((size_t)b * R + best) * splits, splits, false, arg, m2, log2s, H);
         next_token[b] = arg;
     }
+    if (!ca.k_cache) return;  // uniform over the CTA
+    // commit of the accepted path into the KV cache (medusa_commit_kv)
+    __syncthreads();
+    void *kc = ca.k_cache[b];
+    void *vc = ca.v_cache[b];
+    const int P = ca.prefix_len[b];
+    if (i == 0) {
+        s_code = commit_check(kc, vc, P, s_path, s_L, K, R);
+        if (s_code != MEDUSA_DEV_OK) set_status(status, s_code);
+        ca.new_prefix_len[b] = s_code == MEDUSA_DEV_OK ? P + s_L + 1 : P;
+    }
+    __syncthreads();
+    if (s_code != MEDUSA_DEV_OK) return;
+    commit_columns(kc, vc, P, s_path, s_L, ca.row_vecs, i, blockDim.x);
 }
 
 // Slices per logits row: enough CTAs for two per SM on 152 SMs, at most 8.
@@ -304,7 +324,8 @@ cudaError_t run_posterior(const void *logits, const int32_t *tokens, const int32
                           const int32_t *depth, int B, int R, int V, int K, bool typical,
                           float eps, float delta, float temperature, int32_t *accept_len,
                           int32_t *path, int32_t *path_tokens, int32_t *next_token,
-                          int32_t *accept, void *ws, cudaStream_t stream) {
+                          int32_t *accept, const CommitArgs &commit, void *ws,
+                          cudaStream_t stream) {
     int *status = static_cast<int *>(ws);
     RowPart *parts = reinterpret_cast<RowPart *>(static_cast<char *>(ws) + MEDUSA_WS_HEADER);
     const T *lg = static_cast<const T *>(logits);
@@ -318,7 +339,7 @@ cudaError_t run_posterior(const void *logits, const int32_t *tokens, const int32
     e = launch_pdl(posterior_select_kernel<T>, dim3(B), dim3(kSelectThreads), 0, stream, lg, tokens,
                    parent, depth, static_cast<const RowPart *>(parts), splits, R, V, K,
                    typical ? 1 : 0, y_scale, log2f(eps), log2f(delta), accept_len, path,
-                   path_tokens, next_token, accept, status);
+                   path_tokens, next_token, accept, commit, status);
     note_launch();
     return e;
 }
@@ -334,15 +355,24 @@ cudaError_t launch_posterior(medusa_dtype dtype, const void *logits, const int32
                              int K, medusa_accept_mode mode, float eps, float delta,
                              float temperature, int32_t *accept_len, int32_t *path,
                              int32_t *path_tokens, int32_t *next_token, int32_t *accept,
+                             void *const *k_cache, void *const *v_cache,
+                             const int32_t *prefix_len, int H, int dh, int32_t *new_prefix_len,
                              void *ws, cudaStream_t stream) {
     const bool typical = mode == MEDUSA_TYPICAL;
+    const size_t elt = dtype == MEDUSA_BF16 ? 2 : 4;
+    CommitArgs commit;
+    commit.k_cache = k_cache;  // nullptr: no commit
+    commit.v_cache = v_cache;
+    commit.prefix_len = prefix_len;
+    commit.new_prefix_len = new_prefix_len;
+    commit.row_vecs = k_cache ? (int)((size_t)H * dh * elt / 16) : 0;
     if (dtype == MEDUSA_BF16)
         return run_posterior<bf16>(logits, tokens, parent, depth, B, R, V, K, typical, eps, delta,
                                    temperature, accept_len, path, path_tokens, next_token, accept,
-                                   ws, stream);
+                                   commit, ws, stream);
     return run_posterior<float>(logits, tokens, parent, depth, B, R, V, K, typical, eps, delta,
-                                temperature, accept_len, path, path_tokens, next_token, accept, ws,
-                                stream);
+                                temperature, accept_len, path, path_tokens, next_token, accept,
+                                commit, ws, stream);
 }
 
 }  // namespace medusa

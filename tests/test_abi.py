@@ -130,6 +130,51 @@ def test_posterior_rejects(L, kw, code):
     assert L.medusa_launch_count() == before
 
 
+A2 = P(8192)         # a second fake address, for the no-alias rule
+
+
+def _commit(L, **kw):
+    a = dict(dtype=m.BF16, k=A, v=A, pl=A, path=A, al=A, B=1, K=5, R=65, H=32, dh=128, npl=A2,
+             ws=WS, ws_bytes=256)
+    a.update(kw)
+    return L.medusa_commit_kv(a["dtype"], a["k"], a["v"], a["pl"], a["path"], a["al"], a["B"],
+                              a["K"], a["R"], a["H"], a["dh"], a["npl"], a["ws"], a["ws_bytes"],
+                              None)
+
+
+@pytest.mark.parametrize("kw,code", [
+    (dict(dtype=5), 1), (dict(k=None), 1), (dict(v=None), 1), (dict(path=None), 1),
+    (dict(al=None), 1), (dict(npl=None), 1), (dict(npl=A), 1), (dict(k=MISALIGNED), 1),
+    (dict(B=0), 1), (dict(K=9), 1), (dict(K=-1), 1), (dict(R=0), 1), (dict(R=257), 1),
+    (dict(H=0), 1), (dict(H=1, dh=7), 1), (dict(dtype=m.F32, H=1, dh=2), 1), (dict(ws=None), 3),
+    (dict(ws_bytes=255), 3)])
+def test_commit_rejects(L, kw, code):
+    before = L.medusa_launch_count()
+    assert _commit(L, **kw) == code
+    assert L.medusa_launch_count() == before
+    assert L.medusa_last_error().decode()
+
+
+def _post_commit(L, **kw):
+    a = dict(dtype=m.BF16, logits=A, B=1, R=65, V=32000, K=5, mode=m.GREEDY, k=A, v=A, pl=A, H=32,
+             dh=128, npl=A2, ws=WS, ws_bytes=1 << 20)
+    a.update(kw)
+    f = ctypes.c_float
+    return L.medusa_evaluate_posterior_commit(
+        a["dtype"], a["logits"], A, A, A, a["B"], a["R"], a["V"], a["K"], a["mode"], f(0.09),
+        f(0.3), f(1.0), A, A, A, A, None, a["k"], a["v"], a["pl"], a["H"], a["dh"], a["npl"],
+        a["ws"], a["ws_bytes"], None)
+
+
+@pytest.mark.parametrize("kw,code", [
+    (dict(V=32001), 1), (dict(K=9), 1), (dict(k=None), 1), (dict(pl=None), 1), (dict(npl=A), 1),
+    (dict(H=1, dh=4), 1), (dict(v=MISALIGNED), 1), (dict(ws_bytes=64), 3)])
+def test_posterior_commit_rejects(L, kw, code):
+    before = L.medusa_launch_count()
+    assert _post_commit(L, **kw) == code
+    assert L.medusa_launch_count() == before
+
+
 def test_workspace_sizes(L):
     hs = m.heads_workspace_size(1, 5, 4096, 32000, 4)
     assert hs >= 256 + 5 * 4096 * 4
