@@ -354,6 +354,57 @@ def run_ours(args, cfg):
     s_step, value = replica_throughput(total_ms / args.steps * 1e-3, nb["total"], dev)
     ms_step = s_step * 1e3
 
+    # ---- Region 3: the KV-cache commit (a row past the step proper), alone
+    # and fused into the posterior, each timed over a loop with events at the
+    # two ends.  The commit moves the accepted path's rows inside the tree
+    # slots; new_prefix_len goes to its own buffer, so every repetition sees
+    # the same prefix.
+    new_prefix = torch.empty_like(prefix)
+    row_bytes = cfg.H * cfg.dh * 2
+    path_np = post.path.cpu().numpy()
+    moved = int(sum(1 for b in range(B) for qq in range(int(post.accept_len[b]) + 1)
+                    if path_np[b, qq] != qq))
+    commit_bytes = 2 * 2 * moved * row_bytes  # K and V, each row read once and written once
+    reps = max(args.steps, 20)
+
+    def timed_loop(fn):
+        for _ in range(3):
+            fn()
+        a, z = torch.cuda.Event(enable_timing=True), torch.cuda.Event(enable_timing=True)
+        torch.cuda.synchronize(dev)
+        a.record(stream)
+        for _ in range(reps):
+            fn()
+        z.record(stream)
+        torch.cuda.synchronize(dev)
+        return a.elapsed_time(z) / reps * 1e3  # microseconds
+
+    def post_only():
+        m.evaluate_posterior(logits, tree.tokens, tree.parent, tree.depth, K, mode, cfg.eps,
+                             cfg.delta, cfg.temperature, ws=ws, out=post)
+
+    def post_commit():
+        m.evaluate_posterior_commit(logits, tree.tokens, tree.parent, tree.depth, K, kptr, vptr,
+                                    prefix, cfg.H, cfg.dh, new_prefix_len=new_prefix, mode=mode,
+                                    eps=cfg.eps, delta=cfg.delta, temperature=cfg.temperature,
+                                    ws=ws, out=post)
+
+    def commit_only():
+        m.commit_kv(m.BF16, kptr, vptr, prefix, post.path, post.accept_len, R, cfg.H, cfg.dh,
+                    new_prefix_len=new_prefix, ws=ws)
+
+    us_post = timed_loop(post_only)
+    us_post_commit = timed_loop(post_commit)
+    us_commit = timed_loop(commit_only)
+    if m.read_device_status(ws) != 0:
+        raise RuntimeError("device status set by the commit")
+    next_rows = {"commit_kv": {
+        "us": round(us_commit, 2), "rows_moved": moved, "bytes": commit_bytes,
+        "GB/s": round(commit_bytes / (us_commit * 1e-6) / 1e9, 1),
+        "fused_posterior_commit_us": round(us_post_commit, 2),
+        "posterior_alone_us": round(us_post, 2),
+        "note": "launch-latency bound: a few hundred KB per step"}}
+
     # ---- end to end through the public API with pinned host buffers
     host_in = {
         "h": torch.from_numpy(np.ascontiguousarray(hi.h).view(np.int16)).view(torch.bfloat16).pin_memory(),
@@ -440,6 +491,7 @@ def run_ours(args, cfg):
                    "bytes_per_step": int(nb["total"]), "parallelism": f"replicas{world}",
                    "l2": "inputs larger than L2: 1.50 GB of weights, KV and logits per step"},
         "stages": stages,
+        "next_rows": next_rows,
         "roofline": roofline,
         "cpu_baseline": {"value": round(cpu_value, 4), "unit": UNIT, "cores": 1, "kind": "oracle",
                          "sample": f"{len(cpu_secs)} full oracle steps of the same workload "
