@@ -51,6 +51,8 @@ def _load():
             D = ctypes.c_double
             lib.oracle_heads.argtypes = [I, P, P, P, P, I, I, I, I, I, P, P, P, P]
             lib.oracle_heads.restype = I
+            lib.oracle_lm_head.argtypes = [I, P, P, I, I, I, I, P, P, P, P]
+            lib.oracle_lm_head.restype = I
             lib.oracle_build_tree.argtypes = [P, P, P, I, I, P, I, I, P, P, P, P, P, P, P, P, P]
             lib.oracle_build_tree.restype = I
             lib.oracle_tree_attention.argtypes = [I, P, P, P, P, P, I, I, I, I, D, P]
@@ -110,6 +112,30 @@ def heads(h, W1, b1, W2, top_s: int, want_logits: bool = False):
     rc = lib.oracle_heads(dt, _ptr(h), _ptr(W1), _ptr(b1), _ptr(W2), B, d, V, K, top_s,
                           _ptr(ids), _ptr(logp), _ptr(logits), _ptr(logz))
     _check(rc, "heads")
+    return ids, logp, logits, logz
+
+
+def lm_head(h, W_lm, top_s: int = 1, want_logits: bool = False):
+    """The base model's LM head on h: top-s ids and log-probs per sequence;
+    entry 0 is the greedy root token.
+
+    h [B,d], W_lm [V,d], float32 or bf16 bits.  Returns (ids int32 [B,s],
+    logp float64 [B,s], logits [B,V] or None, logz [B]).
+    """
+    lib = _load()
+    h, W_lm = _c(h), _c(W_lm)
+    dt = _dt(h)
+    if _dt(W_lm) != dt:
+        raise TypeError("mixed dtypes")
+    B, d = h.shape
+    V = W_lm.shape[0]
+    ids = np.zeros((B, top_s), np.int32)
+    logp = np.zeros((B, top_s), np.float64)
+    logits = np.zeros((B, V), np.float64) if want_logits else None
+    logz = np.zeros(B, np.float64)
+    rc = lib.oracle_lm_head(dt, _ptr(h), _ptr(W_lm), B, d, V, top_s, _ptr(ids), _ptr(logp),
+                            _ptr(logits), _ptr(logz))
+    _check(rc, "lm_head")
     return ids, logp, logits, logz
 
 

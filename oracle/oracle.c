@@ -30,6 +30,9 @@
  *   oracle_heads              pinned (identity-initialised heads reproduce
  *                             the LM-head softmax; numpy float64 matmul +
  *                             closed-form softmax on tiny sizes)
+ *   oracle_lm_head            pinned (equals oracle_heads with W1 = 0, b1 = 0,
+ *                             W2 = W_lm; hand-built one-hot rows give
+ *                             closed-form logits and log Z)
  *   oracle_build_tree         pinned (worked example of [P2] §6.2; node-count
  *                             closed form of [P2] §6.1; brute-force optimality)
  *   oracle_tree_attention     pinned (per-path causal attention via torch
@@ -140,6 +143,65 @@ int oracle_heads(int dtype, const void *h, const void *W1, const void *b1,
         }
     }
     free(z); free(lg); free(taken);
+    return 0;
+}
+
+/* ------------------------------------------------------------------------ */
+/* O1'. The base model's LM head on the same hidden state.                   */
+/*                                                                            */
+/* [P1] Introduction and [P3] (the heads and the LM head read one final      */
+/* hidden state h): logits = W_lm h, no residual block, no bias.  [P2] §5:   */
+/* the LM head's greedy token is the root of the candidate tree, accepted    */
+/* unconditionally.  Outputs, per sequence: the top-s tokens (larger logit   */
+/* first, equal logits -> smaller id first), their log-probabilities under   */
+/* softmax(logits); entry 0 is the greedy root token.                        */
+/*                                                                            */
+/* h [B][d], W_lm [V][d].  topk_ids/topk_logp [B][s]; optional logits_out    */
+/* [B][V] and logz_out [B].                                                  */
+/* ------------------------------------------------------------------------ */
+int oracle_lm_head(int dtype, const void *h, const void *W_lm, int B, int d,
+                   int V, int s, int32_t *topk_ids, double *topk_logp,
+                   double *logits_out, double *logz_out)
+{
+    if (B < 1 || d < 1 || V < 1 || s < 1 || s > V)
+        return 1;
+    double *lg = (double *)malloc((size_t)V * sizeof(double));
+    char *taken = (char *)malloc((size_t)V);
+    if (!lg || !taken) {
+        free(lg); free(taken);
+        return 2;
+    }
+    for (int b = 0; b < B; ++b) {
+        for (int v = 0; v < V; ++v) {
+            double acc = 0.0;
+            for (int c = 0; c < d; ++c)
+                acc += rd(dtype, W_lm, (size_t)v * d + c) * rd(dtype, h, (size_t)b * d + c);
+            lg[v] = acc;
+        }
+        double m = lg[0];
+        for (int v = 1; v < V; ++v)
+            if (lg[v] > m) m = lg[v];
+        double S = 0.0;
+        for (int v = 0; v < V; ++v)
+            S += exp(lg[v] - m);
+        double logz = m + log(S);
+        memset(taken, 0, (size_t)V);
+        for (int r = 0; r < s; ++r) {
+            int best = -1;
+            for (int v = 0; v < V; ++v) {
+                if (taken[v]) continue;
+                if (best < 0 || lg[v] > lg[best]) best = v;
+            }
+            taken[best] = 1;
+            topk_ids[(size_t)b * s + r] = best;
+            topk_logp[(size_t)b * s + r] = lg[best] - logz;
+        }
+        if (logits_out)
+            memcpy(logits_out + (size_t)b * V, lg, (size_t)V * sizeof(double));
+        if (logz_out)
+            logz_out[b] = logz;
+    }
+    free(lg); free(taken);
     return 0;
 }
 

@@ -222,6 +222,47 @@ def test_heads_bf16_widening_exact():
     assert np.array_equal(a[0], b[0]) and np.array_equal(a[2], b[2])
 
 
+def test_lm_head_equals_identity_initialised_head():
+    """A Medusa head with W1 = 0 and b1 = 0 has z = h + SiLU(0) = h ([P2] §3.1
+    initialisation), so with W2 = W_lm it is the LM head: the separately
+    written LM-head oracle must agree with the heads oracle (itself pinned)
+    logit for logit, in top-s order and log Z."""
+    cfg = synth.tiny().replace(lm_head_variant=True, B=2)
+    hi = synth.heads_inputs(cfg)
+    w_lm = hi.W2[0]
+    ids, logp, logits, logz = oracle.lm_head(hi.h, w_lm, 5, want_logits=True)
+    hids, hlogp, hlogits, hlogz = oracle.heads(hi.h, hi.W1[:1], hi.b1[:1], hi.W2[:1], 5,
+                                               want_logits=True)
+    np.testing.assert_allclose(logits, hlogits[:, 0], rtol=0, atol=1e-12)
+    np.testing.assert_allclose(logz, hlogz[:, 0], rtol=0, atol=1e-12)
+    assert np.array_equal(ids, hids[:, 0])
+    np.testing.assert_allclose(logp, hlogp[:, 0], rtol=0, atol=1e-12)
+
+
+def test_lm_head_one_hot_rows_closed_form():
+    """W_lm row v = c_v e_{j_v} makes logit v = c_v h[j_v]: closed-form logits,
+    log Z and greedy root.  A transposed W_lm, a dropped term or a wrong
+    normaliser changes them.  Equal logits rank the smaller id first."""
+    rng = np.random.default_rng(11)
+    d, V, B = 8, 30, 3
+    h = rng.standard_normal((B, d)).astype(np.float32)
+    col = rng.integers(0, d, size=V)
+    c = rng.uniform(0.5, 3.0, size=V).astype(np.float32)
+    col[17], c[17] = col[4], c[4] = col[4], 10.0   # tokens 4 and 17 tie at the top
+    h[:, col[4]] = np.abs(h[:, col[4]]) + 1.0
+    W = np.zeros((V, d), np.float32)
+    W[np.arange(V), col] = c
+    ids, logp, logits, logz = oracle.lm_head(h, W, 6, want_logits=True)
+    for b in range(B):
+        ref = c.astype(np.float64) * h[b, col].astype(np.float64)
+        np.testing.assert_allclose(logits[b], ref, atol=1e-12)
+        assert logz[b] == pytest.approx(logsumexp(ref), abs=1e-12)
+        assert list(ids[b]) == _ref_topk(ref, 6)
+        np.testing.assert_allclose(logp[b], ref[ids[b]] - logsumexp(ref), atol=1e-12)
+    # the tie at the top: the greedy root is the smaller id, the other is next
+    assert (ids[:, 0] == 4).all() and (ids[:, 1] == 17).all()
+
+
 # ----------------------------------------------------------- attention ----
 
 def _sdpa_path(q_rows, k_rows, v_rows, P, scale):
