@@ -393,6 +393,23 @@ def run_ours(args, cfg):
         m.commit_kv(m.BF16, kptr, vptr, prefix, post.path, post.accept_len, R, cfg.H, cfg.dh,
                     new_prefix_len=new_prefix, ws=ws)
 
+    # the LM head joining the heads' weight pass (the root is produced, not given)
+    w_lm = T(synth.lm_head_weight(cfg))
+    ws_lm = m.new_workspace(m.heads_lm_workspace_size(B, K, cfg.d, cfg.V, S), dev)
+    lm_out = (torch.empty((B,), dtype=torch.int32, device=dev),
+              torch.empty((B,), dtype=torch.float32, device=dev),
+              torch.empty((B, K, S), dtype=torch.int32, device=dev),
+              torch.empty((B, K, S), dtype=torch.float32, device=dev))
+
+    def heads_lm():
+        m.heads_lm(h, w_lm, W1, b1, W2, S, ws=ws_lm, out=lm_out)
+
+    def heads_only():
+        m.heads(h, W1, b1, W2, S, ws=ws, out=(ids, logp))
+
+    us_heads_lm = timed_loop(heads_lm)
+    us_heads = timed_loop(heads_only)
+    lm_bytes = nb["heads"] + cfg.V * cfg.d * 2 + B * 8
     us_post = timed_loop(post_only)
     us_post_commit = timed_loop(post_commit)
     us_commit = timed_loop(commit_only)
@@ -403,7 +420,12 @@ def run_ours(args, cfg):
         "GB/s": round(commit_bytes / (us_commit * 1e-6) / 1e9, 1),
         "fused_posterior_commit_us": round(us_post_commit, 2),
         "posterior_alone_us": round(us_post, 2),
-        "note": "launch-latency bound: a few hundred KB per step"}}
+        "note": "launch-latency bound: a few hundred KB per step"},
+        "heads_lm": {
+            "us": round(us_heads_lm, 2), "bytes": int(lm_bytes),
+            "GB/s": round(lm_bytes / (us_heads_lm * 1e-6) / 1e9, 1),
+            "frac_hbm": None, "heads_alone_us": round(us_heads, 2),
+            "note": "LM head (32000 x 4096) + 5 Medusa heads in one weight pass"}}
 
     # ---- end to end through the public API with pinned host buffers
     host_in = {
@@ -450,6 +472,8 @@ def run_ours(args, cfg):
         return 0
 
     peaks, peak_src = measured_peaks()
+    next_rows["heads_lm"]["frac_hbm"] = round(
+        next_rows["heads_lm"]["GB/s"] / peaks["hbm_gbs"], 4)
     heads_ms = float(np.mean(per_call["heads"]))
     achieved = nb["heads"] / (heads_ms * 1e-3) / 1e9
     traffic = None

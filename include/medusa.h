@@ -4,7 +4,8 @@
  *
  * The step, as the pages define it:
  *   1. medusa_heads               K Medusa heads read the last hidden state and
- *                                 keep their top-s tokens.
+ *                                 keep their top-s tokens (medusa_heads_lm:
+ *                                 the LM head's root token in the same pass).
  *   2. medusa_build_tree          the proposals become a budgeted candidate tree.
  *   3. medusa_tree_attention      every tree node attends to the prefix and to
  *                                 its own ancestors.
@@ -149,6 +150,30 @@ MEDUSA_API medusa_status medusa_heads(medusa_dtype dtype, const void *h, const v
                            int K, int top_s, int32_t *topk_ids,
                            float *topk_logp, void *ws, size_t ws_bytes,
                            medusa_stream stream);
+
+/* ------------------------------------------------------------------------
+ * 1a. The LM head and the Medusa heads in one pass.
+ *
+ * [P1] Introduction and [P3] (the base model's LM head and the Medusa heads
+ * read the same final hidden state): the LM head's logits are W_lm h (no
+ * residual block).  [P2] §5: its greedy token is the tree's root, accepted
+ * unconditionally.  The LM head joins the Medusa heads' weight stream as one
+ * more head, so the whole proposal stage is one pass over W_lm, W1 and W2.
+ *
+ *   W_lm      [V,d]   dtype; row v holds token v's projection
+ *   root      [B]     int32 out: argmax_v (W_lm h[b])_v (equal logits -> the
+ *                     smaller id)
+ *   root_logp [B]     fp32  out: log softmax(W_lm h[b])[root]
+ * Other arguments, outputs and requirements as medusa_heads; the workspace
+ * is medusa_heads_lm_workspace_size(...).
+ * ---------------------------------------------------------------------- */
+MEDUSA_API size_t medusa_heads_lm_workspace_size(int B, int K, int d, int V, int top_s);
+
+MEDUSA_API medusa_status medusa_heads_lm(medusa_dtype dtype, const void *h, const void *W_lm,
+                                         const void *W1, const void *b1, const void *W2, int B,
+                                         int d, int V, int K, int top_s, int32_t *root,
+                                         float *root_logp, int32_t *topk_ids, float *topk_logp,
+                                         void *ws, size_t ws_bytes, medusa_stream stream);
 
 /* ------------------------------------------------------------------------
  * 1b. Medusa heads with library-held scratch (no workspace argument).

@@ -7,7 +7,7 @@ current CUDA stream, allocates outputs and workspaces with torch, and raises
 the compiled library is missing, importing the calls fails loudly.
 
 Public calls (same names as the C ABI in include/medusa.h):
-    heads, heads_noalloc, build_tree, tree_attention, evaluate_posterior,
+    heads, heads_lm, heads_noalloc, build_tree, tree_attention, evaluate_posterior,
     commit_kv, evaluate_posterior_commit
 plus workspace-size queries, device-status helpers and launch_count.
 """
@@ -39,6 +39,7 @@ DEVICE_STATUS = {0: "ok", 1: "bad token", 2: "bad parent", 3: "bad prefix", 4: "
 EXPORTS = ("medusa_status_string", "medusa_last_error", "medusa_launch_count",
            "medusa_read_device_status", "medusa_clear_device_status",
            "medusa_heads_workspace_size", "medusa_heads",
+           "medusa_heads_lm_workspace_size", "medusa_heads_lm",
            "medusa_build_tree_workspace_size", "medusa_build_tree",
            "medusa_tree_attention_workspace_size", "medusa_tree_attention",
            "medusa_posterior_workspace_size", "medusa_evaluate_posterior",
@@ -73,6 +74,8 @@ def lib() -> ctypes.CDLL:
         "medusa_clear_device_status": ([P, P], I),
         "medusa_heads_workspace_size": ([I, I, I, I, I], S),
         "medusa_heads": ([I, P, P, P, P, I, I, I, I, I, P, P, P, S, P], I),
+        "medusa_heads_lm_workspace_size": ([I, I, I, I, I], S),
+        "medusa_heads_lm": ([I, P, P, P, P, P, I, I, I, I, I, P, P, P, P, P, S, P], I),
         "medusa_build_tree_workspace_size": ([I, I, I, I], S),
         "medusa_build_tree": ([P, P, P, I, I, P, I, I, P, P, P, P, P, P, P, P, P, S, P], I),
         "medusa_tree_attention_workspace_size": ([I, I, I, I, I, I], S),
@@ -164,6 +167,33 @@ def heads(h, W1, b1, W2, top_s: int, ws=None, out=None, stream=None):
     _check(lib().medusa_heads(_dtype(h), _ptr(h), _ptr(W1), _ptr(b1), _ptr(W2), B, d, V, K, top_s,
                               _ptr(ids), _ptr(logp), _ptr(ws), ws.numel(), _stream(stream)))
     return ids, logp
+
+
+def heads_lm_workspace_size(B: int, K: int, d: int, V: int, top_s: int) -> int:
+    return int(lib().medusa_heads_lm_workspace_size(B, K, d, V, top_s))
+
+
+def heads_lm(h, W_lm, W1, b1, W2, top_s: int, ws=None, out=None, stream=None):
+    """The LM head and the Medusa heads in one weight pass.  Returns
+    (root int32 [B], root_logp fp32 [B], topk_ids int32 [B,K,top_s],
+    topk_logp fp32 [B,K,top_s])."""
+    for t, name in ((h, "h"), (W_lm, "W_lm"), (W1, "W1"), (W2, "W2")):
+        _need(t, name)
+    B, d = h.shape
+    K, V = W2.shape[0], W2.shape[1]
+    dev = h.device
+    if ws is None:
+        ws = new_workspace(heads_lm_workspace_size(B, K, d, V, top_s), dev)
+    if out is None:
+        out = (torch.empty((B,), dtype=torch.int32, device=dev),
+               torch.empty((B,), dtype=torch.float32, device=dev),
+               torch.empty((B, K, top_s), dtype=torch.int32, device=dev),
+               torch.empty((B, K, top_s), dtype=torch.float32, device=dev))
+    root, root_logp, ids, logp = out
+    _check(lib().medusa_heads_lm(_dtype(h), _ptr(h), _ptr(W_lm), _ptr(W1), _ptr(b1), _ptr(W2), B, d,
+                                 V, K, int(top_s), _ptr(root), _ptr(root_logp), _ptr(ids),
+                                 _ptr(logp), _ptr(ws), ws.numel(), _stream(stream)))
+    return root, root_logp, ids, logp
 
 
 def heads_noalloc(h, W1, b1, W2, top_s: int, out=None, stream=None):

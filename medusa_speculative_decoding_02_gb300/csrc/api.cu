@@ -114,11 +114,18 @@ size_t medusa_heads_workspace_size(int B, int K, int d, int V, int top_s) {
     return heads_workspace_bytes(B, K, d, V, top_s);
 }
 
-medusa_status medusa_heads(medusa_dtype dtype, const void *h, const void *W1, const void *b1,
-                           const void *W2, int B, int d, int V, int K, int top_s,
-                           int32_t *topk_ids, float *topk_logp, void *ws, size_t ws_bytes,
-                           medusa_stream stream) {
-    const char *who = "medusa_heads";
+size_t medusa_heads_lm_workspace_size(int B, int K, int d, int V, int top_s) {
+    if (B < 1 || K < 1 || d < 1 || V < 1 || top_s < 1) return 0;
+    return heads_workspace_bytes(B, K, d, V, top_s, true);
+}
+
+}  // extern "C"
+
+namespace {
+
+medusa_status check_heads(const char *who, medusa_dtype dtype, const void *h, const void *W1,
+                          const void *b1, const void *W2, int B, int d, int V, int K, int top_s,
+                          const int32_t *topk_ids, const float *topk_logp) {
     if (dtype != MEDUSA_F32 && dtype != MEDUSA_BF16)
         return fail(MEDUSA_ERR_INVALID_ARG, "%s: unknown dtype %d", who, (int)dtype);
     if (!h || !W1 || !W2 || !topk_ids || !topk_logp)
@@ -137,9 +144,47 @@ medusa_status medusa_heads(medusa_dtype dtype, const void *h, const void *W1, co
                     (size_t)nb * d * sizeof(float));
     if (!aligned16(h) || !aligned16(W1) || !aligned16(W2) || (b1 && !aligned16(b1)))
         return fail(MEDUSA_ERR_INVALID_ARG, "%s: tensor pointers must be 16-byte aligned", who);
+    return MEDUSA_OK;
+}
+
+}  // namespace
+
+extern "C" {
+
+medusa_status medusa_heads(medusa_dtype dtype, const void *h, const void *W1, const void *b1,
+                           const void *W2, int B, int d, int V, int K, int top_s,
+                           int32_t *topk_ids, float *topk_logp, void *ws, size_t ws_bytes,
+                           medusa_stream stream) {
+    const char *who = "medusa_heads";
+    if (medusa_status s = check_heads(who, dtype, h, W1, b1, W2, B, d, V, K, top_s, topk_ids,
+                                      topk_logp))
+        return s;
     if (medusa_status s = check_ws(ws, ws_bytes, heads_workspace_bytes(B, K, d, V, top_s), who))
         return s;
-    cudaError_t e = launch_heads(dtype, h, W1, b1, W2, B, d, V, K, top_s, topk_ids, topk_logp, ws,
+    cudaError_t e = launch_heads(dtype, h, nullptr, W1, b1, W2, B, d, V, K, top_s, topk_ids,
+                                 topk_logp, nullptr, nullptr, ws,
+                                 static_cast<cudaStream_t>(stream));
+    if (e) return cuda_fail(e, who);
+    return MEDUSA_OK;
+}
+
+medusa_status medusa_heads_lm(medusa_dtype dtype, const void *h, const void *W_lm, const void *W1,
+                              const void *b1, const void *W2, int B, int d, int V, int K,
+                              int top_s, int32_t *root, float *root_logp, int32_t *topk_ids,
+                              float *topk_logp, void *ws, size_t ws_bytes, medusa_stream stream) {
+    const char *who = "medusa_heads_lm";
+    if (medusa_status s = check_heads(who, dtype, h, W1, b1, W2, B, d, V, K, top_s, topk_ids,
+                                      topk_logp))
+        return s;
+    if (!W_lm || !root || !root_logp)
+        return fail(MEDUSA_ERR_INVALID_ARG, "%s: NULL pointer", who);
+    if (!aligned16(W_lm))
+        return fail(MEDUSA_ERR_INVALID_ARG, "%s: W_lm must be 16-byte aligned", who);
+    if (medusa_status s =
+            check_ws(ws, ws_bytes, heads_workspace_bytes(B, K, d, V, top_s, true), who))
+        return s;
+    cudaError_t e = launch_heads(dtype, h, W_lm, W1, b1, W2, B, d, V, K, top_s, topk_ids,
+                                 topk_logp, root, root_logp, ws,
                                  static_cast<cudaStream_t>(stream));
     if (e) return cuda_fail(e, who);
     return MEDUSA_OK;

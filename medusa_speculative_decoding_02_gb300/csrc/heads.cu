@@ -20,6 +20,10 @@
 //                              partial per (head, sequence).
 //   phase 3  heads_reduce_kernel merges the partials of each (head, sequence)
 //                              into log Z and the final top-s log-probs.
+// With the base model's LM head W_lm given (medusa_heads_lm), it joins the
+// pass as head 0 with z = h: its rows stream in the same phase-2 grid as the
+// Medusa heads' W2 rows, and phase 3 emits its greedy token (the tree root)
+// and that token's log-probability.
 // z and h sit in shared memory in a split-plane layout (elements 0-3 and 4-7
 // of each 8-element vector in separate planes) so that a warp's 16-byte
 // shared loads are bank-conflict free.
@@ -98,7 +102,8 @@ __device__ __forceinline__ void row_dot(const uint4 *__restrict__ w, const float
 template <typename T, int NB, int U>
 __global__ void __launch_bounds__(kW1Threads, NB <= 2 ? 4 : 1)
 heads_w1_kernel(const T *__restrict__ h, const T *__restrict__ W1, const T *__restrict__ b1,
-                float *__restrict__ z, int B, int d, int K, int rows_per_warp) {
+                float *__restrict__ z, float *__restrict__ z_lm, int B, int d, int K,
+                int rows_per_warp) {
     pdl_enter();
     extern __shared__ float4 smem4[];
     float *hs = reinterpret_cast<float *>(smem4);
@@ -108,6 +113,9 @@ heads_w1_kernel(const T *__restrict__ h, const T *__restrict__ W1, const T *__re
         const int b = i / d, c = i - b * d;
         hs[plane_index<VN>(b, c, nvec)] = (b < B) ? Vec16<T>::load1(h + (size_t)b * d + c) : 0.f;
     }
+    if (z_lm)  // the LM head's z is h itself (no residual block)
+        for (int i = blockIdx.x * blockDim.x + threadIdx.x; i < B * d; i += gridDim.x * blockDim.x)
+            z_lm[i] = Vec16<T>::load1(h + i);
     __syncthreads();
     const int lane = threadIdx.x & 31;
     const int warp = threadIdx.x >> 5;
@@ -257,11 +265,22 @@ __device__ __forceinline__ void warp_merge_ms(const TopSlot *slots, int stride, 
     s = t.s;
 }
 
+// Row v of head k's vocabulary projection: with the LM head present it is
+// head 0 and the Medusa heads follow.
+template <typename T>
+__device__ __forceinline__ const T *w2_row(const T *W2, const T *Wlm, int k, int v, int V, int d) {
+    if (Wlm) {
+        if (k == 0) return Wlm + (size_t)v * d;
+        --k;
+    }
+    return W2 + ((size_t)k * V + v) * d;
+}
+
 template <typename T, int NB, int U>
 __global__ void __launch_bounds__(kW2Threads, NB <= 1 ? 2 : 1)
-heads_w2_kernel(const float *__restrict__ z, const T *__restrict__ W2, int B, int d, int V, int K,
-                int S, int hpg, float2 *__restrict__ part_ms, float *__restrict__ part_val,
-                int *__restrict__ part_id) {
+heads_w2_kernel(const float *__restrict__ z, const T *__restrict__ W2, const T *__restrict__ Wlm,
+                int B, int d, int V, int K, int S, int hpg, float2 *__restrict__ part_ms,
+                float *__restrict__ part_val, int *__restrict__ part_id) {
     extern __shared__ float4 smem4[];
     constexpr int VN = Vec16<T>::N;
     const int nvec = d / VN;
@@ -278,7 +297,7 @@ heads_w2_kernel(const float *__restrict__ z, const T *__restrict__ W2, int B, in
     // The weights are never written by any kernel, so this warp's first row
     // can be pulled into L2 before the wait for phase 1's z.
     if (lane == 0 && warp < nrows)
-        prefetch_l2_bulk(W2 + (size_t)(r0 + warp) * d, (unsigned)(d * sizeof(T)));
+        prefetch_l2_bulk(w2_row(W2, Wlm, 0, r0 + warp, V, d), (unsigned)(d * sizeof(T)));
     pdl_enter();
 
     for (int k0 = 0; k0 < K; k0 += hpg) {
@@ -310,7 +329,7 @@ heads_w2_kernel(const float *__restrict__ z, const T *__restrict__ W2, int B, in
                 ++cur;
             }
             float acc[NB];
-            const T *wrow = W2 + ((size_t)(k0 + kk) * V + v) * d;
+            const T *wrow = w2_row(W2, Wlm, k0 + kk, v, V, d);
             row_dot<T, NB, U>(reinterpret_cast<const uint4 *>(wrow), zs4 + (size_t)kk * NB * d / 4,
                               nvec, lane, acc);
 #pragma unroll
@@ -418,8 +437,9 @@ __device__ __forceinline__ void warp_select_top(float (&cv)[U + 1], int (&ci)[U 
 // in parallel.
 __global__ void __launch_bounds__(kReduceThreads)
 heads_reduce_kernel(const float2 *__restrict__ part_ms, const float *__restrict__ part_val,
-                    const int *__restrict__ part_id, int G, int B, int K, int S,
-                    int32_t *__restrict__ topk_ids, float *__restrict__ topk_logp) {
+                    const int *__restrict__ part_id, int G, int B, int K, int S, int lm,
+                    int32_t *__restrict__ topk_ids, float *__restrict__ topk_logp,
+                    int32_t *__restrict__ root, float *__restrict__ root_logp) {
     constexpr int U = 4;
     constexpr int NW = kReduceThreads / kWarp;
     pdl_enter();
@@ -427,7 +447,7 @@ heads_reduce_kernel(const float2 *__restrict__ part_ms, const float *__restrict_
     __shared__ float s_logz;
     __shared__ float r_val[MEDUSA_MAX_TOP_S];
     __shared__ int r_id[MEDUSA_MAX_TOP_S];
-    const int kb = blockIdx.x;  // k * B + b
+    const int kb = blockIdx.x;  // k * B + b over all heads (the LM head first if lm)
     const int k = kb / B, b = kb - k * B;
     const int lane = threadIdx.x & 31;
     const int warp = threadIdx.x >> 5;
@@ -476,8 +496,13 @@ heads_reduce_kernel(const float2 *__restrict__ part_ms, const float *__restrict_
     for (int t = threadIdx.x; t < NW * S; t += kReduceThreads)
         rank_merge_entry(slots, 1, NW, S, t / S, t % S, r_val, r_id);
     __syncthreads();
-    if (threadIdx.x < S) {
-        const size_t o = ((size_t)b * K + k) * S + threadIdx.x;
+    if (lm && k == 0) {  // the LM head: its greedy token is the tree root
+        if (threadIdx.x == 0) {
+            root[b] = r_id[0];
+            root_logp[b] = r_val[0] - s_logz;
+        }
+    } else if (threadIdx.x < S) {
+        const size_t o = ((size_t)b * (K - lm) + (k - lm)) * S + threadIdx.x;
         topk_ids[o] = r_id[threadIdx.x];
         topk_logp[o] = r_val[threadIdx.x] - s_logz;
     }
@@ -486,7 +511,12 @@ heads_reduce_kernel(const float2 *__restrict__ part_ms, const float *__restrict_
 // ---------------------------------------------------------------- host ---
 
 constexpr int kMaxW2Ctas = 1024;
+// Shared memory per phase-2 CTA.  One sequence (NB = 1) runs two CTAs per SM,
+// and two CTAs must stay within the 196 KB shared-memory carveout: the
+// largest carveout (228 KB) leaves L1 so small that the weight stream runs
+// ~15% slower (measured on GB300), more than a second head group costs.
 constexpr size_t kSmemBudget = 200 * 1024;
+constexpr size_t kSmemBudgetPair = 97 * 1024;
 
 int nb_bucket(int B) { return B <= 1 ? 1 : B <= 2 ? 2 : B <= 4 ? 4 : 8; }
 
@@ -496,29 +526,33 @@ struct HeadsLayout {
     size_t z_off, ms_off, val_off, id_off, total;
 };
 
-HeadsLayout heads_layout(int B, int K, int d, int S) {
+// Kt = heads in the pass (the Medusa heads, plus the LM head when present).
+HeadsLayout heads_layout(int B, int Kt, int d, int S) {
     HeadsLayout L;
     size_t o = MEDUSA_WS_HEADER;
     L.z_off = o;
-    o = align256(o + (size_t)K * B * d * sizeof(float));
+    o = align256(o + (size_t)Kt * B * d * sizeof(float));
     L.ms_off = o;
-    o = align256(o + (size_t)K * B * kMaxW2Ctas * sizeof(float2));
+    o = align256(o + (size_t)Kt * B * kMaxW2Ctas * sizeof(float2));
     L.val_off = o;
-    o = align256(o + (size_t)K * B * kMaxW2Ctas * S * sizeof(float));
+    o = align256(o + (size_t)Kt * B * kMaxW2Ctas * S * sizeof(float));
     L.id_off = o;
-    o = align256(o + (size_t)K * B * kMaxW2Ctas * S * sizeof(int));
+    o = align256(o + (size_t)Kt * B * kMaxW2Ctas * S * sizeof(int));
     L.total = o;
     return L;
 }
 
 template <typename T, int NB>
-cudaError_t run_heads(const void *h, const void *W1, const void *b1, const void *W2, int B, int d,
-                      int V, int K, int S, int32_t *ids, float *logp, char *ws,
+cudaError_t run_heads(const void *h, const void *Wlm, const void *W1, const void *b1,
+                      const void *W2, int B, int d, int V, int K, int S, int32_t *ids,
+                      float *logp, int32_t *root, float *root_logp, char *ws,
                       cudaStream_t stream) {
     constexpr int U1 = NB <= 4 ? 8 : 4;
     constexpr int U2 = NB <= 4 ? 8 : 4;
-    const HeadsLayout L = heads_layout(B, K, d, S);
-    float *z = reinterpret_cast<float *>(ws + L.z_off);
+    const int lm = Wlm ? 1 : 0;
+    const int Kt = K + lm;
+    const HeadsLayout L = heads_layout(B, Kt, d, S);
+    float *z = reinterpret_cast<float *>(ws + L.z_off);  // [Kt][B][d], the LM head first
     float2 *pms = reinterpret_cast<float2 *>(ws + L.ms_off);
     float *pval = reinterpret_cast<float *>(ws + L.val_off);
     int *pid = reinterpret_cast<int *>(ws + L.id_off);
@@ -538,14 +572,16 @@ cudaError_t run_heads(const void *h, const void *W1, const void *b1, const void 
     const int rpw = std::max(1, (rows1 + slots1 - 1) / slots1);
     const int grid1 = std::max(1, (((rows1 + rpw - 1) / rpw) + warps1 - 1) / warps1);
     e = launch_pdl(k1, dim3(grid1), dim3(kW1Threads), smem1, stream, static_cast<const T *>(h),
-                   static_cast<const T *>(W1), static_cast<const T *>(b1), z, B, d, K, rpw);
+                   static_cast<const T *>(W1), static_cast<const T *>(b1),
+                   z + (size_t)lm * B * d, lm ? z : nullptr, B, d, K, rpw);
     note_launch();
     if (e) return e;
 
     // phase 2
     const size_t per_head = (size_t)NB * d * sizeof(float);
     const size_t slot_per_head = (size_t)kW2Warps * NB * sizeof(TopSlot);
-    int hpg = (int)std::min<size_t>(K, std::max<size_t>(1, kSmemBudget / (per_head + slot_per_head)));
+    const size_t budget = NB == 1 ? kSmemBudgetPair : kSmemBudget;
+    int hpg = (int)std::min<size_t>(Kt, std::max<size_t>(1, budget / (per_head + slot_per_head)));
     const size_t smem2 = hpg * (per_head + slot_per_head);
     auto k2 = heads_w2_kernel<T, NB, U2>;
     if ((e = cudaFuncSetAttribute(k2, cudaFuncAttributeMaxDynamicSharedMemorySize, (int)smem2)))
@@ -554,32 +590,36 @@ cudaError_t run_heads(const void *h, const void *W1, const void *b1, const void 
     if ((e = cudaOccupancyMaxActiveBlocksPerMultiprocessor(&occ2, k2, kW2Threads, smem2))) return e;
     const int G = std::max(1, std::min(kMaxW2Ctas, sms * std::max(occ2, 1)));
     e = launch_pdl(k2, dim3(G), dim3(kW2Threads), smem2, stream, static_cast<const float *>(z),
-                   static_cast<const T *>(W2), B, d, V, K, S, hpg, pms, pval, pid);
+                   static_cast<const T *>(W2), static_cast<const T *>(Wlm), B, d, V, Kt, S, hpg,
+                   pms, pval, pid);
     note_launch();
     if (e) return e;
 
     // phase 3
-    e = launch_pdl(heads_reduce_kernel, dim3(K * B), dim3(kReduceThreads), 0, stream,
+    e = launch_pdl(heads_reduce_kernel, dim3(Kt * B), dim3(kReduceThreads), 0, stream,
                    static_cast<const float2 *>(pms), static_cast<const float *>(pval),
-                   static_cast<const int *>(pid), G, B, K, S, ids, logp);
+                   static_cast<const int *>(pid), G, B, Kt, S, lm, ids, logp, root, root_logp);
     note_launch();
     return e;
 }
 
 }  // namespace
 
-size_t heads_workspace_bytes(int B, int K, int d, int V, int S) {
+size_t heads_workspace_bytes(int B, int K, int d, int V, int S, bool with_lm_head) {
     (void)V;
-    return heads_layout(B, K, d, S).total;
+    return heads_layout(B, K + (with_lm_head ? 1 : 0), d, S).total;
 }
 
-cudaError_t launch_heads(medusa_dtype dtype, const void *h, const void *W1, const void *b1,
-                         const void *W2, int B, int d, int V, int K, int S, int32_t *ids,
-                         float *logp, void *ws, cudaStream_t stream) {
+cudaError_t launch_heads(medusa_dtype dtype, const void *h, const void *Wlm, const void *W1,
+                         const void *b1, const void *W2, int B, int d, int V, int K, int S,
+                         int32_t *ids, float *logp, int32_t *root, float *root_logp, void *ws,
+                         cudaStream_t stream) {
     char *w = static_cast<char *>(ws);
     const int nb = nb_bucket(B);
-#define MEDUSA_HEADS_CASE(T, N) \
-    if (nb == N) return run_heads<T, N>(h, W1, b1, W2, B, d, V, K, S, ids, logp, w, stream);
+#define MEDUSA_HEADS_CASE(T, N)                                                                  \
+    if (nb == N)                                                                                 \
+        return run_heads<T, N>(h, Wlm, W1, b1, W2, B, d, V, K, S, ids, logp, root, root_logp, w, \
+                               stream);
     if (dtype == MEDUSA_BF16) {
         MEDUSA_HEADS_CASE(bf16, 1)
         MEDUSA_HEADS_CASE(bf16, 2)

@@ -34,10 +34,13 @@ int device_sm_count();   // SMs of the current device (cached per device)
 void note_launch();      // count one kernel launch
 void set_last_error(const char *fmt, ...);  // message for medusa_last_error()
 
-size_t heads_workspace_bytes(int B, int K, int d, int V, int S);
-cudaError_t launch_heads(medusa_dtype dtype, const void *h, const void *W1, const void *b1,
-                         const void *W2, int B, int d, int V, int K, int S, int32_t *ids,
-                         float *logp, void *ws, cudaStream_t stream);
+// Wlm == nullptr: the Medusa heads alone; otherwise the LM head joins the
+// pass and writes root / root_logp.
+size_t heads_workspace_bytes(int B, int K, int d, int V, int S, bool with_lm_head = false);
+cudaError_t launch_heads(medusa_dtype dtype, const void *h, const void *Wlm, const void *W1,
+                         const void *b1, const void *W2, int B, int d, int V, int K, int S,
+                         int32_t *ids, float *logp, int32_t *root, float *root_logp, void *ws,
+                         cudaStream_t stream);
 
 size_t tree_workspace_bytes(int B, int K, int S, int n);
 cudaError_t launch_build_tree(const int32_t *root, const int32_t *ids, const float *logp, int B,

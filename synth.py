@@ -199,13 +199,19 @@ def heads_inputs(cfg: StepConfig, rep: int = 0) -> HeadsInputs:
     b1 = _zeros((cfg.K, cfg.d), cfg.dtype)
     if cfg.lm_head_variant:
         W1 = _zeros((cfg.K, cfg.d, cfg.d), cfg.dtype)
-        w_lm = _normal(cfg, "w2", rep, (cfg.V, cfg.d), cfg.w2_std, cfg.dtype, 1)
+        w_lm = lm_head_weight(cfg, rep)
         W2 = np.empty((cfg.K, cfg.V, cfg.d), w_lm.dtype)
         W2[:] = w_lm[None]
     else:
         W1 = _normal(cfg, "w1", rep, (cfg.K, cfg.d, cfg.d), cfg.w1_std, cfg.dtype)
         W2 = _normal(cfg, "w2", rep, (cfg.K, cfg.V, cfg.d), cfg.w2_std, cfg.dtype)
     return HeadsInputs(h=h, W1=W1, b1=b1, W2=W2)
+
+
+def lm_head_weight(cfg: StepConfig, rep: int = 0) -> np.ndarray:
+    """The base model's LM head W_lm [V,d] ~ N(0, w2_std) (the same matrix the
+    LM-head variant copies into every head's W2)."""
+    return _normal(cfg, "w2", rep, (cfg.V, cfg.d), cfg.w2_std, cfg.dtype, 1)
 
 
 def root_tokens(cfg: StepConfig, rep: int = 0) -> np.ndarray:
