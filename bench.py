@@ -37,6 +37,8 @@ if ROOT not in sys.path:
 
 import synth  # noqa: E402
 
+L2_BYTES = 129 * 1024 * 1024  # GB300 L2
+
 METRIC = "Medusa step µs and achieved HBM GB/s (heads+tree attn+posterior), 7B shape, bs1"
 UNIT = "GB/s"
 
@@ -170,6 +172,72 @@ def plant_on(inp, cfg, tree_np):
     synth.plant_chain(lg, tree_np["tokens"], tree_np["parent"], tree_np["depth"], 3,
                       synth.rng_for(cfg, "plant"))
     inp["logits"] = synth.cast(lg, cfg.dtype)
+
+
+def scan_sizes(m, dev, T, timed_loop) -> dict:
+    """Tree attention and the posterior alone on larger workloads than the bs1
+    step (ragged batch of 8, prefix 8192), where their bytes, not the launch
+    latency, set the time.  Trees come from seeded random top-s tables."""
+    import torch
+    out = {"attention": [], "posterior": []}
+    for cfg in (synth.batch8(), synth.sweep(64, 8192)):
+        rng = np.random.default_rng(cfg.seed)
+        B, K, S = cfg.B, cfg.K, cfg.top_s
+        ids = np.stack([np.stack([rng.choice(cfg.V, size=S, replace=False) for _ in range(K)])
+                        for _ in range(B)]).astype(np.int32)
+        p = rng.dirichlet(np.ones(S + 1), size=(B, K))[..., :S]
+        logp = np.log(-np.sort(-p, axis=-1)).astype(np.float32)
+        prefix = T(np.asarray(cfg.prefix, np.int32))
+        tree = m.build_tree(T(np.arange(B, dtype=np.int32)), T(ids), T(logp), cfg.s, cfg.n,
+                            prefix_len=prefix)
+        nb = step_bytes(cfg)
+        # enough copies that consecutive calls never find their inputs in L2
+        copies = max(2, int(np.ceil(2 * L2_BYTES / nb["attention"])))
+        sets = [synth.attention_inputs(cfg, rep=r) for r in range(copies)]
+        q = T(sets[0].q)
+        kc = [[T(x) for x in a.k_cache] for a in sets]
+        vc = [[T(x) for x in a.v_cache] for a in sets]
+        ptrs = [(m.cache_pointers(k, dev), m.cache_pointers(v, dev)) for k, v in zip(kc, vc)]
+        ws = m.new_workspace(max(
+            m.tree_attention_workspace_size(m.BF16, B, cfg.R, cfg.H, cfg.dh, cfg.P_max),
+            m.posterior_workspace_size(B, cfg.R)), dev)
+        o = torch.empty_like(q)
+        it = [0]
+
+        def attn():
+            kp, vp = ptrs[it[0] % copies]
+            it[0] += 1
+            m.tree_attention(q, kp, vp, prefix, cfg.P_max, tree.anc_mask, out=o, ws=ws)
+
+        us = timed_loop(attn)
+        out["attention"].append({"config": cfg.name, "B": B, "prefix": list(cfg.prefix),
+                                 "tree_rows": cfg.R, "us": round(us, 2),
+                                 "bytes": int(nb["attention"]),
+                                 "GB/s": round(nb["attention"] / (us * 1e-6) / 1e9, 1)})
+        if B > 1:
+            lcopies = max(2, int(np.ceil(2 * L2_BYTES / nb["posterior"])))
+            lg0 = T(synth.cast(synth.base_logits(cfg), "bf16"))
+            logits = [lg0] + [lg0.roll(r, dims=-1).contiguous() for r in range(1, lcopies)]
+            post = m.Posterior.empty(B, cfg.R, K, dev, with_accept=False)
+
+            def posterior():
+                lg = logits[it[0] % lcopies]
+                it[0] += 1
+                m.evaluate_posterior(lg, tree.tokens, tree.parent, tree.depth, K, m.TYPICAL,
+                                     ws=ws, out=post)
+
+            us = timed_loop(posterior)
+            out["posterior"].append({"config": cfg.name, "B": B, "tree_rows": cfg.R,
+                                     "us": round(us, 2), "bytes": int(nb["posterior"]),
+                                     "GB/s": round(nb["posterior"] / (us * 1e-6) / 1e9, 1)})
+        if m.read_device_status(ws) != 0:
+            raise RuntimeError(f"device status set in the size scan ({cfg.name})")
+        out["attention"][-1]["input_copies"] = copies
+        if B > 1:
+            out["posterior"][-1]["input_copies"] = lcopies
+            del logits
+        del kc, vc, q, o, sets
+    return out
 
 
 # ------------------------------------------------------------ distributed ---
@@ -415,6 +483,7 @@ def run_ours(args, cfg):
     us_commit = timed_loop(commit_only)
     if m.read_device_status(ws) != 0:
         raise RuntimeError("device status set by the commit")
+    size_scan = scan_sizes(m, dev, T, timed_loop)
     next_rows = {"commit_kv": {
         "us": round(us_commit, 2), "rows_moved": moved, "bytes": commit_bytes,
         "GB/s": round(commit_bytes / (us_commit * 1e-6) / 1e9, 1),
@@ -472,6 +541,9 @@ def run_ours(args, cfg):
         return 0
 
     peaks, peak_src = measured_peaks()
+    for rows in size_scan.values():
+        for r in rows:
+            r["frac_hbm"] = round(r["GB/s"] / peaks["hbm_gbs"], 4)
     next_rows["heads_lm"]["frac_hbm"] = round(
         next_rows["heads_lm"]["GB/s"] / peaks["hbm_gbs"], 4)
     heads_ms = float(np.mean(per_call["heads"]))
@@ -516,6 +588,7 @@ def run_ours(args, cfg):
                    "l2": "inputs larger than L2: 1.50 GB of weights, KV and logits per step"},
         "stages": stages,
         "next_rows": next_rows,
+        "size_scan": size_scan,
         "roofline": roofline,
         "cpu_baseline": {"value": round(cpu_value, 4), "unit": UNIT, "cores": 1, "kind": "oracle",
                          "sample": f"{len(cpu_secs)} full oracle steps of the same workload "

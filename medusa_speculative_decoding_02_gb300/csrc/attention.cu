@@ -309,61 +309,81 @@ __global__ void __launch_bounds__(MAXW * 32, 1) tree_attn_split_kernel(AttnArgs 
 
 // ------------------------------------------------------- tensor-core path ---
 //
-// tree_attn_tc_kernel: one CTA per (key chunk, head, sequence); a chunk is
-// 128 consecutive slots of the cache, prefix and tree slots alike (they are
-// contiguous).  256 threads: threads t and t+128 own query row t (rows >= R
-// are zero), each handling half of the chunk's keys and of the output columns.  Q, K and V are staged by cp.async into 128-byte-swizzled shared
-// memory; one thread issues the MMAs:
-//     S[128 x 128] = Q K^T      (TMEM columns 0..127)
-//     O[128 x DH]  = P V        (TMEM columns 128..)
-// Between them every thread reads its S row from TMEM, masks it (slots past
-// the chunk; tree slots that are not ancestors-or-self of the row), takes the
-// row max m and writes P = 2^(s*scale*log2e - m) as bf16 into shared memory
-// (the K buffer, which the first MMA no longer needs).  The CTA writes the
-// unnormalised partial (O, m, l) rows; tree_attn_combine_kernel merges them.
+// tree_attn_tc_kernel: one CTA per (key range, head, sequence).  The keys of
+// a sequence are its cache slots 0 .. P+R-1, prefix and tree alike (they are
+// contiguous); a key range is `cps` consecutive sub-chunks of 64 keys, walked
+// with a two-stage cp.async pipeline (sub-chunk j+1 loads while j computes).
+// 256 threads: threads t and t+128 own query row t (rows >= R are zero), each
+// taking half of a sub-chunk's keys and half of the output columns.  Q, K and
+// V sit in 128-byte-swizzled shared memory; one thread issues the MMAs:
+//     S[128 x 64] = Q K_j^T           (TMEM columns 0..63)
+//     O[128 x DH] += P_j V_j          (TMEM columns 128..)
+// Between them every thread reads its S row half from TMEM, masks it (slots
+// past the range; tree slots that are not ancestors-or-self of the row) and
+// writes P = 2^(s*scale*log2e - m) as bf16 over K_j (no longer needed).  The
+// row reference m is raised only when a sub-chunk's max exceeds it by more
+// than 2^8; the threads then rescale their O row in TMEM.  Otherwise P may
+// reach 2^8, harmless in bf16 and fp32.  The CTA writes one unnormalised
+// partial (O, m, l) per row; tree_attn_combine_kernel merges the ranges.
 // Every mbarrier wait is bounded; on a timeout the CTA records
-// MEDUSA_DEV_TIMEOUT, waits once more (bounded) for its MMAs and frees its
-// tensor memory before returning.
-constexpr int kChunk = 128;
+// MEDUSA_DEV_TIMEOUT, stops, waits once more (bounded) for its MMAs and frees
+// its tensor memory before returning.
+constexpr int kTcSub = 64;               // keys per pipeline stage
+constexpr float kRescaleLog2 = 8.f;      // lazy-rescale threshold (log2 units)
 constexpr uint32_t kWaitPolls = 1u << 16;
 
 template <int DH>
 struct TcSmem {
     static constexpr int NB = DH / 64;                 // 64-element column blocks of dh
     static constexpr int Q_BYTES = NB * 128 * 128;      // [NB][128 rows][128 B]
-    static constexpr int K_BYTES = NB * kChunk * 128;   // [NB][128 keys][128 B]; P reuses it
-    static constexpr int P_BYTES = 2 * 128 * 128;       // [2][128 rows][64 keys]
+    static constexpr int K_BYTES = NB * kTcSub * 128;     // [NB][64 keys][128 B]
+    static constexpr int P_BYTES = 128 * 128;           // [128 rows][64 keys] bf16
     static constexpr int KP_BYTES = K_BYTES > P_BYTES ? K_BYTES : P_BYTES;
-    static constexpr int V_BYTES = NB * kChunk * 128;   // [NB][128 keys][128 B]
+    static constexpr int V_BYTES = NB * kTcSub * 128;     // [NB][64 keys][128 B]
+    static constexpr int STAGE_BYTES = KP_BYTES + V_BYTES;
     static constexpr int Q_OFF = 0;
-    static constexpr int KP_OFF = Q_OFF + Q_BYTES;
-    static constexpr int V_OFF = KP_OFF + KP_BYTES;
+    static constexpr int ST_OFF = Q_BYTES;              // two stages
     // two CTAs per SM stay within the same shared-memory carveout as the heads
     // kernels (2 x 96 KB): a larger carveout would shrink L1 under them
-    static constexpr int BAR_OFF = V_OFF + V_BYTES;  // two mbarriers, TMEM holder, flag
+    static constexpr int BAR_OFF = ST_OFF + 2 * STAGE_BYTES;  // mbarriers, TMEM holder, flag
     // 2 x (TOTAL + 1 KB reserved per CTA) must stay within a 196 KB carveout
     static constexpr int TOTAL = BAR_OFF + 64;
 };
+
+// Issue the cp.async copies of sub-chunk keys [k0, k0+kTcSub) (rows past kend
+// are zero-filled) into one stage; every thread commits one group.
+template <int DH>
+__device__ __forceinline__ void tc_load_stage(unsigned char *kp_s, unsigned char *v_s,
+                                              const bf16 *kc, const bf16 *vc, int k0, int kend,
+                                              int H, int h, int tid) {
+    constexpr int CPR = (DH / 64) * 8;  // 16-byte chunks per key row
+    for (int i = tid; i < kTcSub * CPR; i += 256) {
+        const int r = i / CPR, c16 = i - r * CPR;
+        const int key = k0 + r;
+        const bool ok = key < kend;
+        const size_t off = ((size_t)(ok ? key : k0) * H + h) * DH + c16 * 8;
+        const uint32_t so = (c16 >> 3) * kTcSub * 128 + tc::sw128(r, c16 & 7);
+        cp_async16(tc::smem_addr(kp_s + so), kc + off, ok ? 16 : 0);
+        cp_async16(tc::smem_addr(v_s + so), vc + off, ok ? 16 : 0);
+    }
+    cp_async_commit();
+}
 
 template <int DH>
 __global__ void __launch_bounds__(256, 2) tree_attn_tc_kernel(AttnArgs a) {
     pdl_enter();
     using L = TcSmem<DH>;
     constexpr int NB = L::NB;
-    constexpr int HALF = kChunk / 2;  // keys per thread: two threads share a row
+    constexpr int HALF = kTcSub / 2;  // keys per thread per sub-chunk
     // operand tiles need 1024-byte alignment (swizzle atoms)
     extern __shared__ __align__(1024) unsigned char tc_raw[];
     unsigned char *q_s = tc_raw + L::Q_OFF;
-    unsigned char *kp_s = tc_raw + L::KP_OFF;
-    unsigned char *v_s = tc_raw + L::V_OFF;
     uint64_t &bar_s = *reinterpret_cast<uint64_t *>(tc_raw + L::BAR_OFF);
     uint64_t &bar_o = *reinterpret_cast<uint64_t *>(tc_raw + L::BAR_OFF + 8);
     uint32_t &tmem_holder = *reinterpret_cast<uint32_t *>(tc_raw + L::BAR_OFF + 16);
     int &failed = *reinterpret_cast<int *>(tc_raw + L::BAR_OFF + 20);
-    // [2][128] row max / sum exchange, in the Q tile (dead once S is computed)
-    float *xch = reinterpret_cast<float *>(q_s);
 
-    const int chunk = blockIdx.x, h = blockIdx.y, b = blockIdx.z;
+    const int split = blockIdx.x, h = blockIdx.y, b = blockIdx.z;
     const int R = a.R, H = a.H;
     const int tid = threadIdx.x, warp = tid >> 5;
     // warp w reads TMEM lanes 32*(w%4)..: row = tid % 128; half = column half
@@ -373,10 +393,10 @@ __global__ void __launch_bounds__(256, 2) tree_attn_tc_kernel(AttnArgs a) {
         set_status(a.status, MEDUSA_DEV_BAD_PREFIX);
         P = 0;
     }
-    const int NS = a.nps;  // chunks per (sequence, head)
-    const size_t pbase = ((size_t)(b * H + h) * NS + chunk) * R;
-    const int kbeg = chunk * kChunk;
-    const int kend = min(kbeg + kChunk, P + R);
+    const int NS = a.nps;  // key ranges per (sequence, head)
+    const size_t pbase = ((size_t)(b * H + h) * NS + split) * R;
+    const int kbeg = split * a.chunk;  // a.chunk = cps * kTcSub keys per range
+    const int kend = min(kbeg + a.chunk, P + R);
     const bf16 *kc = a.kc[b];
     const bf16 *vc = a.vc[b];
     const bool bad_cache = cache_pointers_bad(kc, vc);
@@ -385,44 +405,29 @@ __global__ void __launch_bounds__(256, 2) tree_attn_tc_kernel(AttnArgs a) {
         for (int r = tid; r < R; r += blockDim.x) a.part_ml[pbase + r] = make_float2(-INFINITY, 0.f);
         return;
     }
+    const int nsub = (kend - kbeg + kTcSub - 1) / kTcSub;
+    auto stage_k = [&](int j) { return tc_raw + L::ST_OFF + (j & 1) * L::STAGE_BYTES; };
+    auto stage_v = [&](int j) { return tc_raw + L::ST_OFF + (j & 1) * L::STAGE_BYTES + L::KP_BYTES; };
 
-    // ---- stage Q and K (group 0), V (group 1); 16-byte chunk c of row r
-    constexpr int CPR = NB * 8;
-    for (int i = tid; i < 128 * CPR; i += 256) {
-        const int r = i / CPR, c16 = i - r * CPR;
+    // ---- Q and the first sub-chunk (group 0), the second sub-chunk (group 1)
+    constexpr int CPRQ = NB * 8;
+    for (int i = tid; i < 128 * CPRQ; i += 256) {
+        const int r = i / CPRQ, c16 = i - r * CPRQ;
         const bool ok = r < R;
         const bf16 *src = a.q + (((size_t)b * R + (ok ? r : 0)) * H + h) * DH + c16 * 8;
         cp_async16(tc::smem_addr(q_s + (c16 >> 3) * 128 * 128 + tc::sw128(r, c16 & 7)), src,
                    ok ? 16 : 0);
     }
-    for (int i = tid; i < kChunk * CPR; i += 256) {
-        const int r = i / CPR, c16 = i - r * CPR;
-        const int key = kbeg + r;
-        const bool ok = key < kend;
-        const size_t off = ((size_t)(ok ? key : kbeg) * H + h) * DH + c16 * 8;
-        cp_async16(tc::smem_addr(kp_s + (c16 >> 3) * kChunk * 128 + tc::sw128(r, c16 & 7)),
-                   kc + off, ok ? 16 : 0);
-    }
-    cp_async_commit();
-    for (int i = tid; i < kChunk * CPR; i += 256) {
-        const int r = i / CPR, c16 = i - r * CPR;
-        const int key = kbeg + r;
-        const bool ok = key < kend;
-        const size_t off = ((size_t)(ok ? key : kbeg) * H + h) * DH + c16 * 8;
-        cp_async16(tc::smem_addr(v_s + (c16 >> 3) * kChunk * 128 + tc::sw128(r, c16 & 7)),
-                   vc + off, ok ? 16 : 0);
-    }
-    cp_async_commit();
-    // this row's ancestor-mask words (only chunks that reach the tree)
-    const bool masked = kend > P || kend - kbeg < kChunk;
-    uint64_t am0 = 0, am1 = 0, am2 = 0, am3 = 0;
+    tc_load_stage<DH>(stage_k(0), stage_v(0), kc, vc, kbeg, kend, H, h, tid);
+    if (nsub > 1) tc_load_stage<DH>(stage_k(1), stage_v(1), kc, vc, kbeg + kTcSub, kend, H, h, tid);
+    // this row's ancestor-mask words (only ranges that reach the tree)
+    // (this path serves R <= 128: two mask words)
+    uint64_t am0 = 0, am1 = 0;
     if (kend > P && row < R) {
         const int W = (R + 63) / 64;
         const uint64_t *mr = a.anc_mask + ((size_t)b * R + row) * W;
         am0 = mr[0];
         if (W > 1) am1 = mr[1];
-        if (W > 2) am2 = mr[2];
-        if (W > 3) am3 = mr[3];
     }
     if (tid == 0) {
         tc::mbar_init(&bar_s, 1);
@@ -430,131 +435,176 @@ __global__ void __launch_bounds__(256, 2) tree_attn_tc_kernel(AttnArgs a) {
         failed = 0;
     }
     if (warp == 0) tc::tmem_alloc(&tmem_holder, 256);
-    cp_async_wait<1>();
-    tc::fence_proxy_async_smem();
     tc::fence_before_sync();
     __syncthreads();
     tc::fence_after_sync();
     const uint32_t tmem = tmem_holder;
     const uint32_t t_s = tmem, t_o = tmem + 128;
-
-    // ---- S = Q K^T
-    if (tid == 0) {
-        constexpr uint32_t idesc = tc::idesc_bf16(128, kChunk, 0);
-        for (int ks = 0; ks < DH / 16; ++ks) {
-            const uint32_t off = (ks >> 2) * 128 * 128 + (ks & 3) * 32;
-            const uint64_t ad = tc::sdesc_sw128(tc::smem_addr(q_s) + off, 16, 1024);
-            const uint32_t koff = (ks >> 2) * kChunk * 128 + (ks & 3) * 32;
-            const uint64_t bd = tc::sdesc_sw128(tc::smem_addr(kp_s) + koff, 16, 1024);
-            tc::mma_bf16_ss(t_s, ad, bd, idesc, ks > 0);
-        }
-        tc::mma_commit(&bar_s);
-    }
-    __syncwarp();
-    if (!tc::mbar_wait_bounded(&bar_s, 0, kWaitPolls)) {
-        failed = 1;
-        set_status(a.status, MEDUSA_DEV_TIMEOUT);
-    }
-    tc::fence_after_sync();
-    __syncthreads();
-    const bool ok_s = !failed;
-
-    // ---- softmax over this thread's 64 columns of its row
     const uint32_t lane_base = (uint32_t)((warp & 3) * 32) << 16;
-    const int c0 = half * HALF;
-    float x[HALF];
-    if (ok_s) {
-        tc::tmem_ld32(t_s + lane_base + c0, *reinterpret_cast<float(*)[32]>(&x[0]));
-        tc::tmem_ld32(t_s + lane_base + c0 + 32, *reinterpret_cast<float(*)[32]>(&x[32]));
-    }
-    float mx[4] = {-INFINITY, -INFINITY, -INFINITY, -INFINITY};
-    if (!masked) {
-#pragma unroll
-        for (int j = 0; j < HALF; ++j) {
-            x[j] *= a.scale_log2;
-            mx[j & 3] = fmaxf(mx[j & 3], x[j]);
-        }
-    } else {
-#pragma unroll
-        for (int j = 0; j < HALF; ++j) {
-            const int key = kbeg + c0 + j;
-            bool vis = key < kend;
-            if (vis && key >= P) {
-                const int t = key - P;
-                const uint64_t mw = (t < 64) ? am0 : (t < 128) ? am1 : (t < 192) ? am2 : am3;
-                vis = (mw >> (t & 63)) & 1u;
-            }
-            x[j] = vis ? x[j] * a.scale_log2 : -INFINITY;
-            mx[j & 3] = fmaxf(mx[j & 3], x[j]);
-        }
-    }
-    xch[half * 128 + row] = fmaxf(fmaxf(mx[0], mx[1]), fmaxf(mx[2], mx[3]));
-    __syncthreads();
-    const float m = fmaxf(xch[row], xch[128 + row]);
-    const float mu = (m == -INFINITY) ? 0.f : m;
-    float ls[4] = {0.f, 0.f, 0.f, 0.f};
-#pragma unroll
-    for (int q8 = 0; q8 < HALF / 8; ++q8) {
-        float p[8];
-#pragma unroll
-        for (int e = 0; e < 8; ++e) {
-            p[e] = exp2f(x[q8 * 8 + e] - mu);
-            ls[e & 3] += p[e];
-        }
-        uint4 w;
-        w.x = pack_bf16(p[0], p[1]);
-        w.y = pack_bf16(p[2], p[3]);
-        w.z = pack_bf16(p[4], p[5]);
-        w.w = pack_bf16(p[6], p[7]);
-        // keys c0 + 8*q8 .. +7: column block `half`, 16-byte chunk q8
-        *reinterpret_cast<uint4 *>(kp_s + half * 128 * 128 + tc::sw128(row, q8)) = w;
-    }
-    const float lpart = (ls[0] + ls[1]) + (ls[2] + ls[3]);
-    cp_async_wait<0>();
-    tc::fence_proxy_async_smem();
-    tc::fence_before_sync();
-    __syncthreads();  // every read of xch (max) is done before it is reused for sums
-    xch[half * 128 + row] = lpart;
-    tc::fence_after_sync();
 
-    // ---- O = P V
-    if (ok_s && tid == 0) {
-        constexpr uint32_t idesc = tc::idesc_bf16(128, DH, 1);
-        for (int ks = 0; ks < kChunk / 16; ++ks) {
-            const uint32_t poff = (ks >> 2) * 128 * 128 + (ks & 3) * 32;
-            const uint64_t ad = tc::sdesc_sw128(tc::smem_addr(kp_s) + poff, 16, 1024);
-            const uint64_t bd =
-                tc::sdesc_sw128(tc::smem_addr(v_s) + ks * 16 * 128, kChunk * 128, 1024);
-            tc::mma_bf16_ss(t_o, ad, bd, idesc, ks > 0);
+    float m_run = -INFINITY;  // row reference (log2 units), same in both threads of a row
+    float l_run = 0.f;        // this thread's share of the row sum
+    int done = 0;             // sub-chunks whose P V MMA was issued
+    for (int j = 0; j < nsub; ++j) {
+        unsigned char *kp_s = stage_k(j);
+        unsigned char *v_s = stage_v(j);
+        const int k0 = kbeg + j * kTcSub;
+        if (j > 0) {
+            // P V of sub-chunk j-1 done: its stage may be refilled, O may be rescaled
+            if (!tc::mbar_wait_bounded(&bar_o, (j - 1) & 1, kWaitPolls)) failed = 1;
+            if (j + 1 < nsub)
+                tc_load_stage<DH>(stage_k(j + 1), stage_v(j + 1), kc, vc, k0 + kTcSub, kend, H, h,
+                                  tid);
         }
-        tc::mma_commit(&bar_o);
+        if (j + 1 < nsub)
+            cp_async_wait<1>();  // sub-chunk j+1 may still be in flight
+        else
+            cp_async_wait<0>();
+        tc::fence_proxy_async_smem();
+        tc::fence_before_sync();
+        __syncthreads();
+        tc::fence_after_sync();
+        if (failed) break;  // uniform: read after the barrier
+
+        // ---- S = Q K_j^T
+        if (tid == 0) {
+            constexpr uint32_t idesc = tc::idesc_bf16(128, kTcSub, 0);
+#pragma unroll
+            for (int ks = 0; ks < DH / 16; ++ks) {
+                const uint32_t off = (ks >> 2) * 128 * 128 + (ks & 3) * 32;
+                const uint64_t ad = tc::sdesc_sw128(tc::smem_addr(q_s) + off, 16, 1024);
+                const uint32_t koff = (ks >> 2) * kTcSub * 128 + (ks & 3) * 32;
+                const uint64_t bd = tc::sdesc_sw128(tc::smem_addr(kp_s) + koff, 16, 1024);
+                tc::mma_bf16_ss(t_s, ad, bd, idesc, ks > 0);
+            }
+            tc::mma_commit(&bar_s);
+        }
+        __syncwarp();
+        if (!tc::mbar_wait_bounded(&bar_s, j & 1, kWaitPolls)) failed = 1;
+        tc::fence_after_sync();
+
+        // ---- this thread's 32 keys of the sub-chunk
+        float x[HALF];
+        tc::tmem_ld32(t_s + lane_base + half * HALF, x);
+        const int kc0 = k0 + half * HALF;
+        const bool masked = k0 + kTcSub > P || k0 + kTcSub > kend;
+        float mx[4] = {-INFINITY, -INFINITY, -INFINITY, -INFINITY};
+        if (!masked) {
+#pragma unroll
+            for (int e = 0; e < HALF; ++e) {
+                x[e] *= a.scale_log2;
+                mx[e & 3] = fmaxf(mx[e & 3], x[e]);
+            }
+        } else {
+#pragma unroll
+            for (int e = 0; e < HALF; ++e) {
+                const int key = kc0 + e;
+                bool vis = key < kend;
+                if (vis && key >= P) {
+                    const int t = key - P;
+                    const uint64_t mw = (t < 64) ? am0 : am1;
+                    vis = (mw >> (t & 63)) & 1u;
+                }
+                x[e] = vis ? x[e] * a.scale_log2 : -INFINITY;
+                mx[e & 3] = fmaxf(mx[e & 3], x[e]);
+            }
+        }
+        // row max of the sub-chunk: exchange halves through the dead K_j tile
+        float *xch = reinterpret_cast<float *>(kp_s);
+        xch[half * 128 + row] = fmaxf(fmaxf(mx[0], mx[1]), fmaxf(mx[2], mx[3]));
+        __syncthreads();
+        const float cm = fmaxf(xch[row], xch[128 + row]);
+        __syncthreads();  // both halves have read xch before P overwrites it
+        const bool raise = cm > m_run + kRescaleLog2;
+        const float m_new = raise ? cm : m_run;
+        const float alpha = raise ? exp2f(m_run - m_new) : 1.f;  // 0 when m_run = -inf
+        l_run *= alpha;
+        m_run = m_new;
+        const float mu = (m_run == -INFINITY) ? 0.f : m_run;
+        float ls[4] = {0.f, 0.f, 0.f, 0.f};
+#pragma unroll
+        for (int q8 = 0; q8 < HALF / 8; ++q8) {
+            float p[8];
+#pragma unroll
+            for (int e = 0; e < 8; ++e) p[e] = exp2f(x[q8 * 8 + e] - mu);
+            uint4 w;
+            w.x = pack_bf16(p[0], p[1]);
+            w.y = pack_bf16(p[2], p[3]);
+            w.z = pack_bf16(p[4], p[5]);
+            w.w = pack_bf16(p[6], p[7]);
+            // the row sum adds the rounded weights the MMA uses, so that the
+            // output is an exact convex combination of V rows under them
+            ls[0] += bf_lo(w.x) + bf_hi(w.x);
+            ls[1] += bf_lo(w.y) + bf_hi(w.y);
+            ls[2] += bf_lo(w.z) + bf_hi(w.z);
+            ls[3] += bf_lo(w.w) + bf_hi(w.w);
+            // keys half*32 + 8*q8 .. +7 of the single 64-key column block
+            *reinterpret_cast<uint4 *>(kp_s + tc::sw128(row, half * 4 + q8)) = w;
+        }
+        l_run += (ls[0] + ls[1]) + (ls[2] + ls[3]);
+        if (__any_sync(0xffffffffu, raise && done > 0)) {
+            // rescale this warp's O rows (lanes whose row did not move scale by
+            // 1); P V of sub-chunk j-1 is complete, P V of j not yet issued
+#pragma unroll 1
+            for (int c = 0; c < DH / 2; c += 32) {
+                float ov[32];
+                tc::tmem_ld32(t_o + lane_base + half * (DH / 2) + c, ov);
+#pragma unroll
+                for (int e = 0; e < 32; ++e) ov[e] *= alpha;
+                tc::tmem_st32(t_o + lane_base + half * (DH / 2) + c, ov);
+            }
+        }
+        tc::fence_proxy_async_smem();
+        tc::fence_before_sync();
+        __syncthreads();
+        tc::fence_after_sync();
+
+        // ---- O += P_j V_j
+        if (tid == 0) {
+            constexpr uint32_t idesc = tc::idesc_bf16(128, DH, 1);
+#pragma unroll
+            for (int ks = 0; ks < kTcSub / 16; ++ks) {
+                const uint64_t ad = tc::sdesc_sw128(tc::smem_addr(kp_s) + ks * 32, 16, 1024);
+                const uint64_t bd =
+                    tc::sdesc_sw128(tc::smem_addr(v_s) + ks * 16 * 128, kTcSub * 128, 1024);
+                tc::mma_bf16_ss(t_o, ad, bd, idesc, (done > 0 || ks > 0) ? 1u : 0u);
+            }
+            tc::mma_commit(&bar_o);
+        }
+        __syncwarp();
+        ++done;
     }
-    __syncwarp();
-    if (ok_s && !tc::mbar_wait_bounded(&bar_o, 0, kWaitPolls)) {
+    // ---- wait for the last P V, then write the partial rows
+    if (done > 0 && !tc::mbar_wait_bounded(&bar_o, (done - 1) & 1, kWaitPolls)) {
         failed = 1;
-        set_status(a.status, MEDUSA_DEV_TIMEOUT);
-        tc::mbar_wait_bounded(&bar_o, 0, kWaitPolls);  // let the MMAs drain before freeing TMEM
+        tc::mbar_wait_bounded(&bar_o, (done - 1) & 1, kWaitPolls);  // drain before freeing TMEM
     }
+    cp_async_wait<0>();
     tc::fence_after_sync();
     __syncthreads();
-    const bool ok_o = !failed;  // uniform over the CTA: tcgen05.ld is warp-collective
-    if (ok_o) {
+    const bool ok = !failed && done == nsub;  // uniform over the CTA
+    if (failed && tid == 0) set_status(a.status, MEDUSA_DEV_TIMEOUT);
+    if (ok) {
         // this thread's half of the row's DH output columns
-        float ov[32];
         float *dst = a.part_o + (pbase + row) * DH;
         for (int c = half * (DH / 2); c < (half + 1) * (DH / 2); c += 32) {
+            float ov[32];
             tc::tmem_ld32(t_o + lane_base + c, ov);
             if (row < R) {
 #pragma unroll
-                for (int j = 0; j < 32; j += 4)
-                    *reinterpret_cast<float4 *>(dst + c + j) =
-                        make_float4(ov[j], ov[j + 1], ov[j + 2], ov[j + 3]);
+                for (int e = 0; e < 32; e += 4)
+                    *reinterpret_cast<float4 *>(dst + c + e) =
+                        make_float4(ov[e], ov[e + 1], ov[e + 2], ov[e + 3]);
             }
         }
     }
+    // row sums: halves exchange through the Q tile (no MMA reads it any more)
+    float *xs = reinterpret_cast<float *>(q_s);
+    xs[half * 128 + row] = l_run;
+    __syncthreads();
     if (half == 0 && row < R) {
-        const float l = xch[row] + xch[128 + row];
-        a.part_ml[pbase + row] = ok_o ? make_float2(m, l) : make_float2(-INFINITY, 0.f);
+        const float l = xs[row] + xs[128 + row];
+        a.part_ml[pbase + row] = ok ? make_float2(m_run, l) : make_float2(-INFINITY, 0.f);
     }
     tc::fence_before_sync();
     __syncthreads();
@@ -704,13 +754,27 @@ void split_plan(int B, int H, int P_max, int *nps, int *chunk) {
 
 size_t align256(size_t x) { return (x + 255) & ~size_t(255); }
 
+// Key ranges of the tensor-core path: at least two 64-key sub-chunks per CTA
+// (so that loads overlap compute), and about two waves of two CTAs per SM
+// over the whole grid at P_max (ragged batches balance better with two).
+void tc_plan(int B, int H, int R, int P_max, int *ns, int *chunk) {
+    const int nsub = (P_max + R + kTcSub - 1) / kTcSub;
+    const int per_head = std::max(1, 4 * device_sm_count() / std::max(1, B * H));
+    const int cps = std::max(2, (nsub + per_head - 1) / per_head);
+    *ns = (nsub + cps - 1) / cps;
+    *chunk = cps * kTcSub;
+}
+
 }  // namespace
 
 size_t attention_workspace_bytes(medusa_dtype dtype, int B, int R, int H, int dh, int P_max) {
     if (dtype == MEDUSA_F32) return MEDUSA_WS_HEADER;
     int nps, chunk;
-    split_plan(B, H, P_max, &nps, &chunk);
-    const int NS = R <= 128 ? (P_max + R + kChunk - 1) / kChunk : nps + 1;
+    if (R <= 128)
+        tc_plan(B, H, R, P_max, &nps, &chunk);
+    else
+        split_plan(B, H, P_max, &nps, &chunk);
+    const int NS = R <= 128 ? nps : nps + 1;
     const size_t rows = (size_t)B * H * NS * R;
     return MEDUSA_WS_HEADER + align256(rows * dh * sizeof(float)) + align256(rows * sizeof(float2));
 }
@@ -736,8 +800,10 @@ cudaError_t launch_tree_attention(medusa_dtype dtype, const void *q, const void 
     }
     const bool use_tc = R <= 128;
     int nps, chunk;
-    split_plan(B, H, P_max, &nps, &chunk);
-    if (use_tc) nps = (P_max + R + kChunk - 1) / kChunk;  // chunks per head
+    if (use_tc)
+        tc_plan(B, H, R, P_max, &nps, &chunk);  // key ranges per head
+    else
+        split_plan(B, H, P_max, &nps, &chunk);
     const int NS = use_tc ? nps : nps + 1;
     const size_t rows = (size_t)B * H * NS * R;
     char *w = static_cast<char *>(ws) + MEDUSA_WS_HEADER;
