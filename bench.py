@@ -434,17 +434,29 @@ def run_ours(args, cfg):
                     if path_np[b, qq] != qq))
     commit_bytes = 2 * 2 * moved * row_bytes  # K and V, each row read once and written once
     reps = max(args.steps, 20)
+    host_us = {}  # wall time per call of each timed loop (host enqueue included)
 
     def timed_loop(fn):
+        """GPU microseconds per call.  A short call can take longer to enqueue
+        on the host than to run, so a sleep kernel first holds the stream
+        while the host queues every call; the events then bracket GPU
+        execution alone."""
         for _ in range(3):
             fn()
-        a, z = torch.cuda.Event(enable_timing=True), torch.cuda.Event(enable_timing=True)
         torch.cuda.synchronize(dev)
+        t0 = time.perf_counter()
+        for _ in range(reps):
+            fn()
+        torch.cuda.synchronize(dev)
+        wall = time.perf_counter() - t0
+        a, z = torch.cuda.Event(enable_timing=True), torch.cuda.Event(enable_timing=True)
+        torch.cuda._sleep(int(2.5e9 * (2 * wall + 2e-4)))  # > the enqueue time, at <= 2.5 GHz
         a.record(stream)
         for _ in range(reps):
             fn()
         z.record(stream)
         torch.cuda.synchronize(dev)
+        host_us[fn.__name__] = round(wall / reps * 1e6, 2)
         return a.elapsed_time(z) / reps * 1e3  # microseconds
 
     def post_only():
@@ -489,7 +501,8 @@ def run_ours(args, cfg):
         "GB/s": round(commit_bytes / (us_commit * 1e-6) / 1e9, 1),
         "fused_posterior_commit_us": round(us_post_commit, 2),
         "posterior_alone_us": round(us_post, 2),
-        "note": "launch-latency bound: a few hundred KB per step"},
+        "note": "launch-latency bound: a few hundred KB per step",
+        "host_loop_us": {k: v for k, v in host_us.items()}},
         "heads_lm": {
             "us": round(us_heads_lm, 2), "bytes": int(lm_bytes),
             "GB/s": round(lm_bytes / (us_heads_lm * 1e-6) / 1e9, 1),

@@ -311,41 +311,39 @@ __global__ void __launch_bounds__(MAXW * 32, 1) tree_attn_split_kernel(AttnArgs 
 //
 // tree_attn_tc_kernel: one CTA per (key range, head, sequence).  The keys of
 // a sequence are its cache slots 0 .. P+R-1, prefix and tree alike (they are
-// contiguous); a key range is `cps` consecutive sub-chunks of 64 keys, walked
-// with a two-stage cp.async pipeline (sub-chunk j+1 loads while j computes).
+// contiguous); a key range is `cps` consecutive sub-chunks of 64 keys.  K and
+// V of the sub-chunks stream through a three-stage cp.async ring in shared
+// memory (two sub-chunks in flight while one computes); Q, S, P and O live
+// in tensor memory:
+//     columns [0, 64)        S = Q K_j^T (fp32), then P over it (bf16 pairs)
+//     columns [64, 64+DH/2)  Q (bf16 pairs, one query row per lane)
+//     columns [128, 128+DH)  O += P V_j (fp32)
 // 256 threads: threads t and t+128 own query row t (rows >= R are zero), each
-// taking half of a sub-chunk's keys and half of the output columns.  Q, K and
-// V sit in 128-byte-swizzled shared memory; one thread issues the MMAs:
-//     S[128 x 64] = Q K_j^T           (TMEM columns 0..63)
-//     O[128 x DH] += P_j V_j          (TMEM columns 128..)
-// Between them every thread reads its S row half from TMEM, masks it (slots
-// past the range; tree slots that are not ancestors-or-self of the row) and
-// writes P = 2^(s*scale*log2e - m) as bf16 over K_j (no longer needed).  The
-// row reference m is raised only when a sub-chunk's max exceeds it by more
-// than 2^8; the threads then rescale their O row in TMEM.  Otherwise P may
-// reach 2^8, harmless in bf16 and fp32.  The CTA writes one unnormalised
-// partial (O, m, l) per row; tree_attn_combine_kernel merges the ranges.
-// Every mbarrier wait is bounded; on a timeout the CTA records
-// MEDUSA_DEV_TIMEOUT, stops, waits once more (bounded) for its MMAs and frees
-// its tensor memory before returning.
+// taking half of a sub-chunk's keys and half of the output columns; one
+// thread issues the MMAs (A from tensor memory, B from shared memory).  Every
+// thread reads its S half-row, masks it (slots past the range; tree slots
+// that are not ancestors-or-self of the row) and writes P = 2^(s*scale*log2e
+// - m) back over the S columns it read.  The row reference m is raised only
+// when a sub-chunk's max exceeds it by more than 2^8; the threads then
+// rescale their O row in tensor memory.  Otherwise P may reach 2^8, harmless
+// in bf16 and fp32.  The CTA writes one unnormalised partial (O, m, l) per
+// row; tree_attn_combine_kernel merges the ranges.  Every mbarrier wait is
+// bounded; on a timeout the CTA records MEDUSA_DEV_TIMEOUT, stops, waits once
+// more (bounded) for its MMAs and frees its tensor memory before returning.
 constexpr int kTcSub = 64;               // keys per pipeline stage
+constexpr int kTcStages = 3;
 constexpr float kRescaleLog2 = 8.f;      // lazy-rescale threshold (log2 units)
 constexpr uint32_t kWaitPolls = 1u << 16;
 
 template <int DH>
 struct TcSmem {
     static constexpr int NB = DH / 64;                 // 64-element column blocks of dh
-    static constexpr int Q_BYTES = NB * 128 * 128;      // [NB][128 rows][128 B]
-    static constexpr int K_BYTES = NB * kTcSub * 128;     // [NB][64 keys][128 B]
-    static constexpr int P_BYTES = 128 * 128;           // [128 rows][64 keys] bf16
-    static constexpr int KP_BYTES = K_BYTES > P_BYTES ? K_BYTES : P_BYTES;
-    static constexpr int V_BYTES = NB * kTcSub * 128;     // [NB][64 keys][128 B]
-    static constexpr int STAGE_BYTES = KP_BYTES + V_BYTES;
-    static constexpr int Q_OFF = 0;
-    static constexpr int ST_OFF = Q_BYTES;              // two stages
+    static constexpr int K_BYTES = NB * kTcSub * 128;   // [NB][64 keys][128 B]
+    static constexpr int V_BYTES = NB * kTcSub * 128;   // [NB][64 keys][128 B]
+    static constexpr int STAGE_BYTES = K_BYTES + V_BYTES;
     // two CTAs per SM stay within the same shared-memory carveout as the heads
     // kernels (2 x 96 KB): a larger carveout would shrink L1 under them
-    static constexpr int BAR_OFF = ST_OFF + 2 * STAGE_BYTES;  // mbarriers, TMEM holder, flag
+    static constexpr int BAR_OFF = kTcStages * STAGE_BYTES;  // mbarriers, TMEM holder, flag
     // 2 x (TOTAL + 1 KB reserved per CTA) must stay within a 196 KB carveout
     static constexpr int TOTAL = BAR_OFF + 64;
 };
@@ -353,7 +351,7 @@ struct TcSmem {
 // Issue the cp.async copies of sub-chunk keys [k0, k0+kTcSub) (rows past kend
 // are zero-filled) into one stage; every thread commits one group.
 template <int DH>
-__device__ __forceinline__ void tc_load_stage(unsigned char *kp_s, unsigned char *v_s,
+__device__ __forceinline__ void tc_load_stage(unsigned char *k_s, unsigned char *v_s,
                                               const bf16 *kc, const bf16 *vc, int k0, int kend,
                                               int H, int h, int tid) {
     constexpr int CPR = (DH / 64) * 8;  // 16-byte chunks per key row
@@ -363,7 +361,7 @@ __device__ __forceinline__ void tc_load_stage(unsigned char *kp_s, unsigned char
         const bool ok = key < kend;
         const size_t off = ((size_t)(ok ? key : k0) * H + h) * DH + c16 * 8;
         const uint32_t so = (c16 >> 3) * kTcSub * 128 + tc::sw128(r, c16 & 7);
-        cp_async16(tc::smem_addr(kp_s + so), kc + off, ok ? 16 : 0);
+        cp_async16(tc::smem_addr(k_s + so), kc + off, ok ? 16 : 0);
         cp_async16(tc::smem_addr(v_s + so), vc + off, ok ? 16 : 0);
     }
     cp_async_commit();
@@ -373,17 +371,17 @@ template <int DH>
 __global__ void __launch_bounds__(256, 2) tree_attn_tc_kernel(AttnArgs a) {
     pdl_enter();
     using L = TcSmem<DH>;
-    constexpr int NB = L::NB;
     constexpr int HALF = kTcSub / 2;  // keys per thread per sub-chunk
     // operand tiles need 1024-byte alignment (swizzle atoms)
     extern __shared__ __align__(1024) unsigned char tc_raw[];
-    unsigned char *q_s = tc_raw + L::Q_OFF;
     uint64_t &bar_s = *reinterpret_cast<uint64_t *>(tc_raw + L::BAR_OFF);
     uint64_t &bar_o = *reinterpret_cast<uint64_t *>(tc_raw + L::BAR_OFF + 8);
     uint32_t &tmem_holder = *reinterpret_cast<uint32_t *>(tc_raw + L::BAR_OFF + 16);
     int &failed = *reinterpret_cast<int *>(tc_raw + L::BAR_OFF + 20);
 
-    const int split = blockIdx.x, h = blockIdx.y, b = blockIdx.z;
+    // heads vary fastest in the grid, so CTAs resident together read whole
+    // token rows ([H, dh] per slot) of the same key range
+    const int h = blockIdx.x, split = blockIdx.y, b = blockIdx.z;
     const int R = a.R, H = a.H;
     const int tid = threadIdx.x, warp = tid >> 5;
     // warp w reads TMEM lanes 32*(w%4)..: row = tid % 128; half = column half
@@ -406,22 +404,34 @@ __global__ void __launch_bounds__(256, 2) tree_attn_tc_kernel(AttnArgs a) {
         return;
     }
     const int nsub = (kend - kbeg + kTcSub - 1) / kTcSub;
-    auto stage_k = [&](int j) { return tc_raw + L::ST_OFF + (j & 1) * L::STAGE_BYTES; };
-    auto stage_v = [&](int j) { return tc_raw + L::ST_OFF + (j & 1) * L::STAGE_BYTES + L::KP_BYTES; };
+    auto stage_k = [&](int j) { return tc_raw + (j % kTcStages) * L::STAGE_BYTES; };
+    auto stage_v = [&](int j) { return tc_raw + (j % kTcStages) * L::STAGE_BYTES + L::K_BYTES; };
 
-    // ---- Q and the first sub-chunk (group 0), the second sub-chunk (group 1)
-    constexpr int CPRQ = NB * 8;
-    for (int i = tid; i < 128 * CPRQ; i += 256) {
-        const int r = i / CPRQ, c16 = i - r * CPRQ;
-        const bool ok = r < R;
-        const bf16 *src = a.q + (((size_t)b * R + (ok ? r : 0)) * H + h) * DH + c16 * 8;
-        cp_async16(tc::smem_addr(q_s + (c16 >> 3) * 128 * 128 + tc::sw128(r, c16 & 7)), src,
-                   ok ? 16 : 0);
+    // ---- Q row into registers first (its latency overlaps the K/V issue):
+    // 64 elements per thread (dh 128: each half of the row; dh 64: the whole
+    // row, by the first 128 threads)
+    const bool q_owner = DH == 128 || half == 0;  // warp-uniform
+    const int e0 = DH == 128 ? half * 64 : 0;
+    uint32_t qr[32];
+#pragma unroll
+    for (int i = 0; i < 32; ++i) qr[i] = 0u;
+    if (q_owner && row < R) {
+        const uint4 *src =
+            reinterpret_cast<const uint4 *>(a.q + (((size_t)b * R + row) * H + h) * DH + e0);
+#pragma unroll
+        for (int i = 0; i < 8; ++i) {
+            const uint4 v = src[i];
+            qr[4 * i] = v.x;
+            qr[4 * i + 1] = v.y;
+            qr[4 * i + 2] = v.z;
+            qr[4 * i + 3] = v.w;
+        }
     }
+
+    // ---- the first two sub-chunks start loading
     tc_load_stage<DH>(stage_k(0), stage_v(0), kc, vc, kbeg, kend, H, h, tid);
     if (nsub > 1) tc_load_stage<DH>(stage_k(1), stage_v(1), kc, vc, kbeg + kTcSub, kend, H, h, tid);
-    // this row's ancestor-mask words (only ranges that reach the tree)
-    // (this path serves R <= 128: two mask words)
+    // this row's ancestor-mask words (this path serves R <= 128: two words)
     uint64_t am0 = 0, am1 = 0;
     if (kend > P && row < R) {
         const int W = (R + 63) / 64;
@@ -439,25 +449,38 @@ __global__ void __launch_bounds__(256, 2) tree_attn_tc_kernel(AttnArgs a) {
     __syncthreads();
     tc::fence_after_sync();
     const uint32_t tmem = tmem_holder;
-    const uint32_t t_s = tmem, t_o = tmem + 128;
+    const uint32_t t_s = tmem, t_q = tmem + 64, t_o = tmem + 128;
     const uint32_t lane_base = (uint32_t)((warp & 3) * 32) << 16;
+
+    // ---- Q row into tensor memory
+    if (q_owner) {
+        tc::tmem_st32u(t_q + lane_base + e0 / 2, qr);
+        tc::tmem_wait_st();
+    }
+    // warps whose 32 rows are all padding (>= R) skip the softmax: their S
+    // rows are zero (zero Q rows), which read as zero P, and their O rows are
+    // never written out
+    const bool rows_live = (warp & 3) * 32 < R;  // warp-uniform
 
     float m_run = -INFINITY;  // row reference (log2 units), same in both threads of a row
     float l_run = 0.f;        // this thread's share of the row sum
     int done = 0;             // sub-chunks whose P V MMA was issued
     for (int j = 0; j < nsub; ++j) {
-        unsigned char *kp_s = stage_k(j);
+        unsigned char *k_s = stage_k(j);
         unsigned char *v_s = stage_v(j);
         const int k0 = kbeg + j * kTcSub;
-        if (j > 0) {
-            // P V of sub-chunk j-1 done: its stage may be refilled, O may be rescaled
-            if (!tc::mbar_wait_bounded(&bar_o, (j - 1) & 1, kWaitPolls)) failed = 1;
-            if (j + 1 < nsub)
-                tc_load_stage<DH>(stage_k(j + 1), stage_v(j + 1), kc, vc, k0 + kTcSub, kend, H, h,
-                                  tid);
-        }
-        if (j + 1 < nsub)
-            cp_async_wait<1>();  // sub-chunk j+1 may still be in flight
+        // P V of sub-chunk j-1 done: its stage may be refilled (with j+2) and O
+        // may be rescaled
+        if (j > 0 && !tc::mbar_wait_bounded(&bar_o, (j - 1) & 1, kWaitPolls)) failed = 1;
+        if (j + 2 < nsub)
+            tc_load_stage<DH>(stage_k(j + 2), stage_v(j + 2), kc, vc, k0 + 2 * kTcSub, kend, H, h,
+                              tid);
+        // groups committed after sub-chunk j's: j+1 and j+2 where they exist
+        const int newer = min(2, nsub - 1 - j);
+        if (newer == 2)
+            cp_async_wait<2>();
+        else if (newer == 1)
+            cp_async_wait<1>();
         else
             cp_async_wait<0>();
         tc::fence_proxy_async_smem();
@@ -466,16 +489,14 @@ __global__ void __launch_bounds__(256, 2) tree_attn_tc_kernel(AttnArgs a) {
         tc::fence_after_sync();
         if (failed) break;  // uniform: read after the barrier
 
-        // ---- S = Q K_j^T
+        // ---- S = Q K_j^T (A = Q in tensor memory, B = K_j in shared memory)
         if (tid == 0) {
             constexpr uint32_t idesc = tc::idesc_bf16(128, kTcSub, 0);
 #pragma unroll
             for (int ks = 0; ks < DH / 16; ++ks) {
-                const uint32_t off = (ks >> 2) * 128 * 128 + (ks & 3) * 32;
-                const uint64_t ad = tc::sdesc_sw128(tc::smem_addr(q_s) + off, 16, 1024);
                 const uint32_t koff = (ks >> 2) * kTcSub * 128 + (ks & 3) * 32;
-                const uint64_t bd = tc::sdesc_sw128(tc::smem_addr(kp_s) + koff, 16, 1024);
-                tc::mma_bf16_ss(t_s, ad, bd, idesc, ks > 0);
+                const uint64_t bd = tc::sdesc_sw128(tc::smem_addr(k_s) + koff, 16, 1024);
+                tc::mma_bf16_ts(t_s, t_q + ks * 8, bd, idesc, ks > 0);
             }
             tc::mma_commit(&bar_s);
         }
@@ -485,9 +506,14 @@ __global__ void __launch_bounds__(256, 2) tree_attn_tc_kernel(AttnArgs a) {
 
         // ---- this thread's 32 keys of the sub-chunk
         float x[HALF];
-        tc::tmem_ld32(t_s + lane_base + half * HALF, x);
+        if (rows_live) {
+            tc::tmem_ld32(t_s + lane_base + half * HALF, x);
+        } else {
+#pragma unroll
+            for (int e = 0; e < HALF; ++e) x[e] = -INFINITY;
+        }
         const int kc0 = k0 + half * HALF;
-        const bool masked = k0 + kTcSub > P || k0 + kTcSub > kend;
+        const bool masked = (k0 + kTcSub > P || k0 + kTcSub > kend) && rows_live;
         float mx[4] = {-INFINITY, -INFINITY, -INFINITY, -INFINITY};
         if (!masked) {
 #pragma unroll
@@ -502,47 +528,41 @@ __global__ void __launch_bounds__(256, 2) tree_attn_tc_kernel(AttnArgs a) {
                 bool vis = key < kend;
                 if (vis && key >= P) {
                     const int t = key - P;
-                    const uint64_t mw = (t < 64) ? am0 : am1;
-                    vis = (mw >> (t & 63)) & 1u;
+                    vis = (((t < 64) ? am0 : am1) >> (t & 63)) & 1u;
                 }
                 x[e] = vis ? x[e] * a.scale_log2 : -INFINITY;
                 mx[e & 3] = fmaxf(mx[e & 3], x[e]);
             }
         }
-        // row max of the sub-chunk: exchange halves through the dead K_j tile
-        float *xch = reinterpret_cast<float *>(kp_s);
+        // row max of the sub-chunk: halves exchange through the dead K_j tile
+        // (it is refilled only after the barrier that ends this iteration)
+        float *xch = reinterpret_cast<float *>(k_s);
         xch[half * 128 + row] = fmaxf(fmaxf(mx[0], mx[1]), fmaxf(mx[2], mx[3]));
         __syncthreads();
         const float cm = fmaxf(xch[row], xch[128 + row]);
-        __syncthreads();  // both halves have read xch before P overwrites it
         const bool raise = cm > m_run + kRescaleLog2;
         const float m_new = raise ? cm : m_run;
         const float alpha = raise ? exp2f(m_run - m_new) : 1.f;  // 0 when m_run = -inf
         l_run *= alpha;
         m_run = m_new;
         const float mu = (m_run == -INFINITY) ? 0.f : m_run;
-        float ls[4] = {0.f, 0.f, 0.f, 0.f};
+        if (rows_live) {
+            float ls[4] = {0.f, 0.f, 0.f, 0.f};
+            uint32_t pk[HALF / 2];
 #pragma unroll
-        for (int q8 = 0; q8 < HALF / 8; ++q8) {
-            float p[8];
-#pragma unroll
-            for (int e = 0; e < 8; ++e) p[e] = exp2f(x[q8 * 8 + e] - mu);
-            uint4 w;
-            w.x = pack_bf16(p[0], p[1]);
-            w.y = pack_bf16(p[2], p[3]);
-            w.z = pack_bf16(p[4], p[5]);
-            w.w = pack_bf16(p[6], p[7]);
-            // the row sum adds the rounded weights the MMA uses, so that the
-            // output is an exact convex combination of V rows under them
-            ls[0] += bf_lo(w.x) + bf_hi(w.x);
-            ls[1] += bf_lo(w.y) + bf_hi(w.y);
-            ls[2] += bf_lo(w.z) + bf_hi(w.z);
-            ls[3] += bf_lo(w.w) + bf_hi(w.w);
-            // keys half*32 + 8*q8 .. +7 of the single 64-key column block
-            *reinterpret_cast<uint4 *>(kp_s + tc::sw128(row, half * 4 + q8)) = w;
+            for (int e = 0; e < HALF; e += 2) {
+                const uint32_t w = pack_bf16(exp2f(x[e] - mu), exp2f(x[e + 1] - mu));
+                pk[e / 2] = w;
+                // the row sum adds the rounded weights the MMA uses, so that the
+                // output is an exact convex combination of V rows under them
+                ls[(e / 2) & 3] += bf_lo(w) + bf_hi(w);
+            }
+            l_run += (ls[0] + ls[1]) + (ls[2] + ls[3]);
+            // P over the S columns this thread read: keys half*32.. -> columns
+            // half*32 .. half*32+15
+            tc::tmem_st16(t_s + lane_base + half * HALF, pk);
         }
-        l_run += (ls[0] + ls[1]) + (ls[2] + ls[3]);
-        if (__any_sync(0xffffffffu, raise && done > 0)) {
+        if (rows_live && __any_sync(0xffffffffu, raise && done > 0)) {
             // rescale this warp's O rows (lanes whose row did not move scale by
             // 1); P V of sub-chunk j-1 is complete, P V of j not yet issued
 #pragma unroll 1
@@ -554,20 +574,20 @@ __global__ void __launch_bounds__(256, 2) tree_attn_tc_kernel(AttnArgs a) {
                 tc::tmem_st32(t_o + lane_base + half * (DH / 2) + c, ov);
             }
         }
-        tc::fence_proxy_async_smem();
+        tc::tmem_wait_st();
         tc::fence_before_sync();
         __syncthreads();
         tc::fence_after_sync();
 
-        // ---- O += P_j V_j
+        // ---- O += P_j V_j (A = P in tensor memory, B = V_j in shared memory)
         if (tid == 0) {
             constexpr uint32_t idesc = tc::idesc_bf16(128, DH, 1);
 #pragma unroll
             for (int ks = 0; ks < kTcSub / 16; ++ks) {
-                const uint64_t ad = tc::sdesc_sw128(tc::smem_addr(kp_s) + ks * 32, 16, 1024);
+                const uint32_t pa = t_s + (ks >> 1) * HALF + (ks & 1) * 8;
                 const uint64_t bd =
                     tc::sdesc_sw128(tc::smem_addr(v_s) + ks * 16 * 128, kTcSub * 128, 1024);
-                tc::mma_bf16_ss(t_o, ad, bd, idesc, (done > 0 || ks > 0) ? 1u : 0u);
+                tc::mma_bf16_ts(t_o, pa, bd, idesc, (done > 0 || ks > 0) ? 1u : 0u);
             }
             tc::mma_commit(&bar_o);
         }
@@ -598,8 +618,8 @@ __global__ void __launch_bounds__(256, 2) tree_attn_tc_kernel(AttnArgs a) {
             }
         }
     }
-    // row sums: halves exchange through the Q tile (no MMA reads it any more)
-    float *xs = reinterpret_cast<float *>(q_s);
+    // row sums: halves exchange through stage 0 (no copy is in flight now)
+    float *xs = reinterpret_cast<float *>(tc_raw);
     xs[half * 128 + row] = l_run;
     __syncthreads();
     if (half == 0 && row < R) {
@@ -755,11 +775,14 @@ void split_plan(int B, int H, int P_max, int *nps, int *chunk) {
 size_t align256(size_t x) { return (x + 255) & ~size_t(255); }
 
 // Key ranges of the tensor-core path: at least two 64-key sub-chunks per CTA
-// (so that loads overlap compute), and about two waves of two CTAs per SM
-// over the whole grid at P_max (ragged batches balance better with two).
+// (so that loads overlap compute), and one (B = 1) or two (B > 1) waves of
+// two CTAs per SM over the whole grid at P_max.
 void tc_plan(int B, int H, int R, int P_max, int *ns, int *chunk) {
     const int nsub = (P_max + R + kTcSub - 1) / kTcSub;
-    const int per_head = std::max(1, 4 * device_sm_count() / std::max(1, B * H));
+    // one sequence: every range has the same length, one wave is best; a
+    // batch may be ragged (P_b unknown here), two waves balance it better
+    const int waves = B == 1 ? 1 : 2;
+    const int per_head = std::max(1, 2 * waves * device_sm_count() / std::max(1, B * H));
     const int cps = std::max(2, (nsub + per_head - 1) / per_head);
     *ns = (nsub + cps - 1) / cps;
     *chunk = cps * kTcSub;
@@ -830,7 +853,7 @@ cudaError_t launch_tree_attention(medusa_dtype dtype, const void *q, const void 
         const int smem = dh == 128 ? TcSmem<128>::TOTAL : TcSmem<64>::TOTAL;
         if ((e = cudaFuncSetAttribute(kern, cudaFuncAttributeMaxDynamicSharedMemorySize, smem)))
             return e;
-        e = launch_pdl(kern, dim3(NS, H, B), dim3(256), (size_t)smem, stream, a);
+        e = launch_pdl(kern, dim3(H, NS, B), dim3(256), (size_t)smem, stream, a);
         note_launch();
         if (e) return e;
     } else {
