@@ -6,7 +6,9 @@
  *   1. medusa_heads               K Medusa heads read the last hidden state and
  *                                 keep their top-s tokens (medusa_heads_lm:
  *                                 the LM head's root token in the same pass).
- *   2. medusa_build_tree          the proposals become a budgeted candidate tree.
+ *   2. medusa_build_tree          the proposals become a budgeted candidate tree
+ *                                 (medusa_build_tree_static: its shape from a
+ *                                 calibrated table instead).
  *   3. medusa_tree_attention      every tree node attends to the prefix and to
  *                                 its own ancestors.
  *   4. medusa_evaluate_posterior  greedy or typical acceptance; the longest
@@ -235,6 +237,30 @@ MEDUSA_API medusa_status medusa_build_tree(const int32_t *root, const int32_t *t
                                 int32_t *pos_id, uint64_t *anc_mask,
                                 int32_t *paths, int32_t *n_leaf, void *ws,
                                 size_t ws_bytes, medusa_stream stream);
+
+/* ------------------------------------------------------------------------
+ * 2b. Candidate tree from a calibrated, static table.
+ *
+ * [P2] §6.2: the per-level weights a_k^(i) (how often head k's rank-i token
+ * is right, measured once on a calibration set) fix the tree's shape; the
+ * greedy construction under the budget is the one of medusa_build_tree,
+ * with log a_k^(i) as the weight of rank i at depth k for every sequence.
+ * The shape is therefore the same for every sequence and every step; the
+ * tokens come from each sequence's own top-s lists.  Calibrating the table
+ * is not part of the library.
+ *
+ *   log_a  [K,top_s]  fp32 (device), log a_k^(i) <= 0; entries i >= s[k]
+ *                     are ignored
+ * Other arguments, outputs and requirements as medusa_build_tree.
+ * ---------------------------------------------------------------------- */
+MEDUSA_API medusa_status medusa_build_tree_static(const int32_t *root, const int32_t *topk_ids,
+                                                  const float *log_a, int B, int K,
+                                                  const int32_t *s_host, int top_s, int n,
+                                                  const int32_t *prefix_len, int32_t *tokens,
+                                                  int32_t *parent, int32_t *depth,
+                                                  int32_t *pos_id, uint64_t *anc_mask,
+                                                  int32_t *paths, int32_t *n_leaf, void *ws,
+                                                  size_t ws_bytes, medusa_stream stream);
 
 /* ------------------------------------------------------------------------
  * 3. Tree attention.

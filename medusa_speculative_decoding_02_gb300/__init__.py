@@ -7,7 +7,7 @@ current CUDA stream, allocates outputs and workspaces with torch, and raises
 the compiled library is missing, importing the calls fails loudly.
 
 Public calls (same names as the C ABI in include/medusa.h):
-    heads, heads_lm, heads_noalloc, build_tree, tree_attention, evaluate_posterior,
+    heads, heads_lm, heads_noalloc, build_tree, build_tree_static, tree_attention, evaluate_posterior,
     commit_kv, evaluate_posterior_commit
 plus workspace-size queries, device-status helpers and launch_count.
 """
@@ -40,7 +40,7 @@ EXPORTS = ("medusa_status_string", "medusa_last_error", "medusa_launch_count",
            "medusa_read_device_status", "medusa_clear_device_status",
            "medusa_heads_workspace_size", "medusa_heads",
            "medusa_heads_lm_workspace_size", "medusa_heads_lm",
-           "medusa_build_tree_workspace_size", "medusa_build_tree",
+           "medusa_build_tree_workspace_size", "medusa_build_tree", "medusa_build_tree_static",
            "medusa_tree_attention_workspace_size", "medusa_tree_attention",
            "medusa_posterior_workspace_size", "medusa_evaluate_posterior",
            "medusa_evaluate_posterior_commit", "medusa_commit_kv")
@@ -78,6 +78,7 @@ def lib() -> ctypes.CDLL:
         "medusa_heads_lm": ([I, P, P, P, P, P, I, I, I, I, I, P, P, P, P, P, S, P], I),
         "medusa_build_tree_workspace_size": ([I, I, I, I], S),
         "medusa_build_tree": ([P, P, P, I, I, P, I, I, P, P, P, P, P, P, P, P, P, S, P], I),
+        "medusa_build_tree_static": ([P, P, P, I, I, P, I, I, P, P, P, P, P, P, P, P, P, S, P], I),
         "medusa_tree_attention_workspace_size": ([I, I, I, I, I, I], S),
         "medusa_tree_attention": ([I, P, P, P, P, I, P, I, I, I, I, F, P, P, S, P], I),
         "medusa_posterior_workspace_size": ([I, I], S),
@@ -258,6 +259,27 @@ def build_tree(root, topk_ids, topk_logp, s: Sequence[int], n: int, prefix_len=N
                                    _ptr(prefix_len), _ptr(t.tokens), _ptr(t.parent), _ptr(t.depth),
                                    _ptr(t.pos_id), _ptr(t.anc_mask), _ptr(t.paths), _ptr(t.n_leaf),
                                    _ptr(ws), ws.numel(), _stream(stream)))
+    return t
+
+
+def build_tree_static(root, topk_ids, log_a, s: Sequence[int], n: int, prefix_len=None, ws=None,
+                      out: Optional[Tree] = None, stream=None) -> Tree:
+    """Candidate tree whose shape comes from a calibrated table log_a [K, top_s]
+    (shared by every sequence); tokens from each sequence's top-s lists."""
+    for t, nm in ((root, "root"), (topk_ids, "topk_ids"), (log_a, "log_a")):
+        _need(t, nm)
+    B, K, S = topk_ids.shape
+    if tuple(log_a.shape) != (K, S) or log_a.dtype != torch.float32:
+        raise ValueError(f"log_a must be float32 [{K}, {S}], got {log_a.dtype} {tuple(log_a.shape)}")
+    s_host = (ctypes.c_int32 * K)(*[int(x) for x in s])
+    if ws is None:
+        ws = new_workspace(build_tree_workspace_size(B, K, S, n), root.device)
+    t = out or Tree.empty(B, n, K, root.device)
+    _check(lib().medusa_build_tree_static(_ptr(root), _ptr(topk_ids), _ptr(log_a), B, K, s_host, S,
+                                          n, _ptr(prefix_len), _ptr(t.tokens), _ptr(t.parent),
+                                          _ptr(t.depth), _ptr(t.pos_id), _ptr(t.anc_mask),
+                                          _ptr(t.paths), _ptr(t.n_leaf), _ptr(ws), ws.numel(),
+                                          _stream(stream)))
     return t
 
 

@@ -196,14 +196,17 @@ size_t medusa_build_tree_workspace_size(int B, int K, int top_s, int n) {
     return tree_workspace_bytes(B, K, top_s, n);
 }
 
-medusa_status medusa_build_tree(const int32_t *root, const int32_t *topk_ids,
-                                const float *topk_logp, int B, int K, const int32_t *s_host,
-                                int top_s, int n, const int32_t *prefix_len, int32_t *tokens,
-                                int32_t *parent, int32_t *depth, int32_t *pos_id,
-                                uint64_t *anc_mask, int32_t *paths, int32_t *n_leaf, void *ws,
-                                size_t ws_bytes, medusa_stream stream) {
-    const char *who = "medusa_build_tree";
-    if (!root || !topk_ids || !topk_logp || !s_host || !tokens || !parent || !depth || !pos_id ||
+}  // extern "C"
+
+namespace {
+
+medusa_status check_tree(const char *who, const int32_t *root, const int32_t *topk_ids,
+                         const float *weights, int B, int K, const int32_t *s_host, int top_s,
+                         int n, const int32_t *tokens, const int32_t *parent,
+                         const int32_t *depth, const int32_t *pos_id, const uint64_t *anc_mask,
+                         const int32_t *paths, const int32_t *n_leaf, const void *ws,
+                         size_t ws_bytes) {
+    if (!root || !topk_ids || !weights || !s_host || !tokens || !parent || !depth || !pos_id ||
         !anc_mask || !paths || !n_leaf)
         return fail(MEDUSA_ERR_INVALID_ARG, "%s: NULL pointer", who);
     if (B < 1) return fail(MEDUSA_ERR_INVALID_ARG, "%s: B=%d", who, B);
@@ -225,9 +228,44 @@ medusa_status medusa_build_tree(const int32_t *root, const int32_t *topk_ids,
     if (n > total)
         return fail(MEDUSA_ERR_INVALID_ARG, "%s: n=%d exceeds the %lld nodes of the full tree",
                     who, n, total);
-    if (medusa_status s = check_ws(ws, ws_bytes, tree_workspace_bytes(B, K, top_s, n), who))
+    return check_ws(ws, ws_bytes, tree_workspace_bytes(B, K, top_s, n), who);
+}
+
+}  // namespace
+
+extern "C" {
+
+medusa_status medusa_build_tree(const int32_t *root, const int32_t *topk_ids,
+                                const float *topk_logp, int B, int K, const int32_t *s_host,
+                                int top_s, int n, const int32_t *prefix_len, int32_t *tokens,
+                                int32_t *parent, int32_t *depth, int32_t *pos_id,
+                                uint64_t *anc_mask, int32_t *paths, int32_t *n_leaf, void *ws,
+                                size_t ws_bytes, medusa_stream stream) {
+    const char *who = "medusa_build_tree";
+    if (medusa_status s = check_tree(who, root, topk_ids, topk_logp, B, K, s_host, top_s, n,
+                                     tokens, parent, depth, pos_id, anc_mask, paths, n_leaf, ws,
+                                     ws_bytes))
         return s;
-    cudaError_t e = launch_build_tree(root, topk_ids, topk_logp, B, K, s_host, top_s, n,
+    cudaError_t e = launch_build_tree(root, topk_ids, topk_logp, false, B, K, s_host, top_s, n,
+                                      prefix_len, tokens, parent, depth, pos_id, anc_mask, paths,
+                                      n_leaf, ws, static_cast<cudaStream_t>(stream));
+    if (e) return cuda_fail(e, who);
+    return MEDUSA_OK;
+}
+
+medusa_status medusa_build_tree_static(const int32_t *root, const int32_t *topk_ids,
+                                       const float *log_a, int B, int K, const int32_t *s_host,
+                                       int top_s, int n, const int32_t *prefix_len,
+                                       int32_t *tokens, int32_t *parent, int32_t *depth,
+                                       int32_t *pos_id, uint64_t *anc_mask, int32_t *paths,
+                                       int32_t *n_leaf, void *ws, size_t ws_bytes,
+                                       medusa_stream stream) {
+    const char *who = "medusa_build_tree_static";
+    if (medusa_status s = check_tree(who, root, topk_ids, log_a, B, K, s_host, top_s, n, tokens,
+                                     parent, depth, pos_id, anc_mask, paths, n_leaf, ws,
+                                     ws_bytes))
+        return s;
+    cudaError_t e = launch_build_tree(root, topk_ids, log_a, true, B, K, s_host, top_s, n,
                                       prefix_len, tokens, parent, depth, pos_id, anc_mask, paths,
                                       n_leaf, ws, static_cast<cudaStream_t>(stream));
     if (e) return cuda_fail(e, who);

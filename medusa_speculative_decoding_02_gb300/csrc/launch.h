@@ -43,8 +43,10 @@ cudaError_t launch_heads(medusa_dtype dtype, const void *h, const void *Wlm, con
                          cudaStream_t stream);
 
 size_t tree_workspace_bytes(int B, int K, int S, int n);
-cudaError_t launch_build_tree(const int32_t *root, const int32_t *ids, const float *logp, int B,
-                              int K, const int32_t *s_host, int S, int n,
+// shared_table: logp is one [K, S] table used by every sequence (a calibrated
+// tree), otherwise [B, K, S].
+cudaError_t launch_build_tree(const int32_t *root, const int32_t *ids, const float *logp,
+                              bool shared_table, int B, int K, const int32_t *s_host, int S, int n,
                               const int32_t *prefix_len, int32_t *tokens, int32_t *parent,
                               int32_t *depth, int32_t *pos_id, uint64_t *anc_mask, int32_t *paths,
                               int32_t *n_leaf, void *ws, cudaStream_t stream);

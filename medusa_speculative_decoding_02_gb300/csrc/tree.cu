@@ -120,6 +120,7 @@ struct TreeArgs {
     const int32_t *root;
     const int32_t *ids;
     const float *logp;
+    long long logp_bstride;  // elements between sequences' tables (0: one shared table)
     int K, S, n;
     long long full;  // nodes of the full Cartesian tree (capped)
     int s[MEDUSA_MAX_HEADS];
@@ -165,7 +166,7 @@ __global__ void __launch_bounds__(kTreeThreads) build_tree_kernel(TreeArgs a) {
 
     for (int i = tid; i < K * S; i += nt) {
         const int k = i / S, r = i - k * S;
-        const float v = a.logp[((size_t)b * K + k) * S + r];
+        const float v = a.logp[(size_t)b * a.logp_bstride + (size_t)k * S + r];
         if (r < a.s[k] && (v > 0.f || v != v)) set_status(a.status, MEDUSA_DEV_BAD_SCORE);
         lp[k][r] = (double)v;
         tid_tok[k][r] = a.ids[((size_t)b * K + k) * S + r];
@@ -346,15 +347,16 @@ size_t tree_workspace_bytes(int B, int K, int S, int n) {
     return MEDUSA_WS_HEADER;
 }
 
-cudaError_t launch_build_tree(const int32_t *root, const int32_t *ids, const float *logp, int B,
-                              int K, const int32_t *s_host, int S, int n,
-                              const int32_t *prefix_len, int32_t *tokens, int32_t *parent,
+cudaError_t launch_build_tree(const int32_t *root, const int32_t *ids, const float *logp,
+                              bool shared_table, int B, int K, const int32_t *s_host, int S,
+                              int n, const int32_t *prefix_len, int32_t *tokens, int32_t *parent,
                               int32_t *depth, int32_t *pos_id, uint64_t *anc_mask, int32_t *paths,
                               int32_t *n_leaf, void *ws, cudaStream_t stream) {
     TreeArgs a;
     a.root = root;
     a.ids = ids;
     a.logp = logp;
+    a.logp_bstride = shared_table ? 0 : (long long)K * S;
     a.K = K;
     {
         long long full = 0, level = 1;

@@ -81,6 +81,22 @@ def test_tree_rejects(L, args, code):
     assert L.medusa_launch_count() == before
 
 
+@pytest.mark.parametrize("args,code", [
+    (dict(n=137), 1), (dict(n=0), 1), (dict(K=9, s=(1,) * 9), 1), (dict(root=None), 1),
+    (dict(ws=None), 3), (dict(B=0), 1), (dict(logp=None), 1)])
+def test_tree_static_rejects(L, args, code):
+    s = args.pop("s", (4, 3, 2, 2, 1))
+    n = args.pop("n", 64)
+    a = dict(root=A, ids=A, logp=A, B=1, K=len(s), S=max(s), ws=WS, ws_bytes=1 << 20)
+    a.update(args)
+    sh = (ctypes.c_int32 * len(s))(*s)
+    before = L.medusa_launch_count()
+    rc = L.medusa_build_tree_static(a["root"], a["ids"], a["logp"], a["B"], a["K"], sh, a["S"], n,
+                                    None, A, A, A, A, A, A, A, a["ws"], a["ws_bytes"], None)
+    assert rc == code
+    assert L.medusa_launch_count() == before
+
+
 def test_tree_full_cartesian_budget_accepted_by_validation(L):
     # n equal to the full node count passes validation; with a NULL output the
     # call must still be rejected before any launch.

@@ -40,6 +40,8 @@ def dev():
 
 def T(a, dev):
     a = np.ascontiguousarray(a)
+    if not a.flags.writeable:
+        a = a.copy()
     if a.dtype == np.uint16:
         return torch.from_numpy(a.view(np.int16)).view(torch.bfloat16).to(dev)
     return torch.from_numpy(a).to(dev)
@@ -252,6 +254,69 @@ def test_tree_worked_example_on_gpu(dev):
     assert paths == {tuple(r - 1 for r in p) for p in g["picks_in_order"]}
     cover = sum(math.prod(a[k][r] for k, r in enumerate(p)) for p in paths)
     assert cover == pytest.approx(g["expected_cover_depth"], abs=1e-6)
+
+
+def run_tree_static(dev, root, ids, log_a, s, n, prefix):
+    t = m.build_tree_static(T(root, dev), T(ids, dev), T(log_a.astype(np.float32), dev), s, n,
+                            prefix_len=T(np.asarray(prefix, np.int32), dev))
+    torch.cuda.synchronize()
+    return tree_np(t)
+
+
+def test_tree_static_worked_example(dev):
+    """The calibrated table of the sparse-tree worked example drives the
+    shape for three sequences with different top-s tokens: every sequence
+    gets the six worked-example nodes, its own tokens, and the arrays equal
+    the oracle's tree built from the same table."""
+    import json
+    import os
+    g = json.load(open(os.path.join(os.path.dirname(__file__), "golden",
+                                    "sparse_tree_worked_example.json")))
+    a = np.array(g["a"], np.float64)
+    B = 3
+    ids = np.array([[[1000 * b + 100 * (k + 1) + r for r in range(2)] for k in range(3)]
+                    for b in range(B)], np.int32)
+    log_a = np.log(a).astype(np.float32)
+    root = np.array([5, 6, 7], np.int32)
+    gt = run_tree_static(dev, root, ids, log_a, (2, 2, 2), g["budget"], [0, 3, 9])
+    ot = oracle.build_tree(root, ids, np.broadcast_to(log_a.astype(np.float64), (B, 3, 2)),
+                           (2, 2, 2), g["budget"], prefix_len=np.array([0, 3, 9], np.int32))
+    check_tree(gt, ot)
+    for b in range(B):
+        paths = set()
+        for i in range(1, g["budget"] + 1):
+            p, x = [], i
+            while x > 0:
+                assert int(gt["tokens"][b, x]) // 1000 == b
+                p.append(int(gt["tokens"][b, x]) % 100)
+                x = int(gt["parent"][b, x])
+            paths.add(tuple(reversed(p)))
+        assert paths == {tuple(r - 1 for r in p) for p in g["picks_in_order"]}
+
+
+@pytest.mark.parametrize("s,n,B", [((4, 3, 2, 2, 1), 64, 8), ((8, 4, 4, 2, 2), 128, 2),
+                                   ((16, 16), 255, 1), ((3, 3, 3), 10, 4)])
+def test_tree_static_random_tables(dev, s, n, B):
+    """Random calibrated tables (accuracies decreasing with rank): the shape is
+    the same for every sequence and the arrays equal both the oracle's and
+    the dynamic builder's on the table broadcast to every sequence."""
+    rng = np.random.default_rng(n + B)
+    K, S = len(s), max(s)
+    acc = np.sort(rng.uniform(0.05, 0.9, size=(K, S)), axis=1)[:, ::-1]
+    log_a = np.log(acc).astype(np.float32)
+    ids = np.stack([np.stack([rng.choice(32000, size=S, replace=False) for _ in range(K)])
+                    for _ in range(B)]).astype(np.int32)
+    root = rng.integers(0, 32000, size=B).astype(np.int32)
+    prefix = rng.integers(0, 2000, size=B).astype(np.int32)
+    gt = run_tree_static(dev, root, ids, log_a, s, n, prefix)
+    full = np.ascontiguousarray(np.broadcast_to(log_a, (B, K, S)))
+    ot = oracle.build_tree(root, ids, full.astype(np.float64), s, n, prefix_len=prefix)
+    check_tree(gt, ot)
+    gd = run_tree(dev, root, ids, full, s, n, prefix)
+    check_tree(gt, gd)
+    for b in range(1, B):
+        assert np.array_equal(gt["parent"][b], gt["parent"][0])
+        assert np.array_equal(gt["depth"][b], gt["depth"][0])
 
 
 def test_tree_from_heads_v7b(dev):
