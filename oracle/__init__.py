@@ -61,6 +61,16 @@ def _load():
             lib.oracle_softmax_entropy.restype = D
             lib.oracle_posterior.argtypes = [I, P, P, P, P, I, I, I, I, I, D, D, D, P, P, P, P, P, P, P]
             lib.oracle_posterior.restype = I
+            U64 = ctypes.c_uint64
+            lib.oracle_philox4x64.argtypes = [P, P, P]
+            lib.oracle_philox4x64.restype = None
+            lib.oracle_uniform.argtypes = [U64, U64, I, I, I, I]
+            lib.oracle_uniform.restype = D
+            lib.oracle_draft_sample.argtypes = [I, P, P, P, P, I, I, I, I, D, U64, U64, P, P, P]
+            lib.oracle_draft_sample.restype = I
+            lib.oracle_speculative_posterior.argtypes = [I, P, P, P, I, I, I, D, U64, U64, P, P,
+                                                         P, P, P, P, P, P, P]
+            lib.oracle_speculative_posterior.restype = I
             lib.oracle_commit_kv.argtypes = [P, P, P, P, P, I, I, ctypes.c_size_t, P]
             lib.oracle_commit_kv.restype = I
             _lib = lib
@@ -250,3 +260,72 @@ def commit_kv(k_caches, v_caches, prefix_len, path, accept_len):
                               _ptr(pl), _ptr(path), _ptr(al), B, K, row_bytes, _ptr(new_pl))
     _check(rc, "commit_kv")
     return new_pl
+
+
+# ------------------------------------------------------- exact sampling ---
+
+RNG_DRAFT, RNG_ACCEPT, RNG_RESAMPLE = 1, 2, 3
+
+
+def philox4x64(ctr, key):
+    """Philox4x64-10 block: four 64-bit words for a 4-word counter and a
+    2-word key."""
+    lib = _load()
+    c = _c(ctr, np.uint64)
+    k = _c(key, np.uint64)
+    out = np.zeros(4, np.uint64)
+    lib.oracle_philox4x64(_ptr(c), _ptr(k), _ptr(out))
+    return out
+
+
+def uniform(seed: int, step: int, purpose: int, b: int, row: int, v: int) -> float:
+    return float(_load().oracle_uniform(seed, step, purpose, b, row, v))
+
+
+def draft_sample(h, W1, b1, W2, temperature: float, seed: int, step: int,
+                 want_logits: bool = True, want_keys: bool = False):
+    """Drafts x_k ~ softmax(head logits / T) by Gumbel-max (see oracle.c, O5).
+    Returns (drafts int32 [B,K], logits [B,K,V] or None, keys [B,K,V] or None)."""
+    lib = _load()
+    h, W1, W2 = _c(h), _c(W1), _c(W2)
+    b1 = None if b1 is None else _c(b1)
+    dt = _dt(h)
+    B, d = h.shape
+    K, V = W2.shape[0], W2.shape[1]
+    drafts = np.zeros((B, K), np.int32)
+    logits = np.zeros((B, K, V), np.float64) if want_logits else None
+    keys = np.zeros((B, K, V), np.float64) if want_keys else None
+    rc = lib.oracle_draft_sample(dt, _ptr(h), _ptr(W1), _ptr(b1), _ptr(W2), B, d, V, K,
+                                 float(temperature), int(seed), int(step), _ptr(drafts),
+                                 _ptr(logits), _ptr(keys))
+    _check(rc, "draft_sample")
+    return drafts, logits, keys
+
+
+def speculative_posterior(logits, tokens, draft_logits, temperature: float, seed: int, step: int,
+                          forced_accept=None, forced_next=None):
+    """Exact speculative sampling on a chain (see oracle.c, O5).  logits
+    [B,K+1,V] float32 or bf16 bits, tokens [B,K+1], draft_logits [B,K,V]
+    float32.  Returns a dict of numpy arrays."""
+    lib = _load()
+    logits = _c(logits)
+    dt = _dt(logits)
+    tokens = _c(tokens, np.int32)
+    dl = _c(draft_logits, np.float32)
+    B, R, V = logits.shape
+    K = R - 1
+    fa = None if forced_accept is None else _c(forced_accept, np.int32)
+    fn = None if forced_next is None else _c(forced_next, np.int32)
+    out = dict(accept_len=np.zeros(B, np.int32), path_tokens=np.zeros((B, K + 1), np.int32),
+               next_token=np.zeros(B, np.int32), accept=np.zeros((B, max(K, 1)), np.int32),
+               margin=np.zeros((B, max(K, 1)), np.float64), sample_row=np.zeros(B, np.int32),
+               sample_keys=np.zeros((B, V), np.float64))
+    rc = lib.oracle_speculative_posterior(
+        dt, _ptr(logits), _ptr(tokens), _ptr(dl), B, V, K, float(temperature), int(seed),
+        int(step), _ptr(fa), _ptr(fn), _ptr(out["accept_len"]), _ptr(out["path_tokens"]),
+        _ptr(out["next_token"]), _ptr(out["accept"]), _ptr(out["margin"]),
+        _ptr(out["sample_row"]), _ptr(out["sample_keys"]))
+    _check(rc, "speculative_posterior")
+    out["accept"] = out["accept"][:, :K]
+    out["margin"] = out["margin"][:, :K]
+    return out

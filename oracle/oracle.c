@@ -16,6 +16,8 @@
  *        unconditional first token), §6.1 (Cartesian tree, node count, tree
  *        mask, shared position index), §6.2 (greedy sparse tree under a
  *        budget, worked example).
+ *        Also [P1] "Acceptance rules" (exact speculative decoding) and
+ *        [P2] §3's remark on recovering the target distribution.
  *   [P3] "Medusa Part I" (sudhirpol522.github.io): Part 2 (greedy
  *        verification stops at the first mismatch; progress guarantee),
  *        Part 3 (ResidualBlock: hidden + SiLU(Linear(hidden)), vocab
@@ -42,6 +44,12 @@
  *                             entropy = ln V)
  *   oracle_softmax_entropy    pinned (uniform row, two-point distribution)
  *   oracle_commit_kv          pinned (hand-built gathers in the tests)
+ *   oracle_philox4x64         pinned (numpy's Philox4x64-10 bit generator)
+ *   oracle_draft_sample       pinned (Gumbel-max frequencies against the
+ *                             closed-form softmax, chi-square)
+ *   oracle_speculative_posterior pinned (emitted-token frequencies equal p;
+ *                             acceptance rate = sum_v min(p, q); q = p
+ *                             accepts every draft)
  * The choice among exactly tied alternatives (equal logits, equal path
  * scores) is fixed by a stated convention, not by the pages.
  */
@@ -627,5 +635,201 @@ int oracle_commit_kv(void *const *k_cache, void *const *v_cache,
         new_prefix_len[b] = P + L + 1;
     }
     free(tmp);
+    return 0;
+}
+
+/* ------------------------------------------------------------------------ */
+/* O5. Exact speculative sampling on a chain of sampled drafts.               */
+/*                                                                            */
+/* [P1] Acceptance rules and [P2] §3 (the remark on lossless recovery) and   */
+/* §5: drafts are sampled from the heads' own normalised distributions q_k;  */
+/* each is accepted with probability min(1, p/q) under the verifying model's */
+/* p; at the first rejection a replacement is sampled from the normalised    */
+/* positive residual max(0, p - q); if every draft is accepted, one more     */
+/* token is sampled from p at the last row.  This preserves p exactly.       */
+/*                                                                            */
+/* Readings (the pages leave these open): q_k = softmax(head logits / T) and */
+/* p = softmax(verification logits / T) with one temperature T; the drafts   */
+/* form a chain x_1..x_K, x_k from head k independently (the heads do not see */
+/* each other's drafts, [P2] §3); the root x_0 is given and accepted.         */
+/* Sampling from weights w_v uses the Gumbel-max rule: the token with the    */
+/* largest log w_v + G_v, G_v = -log(-log u_v), smaller id on exact ties.   */
+/*                                                                            */
+/* Random numbers: Philox4x64-10 (Salmon, Moraes, Dror and Shaw, "Parallel   */
+/* random numbers: as easy as 1, 2, 3", SC 2011), counter = (v / 4, row, b,  */
+/* purpose), key = (seed, step); the uniform for index v is word v % 4 of    */
+/* the output, as ((w >> 41) + 0.5) * 2^-23 (24 significant bits, exactly   */
+/* representable in float32, never 0 or 1).                                  */
+/* ------------------------------------------------------------------------ */
+enum { ORC_RNG_DRAFT = 1, ORC_RNG_ACCEPT = 2, ORC_RNG_RESAMPLE = 3 };
+
+/* 64 x 64 -> 128-bit product from 32-bit halves */
+static void orc_mulhilo64(uint64_t a, uint64_t b, uint64_t *hi, uint64_t *lo)
+{
+    uint64_t a0 = a & 0xffffffffu, a1 = a >> 32, b0 = b & 0xffffffffu, b1 = b >> 32;
+    uint64_t p00 = a0 * b0, p01 = a0 * b1, p10 = a1 * b0, p11 = a1 * b1;
+    uint64_t mid = (p00 >> 32) + (p01 & 0xffffffffu) + (p10 & 0xffffffffu);
+    *lo = (mid << 32) | (p00 & 0xffffffffu);
+    *hi = p11 + (p01 >> 32) + (p10 >> 32) + (mid >> 32);
+}
+
+void oracle_philox4x64(const uint64_t *ctr, const uint64_t *key, uint64_t *out)
+{
+    uint64_t x0 = ctr[0], x1 = ctr[1], x2 = ctr[2], x3 = ctr[3];
+    uint64_t k0 = key[0], k1 = key[1];
+    for (int r = 0; r < 10; ++r) {
+        if (r > 0) {
+            k0 += 0x9E3779B97F4A7C15ull;   /* Weyl increments of the key */
+            k1 += 0xBB67AE8584CAA73Bull;
+        }
+        uint64_t hi0, lo0, hi1, lo1;
+        orc_mulhilo64(0xD2E7470EE14C6C93ull, x0, &hi0, &lo0);
+        orc_mulhilo64(0xCA5A826395121157ull, x2, &hi1, &lo1);
+        uint64_t y0 = hi1 ^ x1 ^ k0, y1 = lo1, y2 = hi0 ^ x3 ^ k1, y3 = lo0;
+        x0 = y0; x1 = y1; x2 = y2; x3 = y3;
+    }
+    out[0] = x0; out[1] = x1; out[2] = x2; out[3] = x3;
+}
+
+double oracle_uniform(uint64_t seed, uint64_t step, int purpose, int b, int row, int v)
+{
+    uint64_t ctr[4] = {(uint64_t)v >> 2, (uint64_t)row, (uint64_t)b, (uint64_t)purpose};
+    uint64_t key[2] = {seed, step}, out[4];
+    oracle_philox4x64(ctr, key, out);
+    return ((double)(out[v & 3] >> 41) + 0.5) * (1.0 / 8388608.0);
+}
+
+static double orc_gumbel(uint64_t seed, uint64_t step, int purpose, int b, int row, int v)
+{
+    return -log(-log(oracle_uniform(seed, step, purpose, b, row, v)));
+}
+
+/* log of the softmax normaliser of x/T over a row */
+static double orc_logz_row(int dtype, const void *x, size_t off, int V, double T)
+{
+    double m = -INFINITY;
+    for (int v = 0; v < V; ++v) {
+        double t = rd(dtype, x, off + v) / T;
+        if (t > m) m = t;
+    }
+    double S = 0.0;
+    for (int v = 0; v < V; ++v)
+        S += exp(rd(dtype, x, off + v) / T - m);
+    return m + log(S);
+}
+
+/* Draft sampling: x_k ~ softmax(logits_k / T) for every (sequence, head) by  */
+/* Gumbel-max on the heads' logits (computed by oracle_heads).  Optional     */
+/* outputs: the logits [B][K][V] and the Gumbel keys [B][K][V].              */
+int oracle_draft_sample(int dtype, const void *h, const void *W1, const void *b1,
+                        const void *W2, int B, int d, int V, int K, double T,
+                        uint64_t seed, uint64_t step, int32_t *drafts,
+                        double *logits_out, double *keys_out)
+{
+    if (!(T > 0.0)) return 1;
+    double *lg = (double *)malloc((size_t)B * K * V * sizeof(double));
+    int32_t *ids = (int32_t *)malloc((size_t)B * K * sizeof(int32_t));
+    double *lp = (double *)malloc((size_t)B * K * sizeof(double));
+    double *lz = (double *)malloc((size_t)B * K * sizeof(double));
+    if (!lg || !ids || !lp || !lz) {
+        free(lg); free(ids); free(lp); free(lz);
+        return 2;
+    }
+    int rc = oracle_heads(dtype, h, W1, b1, W2, B, d, V, K, 1, ids, lp, lg, lz);
+    if (rc == 0) {
+        for (int b = 0; b < B; ++b)
+            for (int k = 0; k < K; ++k) {
+                const double *row = lg + ((size_t)b * K + k) * V;
+                int best = -1;
+                double bk = -INFINITY;
+                for (int v = 0; v < V; ++v) {
+                    double key = row[v] / T + orc_gumbel(seed, step, ORC_RNG_DRAFT, b, k, v);
+                    if (keys_out) keys_out[((size_t)b * K + k) * V + v] = key;
+                    if (best < 0 || key > bk) { best = v; bk = key; }
+                }
+                drafts[(size_t)b * K + k] = best;
+            }
+        if (logits_out) memcpy(logits_out, lg, (size_t)B * K * V * sizeof(double));
+    }
+    free(lg); free(ids); free(lp); free(lz);
+    return rc;
+}
+
+/* Verification of the chain.  logits [B][K+1][V] (row j: the verifying      */
+/* model's distribution of the token after x_j), tokens [B][K+1] (x_0 root,  */
+/* x_1..x_K drafts), draft_logits [B][K][V] float32 (head k's logits, the    */
+/* numerators of q_k).  Outputs accept_len [B], path_tokens [B][K+1] (x_0..  */
+/* x_L, -1 padded), next_token [B] (the replacement, or the bonus token),   */
+/* accept [B][K] (1 accepted, 0 rejected, -1 not reached), margin [B][K]     */
+/* (log p - log q - log u; accepted iff > 0), sample_row [B] (the row the    */
+/* next token was drawn from) and sample_keys [B][V] (its Gumbel keys, -inf  */
+/* where the weight is 0).  forced_accept [B][K] (or NULL) replaces the       */
+/* decisions and forced_next [B] (or NULL) the sampled token, for comparison  */
+/* with a run that took a near-tied decision the other way.                  */
+int oracle_speculative_posterior(int dtype, const void *logits, const int32_t *tokens,
+                                 const float *draft_logits, int B, int V, int K, double T,
+                                 uint64_t seed, uint64_t step, const int32_t *forced_accept,
+                                 const int32_t *forced_next, int32_t *accept_len,
+                                 int32_t *path_tokens, int32_t *next_token, int32_t *accept,
+                                 double *margin, int32_t *sample_row, double *sample_keys)
+{
+    if (!(T > 0.0) || K < 0 || V < 1) return 1;
+    double *pr = (double *)malloc((size_t)V * sizeof(double));
+    if (!pr) return 2;
+    for (int b = 0; b < B; ++b) {
+        const int32_t *tk = tokens + (size_t)b * (K + 1);
+        for (int k = 0; k < K; ++k) {
+            accept[(size_t)b * K + k] = -1;
+            margin[(size_t)b * K + k] = 0.0;
+        }
+        int L = 0;
+        for (int k = 1; k <= K; ++k) {
+            const size_t prow = ((size_t)b * (K + 1) + (k - 1)) * V;
+            const size_t qrow = ((size_t)b * K + (k - 1)) * V;
+            const int x = tk[k];
+            if (x < 0 || x >= V) { free(pr); return 3; }
+            double logp = rd(dtype, logits, prow + x) / T - orc_logz_row(dtype, logits, prow, V, T);
+            double logq = (double)draft_logits[qrow + x] / T - orc_logz_row(ORC_F32, draft_logits, qrow, V, T);
+            double u = oracle_uniform(seed, step, ORC_RNG_ACCEPT, b, k, 0);
+            double mg = logp - logq - log(u);
+            margin[(size_t)b * K + (k - 1)] = mg;
+            int acc = forced_accept ? (forced_accept[(size_t)b * K + (k - 1)] != 0) : (mg > 0.0);
+            accept[(size_t)b * K + (k - 1)] = acc;
+            if (!acc) break;
+            L = k;
+        }
+        /* the next token: residual of row L against q_{L+1}, or p_K */
+        const size_t prow = ((size_t)b * (K + 1) + L) * V;
+        const double lzp = orc_logz_row(dtype, logits, prow, V, T);
+        int use_residual = 0;
+        if (L < K) {
+            const size_t qrow = ((size_t)b * K + L) * V;
+            const double lzq = orc_logz_row(ORC_F32, draft_logits, qrow, V, T);
+            for (int v = 0; v < V; ++v) {
+                double r = exp(rd(dtype, logits, prow + v) / T - lzp) -
+                           exp((double)draft_logits[qrow + v] / T - lzq);
+                pr[v] = r > 0.0 ? log(r) : -INFINITY;
+                if (r > 0.0) use_residual = 1;
+            }
+        }
+        if (!use_residual)   /* all accepted (or an empty residual): sample p_L */
+            for (int v = 0; v < V; ++v)
+                pr[v] = rd(dtype, logits, prow + v) / T - lzp;
+        int best = -1;
+        double bk = -INFINITY;
+        for (int v = 0; v < V; ++v) {
+            double key = pr[v] == -INFINITY ? -INFINITY
+                         : pr[v] + orc_gumbel(seed, step, ORC_RNG_RESAMPLE, b, L, v);
+            if (sample_keys) sample_keys[(size_t)b * V + v] = key;
+            if (key > bk) { best = v; bk = key; }
+        }
+        if (best < 0) best = 0;
+        accept_len[b] = L;
+        next_token[b] = forced_next ? forced_next[b] : best;
+        if (sample_row) sample_row[b] = L;
+        for (int q = 0; q <= K; ++q)
+            path_tokens[(size_t)b * (K + 1) + q] = q <= L ? tk[q] : -1;
+    }
+    free(pr);
     return 0;
 }

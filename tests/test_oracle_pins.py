@@ -508,3 +508,151 @@ def test_typical_decision_at_the_crossing():
         o = oracle.posterior(np.stack([x, x])[None], tokens, parent, depth, 1, oracle.TYPICAL,
                              eps, delta)
         assert int(o["accept"][0, 1]) == want, (a, f(float(a)))
+
+
+# ------------------------------------------------------- exact sampling ----
+
+def _chi2_pvalue(counts, probs):
+    from scipy.stats import chisquare
+    counts = np.asarray(counts, np.float64)
+    probs = np.asarray(probs, np.float64)
+    exp = probs / probs.sum() * counts.sum()
+    keep = exp > 0
+    assert counts[~keep].sum() == 0, "a zero-probability outcome occurred"
+    return chisquare(counts[keep], exp[keep]).pvalue
+
+
+@pytest.mark.parametrize("ctr,key", [
+    ([1, 0, 0, 0], [0, 0]), ([6, 7, 9, 11], [123, 456]), ([2 ** 64 - 1, 3, 0, 0], [99, 2 ** 63]),
+    ([12345, 2 ** 40, 77, 3], [2 ** 64 - 1, 1])])
+def test_philox_matches_numpy(ctr, key):
+    """Philox4x64-10 (Salmon et al., SC 2011) against numpy's implementation of
+    the same generator (which advances its counter once before the first
+    block)."""
+    prev = list(ctr)
+    if prev[0] == 0:
+        prev[0] = 2 ** 64 - 1
+        prev[1] -= 1
+    else:
+        prev[0] -= 1
+    g = np.random.Philox(counter=np.array(prev, np.uint64), key=np.array(key, np.uint64))
+    assert np.array_equal(oracle.philox4x64(ctr, key), g.random_raw(4).astype(np.uint64))
+
+
+def test_uniforms_open_interval_float32_exact():
+    us = [oracle.uniform(7, 3, p, b, r, v) for p in (1, 2, 3) for b in (0, 5) for r in (0, 2)
+          for v in range(9)]
+    for u in us:
+        assert 0.0 < u < 1.0
+        assert float(np.float32(u)) == u
+        assert (u * 2 ** 23 - 0.5) == int(u * 2 ** 23 - 0.5)
+    # word v % 4 of the block for counter (v // 4, row, b, purpose)
+    w = oracle.philox4x64([2, 1, 4, 3], [11, 12])
+    for j in range(4):
+        assert oracle.uniform(11, 12, 3, 4, 1, 8 + j) == ((int(w[j]) >> 41) + 0.5) / 2 ** 23
+
+
+def _onehot_heads(c, d=4, j=1):
+    """Heads whose logits are c[k][v] * h[j] (W1 = 0, so z = h; W2 rows are
+    scaled unit vectors)."""
+    K, V = c.shape
+    W1 = np.zeros((K, d, d), np.float32)
+    W2 = np.zeros((K, V, d), np.float32)
+    W2[:, :, j] = c
+    return W1, W2
+
+
+def test_draft_sampling_frequencies():
+    """Gumbel-max drafts follow softmax(logits / T): 40000 independent
+    sequences, chi-square against the closed-form probabilities per head."""
+    rng = np.random.default_rng(5)
+    c = rng.uniform(-2, 2, size=(2, 6)).astype(np.float32)
+    W1, W2 = _onehot_heads(c)
+    B = 40000
+    h = np.zeros((B, 4), np.float32)
+    h[:, 1] = 1.0
+    T = 0.7
+    drafts, logits, _ = oracle.draft_sample(h, W1, None, W2, T, seed=123, step=4)
+    for k in range(2):
+        np.testing.assert_allclose(logits[0, k], c[k], atol=1e-7)
+        ck = c[k].astype(np.float64)
+        p = np.exp(ck / T - logsumexp(ck / T))
+        counts = np.bincount(drafts[:, k], minlength=6)
+        assert _chi2_pvalue(counts, p) > 1e-4, (k, counts, p)
+
+
+def _spec_case(p_logits, q_logits, B, T=1.0, seed=9, step=2):
+    """Chain of K drafts x_k ~ q_k (oracle's draft sampler) verified against
+    fixed rows p_0..p_K; every sequence has its own random streams."""
+    K, V = q_logits.shape
+    W1, W2 = _onehot_heads(q_logits.astype(np.float32))
+    h = np.zeros((B, 4), np.float32)
+    h[:, 1] = 1.0
+    drafts, _, _ = oracle.draft_sample(h, W1, None, W2, T, seed=seed, step=step)
+    tokens = np.concatenate([np.full((B, 1), 0, np.int32), drafts], axis=1)
+    logits = np.broadcast_to(p_logits.astype(np.float32), (B, K + 1, V))
+    dl = np.broadcast_to(q_logits.astype(np.float32), (B, K, V))
+    return tokens, oracle.speculative_posterior(logits, tokens, dl, T, seed, step)
+
+
+def test_speculative_emits_target_distribution():
+    """[P1] Acceptance rules / [P2] §3: accepting x ~ q with probability
+    min(1, p/q) and resampling from (p - q)+ at the first rejection yields
+    tokens distributed exactly as p.  K = 2 over 60000 sequences: the first
+    emitted token follows p_0; after an accepted first draft the second
+    follows p_1; with both accepted the bonus follows p_2.  The acceptance
+    rate of the first draft is sum_v min(p_0, q_1)."""
+    rng = np.random.default_rng(8)
+    V, K, B = 7, 2, 60000
+    p_logits = rng.normal(0, 1.2, size=(K + 1, V))
+    q_logits = rng.normal(0, 1.2, size=(K, V))
+    tokens, o = _spec_case(p_logits, q_logits, B)
+    p = np.exp(p_logits - logsumexp(p_logits, axis=1, keepdims=True))
+    q = np.exp(q_logits - logsumexp(q_logits, axis=1, keepdims=True))
+    L = o["accept_len"]
+    first = np.where(L >= 1, tokens[:, 1], o["next_token"])
+    assert _chi2_pvalue(np.bincount(first, minlength=V), p[0]) > 1e-4
+    sel = L >= 1
+    second = np.where(L[sel] >= 2, tokens[sel, 2], o["next_token"][sel])
+    assert _chi2_pvalue(np.bincount(second, minlength=V), p[1]) > 1e-4
+    both = L == 2
+    assert _chi2_pvalue(np.bincount(o["next_token"][both], minlength=V), p[2]) > 1e-4
+    rate = np.minimum(p[0], q[0]).sum()
+    n1 = (L >= 1).sum()
+    assert abs(n1 / B - rate) < 5 * math.sqrt(rate * (1 - rate) / B)
+    # bookkeeping: accept flags, path tokens and margins agree with L
+    for b in range(50):
+        assert list(o["path_tokens"][b, :L[b] + 1]) == list(tokens[b, :L[b] + 1])
+        assert (o["path_tokens"][b, L[b] + 1:] == -1).all()
+        assert all(o["accept"][b, :L[b]] == 1) and (L[b] == K or o["accept"][b, L[b]] == 0)
+        assert all((o["margin"][b, :L[b]] > 0))
+
+
+def test_speculative_q_equal_p_accepts_everything():
+    """q = p makes p/q = 1 > u for every u in (0, 1): all K drafts are
+    accepted and the next token is the bonus sample from the last row."""
+    rng = np.random.default_rng(3)
+    V, K, B = 5, 3, 2000
+    lg = rng.normal(0, 1, size=(K, V))
+    p_logits = np.concatenate([lg, rng.normal(0, 1, size=(1, V))])
+    _, o = _spec_case(p_logits, lg, B)
+    assert (o["accept_len"] == K).all()
+    assert (o["sample_row"] == K).all()
+
+
+def test_speculative_replacement_has_positive_residual():
+    """A rejected draft is replaced by a token where p > q (the normalised
+    positive residual puts no mass elsewhere), and T divides both sides'
+    logits."""
+    rng = np.random.default_rng(4)
+    V, K, B, T = 6, 1, 5000, 1.7
+    p_logits = rng.normal(0, 2, size=(K + 1, V))
+    q_logits = rng.normal(0, 2, size=(K, V))
+    tokens, o = _spec_case(p_logits, q_logits, B, T=T)
+    p = np.exp(p_logits[0] / T - logsumexp(p_logits[0] / T))
+    q = np.exp(q_logits[0] / T - logsumexp(q_logits[0] / T))
+    rej = o["accept_len"] == 0
+    assert rej.any()
+    assert (p[o["next_token"][rej]] > q[o["next_token"][rej]]).all()
+    first = np.where(o["accept_len"] >= 1, tokens[:, 1], o["next_token"])
+    assert _chi2_pvalue(np.bincount(first, minlength=V), p) > 1e-4
