@@ -203,6 +203,31 @@ MEDUSA_API medusa_status medusa_heads_noalloc(medusa_dtype dtype, const void *h,
                                               medusa_stream stream);
 
 /* ------------------------------------------------------------------------
+ * 1c. Sampled drafts (for exact speculative sampling, section 6).
+ *
+ * [P1] Acceptance rules and [P2] §3: for the verification to preserve the
+ * verifying model's distribution, each draft must be a sample of its head's
+ * own normalised distribution q_k = softmax(logits_k / temperature).  Same
+ * pass as medusa_heads; instead of the top-s list, head k of sequence b
+ * draws x_k = argmax_v (logits_k[v] / T + G_v) (Gumbel-max, the smaller id
+ * on exact ties), G_v = -log(-log u) with u the Philox4x64-10 uniform of
+ * stream (purpose 1, row k, sequence b) at index v under key (seed, step)
+ * (counter (v/4, k, b, 1), word v%4, u = ((w >> 41) + 0.5) * 2^-23).
+ *
+ *   drafts       [B,K]    int32 out
+ *   draft_logits [B,K,V]  fp32 out: the heads' logits (before 1/T), which
+ *                         medusa_speculative_posterior needs for q
+ * Requirements as medusa_heads; temperature > 0; workspace
+ * medusa_heads_workspace_size(B, K, d, V, 1).
+ * ---------------------------------------------------------------------- */
+MEDUSA_API medusa_status medusa_heads_sample(medusa_dtype dtype, const void *h, const void *W1,
+                                             const void *b1, const void *W2, int B, int d,
+                                             int V, int K, float temperature, uint64_t seed,
+                                             uint64_t step, int32_t *drafts,
+                                             float *draft_logits, void *ws, size_t ws_bytes,
+                                             medusa_stream stream);
+
+/* ------------------------------------------------------------------------
  * 2. Candidate tree under a node budget.
  *
  * [P2] §6.2 (greedy construction within a budget: repeatedly take the
@@ -330,6 +355,37 @@ MEDUSA_API medusa_status medusa_evaluate_posterior(medusa_dtype dtype, const voi
                                         int32_t *next_token, int32_t *accept,
                                         void *ws, size_t ws_bytes,
                                         medusa_stream stream);
+
+/* ------------------------------------------------------------------------
+ * 6. Exact speculative sampling on a chain of sampled drafts.
+ *
+ * [P1] Acceptance rules; [P2] §3 (drafts from known normalised q_k with
+ * p/q acceptance and (p - q)+ correction recover the target distribution)
+ * and §5.  The candidate is a chain x_0 (the root, accepted), x_1..x_K
+ * (x_k sampled from q_k by medusa_heads_sample).  With p_j = softmax(logits
+ * row j / T): draft x_k is accepted iff u_k * q_k(x_k) < p_{k-1}(x_k), u_k
+ * the uniform of stream (purpose 2, row k, sequence b) at index 0; the
+ * first rejection at k = L+1 ends the chain and the next token is sampled
+ * from max(0, p_L - q_{L+1}) normalised (if that residual is empty in fp32,
+ * from p_L); with all K accepted it is sampled from p_K.  Samples use the
+ * Gumbel-max rule with stream (purpose 3, row L, sequence b).
+ *
+ *   logits       [B,K+1,V] dtype  verification rows of x_0..x_K
+ *   tokens       [B,K+1]   int32  x_0..x_K (a chain: row j judges x_{j+1})
+ *   draft_logits [B,K,V]   fp32   from medusa_heads_sample
+ * Outputs: accept_len [B] = L; path_tokens [B,K+1] = x_0..x_L, -1 padded;
+ * next_token [B]; accept [B,K] or NULL (1 accepted, 0 the rejection, -1
+ * not reached).  Requirements: 1 <= K <= 8, V % 8 == 0, temperature > 0.
+ * A draft token outside [0, V) counts as rejected and sets
+ * MEDUSA_DEV_BAD_TOKEN.
+ * ---------------------------------------------------------------------- */
+MEDUSA_API size_t medusa_speculative_workspace_size(int B, int K);
+
+MEDUSA_API medusa_status medusa_speculative_posterior(
+    medusa_dtype dtype, const void *logits, const int32_t *tokens, const float *draft_logits,
+    int B, int V, int K, float temperature, uint64_t seed, uint64_t step, int32_t *accept_len,
+    int32_t *path_tokens, int32_t *next_token, int32_t *accept, void *ws, size_t ws_bytes,
+    medusa_stream stream);
 
 /* ------------------------------------------------------------------------
  * 5. Commit of the accepted path into the KV cache.

@@ -7,8 +7,8 @@ current CUDA stream, allocates outputs and workspaces with torch, and raises
 the compiled library is missing, importing the calls fails loudly.
 
 Public calls (same names as the C ABI in include/medusa.h):
-    heads, heads_lm, heads_noalloc, build_tree, build_tree_static, tree_attention, evaluate_posterior,
-    commit_kv, evaluate_posterior_commit
+    heads, heads_lm, heads_sample, heads_noalloc, build_tree, build_tree_static, tree_attention, evaluate_posterior,
+    speculative_posterior, commit_kv, evaluate_posterior_commit
 plus workspace-size queries, device-status helpers and launch_count.
 """
 from __future__ import annotations
@@ -43,7 +43,8 @@ EXPORTS = ("medusa_status_string", "medusa_last_error", "medusa_launch_count",
            "medusa_build_tree_workspace_size", "medusa_build_tree", "medusa_build_tree_static",
            "medusa_tree_attention_workspace_size", "medusa_tree_attention",
            "medusa_posterior_workspace_size", "medusa_evaluate_posterior",
-           "medusa_evaluate_posterior_commit", "medusa_commit_kv")
+           "medusa_evaluate_posterior_commit", "medusa_commit_kv", "medusa_heads_sample",
+           "medusa_speculative_workspace_size", "medusa_speculative_posterior")
 
 
 class MedusaError(RuntimeError):
@@ -66,6 +67,7 @@ def lib() -> ctypes.CDLL:
             "`python -c 'import __graft_entry__ as g; g.build()'` (needs nvcc, sm_103a)")
     L = ctypes.CDLL(LIB_PATH)
     P, I, F, S = ctypes.c_void_p, ctypes.c_int, ctypes.c_float, ctypes.c_size_t
+    U64 = ctypes.c_uint64
     sig = {
         "medusa_status_string": ([I], ctypes.c_char_p),
         "medusa_last_error": ([], ctypes.c_char_p),
@@ -86,6 +88,10 @@ def lib() -> ctypes.CDLL:
         "medusa_evaluate_posterior_commit": ([I, P, P, P, P, I, I, I, I, I, F, F, F, P, P, P, P, P,
                                               P, P, P, I, I, P, P, S, P], I),
         "medusa_commit_kv": ([I, P, P, P, P, P, I, I, I, I, I, P, P, S, P], I),
+        "medusa_heads_sample": ([I, P, P, P, P, I, I, I, I, F, U64, U64, P, P, P, S, P], I),
+        "medusa_speculative_workspace_size": ([I, I], S),
+        "medusa_speculative_posterior": ([I, P, P, P, I, I, I, F, U64, U64, P, P, P, P, P, S, P],
+                                         I),
     }
     for name, (args, res) in sig.items():
         fn = getattr(L, name)
@@ -393,3 +399,62 @@ def commit_kv(dtype: int, k_ptrs, v_ptrs, prefix_len, path, accept_len, R: int, 
                                   _ptr(path), _ptr(accept_len), B, K1 - 1, int(R), int(H), int(dh),
                                   _ptr(new_prefix_len), _ptr(ws), ws.numel(), _stream(stream)))
     return new_prefix_len
+
+
+# --------------------------------------------------------------- sampling ---
+
+def heads_sample(h, W1, b1, W2, temperature: float, seed: int, step: int, ws=None, out=None,
+                 stream=None):
+    """One draft per head sampled from softmax(logits / T) (Gumbel-max with the
+    library's Philox streams).  Returns (drafts int32 [B,K], draft_logits fp32
+    [B,K,V])."""
+    for t, name in ((h, "h"), (W1, "W1"), (W2, "W2")):
+        _need(t, name)
+    B, d = h.shape
+    K, V = W2.shape[0], W2.shape[1]
+    dev = h.device
+    if ws is None:
+        ws = new_workspace(heads_workspace_size(B, K, d, V, 1), dev)
+    if out is None:
+        out = (torch.empty((B, K), dtype=torch.int32, device=dev),
+               torch.empty((B, K, V), dtype=torch.float32, device=dev))
+    drafts, dl = out
+    _check(lib().medusa_heads_sample(_dtype(h), _ptr(h), _ptr(W1), _ptr(b1), _ptr(W2), B, d, V, K,
+                                     float(temperature), int(seed), int(step), _ptr(drafts),
+                                     _ptr(dl), _ptr(ws), ws.numel(), _stream(stream)))
+    return drafts, dl
+
+
+@dataclass
+class Speculative:
+    accept_len: torch.Tensor
+    path_tokens: torch.Tensor
+    next_token: torch.Tensor
+    accept: Optional[torch.Tensor]
+
+
+def speculative_workspace_size(B: int, K: int) -> int:
+    return int(lib().medusa_speculative_workspace_size(B, K))
+
+
+def speculative_posterior(logits, tokens, draft_logits, temperature: float, seed: int, step: int,
+                          ws=None, out: Optional[Speculative] = None, with_accept: bool = True,
+                          stream=None) -> Speculative:
+    """Exact speculative sampling on a chain: logits [B,K+1,V], tokens [B,K+1]
+    (root then drafts), draft_logits fp32 [B,K,V]."""
+    _need(logits, "logits")
+    B, R, V = logits.shape
+    K = R - 1
+    dev = logits.device
+    if ws is None:
+        ws = new_workspace(speculative_workspace_size(B, K), dev)
+    if out is None:
+        i32 = dict(dtype=torch.int32, device=dev)
+        out = Speculative(torch.empty((B,), **i32), torch.empty((B, K + 1), **i32),
+                          torch.empty((B,), **i32),
+                          torch.empty((B, K), **i32) if with_accept else None)
+    _check(lib().medusa_speculative_posterior(
+        _dtype(logits), _ptr(logits), _ptr(tokens), _ptr(draft_logits), B, V, K,
+        float(temperature), int(seed), int(step), _ptr(out.accept_len), _ptr(out.path_tokens),
+        _ptr(out.next_token), _ptr(out.accept), _ptr(ws), ws.numel(), _stream(stream)))
+    return out

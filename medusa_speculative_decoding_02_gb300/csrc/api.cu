@@ -125,10 +125,10 @@ namespace {
 
 medusa_status check_heads(const char *who, medusa_dtype dtype, const void *h, const void *W1,
                           const void *b1, const void *W2, int B, int d, int V, int K, int top_s,
-                          const int32_t *topk_ids, const float *topk_logp) {
+                          const int32_t *topk_ids, const float *topk_logp, bool need_logp = true) {
     if (dtype != MEDUSA_F32 && dtype != MEDUSA_BF16)
         return fail(MEDUSA_ERR_INVALID_ARG, "%s: unknown dtype %d", who, (int)dtype);
-    if (!h || !W1 || !W2 || !topk_ids || !topk_logp)
+    if (!h || !W1 || !W2 || !topk_ids || (need_logp && !topk_logp))
         return fail(MEDUSA_ERR_INVALID_ARG, "%s: NULL tensor pointer", who);
     if (B < 1 || B > MEDUSA_MAX_BATCH)
         return fail(MEDUSA_ERR_UNSUPPORTED, "%s: B=%d outside 1..%d", who, B, MEDUSA_MAX_BATCH);
@@ -162,7 +162,7 @@ medusa_status medusa_heads(medusa_dtype dtype, const void *h, const void *W1, co
     if (medusa_status s = check_ws(ws, ws_bytes, heads_workspace_bytes(B, K, d, V, top_s), who))
         return s;
     cudaError_t e = launch_heads(dtype, h, nullptr, W1, b1, W2, B, d, V, K, top_s, topk_ids,
-                                 topk_logp, nullptr, nullptr, ws,
+                                 topk_logp, nullptr, nullptr, nullptr, ws,
                                  static_cast<cudaStream_t>(stream));
     if (e) return cuda_fail(e, who);
     return MEDUSA_OK;
@@ -184,8 +184,35 @@ medusa_status medusa_heads_lm(medusa_dtype dtype, const void *h, const void *W_l
             check_ws(ws, ws_bytes, heads_workspace_bytes(B, K, d, V, top_s, true), who))
         return s;
     cudaError_t e = launch_heads(dtype, h, W_lm, W1, b1, W2, B, d, V, K, top_s, topk_ids,
-                                 topk_logp, root, root_logp, ws,
+                                 topk_logp, root, root_logp, nullptr, ws,
                                  static_cast<cudaStream_t>(stream));
+    if (e) return cuda_fail(e, who);
+    return MEDUSA_OK;
+}
+
+medusa_status medusa_heads_sample(medusa_dtype dtype, const void *h, const void *W1,
+                                  const void *b1, const void *W2, int B, int d, int V, int K,
+                                  float temperature, uint64_t seed, uint64_t step,
+                                  int32_t *drafts, float *draft_logits, void *ws,
+                                  size_t ws_bytes, medusa_stream stream) {
+    const char *who = "medusa_heads_sample";
+    // drafts is the top-1 list of the perturbed keys; no log-probabilities
+    if (medusa_status s =
+            check_heads(who, dtype, h, W1, b1, W2, B, d, V, K, 1, drafts, nullptr, false))
+        return s;
+    if (!draft_logits) return fail(MEDUSA_ERR_INVALID_ARG, "%s: NULL draft_logits", who);
+    if (!(temperature > 0.f) || !(temperature < 1e30f))
+        return fail(MEDUSA_ERR_INVALID_ARG, "%s: temperature must be positive and finite", who);
+    if (medusa_status s = check_ws(ws, ws_bytes, heads_workspace_bytes(B, K, d, V, 1), who))
+        return s;
+    SampleArgs smp;
+    smp.on = 1;
+    smp.inv_T = 1.f / temperature;
+    smp.seed = seed;
+    smp.step = step;
+    smp.logits_out = draft_logits;
+    cudaError_t e = launch_heads(dtype, h, nullptr, W1, b1, W2, B, d, V, K, 1, drafts, nullptr,
+                                 nullptr, nullptr, &smp, ws, static_cast<cudaStream_t>(stream));
     if (e) return cuda_fail(e, who);
     return MEDUSA_OK;
 }
@@ -415,6 +442,40 @@ medusa_status medusa_evaluate_posterior_commit(
                                      delta, temperature, accept_len, path, path_tokens, next_token,
                                      accept, k_cache, v_cache, prefix_len, H, dh, new_prefix_len,
                                      ws, static_cast<cudaStream_t>(stream));
+    if (e) return cuda_fail(e, who);
+    return MEDUSA_OK;
+}
+
+// ----------------------------------------------------------- speculative ---
+
+size_t medusa_speculative_workspace_size(int B, int K) {
+    if (B < 1 || K < 1) return 0;
+    return speculative_workspace_bytes(B, K);
+}
+
+medusa_status medusa_speculative_posterior(medusa_dtype dtype, const void *logits,
+                                           const int32_t *tokens, const float *draft_logits,
+                                           int B, int V, int K, float temperature, uint64_t seed,
+                                           uint64_t step, int32_t *accept_len,
+                                           int32_t *path_tokens, int32_t *next_token,
+                                           int32_t *accept, void *ws, size_t ws_bytes,
+                                           medusa_stream stream) {
+    const char *who = "medusa_speculative_posterior";
+    if (dtype != MEDUSA_F32 && dtype != MEDUSA_BF16)
+        return fail(MEDUSA_ERR_INVALID_ARG, "%s: unknown dtype %d", who, (int)dtype);
+    if (!logits || !tokens || !draft_logits || !accept_len || !path_tokens || !next_token)
+        return fail(MEDUSA_ERR_INVALID_ARG, "%s: NULL pointer", who);
+    if (B < 1) return fail(MEDUSA_ERR_INVALID_ARG, "%s: B=%d", who, B);
+    if (K < 1 || K > MEDUSA_MAX_HEADS)
+        return fail(MEDUSA_ERR_INVALID_ARG, "%s: K=%d outside 1..%d", who, K, MEDUSA_MAX_HEADS);
+    if (V < 1 || V % 8)
+        return fail(MEDUSA_ERR_INVALID_ARG, "%s: V=%d must be a positive multiple of 8", who, V);
+    if (!(temperature > 0.f) || !(temperature < 1e30f))
+        return fail(MEDUSA_ERR_INVALID_ARG, "%s: temperature must be positive and finite", who);
+    if (medusa_status s = check_ws(ws, ws_bytes, speculative_workspace_bytes(B, K), who)) return s;
+    cudaError_t e = launch_speculative(dtype, logits, tokens, draft_logits, B, V, K, temperature,
+                                       seed, step, accept_len, path_tokens, next_token, accept, ws,
+                                       static_cast<cudaStream_t>(stream));
     if (e) return cuda_fail(e, who);
     return MEDUSA_OK;
 }

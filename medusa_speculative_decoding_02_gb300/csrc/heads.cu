@@ -32,6 +32,7 @@
 
 #include "common.cuh"
 #include "launch.h"
+#include "philox.cuh"
 
 namespace medusa {
 
@@ -185,6 +186,16 @@ struct WarpTop {
             id = up_i;
         }
     }
+    // sampling: fold y = logit / T into (m, s), rank by the perturbed key
+    __device__ __forceinline__ void push_key(float y, float key, int cid, int S, int lane) {
+        if (y > m) {
+            s = s * expf(m - y) + 1.f;
+            m = y;
+        } else {
+            s += expf(y - m);
+        }
+        insert(key, cid, S, lane);
+    }
     // merge another (m, s) pair
     __device__ __forceinline__ void merge_ms(float om, float os) {
         if (om == -INFINITY) return;
@@ -276,11 +287,11 @@ __device__ __forceinline__ const T *w2_row(const T *W2, const T *Wlm, int k, int
     return W2 + ((size_t)k * V + v) * d;
 }
 
-template <typename T, int NB, int U>
+template <typename T, int NB, int U, bool SAMPLE>
 __global__ void __launch_bounds__(kW2Threads, NB <= 1 ? 2 : 1)
 heads_w2_kernel(const float *__restrict__ z, const T *__restrict__ W2, const T *__restrict__ Wlm,
                 int B, int d, int V, int K, int S, int hpg, float2 *__restrict__ part_ms,
-                float *__restrict__ part_val, int *__restrict__ part_id) {
+                float *__restrict__ part_val, int *__restrict__ part_id, SampleArgs smp) {
     extern __shared__ float4 smem4[];
     constexpr int VN = Vec16<T>::N;
     const int nvec = d / VN;
@@ -317,9 +328,25 @@ heads_w2_kernel(const float *__restrict__ z, const T *__restrict__ W2, const T *
         for (int b = 0; b < NB; ++b) st[b].reset();
         int cur = 0;
         const int items = hk * nrows;
-        for (int it = warp; it < items; it += kW2Warps) {
+        // sampling: lane l holds the Gumbel draws of this warp's l-th next item,
+        // refilled every 32 items (one Philox block per lane per 32 rows)
+        float gz[NB];
+#pragma unroll
+        for (int b = 0; b < NB; ++b) gz[b] = 0.f;
+        int jb = 0;
+        for (int it = warp; it < items; it += kW2Warps, ++jb) {
             const int kk = it / nrows;
             const int v = r0 + (it - kk * nrows);
+            if (SAMPLE && (jb & 31) == 0) {
+                const int itl = it + lane * kW2Warps;
+                if (itl < items) {
+                    const int kl = itl / nrows;
+                    const int vl = r0 + (itl - kl * nrows);
+#pragma unroll
+                    for (int b = 0; b < NB; ++b)
+                        if (b < B) gz[b] = gumbel_at(smp.seed, smp.step, kRngDraft, b, k0 + kl, vl);
+                }
+            }
             while (cur < kk) {
 #pragma unroll
                 for (int b = 0; b < NB; ++b) {
@@ -332,9 +359,22 @@ heads_w2_kernel(const float *__restrict__ z, const T *__restrict__ W2, const T *
             const T *wrow = w2_row(W2, Wlm, k0 + kk, v, V, d);
             row_dot<T, NB, U>(reinterpret_cast<const uint4 *>(wrow), zs4 + (size_t)kk * NB * d / 4,
                               nvec, lane, acc);
+            if (!SAMPLE) {
 #pragma unroll
-            for (int b = 0; b < NB; ++b)
-                if (b < B) st[b].push(acc[b], v, S, lane);
+                for (int b = 0; b < NB; ++b)
+                    if (b < B) st[b].push(acc[b], v, S, lane);
+            } else {
+#pragma unroll
+                for (int b = 0; b < NB; ++b) {
+                    const float g = __shfl_sync(0xffffffffu, gz[b], jb & 31);
+                    if (b < B) {
+                        const float y = acc[b] * smp.inv_T;
+                        st[b].push_key(y, y + g, v, S, lane);
+                        if (smp.logits_out && lane == 0)
+                            smp.logits_out[((size_t)b * K + (k0 + kk)) * V + v] = acc[b];
+                    }
+                }
+            }
         }
         while (cur < hk) {
 #pragma unroll
@@ -504,7 +544,7 @@ heads_reduce_kernel(const float2 *__restrict__ part_ms, const float *__restrict_
     } else if (threadIdx.x < S) {
         const size_t o = ((size_t)b * (K - lm) + (k - lm)) * S + threadIdx.x;
         topk_ids[o] = r_id[threadIdx.x];
-        topk_logp[o] = r_val[threadIdx.x] - s_logz;
+        if (topk_logp) topk_logp[o] = r_val[threadIdx.x] - s_logz;
     }
 }
 
@@ -545,8 +585,8 @@ HeadsLayout heads_layout(int B, int Kt, int d, int S) {
 template <typename T, int NB>
 cudaError_t run_heads(const void *h, const void *Wlm, const void *W1, const void *b1,
                       const void *W2, int B, int d, int V, int K, int S, int32_t *ids,
-                      float *logp, int32_t *root, float *root_logp, char *ws,
-                      cudaStream_t stream) {
+                      float *logp, int32_t *root, float *root_logp, const SampleArgs &smp,
+                      char *ws, cudaStream_t stream) {
     constexpr int U1 = NB <= 4 ? 8 : 4;
     constexpr int U2 = NB <= 4 ? 8 : 4;
     const int lm = Wlm ? 1 : 0;
@@ -583,7 +623,7 @@ cudaError_t run_heads(const void *h, const void *Wlm, const void *W1, const void
     const size_t budget = NB == 1 ? kSmemBudgetPair : kSmemBudget;
     int hpg = (int)std::min<size_t>(Kt, std::max<size_t>(1, budget / (per_head + slot_per_head)));
     const size_t smem2 = hpg * (per_head + slot_per_head);
-    auto k2 = heads_w2_kernel<T, NB, U2>;
+    auto k2 = smp.on ? heads_w2_kernel<T, NB, U2, true> : heads_w2_kernel<T, NB, U2, false>;
     if ((e = cudaFuncSetAttribute(k2, cudaFuncAttributeMaxDynamicSharedMemorySize, (int)smem2)))
         return e;
     int occ2 = 0;
@@ -591,7 +631,7 @@ cudaError_t run_heads(const void *h, const void *Wlm, const void *W1, const void
     const int G = std::max(1, std::min(kMaxW2Ctas, sms * std::max(occ2, 1)));
     e = launch_pdl(k2, dim3(G), dim3(kW2Threads), smem2, stream, static_cast<const float *>(z),
                    static_cast<const T *>(W2), static_cast<const T *>(Wlm), B, d, V, Kt, S, hpg,
-                   pms, pval, pid);
+                   pms, pval, pid, smp);
     note_launch();
     if (e) return e;
 
@@ -612,14 +652,16 @@ size_t heads_workspace_bytes(int B, int K, int d, int V, int S, bool with_lm_hea
 
 cudaError_t launch_heads(medusa_dtype dtype, const void *h, const void *Wlm, const void *W1,
                          const void *b1, const void *W2, int B, int d, int V, int K, int S,
-                         int32_t *ids, float *logp, int32_t *root, float *root_logp, void *ws,
-                         cudaStream_t stream) {
+                         int32_t *ids, float *logp, int32_t *root, float *root_logp,
+                         const SampleArgs *sample, void *ws, cudaStream_t stream) {
     char *w = static_cast<char *>(ws);
     const int nb = nb_bucket(B);
+    SampleArgs smp = {};
+    if (sample) smp = *sample;
 #define MEDUSA_HEADS_CASE(T, N)                                                                  \
     if (nb == N)                                                                                 \
-        return run_heads<T, N>(h, Wlm, W1, b1, W2, B, d, V, K, S, ids, logp, root, root_logp, w, \
-                               stream);
+        return run_heads<T, N>(h, Wlm, W1, b1, W2, B, d, V, K, S, ids, logp, root, root_logp,   \
+                               smp, w, stream);
     if (dtype == MEDUSA_BF16) {
         MEDUSA_HEADS_CASE(bf16, 1)
         MEDUSA_HEADS_CASE(bf16, 2)

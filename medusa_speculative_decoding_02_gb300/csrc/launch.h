@@ -34,13 +34,24 @@ int device_sm_count();   // SMs of the current device (cached per device)
 void note_launch();      // count one kernel launch
 void set_last_error(const char *fmt, ...);  // message for medusa_last_error()
 
+// Sampling mode of the heads pass: each head draws one token from
+// softmax(logits * inv_T) by Gumbel-max (random stream: purpose 1, row =
+// head, key = (seed, step)); the raw logits go to logits_out [B,K,V] when it
+// is not null.
+struct SampleArgs {
+    int on;
+    float inv_T;
+    uint64_t seed, step;
+    float *logits_out;
+};
+
 // Wlm == nullptr: the Medusa heads alone; otherwise the LM head joins the
-// pass and writes root / root_logp.
+// pass and writes root / root_logp.  sample == nullptr: top-s mode.
 size_t heads_workspace_bytes(int B, int K, int d, int V, int S, bool with_lm_head = false);
 cudaError_t launch_heads(medusa_dtype dtype, const void *h, const void *Wlm, const void *W1,
                          const void *b1, const void *W2, int B, int d, int V, int K, int S,
-                         int32_t *ids, float *logp, int32_t *root, float *root_logp, void *ws,
-                         cudaStream_t stream);
+                         int32_t *ids, float *logp, int32_t *root, float *root_logp,
+                         const SampleArgs *sample, void *ws, cudaStream_t stream);
 
 size_t tree_workspace_bytes(int B, int K, int S, int n);
 // shared_table: logp is one [K, S] table used by every sequence (a calibrated
@@ -56,6 +67,13 @@ cudaError_t launch_tree_attention(medusa_dtype dtype, const void *q, const void 
                                   const void *const *v_cache, const int32_t *prefix_len,
                                   int P_max, const uint64_t *anc_mask, int B, int R, int H,
                                   int dh, float scale, void *out, void *ws, cudaStream_t stream);
+
+size_t speculative_workspace_bytes(int B, int K);
+cudaError_t launch_speculative(medusa_dtype dtype, const void *logits, const int32_t *tokens,
+                               const float *draft_logits, int B, int V, int K, float temperature,
+                               uint64_t seed, uint64_t step, int32_t *accept_len,
+                               int32_t *path_tokens, int32_t *next_token, int32_t *accept,
+                               void *ws, cudaStream_t stream);
 
 size_t posterior_workspace_bytes(int B, int R);
 cudaError_t launch_posterior(medusa_dtype dtype, const void *logits, const int32_t *tokens,
