@@ -490,6 +490,32 @@ def run_ours(args, cfg):
     us_heads_lm = timed_loop(heads_lm)
     us_heads = timed_loop(heads_only)
     lm_bytes = nb["heads"] + cfg.V * cfg.d * 2 + B * 8
+
+    # exact speculative sampling: drafts sampled in the heads pass, then the
+    # p/q posterior on a chain (verification rows: this step's first K+1 rows)
+    ws_smp = m.new_workspace(max(m.heads_workspace_size(B, K, cfg.d, cfg.V, 1),
+                                 m.speculative_workspace_size(B, K)), dev)
+    smp_out = (torch.empty((B, K), dtype=torch.int32, device=dev),
+               torch.empty((B, K, cfg.V), dtype=torch.float32, device=dev))
+    chain = torch.empty((B, K + 1), dtype=torch.int32, device=dev)
+    chain_logits = logits[:, :K + 1].contiguous()
+    spec_out = m.Speculative(*[torch.empty(sh, dtype=torch.int32, device=dev)
+                               for sh in ((B,), (B, K + 1), (B,), (B, K))])
+
+    def heads_sample():
+        m.heads_sample(h, W1, b1, W2, 1.0, 11, 0, ws=ws_smp, out=smp_out)
+
+    def spec_post():
+        m.speculative_posterior(chain_logits, chain, smp_out[1], 1.0, 11, 0, ws=ws_smp,
+                                out=spec_out)
+
+    heads_sample()
+    chain[:, 0] = root
+    chain[:, 1:] = smp_out[0]
+    us_heads_sample = timed_loop(heads_sample)
+    us_spec = timed_loop(spec_post)
+    smp_bytes = nb["heads"] + B * K * cfg.V * 4                       # + the drafts' logits
+    spec_bytes = B * (K + 1) * cfg.V * 2 + 2 * B * K * cfg.V * 4     # p rows; q rows twice
     us_post = timed_loop(post_only)
     us_post_commit = timed_loop(post_commit)
     us_commit = timed_loop(commit_only)
@@ -503,6 +529,11 @@ def run_ours(args, cfg):
         "posterior_alone_us": round(us_post, 2),
         "note": "launch-latency bound: a few hundred KB per step",
         "host_loop_us": {k: v for k, v in host_us.items()}},
+        "speculative_sampling": {
+            "heads_sample_us": round(us_heads_sample, 2), "heads_sample_bytes": int(smp_bytes),
+            "heads_sample_GB/s": round(smp_bytes / (us_heads_sample * 1e-6) / 1e9, 1),
+            "posterior_us": round(us_spec, 2), "posterior_bytes": int(spec_bytes),
+            "note": "drafts by Gumbel-max in the weight pass; posterior on a chain of K drafts"},
         "heads_lm": {
             "us": round(us_heads_lm, 2), "bytes": int(lm_bytes),
             "GB/s": round(lm_bytes / (us_heads_lm * 1e-6) / 1e9, 1),
