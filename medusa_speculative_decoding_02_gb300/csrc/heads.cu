@@ -104,7 +104,7 @@ template <typename T, int NB, int U>
 __global__ void __launch_bounds__(kW1Threads, NB <= 2 ? 4 : 1)
 heads_w1_kernel(const T *__restrict__ h, const T *__restrict__ W1, const T *__restrict__ b1,
                 float *__restrict__ z, float *__restrict__ z_lm, int B, int d, int K,
-                int rows_per_warp) {
+                int total_warps) {
     pdl_enter();
     extern __shared__ float4 smem4[];
     float *hs = reinterpret_cast<float *>(smem4);
@@ -122,11 +122,12 @@ heads_w1_kernel(const T *__restrict__ h, const T *__restrict__ W1, const T *__re
     const int warp = threadIdx.x >> 5;
     const int nwarps = blockDim.x >> 5;
     const int rows = K * d;
-    // every warp owns rows_per_warp consecutive rows (the host sizes the grid
-    // so that the warps' shares are equal)
+    // the grid fills every resident warp slot once, and warp gw owns rows
+    // [gw*rows/total, (gw+1)*rows/total): shares differ by at most one row, so
+    // every SM streams the same number of bytes
     const int gw = blockIdx.x * nwarps + warp;
-    const int r_begin = gw * rows_per_warp;
-    const int r_end = min(rows, r_begin + rows_per_warp);
+    const int r_begin = (int)(((long long)gw * rows) / total_warps);
+    const int r_end = (int)(((long long)(gw + 1) * rows) / total_warps);
     for (int row = r_begin; row < r_end; ++row) {
         float acc[NB];
         row_dot<T, NB, U>(reinterpret_cast<const uint4 *>(W1 + (size_t)row * d), smem4, nvec, lane,
@@ -608,12 +609,11 @@ cudaError_t run_heads(const void *h, const void *Wlm, const void *W1, const void
     if ((e = cudaOccupancyMaxActiveBlocksPerMultiprocessor(&occ1, k1, kW1Threads, smem1))) return e;
     const int rows1 = K * d;
     const int warps1 = kW1Threads / kWarp;
-    const int slots1 = sms * std::max(occ1, 1) * warps1;
-    const int rpw = std::max(1, (rows1 + slots1 - 1) / slots1);
-    const int grid1 = std::max(1, (((rows1 + rpw - 1) / rpw) + warps1 - 1) / warps1);
+    const int grid1 = sms * std::max(occ1, 1);  // one full wave
+    const int total_warps = grid1 * warps1;
     e = launch_pdl(k1, dim3(grid1), dim3(kW1Threads), smem1, stream, static_cast<const T *>(h),
                    static_cast<const T *>(W1), static_cast<const T *>(b1),
-                   z + (size_t)lm * B * d, lm ? z : nullptr, B, d, K, rpw);
+                   z + (size_t)lm * B * d, lm ? z : nullptr, B, d, K, total_warps);
     note_launch();
     if (e) return e;
 
