@@ -331,8 +331,15 @@ def run_ours(args, cfg):
 
     inp = make_inputs(cfg)
     hi = inp["heads"]
-    h, W1, b1, W2 = T(hi.h), T(hi.W1), T(hi.b1), T(hi.W2)
-    root = T(inp["root"])
+    W1, b1, W2 = T(hi.W1), T(hi.b1), T(hi.W2)
+    # h and the root share one device buffer, so that a step's first inputs
+    # arrive in one copy
+    h_bytes = cfg.B * cfg.d * 2
+    start = torch.empty(h_bytes + 16 * ((cfg.B * 4 + 15) // 16), dtype=torch.uint8, device=dev)
+    h = start[:h_bytes].view(torch.bfloat16).view(cfg.B, cfg.d)
+    root = start[h_bytes:h_bytes + cfg.B * 4].view(torch.int32)
+    h.copy_(T(hi.h))
+    root.copy_(T(inp["root"]))
     ai = inp["attn"]
     q = T(ai.q)
     kc = [T(x) for x in ai.k_cache]
@@ -349,7 +356,16 @@ def run_ours(args, cfg):
     logp = torch.empty((B, K, S), dtype=torch.float32, device=dev)
     tree = m.Tree.empty(B, n, K, dev)
     out = torch.empty_like(q)
-    post = m.Posterior.empty(B, R, K, dev, with_accept=False)
+    # the posterior's results share one device buffer (one copy back per step)
+    quad = lambda n: (n + 3) // 4 * 4  # int32 slots, 16-byte aligned pieces
+    res_sizes = (B, B * (K + 1), B * (K + 1), B)
+    results = torch.zeros(sum(quad(x) for x in res_sizes), dtype=torch.int32, device=dev)
+    res_views, o = [], 0
+    for x in res_sizes:
+        res_views.append(results[o:o + x])
+        o += quad(x)
+    post = m.Posterior(res_views[0], res_views[1].view(B, K + 1), res_views[2].view(B, K + 1),
+                       res_views[3], None)
     stream = torch.cuda.current_stream(dev)
 
     # the verification logits carry one planted chain on this step's tree
@@ -362,7 +378,7 @@ def run_ours(args, cfg):
 
     ev = [torch.cuda.Event(enable_timing=True) for _ in range(5)]
 
-    def step(record=None):
+    def step(record=None, before_attention=None):
         if record is not None:
             record[0].record(stream)
         m.heads(h, W1, b1, W2, S, ws=ws, out=(ids, logp))
@@ -371,6 +387,8 @@ def run_ours(args, cfg):
         m.build_tree(root, ids, logp, cfg.s, n, prefix_len=prefix, ws=ws, out=tree)
         if record is not None:
             record[2].record(stream)
+        if before_attention is not None:
+            before_attention()
         m.tree_attention(q, kptr, vptr, prefix, cfg.P_max, tree.anc_mask, out=out, ws=ws)
         if record is not None:
             record[3].record(stream)
@@ -541,41 +559,62 @@ def run_ours(args, cfg):
             "note": "LM head (32000 x 4096) + 5 Medusa heads in one weight pass"}}
 
     # ---- end to end through the public API with pinned host buffers
+    host_start = torch.empty(start.numel(), dtype=torch.uint8).pin_memory()
+    host_start.copy_(start.cpu())
     host_in = {
-        "h": torch.from_numpy(np.ascontiguousarray(hi.h).view(np.int16)).view(torch.bfloat16).pin_memory(),
-        "root": torch.from_numpy(inp["root"]).pin_memory(),
+        "start": host_start,  # h and the root
         "q": torch.from_numpy(np.ascontiguousarray(ai.q).view(np.int16)).view(torch.bfloat16).pin_memory(),
         "k_tree": torch.from_numpy(ai.k_cache[0][cfg.prefix[0]:].view(np.int16)).view(torch.bfloat16).pin_memory(),
         "v_tree": torch.from_numpy(ai.v_cache[0][cfg.prefix[0]:].view(np.int16)).view(torch.bfloat16).pin_memory(),
         "logits": torch.from_numpy(inp["logits"].view(np.int16)).view(torch.bfloat16).pin_memory(),
     }
-    host_out = {k: torch.empty(v.shape, dtype=v.dtype).pin_memory()
-                for k, v in (("accept_len", post.accept_len), ("path", post.path),
-                             ("path_tokens", post.path_tokens), ("next_token", post.next_token))}
+    host_out = {"results": torch.empty(results.shape, dtype=torch.int32).pin_memory()}
     h2d = sum(v.numel() * v.element_size() for v in host_in.values())
     d2h = sum(v.numel() * v.element_size() for v in host_out.values())
     P0 = cfg.prefix[0]
 
-    def e2e_step():
-        h.copy_(host_in["h"], non_blocking=True)
-        root.copy_(host_in["root"], non_blocking=True)
-        q.copy_(host_in["q"], non_blocking=True)
-        kc[0][P0:].copy_(host_in["k_tree"], non_blocking=True)
-        vc[0][P0:].copy_(host_in["v_tree"], non_blocking=True)
-        logits.copy_(host_in["logits"], non_blocking=True)
-        step()
-        for k, v in host_out.items():
-            v.copy_(getattr(post, k), non_blocking=True)
-        stream.synchronize()
+    copy_stream = torch.cuda.Stream(dev)
+
+    def e2e_issue():
+        # h and the root start the step; q, the tree's K/V rows and the
+        # verification logits are first read by the attention and the
+        # posterior, so they travel on a second stream during the heads pass
+        main = torch.cuda.current_stream(dev)
+        copy_stream.wait_stream(main)
+        start.copy_(host_in["start"], non_blocking=True)
+        with torch.cuda.stream(copy_stream):
+            q.copy_(host_in["q"], non_blocking=True)
+            kc[0][P0:].copy_(host_in["k_tree"], non_blocking=True)
+            vc[0][P0:].copy_(host_in["v_tree"], non_blocking=True)
+            logits.copy_(host_in["logits"], non_blocking=True)
+        step(before_attention=lambda: main.wait_stream(copy_stream))
+        host_out["results"].copy_(results, non_blocking=True)
+
+    def e2e_eager():
+        e2e_issue()
+        torch.cuda.current_stream(dev).synchronize()
+
+    # the public step API: the whole step (input copies, calls, result
+    # copies) captured once as a CUDA graph, replayed every step
+    graph = m.StepGraph(e2e_issue)
+
+    def e2e_graph():
+        graph.replay()
+        torch.cuda.current_stream(dev).synchronize()
 
     e2e_steps = max(3, min(args.steps, 50))
-    for _ in range(2):
-        e2e_step()
-    barrier()
-    t0 = time.perf_counter()
-    for _ in range(e2e_steps):
-        e2e_step()
-    e2e_s, e2e_value = replica_throughput((time.perf_counter() - t0) / e2e_steps, nb["total"], dev)
+
+    def time_e2e(fn):
+        for _ in range(2):
+            fn()
+        barrier()
+        t0 = time.perf_counter()
+        for _ in range(e2e_steps):
+            fn()
+        return replica_throughput((time.perf_counter() - t0) / e2e_steps, nb["total"], dev)
+
+    eager_s, eager_value = time_e2e(e2e_eager)
+    e2e_s, e2e_value = time_e2e(e2e_graph)
 
     if world > 1:
         import torch.distributed as dist
@@ -640,7 +679,9 @@ def run_ours(args, cfg):
                                    f"{float(np.mean(cpu_secs)):.2f} s per step"},
         "e2e": {"value": round(e2e_value, 2), "unit": UNIT, "h2d_bytes_per_step": int(h2d),
                 "d2h_bytes_per_step": int(d2h), "us_per_step": round(e2e_s * 1e6, 2),
-                "steps": e2e_steps},
+                "steps": e2e_steps, "api": "StepGraph.replay (copies + calls in one CUDA graph)",
+                "eager_value": round(eager_value, 2),
+                "eager_us_per_step": round(eager_s * 1e6, 2)},
         "gpu_launches": int(launches),
         "clocks": clk.summary(),
     }

@@ -9,7 +9,9 @@ the compiled library is missing, importing the calls fails loudly.
 Public calls (same names as the C ABI in include/medusa.h):
     heads, heads_lm, heads_sample, heads_noalloc, build_tree, build_tree_static, tree_attention, evaluate_posterior,
     speculative_posterior, commit_kv, evaluate_posterior_commit
-plus workspace-size queries, device-status helpers and launch_count.
+plus workspace-size queries, device-status helpers, launch_count, and
+``StepGraph``, which captures a whole decoding step (copies and calls) into a
+CUDA graph once and replays it per step.
 """
 from __future__ import annotations
 
@@ -458,3 +460,34 @@ def speculative_posterior(logits, tokens, draft_logits, temperature: float, seed
         float(temperature), int(seed), int(step), _ptr(out.accept_len), _ptr(out.path_tokens),
         _ptr(out.next_token), _ptr(out.accept), _ptr(ws), ws.numel(), _stream(stream)))
     return out
+
+
+# ------------------------------------------------------------- step graph ---
+
+class StepGraph:
+    """A decoding step captured once into a CUDA graph and replayed.
+
+    ``fn`` issues the step on the current stream: copies of the step's
+    inputs from pinned host buffers, the library calls (heads, tree,
+    attention, posterior, ...), and copies of the results back to pinned
+    host buffers.  Every buffer it touches must stay allocated and at the
+    same address while the graph lives; new inputs are written into the same
+    pinned host buffers before each ``replay``.  The launches keep their
+    programmatic-dependent-launch edges inside the graph.
+    """
+
+    def __init__(self, fn, warmup: int = 2):
+        side = torch.cuda.Stream()
+        side.wait_stream(torch.cuda.current_stream())
+        with torch.cuda.stream(side):
+            for _ in range(warmup):
+                fn()
+        torch.cuda.current_stream().wait_stream(side)
+        torch.cuda.synchronize()
+        self.graph = torch.cuda.CUDAGraph()
+        with torch.cuda.graph(self.graph):
+            fn()
+        torch.cuda.synchronize()
+
+    def replay(self):
+        self.graph.replay()
