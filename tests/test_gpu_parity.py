@@ -363,7 +363,8 @@ def test_attention_tiny_f32(dev):
     (1, (2, 2, 2), 14, 2, 64, (0,)), (2, (4, 4), 16, 3, 128, (1, 70)),
     (1, (4, 3, 2, 2, 1), 64, 4, 128, (1023,)), (3, (8, 4, 4), 128, 2, 128, (5, 300, 64)),
     (1, (16, 16), 255, 1, 128, (100,)), (2, (4, 4, 2), 32, 2, 64, (128, 0)),
-    (1, (1,), 1, 2, 128, (10,)), (2, (8, 4, 4, 2, 2), 200, 1, 64, (65, 1))])
+    (1, (1,), 1, 2, 128, (10,)), (2, (8, 4, 4, 2, 2), 200, 1, 64, (65, 1)),
+    (1, (4, 3, 2, 2, 1), 64, 2, 64, (3000,)), (3, (4, 4, 2), 32, 3, 128, (2500, 40, 1700))])
 def test_attention_shapes(dev, B, s, n, H, dh, prefix):
     """Ragged prefixes (0, 1, non-multiples of the 64-key tile), tree sizes
     from 2 to 256 rows (both warp-count instantiations), dh 64 and 128."""
