@@ -631,336 +631,6 @@ __global__ void __launch_bounds__(256, 2) tree_attn_tc_kernel(AttnArgs a) {
     if (warp == 0) tc::tmem_dealloc(tmem, 256);
 }
 
-// ------------------------------------------------- warp-specialised path ---
-//
-// tree_attn_ws_kernel: the same computation as tree_attn_tc_kernel for long
-// key ranges, with the work split by role so that loads, MMAs and softmax
-// overlap.  One CTA per SM (416 threads):
-//   warps 0..7   softmax: threads t and t+128 own query row t (as above)
-//   warps 8..11  loaders: cp.async of 64-key K/V sub-chunks into a six-stage
-//                ring; each thread's copies arrive on the stage's "full"
-//                mbarrier when they land
-//   warp 12      lane 0 issues the MMAs: S_j = Q K_j^T into one of four S
-//                buffers while the softmax warps still work on S_{j-1}, then
-//                O += P_{j-1} V_{j-1} once they have written P_{j-1}; P_j is
-//                written over S_j, so S_{j+4} waits for P_j V_j, long done
-// Tensor memory (512 columns): S/P buffers [64 i, 64 i + 64) for i < 4, Q
-// [256, 320), O [384, 384+DH).  mbarriers: full/empty per stage, s_full /
-// s_free per S buffer (s_free also tells the softmax warps that O is up to
-// date before a rescale), p_ready per S buffer.  Every waiter of a barrier is at most one
-// phase behind it, so parity waits cannot alias.  Every wait is bounded; a
-// role that times out records MEDUSA_DEV_TIMEOUT and carries on without
-// waiting (the softmax warps still take every named barrier), so all threads
-// reach the final barrier and the tensor memory is freed.
-constexpr int kWsStages = 6;
-constexpr int kWsSoftWarps = 8;
-constexpr int kWsLoadWarps = 4;
-constexpr int kWsMmaWarp = kWsSoftWarps + kWsLoadWarps;
-constexpr int kWsThreads = (kWsMmaWarp + 1) * 32;
-constexpr int kWsSBufs = 4;
-
-template <int DH>
-struct WsSmem {
-    static constexpr int NB = DH / 64;
-    static constexpr int K_BYTES = NB * kTcSub * 128;  // [NB][64 keys][128 B]
-    static constexpr int STAGE_BYTES = 2 * K_BYTES;    // K then V
-    static constexpr int XCH_OFF = kWsStages * STAGE_BYTES;  // [3][2][128] floats
-    static constexpr int BAR_OFF = XCH_OFF + 3 * 2 * 128 * 4;
-    static constexpr int N_BARS = 2 * kWsStages + 3 * kWsSBufs;
-    static constexpr int HOLDER_OFF = BAR_OFF + N_BARS * 8;
-    static constexpr int TOTAL = HOLDER_OFF + 16;
-};
-
-template <int DH>
-__global__ void __launch_bounds__(kWsThreads, 1) tree_attn_ws_kernel(AttnArgs a) {
-    pdl_enter();
-    using L = WsSmem<DH>;
-    constexpr int HALF = kTcSub / 2;
-    extern __shared__ __align__(1024) unsigned char ws_raw[];
-    uint64_t *bars = reinterpret_cast<uint64_t *>(ws_raw + L::BAR_OFF);
-    uint64_t *full = bars, *empty = bars + kWsStages;
-    uint64_t *s_full = bars + 2 * kWsStages, *s_free = s_full + kWsSBufs;
-    uint64_t *p_ready = s_free + kWsSBufs;
-    uint32_t &tmem_holder = *reinterpret_cast<uint32_t *>(ws_raw + L::HOLDER_OFF);
-    int &failed = *reinterpret_cast<int *>(ws_raw + L::HOLDER_OFF + 4);
-    float *xch = reinterpret_cast<float *>(ws_raw + L::XCH_OFF);
-
-    const int h = blockIdx.x, split = blockIdx.y, b = blockIdx.z;
-    const int R = a.R, H = a.H;
-    const int tid = threadIdx.x, warp = tid >> 5, lane = tid & 31;
-    int P = a.prefix_len[b];
-    if (P < 0 || P > a.P_max) {
-        set_status(a.status, MEDUSA_DEV_BAD_PREFIX);
-        P = 0;
-    }
-    const int NS = a.nps;
-    const size_t pbase = ((size_t)(b * H + h) * NS + split) * R;
-    const int kbeg = split * a.chunk;
-    const int kend = min(kbeg + a.chunk, P + R);
-    const bf16 *kc = a.kc[b];
-    const bf16 *vc = a.vc[b];
-    const bool bad_cache = cache_pointers_bad(kc, vc);
-    if (bad_cache) set_status(a.status, MEDUSA_DEV_BAD_CACHE);
-    if (kend <= kbeg || bad_cache) {
-        for (int r = tid; r < R; r += blockDim.x) a.part_ml[pbase + r] = make_float2(-INFINITY, 0.f);
-        return;
-    }
-    const int nsub = (kend - kbeg + kTcSub - 1) / kTcSub;
-    auto stage_k = [&](int j) { return ws_raw + (j % kWsStages) * L::STAGE_BYTES; };
-    auto stage_v = [&](int j) { return ws_raw + (j % kWsStages) * L::STAGE_BYTES + L::K_BYTES; };
-
-    const bool soft = warp < kWsSoftWarps;
-    const int row = tid & 127, half = (tid >> 7) & 1;  // meaningful for the softmax warps
-    const bool q_owner = soft && (DH == 128 || half == 0);  // warp-uniform
-    const int e0 = DH == 128 ? half * 64 : 0;
-    uint32_t qr[32];
-#pragma unroll
-    for (int i = 0; i < 32; ++i) qr[i] = 0u;
-    if (q_owner && row < R) {
-        const uint4 *src =
-            reinterpret_cast<const uint4 *>(a.q + (((size_t)b * R + row) * H + h) * DH + e0);
-#pragma unroll
-        for (int i = 0; i < 8; ++i) {
-            const uint4 v = src[i];
-            qr[4 * i] = v.x;
-            qr[4 * i + 1] = v.y;
-            qr[4 * i + 2] = v.z;
-            qr[4 * i + 3] = v.w;
-        }
-    }
-    uint64_t am0 = 0, am1 = 0;
-    if (soft && kend > P && row < R) {
-        const int W = (R + 63) / 64;
-        const uint64_t *mr = a.anc_mask + ((size_t)b * R + row) * W;
-        am0 = mr[0];
-        if (W > 1) am1 = mr[1];
-    }
-    if (tid == 0) {
-        for (int s = 0; s < kWsStages; ++s) {
-            tc::mbar_init(&full[s], kWsLoadWarps * 32);
-            tc::mbar_init(&empty[s], 1);
-        }
-        for (int i = 0; i < kWsSBufs; ++i) {
-            tc::mbar_init(&s_full[i], 1);
-            tc::mbar_init(&s_free[i], 1);
-            tc::mbar_init(&p_ready[i], kWsSoftWarps);
-        }
-        failed = 0;
-    }
-    if (warp == 0) tc::tmem_alloc(&tmem_holder, 512);
-    tc::fence_before_sync();
-    __syncthreads();
-    tc::fence_after_sync();
-    const uint32_t tmem = tmem_holder;
-    const uint32_t t_q = tmem + 256, t_o = tmem + 384;
-    const uint32_t lane_base = (uint32_t)((warp & 3) * 32) << 16;
-    if (q_owner) {
-        tc::tmem_st32u(t_q + lane_base + e0 / 2, qr);
-        tc::tmem_wait_st();
-    }
-    tc::fence_before_sync();
-    __syncthreads();  // Q is in tensor memory before the first MMA
-    tc::fence_after_sync();
-
-    if (warp >= kWsSoftWarps && warp < kWsMmaWarp) {
-        // ---------------------------------------------------------- loaders
-        const int lt = tid - kWsSoftWarps * 32;
-        constexpr int CPR = (DH / 64) * 8;
-        bool dead = false;
-        for (int j = 0; j < nsub; ++j) {
-            const int s = j % kWsStages;
-            if (j >= kWsStages && !dead &&
-                !tc::mbar_wait_bounded(&empty[s], ((j / kWsStages) - 1) & 1, kWaitPolls)) {
-                dead = true;
-                failed = 1;
-            }
-            if (dead) break;
-            const int k0 = kbeg + j * kTcSub;
-            unsigned char *k_s = stage_k(j);
-            unsigned char *v_s = stage_v(j);
-            for (int i = lt; i < kTcSub * CPR; i += kWsLoadWarps * 32) {
-                const int r = i / CPR, c16 = i - r * CPR;
-                const int key = k0 + r;
-                const bool ok = key < kend;
-                const size_t off = ((size_t)(ok ? key : k0) * H + h) * DH + c16 * 8;
-                const uint32_t so = (c16 >> 3) * kTcSub * 128 + tc::sw128(r, c16 & 7);
-                cp_async16(tc::smem_addr(k_s + so), kc + off, ok ? 16 : 0);
-                cp_async16(tc::smem_addr(v_s + so), vc + off, ok ? 16 : 0);
-            }
-            tc::mbar_arrive_cp_async(&full[s]);
-        }
-        cp_async_wait<0>();
-    } else if (warp == kWsMmaWarp) {
-        // ------------------------------------------------------------- MMAs
-        if (lane == 0) {
-            bool dead = false;
-            for (int j = 0; j <= nsub && !dead; ++j) {
-                if (j < nsub) {
-                    const int s = j % kWsStages;
-                    dead = !tc::mbar_wait_bounded(&full[s], (j / kWsStages) & 1, kWaitPolls);
-                    if (!dead && j >= kWsSBufs)
-                        dead = !tc::mbar_wait_bounded(&s_free[j & 3], ((j >> 2) - 1) & 1,
-                                                      kWaitPolls);
-                    if (dead) break;
-                    tc::fence_proxy_async_smem();  // the copies, seen by the tensor cores
-                    tc::fence_after_sync();
-                    constexpr uint32_t idesc = tc::idesc_bf16(128, kTcSub, 0);
-                    const uint32_t t_s = tmem + (j & 3) * 64;
-                    const unsigned char *k_s = stage_k(j);
-#pragma unroll
-                    for (int ks = 0; ks < DH / 16; ++ks) {
-                        const uint32_t koff = (ks >> 2) * kTcSub * 128 + (ks & 3) * 32;
-                        const uint64_t bd = tc::sdesc_sw128(tc::smem_addr(k_s) + koff, 16, 1024);
-                        tc::mma_bf16_ts(t_s, t_q + ks * 8, bd, idesc, ks > 0);
-                    }
-                    tc::mma_commit(&s_full[j & 3]);
-                }
-                if (j >= 1) {
-                    const int jp = j - 1;
-                    if (!tc::mbar_wait_bounded(&p_ready[jp & 3], (jp >> 2) & 1, kWaitPolls)) {
-                        dead = true;
-                        break;
-                    }
-                    tc::fence_after_sync();
-                    constexpr uint32_t idesc = tc::idesc_bf16(128, DH, 1);
-                    const uint32_t t_p = tmem + (jp & 3) * 64;
-                    const unsigned char *v_s = stage_v(jp);
-#pragma unroll
-                    for (int ks = 0; ks < kTcSub / 16; ++ks) {
-                        const uint32_t pa = t_p + (ks >> 1) * HALF + (ks & 1) * 8;
-                        const uint64_t bd = tc::sdesc_sw128(tc::smem_addr(v_s) + ks * 16 * 128,
-                                                            kTcSub * 128, 1024);
-                        tc::mma_bf16_ts(t_o, pa, bd, idesc, (jp > 0 || ks > 0) ? 1u : 0u);
-                    }
-                    tc::mma_commit(&empty[jp % kWsStages]);
-                    tc::mma_commit(&s_free[jp & 3]);
-                }
-            }
-            if (dead) failed = 1;
-        }
-        __syncwarp();
-    } else {
-        // ---------------------------------------------------------- softmax
-        const bool rows_live = (warp & 3) * 32 < R;  // warp-uniform
-        float m_run = -INFINITY, l_run = 0.f;
-        bool dead = false;
-        for (int j = 0; j < nsub; ++j) {
-            const int k0 = kbeg + j * kTcSub;
-            const uint32_t t_s = tmem + (j & 3) * 64;
-            if (!dead && !tc::mbar_wait_bounded(&s_full[j & 3], (j >> 2) & 1, kWaitPolls)) {
-                dead = true;
-                failed = 1;
-            }
-            tc::fence_after_sync();
-            float x[HALF];
-            if (rows_live && !dead) {
-                tc::tmem_ld32(t_s + lane_base + half * HALF, x);
-            } else {
-#pragma unroll
-                for (int e = 0; e < HALF; ++e) x[e] = -INFINITY;
-            }
-            const int kc0 = k0 + half * HALF;
-            const bool masked = (k0 + kTcSub > P || k0 + kTcSub > kend) && rows_live;
-            float mx[4] = {-INFINITY, -INFINITY, -INFINITY, -INFINITY};
-            if (!masked) {
-#pragma unroll
-                for (int e = 0; e < HALF; ++e) {
-                    x[e] *= a.scale_log2;
-                    mx[e & 3] = fmaxf(mx[e & 3], x[e]);
-                }
-            } else {
-#pragma unroll
-                for (int e = 0; e < HALF; ++e) {
-                    const int key = kc0 + e;
-                    bool vis = key < kend;
-                    if (vis && key >= P) {
-                        const int t = key - P;
-                        vis = (((t < 64) ? am0 : am1) >> (t & 63)) & 1u;
-                    }
-                    x[e] = vis ? x[e] * a.scale_log2 : -INFINITY;
-                    mx[e & 3] = fmaxf(mx[e & 3], x[e]);
-                }
-            }
-            float *xj = xch + (j & 1) * 256;
-            xj[half * 128 + row] = fmaxf(fmaxf(mx[0], mx[1]), fmaxf(mx[2], mx[3]));
-            tc::named_sync(1, kWsSoftWarps * 32);
-            const float cm = fmaxf(xj[row], xj[128 + row]);
-            const bool raise = cm > m_run + kRescaleLog2;
-            const float m_new = raise ? cm : m_run;
-            const float alpha = raise ? exp2f(m_run - m_new) : 1.f;
-            l_run *= alpha;
-            m_run = m_new;
-            const float mu = (m_run == -INFINITY) ? 0.f : m_run;
-            if (rows_live && !dead) {
-                float ls[4] = {0.f, 0.f, 0.f, 0.f};
-                uint32_t pk[HALF / 2];
-#pragma unroll
-                for (int e = 0; e < HALF; e += 2) {
-                    const uint32_t w = pack_bf16(exp2f(x[e] - mu), exp2f(x[e + 1] - mu));
-                    pk[e / 2] = w;
-                    ls[(e / 2) & 3] += bf_lo(w) + bf_hi(w);
-                }
-                l_run += (ls[0] + ls[1]) + (ls[2] + ls[3]);
-                tc::tmem_st16(t_s + lane_base + half * HALF, pk);
-                if (__any_sync(0xffffffffu, raise && j > 0)) {
-                    // O must hold every P V up to j-1 and none after
-                    if (!tc::mbar_wait_bounded(&s_free[(j - 1) & 3], ((j - 1) >> 2) & 1,
-                                               kWaitPolls)) {
-                        dead = true;
-                        failed = 1;
-                    }
-                    tc::fence_after_sync();
-                    if (!dead) {
-#pragma unroll 1
-                        for (int c = 0; c < DH / 2; c += 32) {
-                            float ov[32];
-                            tc::tmem_ld32(t_o + lane_base + half * (DH / 2) + c, ov);
-#pragma unroll
-                            for (int e = 0; e < 32; ++e) ov[e] *= alpha;
-                            tc::tmem_st32(t_o + lane_base + half * (DH / 2) + c, ov);
-                        }
-                    }
-                }
-                tc::tmem_wait_st();
-            }
-            tc::fence_before_sync();
-            __syncwarp();
-            if (lane == 0) tc::mbar_arrive(&p_ready[j & 3]);
-        }
-        // ---- the last P V, then the partial rows
-        const int jl = nsub - 1;
-        if (!dead && !tc::mbar_wait_bounded(&s_free[jl & 3], (jl >> 2) & 1, kWaitPolls)) {
-            dead = true;
-            failed = 1;
-        }
-        tc::fence_after_sync();
-        if (!dead) {
-            float *dst = a.part_o + (pbase + row) * DH;
-            for (int c = half * (DH / 2); c < (half + 1) * (DH / 2); c += 32) {
-                float ov[32];
-                tc::tmem_ld32(t_o + lane_base + c, ov);
-                if (row < R) {
-#pragma unroll
-                    for (int e = 0; e < 32; e += 4)
-                        *reinterpret_cast<float4 *>(dst + c + e) =
-                            make_float4(ov[e], ov[e + 1], ov[e + 2], ov[e + 3]);
-                }
-            }
-        }
-        float *xs = xch + 2 * 256;
-        xs[half * 128 + row] = l_run;
-        tc::named_sync(1, kWsSoftWarps * 32);
-        if (half == 0 && row < R) {
-            const float l = xs[row] + xs[128 + row];
-            a.part_ml[pbase + row] = dead ? make_float2(-INFINITY, 0.f) : make_float2(m_run, l);
-        }
-    }
-    tc::fence_before_sync();
-    __syncthreads();
-    if (failed && tid == 0) set_status(a.status, MEDUSA_DEV_TIMEOUT);
-    if (warp == 0) tc::tmem_dealloc(tmem, 512);
-}
-
 // One warp per (sequence, row, head).  Lane s reads split s's (m, l), so the
 // weights come from one round of independent loads; the O partials of all
 // splits are then read with independent loads as well (no load waits on
@@ -1104,16 +774,10 @@ void split_plan(int B, int H, int P_max, int *nps, int *chunk) {
 
 size_t align256(size_t x) { return (x + 255) & ~size_t(255); }
 
-// Key ranges of the tensor-core paths.  Long ranges (>= kWsMinSub 64-key
-// sub-chunks at P_max) go to the warp-specialised kernel: one CTA per SM,
-// one wave for a single sequence, two for a batch (P_b may be ragged), at
-// least four sub-chunks per CTA.  Shorter ones go to tree_attn_tc_kernel:
-// at least two sub-chunks per CTA (so that loads overlap compute), one
-// (B = 1) or two (B > 1) waves of two CTAs per SM.
-constexpr int kWsMinSub = 24;
-
+// Key ranges of the tensor-core path: at least two 64-key sub-chunks per CTA
+// (so that loads overlap compute), and one (B = 1) or two (B > 1) waves of
+// two CTAs per SM over the whole grid at P_max.
 struct TcPlan {
-    bool ws;
     int ns, chunk;
 };
 
@@ -1121,10 +785,8 @@ TcPlan tc_plan(int B, int H, int R, int P_max) {
     TcPlan p;
     const int nsub = (P_max + R + kTcSub - 1) / kTcSub;
     const int waves = B == 1 ? 1 : 2;
-    p.ws = nsub >= kWsMinSub;
-    const int slots = p.ws ? waves * device_sm_count() : 2 * waves * device_sm_count();
-    const int per_head = std::max(1, slots / std::max(1, B * H));
-    const int cps = std::max(p.ws ? 4 : 2, (nsub + per_head - 1) / per_head);
+    const int per_head = std::max(1, 2 * waves * device_sm_count() / std::max(1, B * H));
+    const int cps = std::max(2, (nsub + per_head - 1) / per_head);
     p.ns = (nsub + cps - 1) / cps;
     p.chunk = cps * kTcSub;
     return p;
@@ -1168,12 +830,10 @@ cudaError_t launch_tree_attention(medusa_dtype dtype, const void *q, const void 
     }
     const bool use_tc = R <= 128;
     int nps, chunk;
-    bool use_ws = false;
     if (use_tc) {
         const TcPlan tp = tc_plan(B, H, R, P_max);  // key ranges per head
         nps = tp.ns;
         chunk = tp.chunk;
-        use_ws = tp.ws;
     } else {
         split_plan(B, H, P_max, &nps, &chunk);
     }
@@ -1198,15 +858,7 @@ cudaError_t launch_tree_attention(medusa_dtype dtype, const void *q, const void 
     a.part_o = part_o;
     a.part_ml = part_ml;
     a.status = status;
-    if (use_ws) {
-        auto kern = dh == 128 ? tree_attn_ws_kernel<128> : tree_attn_ws_kernel<64>;
-        const int smem = dh == 128 ? WsSmem<128>::TOTAL : WsSmem<64>::TOTAL;
-        if ((e = cudaFuncSetAttribute(kern, cudaFuncAttributeMaxDynamicSharedMemorySize, smem)))
-            return e;
-        e = launch_pdl(kern, dim3(H, NS, B), dim3(kWsThreads), (size_t)smem, stream, a);
-        note_launch();
-        if (e) return e;
-    } else if (use_tc) {
+    if (use_tc) {
         auto kern = dh == 128 ? tree_attn_tc_kernel<128> : tree_attn_tc_kernel<64>;
         const int smem = dh == 128 ? TcSmem<128>::TOTAL : TcSmem<64>::TOTAL;
         if ((e = cudaFuncSetAttribute(kern, cudaFuncAttributeMaxDynamicSharedMemorySize, smem)))

@@ -41,27 +41,6 @@ __device__ __forceinline__ bool mbar_try_wait(uint64_t *bar, uint32_t parity) {
     return ok != 0;
 }
 
-// plain arrive (count 1) by the executing thread
-__device__ __forceinline__ void mbar_arrive(uint64_t *bar) {
-    asm volatile(
-        "{\n.reg .b64 st;\n"
-        "mbarrier.arrive.shared::cta.b64 st, [%0];\n}\n" ::"r"(smem_addr(bar))
-        : "memory");
-}
-
-// arrive on `bar` once every cp.async issued so far by this thread has
-// landed (the barrier's expected count includes this arrival)
-__device__ __forceinline__ void mbar_arrive_cp_async(uint64_t *bar) {
-    asm volatile("cp.async.mbarrier.arrive.noinc.shared::cta.b64 [%0];\n" ::"r"(smem_addr(bar))
-                 : "memory");
-}
-
-// barrier among `count` threads (a multiple of 32) on hardware barrier `id`
-// (1..15; 0 is __syncthreads)
-__device__ __forceinline__ void named_sync(int id, int count) {
-    asm volatile("bar.sync %0, %1;\n" ::"r"(id), "r"(count) : "memory");
-}
-
 // Wait for phase `parity` of `bar`, giving up after `limit` polls (each poll
 // itself blocks for a hardware-defined interval).  Returns false on timeout.
 __device__ __forceinline__ bool mbar_wait_bounded(uint64_t *bar, uint32_t parity, uint32_t limit) {
