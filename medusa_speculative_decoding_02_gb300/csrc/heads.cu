@@ -105,6 +105,16 @@ __global__ void __launch_bounds__(kW1Threads, NB <= 2 ? 4 : 1)
 heads_w1_kernel(const T *__restrict__ h, const T *__restrict__ W1, const T *__restrict__ b1,
                 float *__restrict__ z, float *__restrict__ z_lm, int B, int d, int K,
                 int total_warps) {
+    {
+        // The weights are never written by any kernel, so each warp pulls its
+        // first two rows into L2 before the wait for the previous kernel
+        const int gw0 = blockIdx.x * (blockDim.x >> 5) + (threadIdx.x >> 5);
+        const int rows0 = K * d;
+        const int rb = (int)(((long long)gw0 * rows0) / total_warps);
+        const int re = min((int)(((long long)(gw0 + 1) * rows0) / total_warps), rb + 2);
+        if ((threadIdx.x & 31) == 0 && re > rb)
+            prefetch_l2_bulk(W1 + (size_t)rb * d, (unsigned)((re - rb) * d * sizeof(T)));
+    }
     pdl_enter();
     extern __shared__ float4 smem4[];
     float *hs = reinterpret_cast<float *>(smem4);
