@@ -237,40 +237,6 @@ __device__ __forceinline__ void flush_slot(TopSlot &slot, const WarpTop &st, int
     }
 }
 
-// Number of entries of a best-first list that rank before (cv, ci); empty
-// entries (id INT_MAX) sit at the tail and rank after everything.
-__device__ __forceinline__ int count_better(const TopSlot &sl, float cv, int ci, int S) {
-    int lo = 0, hi = S;
-    while (lo < hi) {
-        const int mid = (lo + hi) >> 1;
-        const int id = sl.id[mid];
-        if (id != INT_MAX && better(sl.val[mid], id, cv, ci))
-            lo = mid + 1;
-        else
-            hi = mid;
-    }
-    return lo;
-}
-
-// Merge nslot best-first lists (slot w at slots[w * stride]) by ranking every
-// entry against the other lists (binary search each); the entry of rank r < S
-// goes to out_val[r] / out_id[r].  One thread per entry, no serial chain.
-__device__ __forceinline__ void rank_merge_entry(const TopSlot *slots, int stride, int nslot,
-                                                 int S, int w, int j, float *out_val,
-                                                 int *out_id) {
-    const TopSlot &me = slots[w * stride];
-    const int ci = me.id[j];
-    if (ci == INT_MAX) return;
-    const float cv = me.val[j];
-    int rank = j;
-    for (int o = 0; o < nslot; ++o)
-        if (o != w) rank += count_better(slots[o * stride], cv, ci, S);
-    if (rank < S) {
-        out_val[rank] = cv;
-        out_id[rank] = ci;
-    }
-}
-
 // (max, sum-exp) of nslot slots, merged by one warp; valid in every lane.
 __device__ __forceinline__ void warp_merge_ms(const TopSlot *slots, int stride, int nslot,
                                               int lane, float &m, float &s) {
@@ -285,6 +251,89 @@ __device__ __forceinline__ void warp_merge_ms(const TopSlot *slots, int stride, 
     }
     m = t.m;
     s = t.s;
+}
+
+// compare-exchange so that (va, ia) ends up the better of the two
+__device__ __forceinline__ void cx(float &va, int &ia, float &vb, int &ib) {
+    if (better(vb, ib, va, ia)) {
+        const float tv = va; va = vb; vb = tv;
+        const int ti = ia; ia = ib; ib = ti;
+    }
+}
+
+// Warp top-S selection over up to 32*U candidates plus the warp's running
+// list (lanes < S): every lane sorts its own few candidates in registers, then
+// S rounds each take the best lane head by a five-step shuffle argmax and pop
+// it.  The result is left sorted best-first in lanes 0..S-1 (val, id).
+template <int U>
+__device__ __forceinline__ void warp_select_top(float (&cv)[U + 1], int (&ci)[U + 1], int S,
+                                                int lane, float &val, int &id) {
+    // sort the lane's U+1 entries best-first (odd-even transposition)
+#pragma unroll
+    for (int r = 0; r < U + 1; ++r)
+#pragma unroll
+        for (int e = (r & 1); e + 1 < U + 1; e += 2) cx(cv[e], ci[e], cv[e + 1], ci[e + 1]);
+    float nv = -INFINITY;
+    int ni = INT_MAX;
+    for (int k = 0; k < S; ++k) {
+        float bv = cv[0];
+        int bi = ci[0];
+#pragma unroll
+        for (int o = 16; o > 0; o >>= 1) {
+            const float ov = __shfl_xor_sync(0xffffffffu, bv, o);
+            const int oi = __shfl_xor_sync(0xffffffffu, bi, o);
+            if (better(ov, oi, bv, bi)) {
+                bv = ov;
+                bi = oi;
+            }
+        }
+        if (lane == k) {
+            nv = bv;
+            ni = bi;
+        }
+        if (bi != INT_MAX && ci[0] == bi) {  // this lane's head won: pop it
+#pragma unroll
+            for (int e = 0; e < U; ++e) {
+                cv[e] = cv[e + 1];
+                ci[e] = ci[e + 1];
+            }
+            cv[U] = -INFINITY;
+            ci[U] = INT_MAX;
+        }
+    }
+    val = nv;
+    id = ni;
+}
+
+// Top-S of nslot best-first lists (list w at slots[w * stride], S entries
+// each, empty entries at the tail) by one warp: groups of 64 candidates (two
+// per lane) join the warp's running list in warp_select_top.  The result is
+// sorted best-first in lanes 0..S-1.
+__device__ __forceinline__ void warp_merge_top(const TopSlot *slots, int stride, int nslot, int S,
+                                               int lane, float &val, int &id) {
+    constexpr int U = 2;
+    const int n = nslot * S;
+    val = -INFINITY;
+    id = INT_MAX;
+    for (int c0 = 0; c0 < n; c0 += kWarp * U) {
+        float cv[U + 1];
+        int ci[U + 1];
+#pragma unroll
+        for (int u = 0; u < U; ++u) {
+            const int c = c0 + u * kWarp + lane;
+            if (c < n) {
+                const int w = c / S, j = c - w * S;
+                cv[u] = slots[w * stride].val[j];
+                ci[u] = slots[w * stride].id[j];
+            } else {
+                cv[u] = -INFINITY;
+                ci[u] = INT_MAX;
+            }
+        }
+        cv[U] = lane < S ? val : -INFINITY;  // the running list joins the pool
+        ci[U] = lane < S ? id : INT_MAX;
+        warp_select_top<U>(cv, ci, S, lane, val, id);
+    }
 }
 
 // Row v of head k's vocabulary projection: with the LM head present it is
@@ -397,89 +446,27 @@ heads_w2_kernel(const float *__restrict__ z, const T *__restrict__ W2, const T *
         }
         __syncthreads();
 
-        // merge the warps' states per (head, sequence): empty defaults first,
-        // then every warp entry is ranked against the other warps' lists
+        // merge the warps' states per (head, sequence), one warp per pair
         const int pairs = hk * B;
-        for (int t = threadIdx.x; t < pairs * S; t += blockDim.x) {
-            const int pair = t / S, j = t - pair * S;
-            const int kk = pair / B, b = pair - kk * B;
-            const size_t o = ((size_t)(k0 + kk) * B + b) * G + g;
-            part_val[o * S + j] = -INFINITY;
-            part_id[o * S + j] = INT_MAX;
-        }
         for (int pair = warp; pair < pairs; pair += kW2Warps) {
             const int kk = pair / B, b = pair - kk * B;
+            const size_t o = ((size_t)(k0 + kk) * B + b) * G + g;
             float m, sum;
             warp_merge_ms(slots + kk * NB + b, hpg * NB, kW2Warps, lane, m, sum);
-            if (lane == 0) part_ms[((size_t)(k0 + kk) * B + b) * G + g] = make_float2(m, sum);
-        }
-        __syncthreads();
-        for (int t = threadIdx.x; t < pairs * kW2Warps * S; t += blockDim.x) {
-            const int pair = t / (kW2Warps * S);
-            const int rem = t - pair * kW2Warps * S;
-            const int w = rem / S, j = rem - w * S;
-            const int kk = pair / B, b = pair - kk * B;
-            const size_t o = ((size_t)(k0 + kk) * B + b) * G + g;
-            rank_merge_entry(slots + kk * NB + b, hpg * NB, kW2Warps, S, w, j, part_val + o * S,
-                             part_id + o * S);
+            float tv;
+            int ti;
+            warp_merge_top(slots + kk * NB + b, hpg * NB, kW2Warps, S, lane, tv, ti);
+            if (lane == 0) part_ms[o] = make_float2(m, sum);
+            if (lane < S) {
+                part_val[o * S + lane] = tv;
+                part_id[o * S + lane] = ti;
+            }
         }
         __syncthreads();
     }
 }
 
 // ------------------------------------------------------------- phase 3 ---
-
-// compare-exchange so that (va, ia) ends up the better of the two
-__device__ __forceinline__ void cx(float &va, int &ia, float &vb, int &ib) {
-    if (better(vb, ib, va, ia)) {
-        const float tv = va; va = vb; vb = tv;
-        const int ti = ia; ia = ib; ib = ti;
-    }
-}
-
-// Warp top-S selection over up to 32*U candidates plus the warp's running
-// list (lanes < S): every lane sorts its own few candidates in registers, then
-// S rounds each take the best lane head by a five-step shuffle argmax and pop
-// it.  The result is left sorted best-first in lanes 0..S-1 (val, id).
-template <int U>
-__device__ __forceinline__ void warp_select_top(float (&cv)[U + 1], int (&ci)[U + 1], int S,
-                                                int lane, float &val, int &id) {
-    // sort the lane's U+1 entries best-first (odd-even transposition)
-#pragma unroll
-    for (int r = 0; r < U + 1; ++r)
-#pragma unroll
-        for (int e = (r & 1); e + 1 < U + 1; e += 2) cx(cv[e], ci[e], cv[e + 1], ci[e + 1]);
-    float nv = -INFINITY;
-    int ni = INT_MAX;
-    for (int k = 0; k < S; ++k) {
-        float bv = cv[0];
-        int bi = ci[0];
-#pragma unroll
-        for (int o = 16; o > 0; o >>= 1) {
-            const float ov = __shfl_xor_sync(0xffffffffu, bv, o);
-            const int oi = __shfl_xor_sync(0xffffffffu, bi, o);
-            if (better(ov, oi, bv, bi)) {
-                bv = ov;
-                bi = oi;
-            }
-        }
-        if (lane == k) {
-            nv = bv;
-            ni = bi;
-        }
-        if (bi != INT_MAX && ci[0] == bi) {  // this lane's head won: pop it
-#pragma unroll
-            for (int e = 0; e < U; ++e) {
-                cv[e] = cv[e + 1];
-                ci[e] = ci[e + 1];
-            }
-            cv[U] = -INFINITY;
-            ci[U] = INT_MAX;
-        }
-    }
-    val = nv;
-    id = ni;
-}
 
 // One CTA per (head, sequence).  The G partial top-s lists sit contiguously
 // (G*S candidates); each warp selects the top-s of its share with
@@ -544,8 +531,15 @@ heads_reduce_kernel(const float2 *__restrict__ part_ms, const float *__restrict_
         warp_merge_ms(slots, 1, NW, lane, m, sum);
         if (lane == 0) s_logz = m + logf(sum);
     }
-    for (int t = threadIdx.x; t < NW * S; t += kReduceThreads)
-        rank_merge_entry(slots, 1, NW, S, t / S, t % S, r_val, r_id);
+    if (warp == 1) {
+        float tv;
+        int ti;
+        warp_merge_top(slots, 1, NW, S, lane, tv, ti);
+        if (lane < S) {
+            r_val[lane] = tv;
+            r_id[lane] = ti;
+        }
+    }
     __syncthreads();
     if (lm && k == 0) {  // the LM head: its greedy token is the tree root
         if (threadIdx.x == 0) {
