@@ -147,9 +147,30 @@ __device__ __forceinline__ int count_before(const uint64_t *key, const uint64_t 
     return warp_sum_int(cnt);
 }
 
-// Every counting pass gives one warp per item and splits the comparisons over
-// its lanes, so the longest dependent chain is ~c/32 shared loads plus a
-// five-step shuffle.
+// Rank every item i < c of (key, lo)[0..c) -- the number of entries taken
+// before it -- with four threads per item, each counting a quarter of the
+// entries (threads of an item read the same words: shared-memory
+// broadcasts), combined by two shuffles; the entry of rank r < n goes to
+// out[r].  All threads of the CTA call it (the shuffles need full warps).
+__device__ __forceinline__ void rank_quad(const uint64_t *key, const uint64_t *lo, int c, int n,
+                                          uint64_t *out, int tid, int nt) {
+    for (int base = 0; base < c; base += nt / 4) {
+        const int i = base + (tid >> 2), q = tid & 3;
+        int cnt = 0;
+        if (i < c) {
+            const uint64_t ki = key[i], li = lo[i];
+#pragma unroll 4
+            for (int j = q; j < c; j += 4) cnt += precedes(key[j], lo[j], ki, li);
+        }
+        cnt += __shfl_xor_sync(0xffffffffu, cnt, 1);
+        cnt += __shfl_xor_sync(0xffffffffu, cnt, 2);
+        if (i < c && q == 0 && cnt < n) out[cnt] = lo[i];
+    }
+}
+
+// The level-wise passes of large trees give one warp per item and split the
+// comparisons over its lanes, so the longest dependent chain is ~c/32 shared
+// loads plus a five-step shuffle.
 __global__ void __launch_bounds__(kTreeThreads) build_tree_kernel(TreeArgs a) {
     pdl_enter();
     extern __shared__ __align__(16) char tsm[];
@@ -164,6 +185,12 @@ __global__ void __launch_bounds__(kTreeThreads) build_tree_kernel(TreeArgs a) {
     const int K = a.K, S = a.S, n = a.n, R = n + 1;
     const int W = (R + 63) / 64;
 
+    // the scalars the last phase needs, loaded with the tables
+    __shared__ int s_root, s_prefix;
+    if (tid == 0) {
+        s_root = a.root[b];
+        s_prefix = a.prefix_len ? a.prefix_len[b] : 0;
+    }
     for (int i = tid; i < K * S; i += nt) {
         const int k = i / S, r = i - k * S;
         const float v = a.logp[(size_t)b * a.logp_bstride + (size_t)k * S + r];
@@ -199,11 +226,7 @@ __global__ void __launch_bounds__(kTreeThreads) build_tree_kernel(TreeArgs a) {
             sm.cand_lo[t] = ((uint64_t)D << 32) | path;
         }
         __syncthreads();
-        for (int i = warp; i < full; i += nw) {
-            const int cnt = count_before(sm.cand_key, sm.cand_lo, full, sm.cand_key[i],
-                                         sm.cand_lo[i], lane);
-            if (lane == 0 && cnt < n) sm.sel_lo[cnt] = sm.cand_lo[i];
-        }
+        rank_quad(sm.cand_key, sm.cand_lo, full, n, sm.sel_lo, tid, nt);
     } else {
         // ---- large tree: level D keeps its best n candidates (a node
         // outside them cannot be among the first n overall)
@@ -251,14 +274,20 @@ __global__ void __launch_bounds__(kTreeThreads) build_tree_kernel(TreeArgs a) {
     }
     __syncthreads();
 
-    // ---- canonical order: root, then (depth, rank path) ascending
-    for (int i = warp; i < n; i += nw) {
-        const uint64_t li = sm.sel_lo[i];
+    // ---- canonical order: root, then (depth, rank path) ascending (the lo
+    // words are distinct), four threads per node
+    for (int base = 0; base < n; base += nt / 4) {
+        const int i = base + (tid >> 2), q = tid & 3;
         int cnt = 0;
+        uint64_t li = 0;
+        if (i < n) {
+            li = sm.sel_lo[i];
 #pragma unroll 4
-        for (int j = lane; j < n; j += kWarp) cnt += sm.sel_lo[j] < li;
-        cnt = warp_sum_int(cnt);
-        if (lane == 0) sm.c_lo[1 + cnt] = li;
+            for (int j = q; j < n; j += 4) cnt += sm.sel_lo[j] < li;
+        }
+        cnt += __shfl_xor_sync(0xffffffffu, cnt, 1);
+        cnt += __shfl_xor_sync(0xffffffffu, cnt, 2);
+        if (i < n && q == 0) sm.c_lo[1 + cnt] = li;
     }
     if (tid == 0) sm.c_lo[0] = 0;
     for (int i = tid; i < R; i += nt) sm.has_child[i] = 0;
@@ -288,16 +317,21 @@ __global__ void __launch_bounds__(kTreeThreads) build_tree_kernel(TreeArgs a) {
     __syncthreads();
 
     // ---- per-node outputs; leaves numbered by a ballot scan
-    const int P = a.prefix_len ? a.prefix_len[b] : 0;
+    const int P = s_prefix;
     const bool leaf = tid < R && !sm.has_child[tid];
     const unsigned bal = __ballot_sync(0xffffffffu, leaf);
     if (lane == 0) warp_leaves[warp] = __popc(bal);
     __syncthreads();
-    int before = 0, nl = 0;
-    for (int w = 0; w < nw; ++w) {
-        if (w < warp) before += warp_leaves[w];
-        nl += warp_leaves[w];
+    // leaves before this warp and in total: one shuffle scan of the per-warp
+    // counts (nw <= 32)
+    int incl = lane < nw ? warp_leaves[lane] : 0;
+#pragma unroll
+    for (int o = 1; o < kWarp; o <<= 1) {
+        const int v = __shfl_up_sync(0xffffffffu, incl, o);
+        if (lane >= o) incl += v;
     }
+    const int nl = __shfl_sync(0xffffffffu, incl, kWarp - 1);
+    const int before = warp > 0 ? __shfl_sync(0xffffffffu, incl, warp - 1) : 0;
     if (leaf) sm.leaf_of[before + __popc(bal & ((1u << lane) - 1u))] = tid;
     if (tid < R) {
         const int i = tid;
@@ -306,7 +340,7 @@ __global__ void __launch_bounds__(kTreeThreads) build_tree_kernel(TreeArgs a) {
         const size_t o = (size_t)b * R + i;
         int tok;
         if (i == 0) {
-            tok = a.root[b];
+            tok = s_root;
         } else {
             const int r = (int)(((uint32_t)li >> nib_shift(D)) & 0xF);
             tok = tid_tok[D - 1][r];
@@ -315,12 +349,17 @@ __global__ void __launch_bounds__(kTreeThreads) build_tree_kernel(TreeArgs a) {
         a.parent[o] = sm.c_parent[i];
         a.depth[o] = D;
         a.pos_id[o] = P + D;
-        for (int w = 0; w < W; ++w) {
-            uint64_t m = 0;
-            for (int x = i; x >= 0; x = sm.c_parent[x])
-                if ((x >> 6) == w) m |= (uint64_t)1 << (x & 63);
-            a.anc_mask[o * W + w] = m;
+        // one walk up the ancestors sets the bits of every mask word
+        uint64_t mw[4] = {0, 0, 0, 0};  // W <= 4 (R <= 256)
+        for (int x = i; x >= 0; x = sm.c_parent[x]) {
+            const uint64_t bit = (uint64_t)1 << (x & 63);
+            const int w = x >> 6;
+            mw[0] |= w == 0 ? bit : 0;
+            mw[1] |= w == 1 ? bit : 0;
+            mw[2] |= w == 2 ? bit : 0;
+            mw[3] |= w == 3 ? bit : 0;
         }
+        for (int w = 0; w < W; ++w) a.anc_mask[o * W + w] = w == 0 ? mw[0] : w == 1 ? mw[1] : w == 2 ? mw[2] : mw[3];
     }
     __syncthreads();
     if (tid == 0) a.n_leaf[b] = nl;
