@@ -299,7 +299,7 @@ def run_reference(args, cfg):
         "n_gpus": args.gpus, "steps": args.steps, "warmup": args.warmup,
         "ms_per_step": round(per * 1e3, 3), "higher_is_better": True, "scaling": "weak",
         "vs_baseline": None, "dtype": "f64", "data": "synthetic (seeded, Vicuna-7B shapes)",
-        "config": {"workload": cfg.name + "_bs1_step", "sample": sample},
+        "config": workload_config(cfg, args.gpus),
         "cpu_baseline": {"value": round(value, 4), "unit": UNIT, "cores": 1, "kind": "oracle",
                          "sample": sample},
         "e2e": {"value": round(value, 4), "unit": UNIT, "h2d_bytes_per_step": 0,
@@ -307,6 +307,15 @@ def run_reference(args, cfg):
     }
     print(json.dumps(line), flush=True)
     return 0
+
+
+def workload_config(cfg, world: int) -> dict:
+    """The `config` object of both arms' JSON lines."""
+    return {"workload": "v7b_bs1_step", "d": cfg.d, "V": cfg.V, "K": cfg.K, "s": list(cfg.s),
+            "tree_nodes": cfg.n, "attn_heads": cfg.H, "head_dim": cfg.dh, "prefix": cfg.P_max,
+            "batch": cfg.B, "accept": cfg.mode, "bytes_per_step": int(step_bytes(cfg)["total"]),
+            "parallelism": f"replicas{world}",
+            "l2": "inputs larger than L2: 1.50 GB of weights, KV and logits per step"}
 
 
 # -------------------------------------------------------------------- ours ---
@@ -664,11 +673,7 @@ def run_ours(args, cfg):
         "step_us": round(ms_step * 1e3, 2), "higher_is_better": True,
         "scaling": "weak", "vs_baseline": None, "dtype": "bf16",
         "data": "synthetic (seeded, Vicuna-7B shapes: random weights, KV and logits)",
-        "config": {"workload": "v7b_bs1_step", "d": cfg.d, "V": cfg.V, "K": cfg.K,
-                   "s": list(cfg.s), "tree_nodes": cfg.n, "attn_heads": cfg.H, "head_dim": cfg.dh,
-                   "prefix": cfg.P_max, "batch": cfg.B, "accept": cfg.mode,
-                   "bytes_per_step": int(nb["total"]), "parallelism": f"replicas{world}",
-                   "l2": "inputs larger than L2: 1.50 GB of weights, KV and logits per step"},
+        "config": workload_config(cfg, world),
         "stages": stages,
         "next_rows": next_rows,
         "size_scan": size_scan,
