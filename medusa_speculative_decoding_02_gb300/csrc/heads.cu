@@ -611,7 +611,6 @@ cudaError_t run_heads(const void *h, const void *Wlm, const void *W1, const void
         return e;
     int occ1 = 0;
     if ((e = cudaOccupancyMaxActiveBlocksPerMultiprocessor(&occ1, k1, kW1Threads, smem1))) return e;
-    const int rows1 = K * d;
     const int warps1 = kW1Threads / kWarp;
     const int grid1 = sms * std::max(occ1, 1);  // one full wave
     const int total_warps = grid1 * warps1;
