@@ -7,18 +7,12 @@
 // in slots P_b..P_b+R-1; node i may see tree slot t iff bit t of its
 // ancestor-mask row is set.
 //
-// bf16 path (tensor cores, split-KV):
-//   tree_attn_split_kernel  grid (prefix splits + 1, H, B).  One CTA owns one
-//       head of one sequence and one key range; its warps own 16 query rows
-//       each, so all R tree rows share every K/V tile, which is staged into
-//       shared memory with cp.async (double-buffered, XOR-swizzled rows).
-//       S = Q K^T and O += P V run as m16n8k16 bf16 MMAs with fp32
-//       accumulation; the softmax is online in the log2 domain.  The last
-//       split covers the R tree slots and applies the ancestor bitmask; the
-//       prefix splits need no mask.  Each CTA writes unnormalised partial
-//       (O, m, l) rows.
-//   tree_attn_combine_kernel  merges the splits of each (b, row, head) with a
-//       log-sum-exp rescale and writes the bf16 output.
+// bf16 path (tcgen05 tensor cores, split-KV):
+//   tree_attn_tc_kernel  grid (H * row tiles, key ranges, B): one CTA per
+//       (128-row tile of the tree, head, key range, sequence) computes
+//       unnormalised partial (O, m, l) rows over its keys (below).
+//   tree_attn_combine_kernel  merges the key ranges of each (b, row, head)
+//       with a log-sum-exp rescale and writes the bf16 output.
 // f32 path (small problems): tree_attn_f32_kernel, one CTA per
 // (row, head, sequence) on CUDA cores, exact softmax.
 #include <algorithm>
@@ -31,16 +25,9 @@ namespace medusa {
 
 namespace {
 
-constexpr int kTile = 64;        // keys per shared-memory stage
-constexpr int kSub = 32;         // keys per softmax/MMA sub-step
-constexpr int kTargetCtas = 304; // split-KV aim: two CTAs per SM on 152 SMs
 constexpr float kLog2e = 1.4426950408889634f;
 
-__device__ __forceinline__ unsigned smem_u32(const void *p) {
-    return static_cast<unsigned>(__cvta_generic_to_shared(p));
-}
-
-__device__ __forceinline__ void cp_async16(unsigned dst, const void *src, int src_bytes) {
+__device__ __forceinline__ void cp_async16(uint32_t dst, const void *src, int src_bytes) {
     asm volatile("cp.async.cg.shared.global [%0], [%1], 16, %2;\n" ::"r"(dst), "l"(src),
                  "r"(src_bytes));
 }
@@ -50,37 +37,9 @@ __device__ __forceinline__ void cp_async_wait() {
     asm volatile("cp.async.wait_group %0;\n" ::"n"(N));
 }
 
-__device__ __forceinline__ void ldsm_x4(unsigned addr, uint32_t &r0, uint32_t &r1, uint32_t &r2,
-                                        uint32_t &r3) {
-    asm volatile("ldmatrix.sync.aligned.m8n8.x4.shared.b16 {%0,%1,%2,%3}, [%4];\n"
-                 : "=r"(r0), "=r"(r1), "=r"(r2), "=r"(r3)
-                 : "r"(addr));
-}
-__device__ __forceinline__ void ldsm_x4_t(unsigned addr, uint32_t &r0, uint32_t &r1, uint32_t &r2,
-                                          uint32_t &r3) {
-    asm volatile("ldmatrix.sync.aligned.m8n8.x4.trans.shared.b16 {%0,%1,%2,%3}, [%4];\n"
-                 : "=r"(r0), "=r"(r1), "=r"(r2), "=r"(r3)
-                 : "r"(addr));
-}
-
-__device__ __forceinline__ void mma_bf16(float (&c)[4], const uint32_t (&a)[4], uint32_t b0,
-                                         uint32_t b1) {
-    asm volatile(
-        "mma.sync.aligned.m16n8k16.row.col.f32.bf16.bf16.f32 {%0,%1,%2,%3}, {%4,%5,%6,%7}, "
-        "{%8,%9}, {%0,%1,%2,%3};\n"
-        : "+f"(c[0]), "+f"(c[1]), "+f"(c[2]), "+f"(c[3])
-        : "r"(a[0]), "r"(a[1]), "r"(a[2]), "r"(a[3]), "r"(b0), "r"(b1));
-}
-
 __device__ __forceinline__ uint32_t pack_bf16(float lo, float hi) {
     __nv_bfloat162 v = __floats2bfloat162_rn(lo, hi);
     return *reinterpret_cast<uint32_t *>(&v);
-}
-
-// byte offset of 16-byte chunk `ch` of row `row` in a tile of DH bf16 per row
-template <int DH>
-__device__ __forceinline__ unsigned swz(int row, int ch) {
-    return row * (DH * 2) + ((ch ^ (row & 7)) << 4);
 }
 
 // A sequence's cache pointers are read on the device, so their checks run
@@ -99,217 +58,17 @@ struct AttnArgs {
     const uint64_t *anc_mask;
     int B, R, H, P_max;
     int chunk, nps;
+    int row_tiles;  // 128-row tiles of the R tree rows
     float scale_log2;
     float *part_o;
     float2 *part_ml;
     int *status;
 };
 
-template <int DH, int MAXW>
-__global__ void __launch_bounds__(MAXW * 32, 1) tree_attn_split_kernel(AttnArgs a) {
-    pdl_enter();
-    extern __shared__ __align__(128) unsigned char asmem[];
-    constexpr int CPR = DH / 8;  // 16-byte chunks per row
-    const int NW = blockDim.x >> 5;
-    const int QROWS = NW * 16;
-    unsigned char *q_s = asmem;
-    unsigned char *k_s = q_s + QROWS * DH * 2;
-    unsigned char *v_s = k_s + 2 * kTile * DH * 2;
-    uint64_t *mask_s = reinterpret_cast<uint64_t *>(v_s + 2 * kTile * DH * 2);  // [QROWS][4]
-    const int sp = blockIdx.x, h = blockIdx.y, b = blockIdx.z;
-    const int NS = a.nps + 1;
-    const int R = a.R, H = a.H;
-    const int tid = threadIdx.x, lane = tid & 31, warp = tid >> 5;
-    const int g = lane >> 2, t4 = lane & 3;
-
-    int P = a.prefix_len[b];
-    if (P < 0 || P > a.P_max) {
-        set_status(a.status, MEDUSA_DEV_BAD_PREFIX);
-        P = 0;
-    }
-    const bool tree_split = (sp == a.nps);
-    const int kbeg = tree_split ? P : sp * a.chunk;
-    const int kend = tree_split ? P + R : min((sp + 1) * a.chunk, P);
-    const size_t pbase = ((size_t)(b * H + h) * NS + sp) * R;
-    const bf16 *kc = a.kc[b];
-    const bf16 *vc = a.vc[b];
-    const bool bad_cache = cache_pointers_bad(kc, vc);
-    if (bad_cache) set_status(a.status, MEDUSA_DEV_BAD_CACHE);
-
-    if (kend <= kbeg || bad_cache) {
-        for (int r = tid; r < R; r += blockDim.x)
-            a.part_ml[pbase + r] = make_float2(-INFINITY, 0.f);
-        return;
-    }
-
-    // stage Q (rows >= R zero-filled)
-    for (int i = tid; i < QROWS * CPR; i += blockDim.x) {
-        const int row = i / CPR, ch = i - row * CPR;
-        const bool ok = row < R;
-        const bf16 *src = a.q + (((size_t)b * R + (ok ? row : 0)) * H + h) * DH + ch * 8;
-        cp_async16(smem_u32(q_s + swz<DH>(row, ch)), src, ok ? 16 : 0);
-    }
-    auto load_tile = [&](int tile, int stage) {
-        const int base = kbeg + tile * kTile;
-        unsigned char *ks = k_s + stage * kTile * DH * 2;
-        unsigned char *vs = v_s + stage * kTile * DH * 2;
-        for (int i = tid; i < kTile * CPR; i += blockDim.x) {
-            const int row = i / CPR, ch = i - row * CPR;
-            const int key = base + row;
-            const bool ok = key < kend;
-            const size_t off = ((size_t)(ok ? key : kbeg) * H + h) * DH + ch * 8;
-            cp_async16(smem_u32(ks + swz<DH>(row, ch)), kc + off, ok ? 16 : 0);
-            cp_async16(smem_u32(vs + swz<DH>(row, ch)), vc + off, ok ? 16 : 0);
-        }
-    };
-    const int ntiles = (kend - kbeg + kTile - 1) / kTile;
-    load_tile(0, 0);
-    cp_async_commit();
-
-    // tree-split ancestor masks of every query row (rows >= R see nothing)
-    const int row0 = warp * 16 + g, row1 = row0 + 8;
-    if (tree_split) {
-        const int W = (R + 63) / 64;
-        for (int i = tid; i < QROWS * 4; i += blockDim.x) {
-            const int row = i >> 2, w = i & 3;
-            mask_s[i] = (row < R && w < W) ? a.anc_mask[((size_t)b * R + row) * W + w] : 0ull;
-        }
-    }
-
-    float o[DH / 8][4];
-#pragma unroll
-    for (int i = 0; i < DH / 8; ++i) o[i][0] = o[i][1] = o[i][2] = o[i][3] = 0.f;
-    float mrow[2] = {-INFINITY, -INFINITY}, lrow[2] = {0.f, 0.f};
-
-    for (int tile = 0; tile < ntiles; ++tile) {
-        if (tile + 1 < ntiles) {
-            load_tile(tile + 1, (tile + 1) & 1);
-            cp_async_commit();
-            cp_async_wait<1>();
-        } else {
-            cp_async_wait<0>();
-        }
-        __syncthreads();
-        const unsigned char *ks_ = k_s + (tile & 1) * kTile * DH * 2;
-        const unsigned char *vs_ = v_s + (tile & 1) * kTile * DH * 2;
-        const int tbase = kbeg + tile * kTile;
-#pragma unroll
-        for (int sub = 0; sub < kTile / kSub; ++sub) {
-            float s[kSub / 8][4];
-#pragma unroll
-            for (int nt = 0; nt < kSub / 8; ++nt) s[nt][0] = s[nt][1] = s[nt][2] = s[nt][3] = 0.f;
-#pragma unroll
-            for (int ks = 0; ks < DH / 16; ks += 2) {
-                const int i = lane >> 3, r8 = lane & 7;
-                uint32_t qa[2][4];
-#pragma unroll
-                for (int j = 0; j < 2; ++j) {
-                    const int row = warp * 16 + (i & 1) * 8 + r8;
-                    const int ch = (ks + j) * 2 + (i >> 1);
-                    ldsm_x4(smem_u32(q_s + swz<DH>(row, ch)), qa[j][0], qa[j][1], qa[j][2],
-                            qa[j][3]);
-                }
-#pragma unroll
-                for (int nt = 0; nt < kSub / 8; ++nt) {
-                    const int key = sub * kSub + nt * 8 + r8;
-                    const int ch = (ks + (i >> 1)) * 2 + (i & 1);
-                    uint32_t b0, b1, b2, b3;
-                    ldsm_x4(smem_u32(ks_ + swz<DH>(key, ch)), b0, b1, b2, b3);
-                    mma_bf16(s[nt], qa[0], b0, b1);
-                    mma_bf16(s[nt], qa[1], b2, b3);
-                }
-            }
-            // scale, mask, running max
-            float mx[2] = {-INFINITY, -INFINITY};
-#pragma unroll
-            for (int nt = 0; nt < kSub / 8; ++nt) {
-#pragma unroll
-                for (int e = 0; e < 4; ++e) {
-                    const int key = tbase + sub * kSub + nt * 8 + 2 * t4 + (e & 1);
-                    bool ok = key < kend;
-                    if (tree_split && ok) {
-                        const int tslot = key - P;
-                        const int row = (e < 2) ? row0 : row1;
-                        ok = (mask_s[row * 4 + (tslot >> 6)] >> (tslot & 63)) & 1u;
-                    }
-                    const float v = ok ? s[nt][e] * a.scale_log2 : -INFINITY;
-                    s[nt][e] = v;
-                    mx[e >> 1] = fmaxf(mx[e >> 1], v);
-                }
-            }
-            float corr[2], muse[2];
-#pragma unroll
-            for (int r = 0; r < 2; ++r) {
-                mx[r] = fmaxf(mx[r], __shfl_xor_sync(0xffffffffu, mx[r], 1));
-                mx[r] = fmaxf(mx[r], __shfl_xor_sync(0xffffffffu, mx[r], 2));
-                const float mn = fmaxf(mrow[r], mx[r]);
-                muse[r] = (mn == -INFINITY) ? 0.f : mn;
-                corr[r] = exp2f(mrow[r] - muse[r]);
-                mrow[r] = mn;
-                lrow[r] *= corr[r];
-            }
-#pragma unroll
-            for (int nt = 0; nt < kSub / 8; ++nt) {
-#pragma unroll
-                for (int e = 0; e < 4; ++e) {
-                    const float p = exp2f(s[nt][e] - muse[e >> 1]);
-                    s[nt][e] = p;
-                    lrow[e >> 1] += p;
-                }
-            }
-#pragma unroll
-            for (int dn = 0; dn < DH / 8; ++dn) {
-                o[dn][0] *= corr[0];
-                o[dn][1] *= corr[0];
-                o[dn][2] *= corr[1];
-                o[dn][3] *= corr[1];
-            }
-            // O += P V
-#pragma unroll
-            for (int kk = 0; kk < kSub / 16; ++kk) {
-                uint32_t pa[4];
-                pa[0] = pack_bf16(s[2 * kk][0], s[2 * kk][1]);
-                pa[1] = pack_bf16(s[2 * kk][2], s[2 * kk][3]);
-                pa[2] = pack_bf16(s[2 * kk + 1][0], s[2 * kk + 1][1]);
-                pa[3] = pack_bf16(s[2 * kk + 1][2], s[2 * kk + 1][3]);
-#pragma unroll
-                for (int dn = 0; dn < DH / 16; ++dn) {
-                    const int i = lane >> 3, r8 = lane & 7;
-                    const int key = sub * kSub + kk * 16 + (i & 1) * 8 + r8;
-                    const int ch = dn * 2 + (i >> 1);
-                    uint32_t b0, b1, b2, b3;
-                    ldsm_x4_t(smem_u32(vs_ + swz<DH>(key, ch)), b0, b1, b2, b3);
-                    mma_bf16(o[2 * dn], pa, b0, b1);
-                    mma_bf16(o[2 * dn + 1], pa, b2, b3);
-                }
-            }
-        }
-        __syncthreads();
-    }
-
-    // finish the row sums across the quad and write the partials
-#pragma unroll
-    for (int r = 0; r < 2; ++r) {
-        lrow[r] += __shfl_xor_sync(0xffffffffu, lrow[r], 1);
-        lrow[r] += __shfl_xor_sync(0xffffffffu, lrow[r], 2);
-    }
-#pragma unroll
-    for (int r = 0; r < 2; ++r) {
-        const int row = r == 0 ? row0 : row1;
-        if (row < R) {
-            float *dst = a.part_o + (pbase + row) * DH;
-#pragma unroll
-            for (int dn = 0; dn < DH / 8; ++dn)
-                *reinterpret_cast<float2 *>(dst + dn * 8 + 2 * t4) =
-                    make_float2(o[dn][2 * r], o[dn][2 * r + 1]);
-            if (t4 == 0) a.part_ml[pbase + row] = make_float2(mrow[r], lrow[r]);
-        }
-    }
-}
-
 // ------------------------------------------------------- tensor-core path ---
 //
-// tree_attn_tc_kernel: one CTA per (key range, head, sequence).  The keys of
+// tree_attn_tc_kernel: one CTA per (key range, head, 128-row tile of the
+// tree, sequence); trees of more than 128 rows take two tiles.  The keys of
 // a sequence are its cache slots 0 .. P+R-1, prefix and tree alike (they are
 // contiguous); a key range is `cps` consecutive sub-chunks of 64 keys.  K and
 // V of the sub-chunks stream through a three-stage cp.async ring in shared
@@ -318,7 +77,8 @@ __global__ void __launch_bounds__(MAXW * 32, 1) tree_attn_split_kernel(AttnArgs 
 //     columns [0, 64)        S = Q K_j^T (fp32), then P over it (bf16 pairs)
 //     columns [64, 64+DH/2)  Q (bf16 pairs, one query row per lane)
 //     columns [128, 128+DH)  O += P V_j (fp32)
-// 256 threads: threads t and t+128 own query row t (rows >= R are zero), each
+// 256 threads: threads t and t+128 own query row 128*tile + t (rows >= R are
+// zero), each
 // taking half of a sub-chunk's keys and half of the output columns; one
 // thread issues the MMAs (A from tensor memory, B from shared memory).  Every
 // thread reads its S half-row, masks it (slots past the range; tree slots
@@ -367,7 +127,8 @@ __device__ __forceinline__ void tc_load_stage(unsigned char *k_s, unsigned char 
     cp_async_commit();
 }
 
-template <int DH>
+// WIDE: trees of more than 128 rows (row tiles, four mask words per row)
+template <int DH, bool WIDE>
 __global__ void __launch_bounds__(256, 2) tree_attn_tc_kernel(AttnArgs a) {
     pdl_enter();
     using L = TcSmem<DH>;
@@ -379,13 +140,18 @@ __global__ void __launch_bounds__(256, 2) tree_attn_tc_kernel(AttnArgs a) {
     uint32_t &tmem_holder = *reinterpret_cast<uint32_t *>(tc_raw + L::BAR_OFF + 16);
     int &failed = *reinterpret_cast<int *>(tc_raw + L::BAR_OFF + 20);
 
-    // heads vary fastest in the grid, so CTAs resident together read whole
-    // token rows ([H, dh] per slot) of the same key range
-    const int h = blockIdx.x, split = blockIdx.y, b = blockIdx.z;
+    // heads (and the row tiles of a head) vary fastest in the grid, so CTAs
+    // resident together read whole token rows ([H, dh] per slot) of the same
+    // key range; row tile rt of head h holds tree rows [128*rt, 128*rt + 128)
+    const int h = WIDE ? blockIdx.x / a.row_tiles : blockIdx.x;
+    const int rt = WIDE ? blockIdx.x - h * a.row_tiles : 0;
+    const int split = blockIdx.y, b = blockIdx.z;
     const int R = a.R, H = a.H;
     const int tid = threadIdx.x, warp = tid >> 5;
-    // warp w reads TMEM lanes 32*(w%4)..: row = tid % 128; half = column half
-    const int row = tid & 127, half = tid >> 7;
+    // warp w reads TMEM lanes 32*(w%4)..: lane = tid % 128 holds tree row
+    // row0 + lane; half = column half
+    const int lrow = tid & 127, half = tid >> 7;
+    const int row0 = rt * 128, row = row0 + lrow;
     int P = a.prefix_len[b];
     if (P < 0 || P > a.P_max) {
         set_status(a.status, MEDUSA_DEV_BAD_PREFIX);
@@ -400,7 +166,7 @@ __global__ void __launch_bounds__(256, 2) tree_attn_tc_kernel(AttnArgs a) {
     const bool bad_cache = cache_pointers_bad(kc, vc);
     if (bad_cache) set_status(a.status, MEDUSA_DEV_BAD_CACHE);
     if (kend <= kbeg || bad_cache) {
-        for (int r = tid; r < R; r += blockDim.x) a.part_ml[pbase + r] = make_float2(-INFINITY, 0.f);
+        if (row < R && half == 0) a.part_ml[pbase + row] = make_float2(-INFINITY, 0.f);
         return;
     }
     const int nsub = (kend - kbeg + kTcSub - 1) / kTcSub;
@@ -431,13 +197,15 @@ __global__ void __launch_bounds__(256, 2) tree_attn_tc_kernel(AttnArgs a) {
     // ---- the first two sub-chunks start loading
     tc_load_stage<DH>(stage_k(0), stage_v(0), kc, vc, kbeg, kend, H, h, tid);
     if (nsub > 1) tc_load_stage<DH>(stage_k(1), stage_v(1), kc, vc, kbeg + kTcSub, kend, H, h, tid);
-    // this row's ancestor-mask words (this path serves R <= 128: two words)
-    uint64_t am0 = 0, am1 = 0;
+    // this row's ancestor-mask words (R <= 256: up to four)
+    uint64_t am0 = 0, am1 = 0, am2 = 0, am3 = 0;
     if (kend > P && row < R) {
         const int W = (R + 63) / 64;
         const uint64_t *mr = a.anc_mask + ((size_t)b * R + row) * W;
         am0 = mr[0];
         if (W > 1) am1 = mr[1];
+        if (WIDE && W > 2) am2 = mr[2];
+        if (WIDE && W > 3) am3 = mr[3];
     }
     if (tid == 0) {
         tc::mbar_init(&bar_s, 1);
@@ -460,7 +228,7 @@ __global__ void __launch_bounds__(256, 2) tree_attn_tc_kernel(AttnArgs a) {
     // warps whose 32 rows are all padding (>= R) skip the softmax: their S
     // rows are zero (zero Q rows), which read as zero P, and their O rows are
     // never written out
-    const bool rows_live = (warp & 3) * 32 < R;  // warp-uniform
+    const bool rows_live = row0 + (warp & 3) * 32 < R;  // warp-uniform
 
     float m_run = -INFINITY;  // row reference (log2 units), same in both threads of a row
     float l_run = 0.f;        // this thread's share of the row sum
@@ -528,7 +296,9 @@ __global__ void __launch_bounds__(256, 2) tree_attn_tc_kernel(AttnArgs a) {
                 bool vis = key < kend;
                 if (vis && key >= P) {
                     const int t = key - P;
-                    vis = (((t < 64) ? am0 : am1) >> (t & 63)) & 1u;
+                    const uint64_t w = WIDE && t >= 128 ? (t < 192 ? am2 : am3)
+                                                        : (t < 64 ? am0 : am1);
+                    vis = (w >> (t & 63)) & 1u;
                 }
                 x[e] = vis ? x[e] * a.scale_log2 : -INFINITY;
                 mx[e & 3] = fmaxf(mx[e & 3], x[e]);
@@ -537,9 +307,9 @@ __global__ void __launch_bounds__(256, 2) tree_attn_tc_kernel(AttnArgs a) {
         // row max of the sub-chunk: halves exchange through the dead K_j tile
         // (it is refilled only after the barrier that ends this iteration)
         float *xch = reinterpret_cast<float *>(k_s);
-        xch[half * 128 + row] = fmaxf(fmaxf(mx[0], mx[1]), fmaxf(mx[2], mx[3]));
+        xch[half * 128 + lrow] = fmaxf(fmaxf(mx[0], mx[1]), fmaxf(mx[2], mx[3]));
         __syncthreads();
-        const float cm = fmaxf(xch[row], xch[128 + row]);
+        const float cm = fmaxf(xch[lrow], xch[128 + lrow]);
         const bool raise = cm > m_run + kRescaleLog2;
         const float m_new = raise ? cm : m_run;
         const float alpha = raise ? exp2f(m_run - m_new) : 1.f;  // 0 when m_run = -inf
@@ -620,10 +390,10 @@ __global__ void __launch_bounds__(256, 2) tree_attn_tc_kernel(AttnArgs a) {
     }
     // row sums: halves exchange through stage 0 (no copy is in flight now)
     float *xs = reinterpret_cast<float *>(tc_raw);
-    xs[half * 128 + row] = l_run;
+    xs[half * 128 + lrow] = l_run;
     __syncthreads();
     if (half == 0 && row < R) {
-        const float l = xs[row] + xs[128 + row];
+        const float l = xs[lrow] + xs[128 + lrow];
         a.part_ml[pbase + row] = ok ? make_float2(m_run, l) : make_float2(-INFINITY, 0.f);
     }
     tc::fence_before_sync();
@@ -761,31 +531,22 @@ tree_attn_f32_kernel(const float *__restrict__ q, const float *const *kcs, const
 
 // ---------------------------------------------------------------- host ---
 
-void split_plan(int B, int H, int P_max, int *nps, int *chunk) {
-    const int per_head = std::max(1, (kTargetCtas + B * H - 1) / (B * H));
-    int n = std::max(1, per_head - 1);
-    const int max_n = std::max(1, (P_max + kTile - 1) / kTile);
-    n = std::min(n, max_n);
-    int c = (P_max + n - 1) / n;
-    c = std::max(kTile, (c + kTile - 1) / kTile * kTile);
-    *chunk = c;
-    *nps = std::max(1, (P_max + c - 1) / c);
-}
-
 size_t align256(size_t x) { return (x + 255) & ~size_t(255); }
 
 // Key ranges of the tensor-core path: at least two 64-key sub-chunks per CTA
 // (so that loads overlap compute), and one (B = 1) or two (B > 1) waves of
 // two CTAs per SM over the whole grid at P_max.
 struct TcPlan {
-    int ns, chunk;
+    int ns, chunk, row_tiles;
 };
 
 TcPlan tc_plan(int B, int H, int R, int P_max) {
     TcPlan p;
+    p.row_tiles = (R + 127) / 128;
     const int nsub = (P_max + R + kTcSub - 1) / kTcSub;
     const int waves = B == 1 ? 1 : 2;
-    const int per_head = std::max(1, 2 * waves * device_sm_count() / std::max(1, B * H));
+    const int per_head =
+        std::max(1, 2 * waves * device_sm_count() / std::max(1, B * H * p.row_tiles));
     const int cps = std::max(2, (nsub + per_head - 1) / per_head);
     p.ns = (nsub + cps - 1) / cps;
     p.chunk = cps * kTcSub;
@@ -796,16 +557,8 @@ TcPlan tc_plan(int B, int H, int R, int P_max) {
 
 size_t attention_workspace_bytes(medusa_dtype dtype, int B, int R, int H, int dh, int P_max) {
     if (dtype == MEDUSA_F32) return MEDUSA_WS_HEADER;
-    int nps, chunk;
-    if (R <= 128) {
-        const TcPlan tp = tc_plan(B, H, R, P_max);
-        nps = tp.ns;
-        chunk = tp.chunk;
-    } else {
-        split_plan(B, H, P_max, &nps, &chunk);
-    }
-    const int NS = R <= 128 ? nps : nps + 1;
-    const size_t rows = (size_t)B * H * NS * R;
+    const TcPlan tp = tc_plan(B, H, R, P_max);
+    const size_t rows = (size_t)B * H * tp.ns * R;
     return MEDUSA_WS_HEADER + align256(rows * dh * sizeof(float)) + align256(rows * sizeof(float2));
 }
 
@@ -828,16 +581,8 @@ cudaError_t launch_tree_attention(medusa_dtype dtype, const void *q, const void 
         note_launch();
         return e;
     }
-    const bool use_tc = R <= 128;
-    int nps, chunk;
-    if (use_tc) {
-        const TcPlan tp = tc_plan(B, H, R, P_max);  // key ranges per head
-        nps = tp.ns;
-        chunk = tp.chunk;
-    } else {
-        split_plan(B, H, P_max, &nps, &chunk);
-    }
-    const int NS = use_tc ? nps : nps + 1;
+    const TcPlan tp = tc_plan(B, H, R, P_max);
+    const int NS = tp.ns;
     const size_t rows = (size_t)B * H * NS * R;
     char *w = static_cast<char *>(ws) + MEDUSA_WS_HEADER;
     float *part_o = reinterpret_cast<float *>(w);
@@ -852,36 +597,22 @@ cudaError_t launch_tree_attention(medusa_dtype dtype, const void *q, const void 
     a.R = R;
     a.H = H;
     a.P_max = P_max;
-    a.chunk = chunk;
-    a.nps = nps;
+    a.chunk = tp.chunk;
+    a.nps = NS;
+    a.row_tiles = tp.row_tiles;
     a.scale_log2 = scale * kLog2e;
     a.part_o = part_o;
     a.part_ml = part_ml;
     a.status = status;
-    if (use_tc) {
-        auto kern = dh == 128 ? tree_attn_tc_kernel<128> : tree_attn_tc_kernel<64>;
-        const int smem = dh == 128 ? TcSmem<128>::TOTAL : TcSmem<64>::TOTAL;
-        if ((e = cudaFuncSetAttribute(kern, cudaFuncAttributeMaxDynamicSharedMemorySize, smem)))
-            return e;
-        e = launch_pdl(kern, dim3(H, NS, B), dim3(256), (size_t)smem, stream, a);
-        note_launch();
-        if (e) return e;
-    } else {
-        const int NW = (R + 15) / 16;
-        const int threads = NW * 32;
-        const size_t smem = (size_t)(NW * 16 + 4 * kTile) * dh * 2 + (size_t)NW * 16 * 4 * sizeof(uint64_t);
-        dim3 grid(NS, H, B);
-        auto kern = tree_attn_split_kernel<128, 8>;
-        if (dh == 128)
-            kern = NW <= 8 ? tree_attn_split_kernel<128, 8> : tree_attn_split_kernel<128, 16>;
-        else
-            kern = NW <= 8 ? tree_attn_split_kernel<64, 8> : tree_attn_split_kernel<64, 16>;
-        if ((e = cudaFuncSetAttribute(kern, cudaFuncAttributeMaxDynamicSharedMemorySize, (int)smem)))
-            return e;
-        e = launch_pdl(kern, grid, dim3(threads), smem, stream, a);
-        note_launch();
-        if (e) return e;
-    }
+    const bool wide = tp.row_tiles > 1;
+    auto kern = wide ? tree_attn_tc_kernel<64, true> : tree_attn_tc_kernel<64, false>;
+    if (dh == 128) kern = wide ? tree_attn_tc_kernel<128, true> : tree_attn_tc_kernel<128, false>;
+    const int smem = dh == 128 ? TcSmem<128>::TOTAL : TcSmem<64>::TOTAL;
+    if ((e = cudaFuncSetAttribute(kern, cudaFuncAttributeMaxDynamicSharedMemorySize, smem)))
+        return e;
+    e = launch_pdl(kern, dim3(H * tp.row_tiles, NS, B), dim3(256), (size_t)smem, stream, a);
+    note_launch();
+    if (e) return e;
     const long long items = (long long)B * R * H;
     const int cblocks = (int)((items + 7) / 8);
     e = launch_pdl(dh == 128 ? tree_attn_combine_kernel<128> : tree_attn_combine_kernel<64>,
