@@ -79,33 +79,43 @@ posterior_rows_kernel(const T *__restrict__ logits, int R, int V, int splits, fl
     const int nvec = V / VN;
     const int v_lo = (int)(((long long)sp * nvec) / splits);
     const int v_hi = (int)(((long long)(sp + 1) * nvec) / splits);
-    float bv = -INFINITY;
-    int bi = INT_MAX;
+    // argmax by 16-byte group: the running best group (its max, index and
+    // raw words) moves only on a strictly larger group max, so the earliest
+    // group holding the thread's max wins; its first element equal to that
+    // max is the smallest id (a group of all -inf or NaN still enters first)
+    float gbest = -INFINITY;
+    int gidx = -1;
+    uint4 graw = make_uint4(0u, 0u, 0u, 0u);
     Moments mo{-INFINITY, 0.f, 0.f};
-    for (int base = v_lo + threadIdx.x; base < v_hi; base += kRowThreads * U) {
-        uint4 v[U];
+    // two register buffers: the next batch's loads are in flight while this
+    // batch is reduced
+    uint4 cur[U], nxt[U];
+    int base = v_lo + threadIdx.x;
+#pragma unroll
+    for (int u = 0; u < U; ++u) {
+        const int idx = base + u * kRowThreads;
+        if (idx < v_hi) cur[u] = ld_stream16(x + idx);
+    }
+    for (; base < v_hi; base += kRowThreads * U) {
+        const int nb = base + kRowThreads * U;
 #pragma unroll
         for (int u = 0; u < U; ++u) {
-            const int idx = base + u * kRowThreads;
-            if (idx < v_hi) v[u] = ld_stream16(x + idx);
+            const int idx = nb + u * kRowThreads;
+            if (idx < v_hi) nxt[u] = ld_stream16(x + idx);
         }
 #pragma unroll
         for (int u = 0; u < U; ++u) {
             const int idx = base + u * kRowThreads;
             if (idx < v_hi) {
                 float f[VN];
-                Vec16<T>::widen(v[u], f);
+                Vec16<T>::widen(cur[u], f);
                 float vm = f[0];
-                // ids rise within a thread, so a strict > keeps the smallest
-                // id among equal values (the first element always enters, so a
-                // row of -inf still yields its first id)
 #pragma unroll
-                for (int e = 0; e < VN; ++e) {
-                    if (f[e] > bv || bi == INT_MAX) {
-                        bv = f[e];
-                        bi = idx * VN + e;
-                    }
-                    vm = fmaxf(vm, f[e]);
+                for (int e = 1; e < VN; ++e) vm = fmaxf(vm, f[e]);
+                if (vm > gbest || gidx < 0) {
+                    gbest = vm;
+                    gidx = idx;
+                    graw = cur[u];
                 }
                 if (TYPICAL) {
                     const float m_new = fmaxf(mo.m, vm * y_scale);
@@ -127,6 +137,20 @@ posterior_rows_kernel(const T *__restrict__ logits, int R, int V, int splits, fl
                 }
             }
         }
+#pragma unroll
+        for (int u = 0; u < U; ++u) cur[u] = nxt[u];
+    }
+    float bv = -INFINITY;
+    int bi = INT_MAX;
+    if (gidx >= 0) {
+        float f[VN];
+        Vec16<T>::widen(graw, f);
+        int e0 = 0;  // no element equals a NaN group max: its first element
+#pragma unroll
+        for (int e = VN - 1; e >= 0; --e)
+            if (f[e] == gbest) e0 = e;
+        bv = f[e0];
+        bi = gidx * VN + e0;
     }
     // warp reductions
     const int lane = threadIdx.x & 31, warp = threadIdx.x >> 5;
