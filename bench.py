@@ -180,7 +180,7 @@ def scan_sizes(m, dev, T, timed_loop) -> dict:
     latency, set the time.  Trees come from seeded random top-s tables."""
     import torch
     out = {"attention": [], "posterior": []}
-    for cfg in (synth.batch8(), synth.sweep(64, 8192)):
+    for cfg in (synth.batch8(), synth.sweep(64, 8192), synth.sweep(128, 8192)):
         rng = np.random.default_rng(cfg.seed)
         B, K, S = cfg.B, cfg.K, cfg.top_s
         ids = np.stack([np.stack([rng.choice(cfg.V, size=S, replace=False) for _ in range(K)])
@@ -210,10 +210,15 @@ def scan_sizes(m, dev, T, timed_loop) -> dict:
             m.tree_attention(q, kp, vp, prefix, cfg.P_max, tree.anc_mask, out=o, ws=ws)
 
         us = timed_loop(attn)
+        # algorithmic MMA work: q.k and p.v over every prefix slot and over
+        # the ancestors-or-self of each node
+        depth = tree.depth.cpu().numpy()
+        flops = 4.0 * cfg.H * cfg.dh * (cfg.R * sum(cfg.prefix) + float((depth + 1).sum()))
         out["attention"].append({"config": cfg.name, "B": B, "prefix": list(cfg.prefix),
                                  "tree_rows": cfg.R, "us": round(us, 2),
                                  "bytes": int(nb["attention"]),
-                                 "GB/s": round(nb["attention"] / (us * 1e-6) / 1e9, 1)})
+                                 "GB/s": round(nb["attention"] / (us * 1e-6) / 1e9, 1),
+                                 "TFLOP/s": round(flops / (us * 1e-6) / 1e12, 1)})
         if B > 1:
             lcopies = max(2, int(np.ceil(2 * L2_BYTES / nb["posterior"])))
             lg0 = T(synth.cast(synth.base_logits(cfg), "bf16"))
@@ -664,6 +669,7 @@ def run_ours(args, cfg):
     cpu_value = nb["total"] / float(np.mean(cpu_secs)) / 1e9
 
     stages = {k: {"us": round(float(np.mean(v)) * 1e3, 2),
+                  "us_median": round(float(np.median(v)) * 1e3, 2),
                   "GB/s": round(nb[k] / (float(np.mean(v)) * 1e-3) / 1e9, 1),
                   "frac_hbm": round(nb[k] / (float(np.mean(v)) * 1e-3) / 1e9 / peaks["hbm_gbs"], 4)}
               for k, v in per_call.items()}
