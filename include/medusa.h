@@ -117,6 +117,18 @@ MEDUSA_API const char *medusa_last_error(void);
 /* Number of kernels this library has launched in this process. */
 MEDUSA_API uint64_t medusa_launch_count(void);
 
+/* Fault injection for the bounded device waits.  The tensor-core attention
+ * waits on mbarriers for its own MMAs; each wait gives up after `polls`
+ * polls (each poll blocks for a hardware-defined interval), sets
+ * MEDUSA_DEV_TIMEOUT, stops the key loop, drains its MMAs and copies with a
+ * fixed limit, frees its tensor memory and publishes an empty key range, so
+ * the context stays usable.  Default 65536 polls; the environment variable
+ * MEDUSA_FAULT_WAIT_BUDGET sets the value the library starts with.  A budget
+ * of 0 makes every such wait fail at once: it exercises the timeout path
+ * without a hung GPU.  Process-wide; affects launches made after the call. */
+MEDUSA_API uint32_t medusa_wait_budget(void);
+MEDUSA_API void medusa_set_wait_budget(uint32_t polls);
+
 /* Copy the workspace status word to *status_host.  Synchronises `stream`. */
 MEDUSA_API medusa_status medusa_read_device_status(const void *ws, int32_t *status_host,
                                         medusa_stream stream);

@@ -39,6 +39,7 @@ DEVICE_STATUS = {0: "ok", 1: "bad token", 2: "bad parent", 3: "bad prefix", 4: "
                  5: "bad depth", 6: "timeout", 7: "bad path", 8: "bad cache"}
 
 EXPORTS = ("medusa_status_string", "medusa_last_error", "medusa_launch_count",
+           "medusa_wait_budget", "medusa_set_wait_budget",
            "medusa_read_device_status", "medusa_clear_device_status",
            "medusa_heads_workspace_size", "medusa_heads",
            "medusa_heads_lm_workspace_size", "medusa_heads_lm",
@@ -74,6 +75,8 @@ def lib() -> ctypes.CDLL:
         "medusa_status_string": ([I], ctypes.c_char_p),
         "medusa_last_error": ([], ctypes.c_char_p),
         "medusa_launch_count": ([], ctypes.c_uint64),
+        "medusa_wait_budget": ([], ctypes.c_uint32),
+        "medusa_set_wait_budget": ([ctypes.c_uint32], None),
         "medusa_read_device_status": ([P, P, P], I),
         "medusa_clear_device_status": ([P, P], I),
         "medusa_heads_workspace_size": ([I, I, I, I, I], S),
@@ -135,6 +138,16 @@ def _need(t: torch.Tensor, name: str):
 
 def launch_count() -> int:
     return int(lib().medusa_launch_count())
+
+
+def wait_budget() -> int:
+    """Poll limit of the bounded device waits (fault injection: 0 makes
+    them time out at once and set the "timeout" device status)."""
+    return int(lib().medusa_wait_budget())
+
+
+def set_wait_budget(polls: int) -> None:
+    lib().medusa_set_wait_budget(int(polls))
 
 
 def new_workspace(nbytes: int, device=None) -> torch.Tensor:

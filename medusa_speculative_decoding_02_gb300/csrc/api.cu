@@ -6,8 +6,11 @@
 #include <atomic>
 #include <cstdarg>
 #include <cstdio>
+#include <cstdlib>
 #include <cstring>
 #include <mutex>
+
+#include <nvtx3/nvToolsExt.h>
 
 #include "launch.h"
 
@@ -42,6 +45,32 @@ medusa_status check_ws(const void *ws, size_t have, size_t need, const char *who
 }
 
 }  // namespace
+
+namespace {
+
+// Poll limit of the bounded device waits; MEDUSA_FAULT_WAIT_BUDGET sets the
+// first value (fault injection), medusa_set_wait_budget any later one.
+constexpr uint32_t kDefaultWaitPolls = 1u << 16;
+std::atomic<uint32_t> g_wait_polls{kDefaultWaitPolls};
+std::once_flag g_wait_env_once;
+
+void read_wait_env() {
+    const char *v = std::getenv("MEDUSA_FAULT_WAIT_BUDGET");
+    if (!v || !*v) return;
+    char *end = nullptr;
+    const unsigned long n = std::strtoul(v, &end, 10);
+    if (end && *end == '\0' && n <= 0xffffffffUL) g_wait_polls.store((uint32_t)n);
+}
+
+}  // namespace
+
+uint32_t wait_budget() {
+    std::call_once(g_wait_env_once, read_wait_env);
+    return g_wait_polls.load(std::memory_order_relaxed);
+}
+
+NvtxRange::NvtxRange(const char *name) { nvtxRangePushA(name); }
+NvtxRange::~NvtxRange() { nvtxRangePop(); }
 
 int device_sm_count() {
     static std::mutex mu;
@@ -89,6 +118,13 @@ const char *medusa_status_string(medusa_status s) {
 const char *medusa_last_error(void) { return g_err; }
 
 uint64_t medusa_launch_count(void) { return g_launches.load(std::memory_order_relaxed); }
+
+uint32_t medusa_wait_budget(void) { return wait_budget(); }
+
+void medusa_set_wait_budget(uint32_t polls) {
+    std::call_once(g_wait_env_once, read_wait_env);
+    g_wait_polls.store(polls, std::memory_order_relaxed);
+}
 
 medusa_status medusa_read_device_status(const void *ws, int32_t *status_host, medusa_stream stream) {
     if (!ws || !status_host) return fail(MEDUSA_ERR_INVALID_ARG, "read_device_status: NULL pointer");
@@ -155,6 +191,7 @@ medusa_status medusa_heads(medusa_dtype dtype, const void *h, const void *W1, co
                            const void *W2, int B, int d, int V, int K, int top_s,
                            int32_t *topk_ids, float *topk_logp, void *ws, size_t ws_bytes,
                            medusa_stream stream) {
+    const NvtxRange range("medusa_heads");
     const char *who = "medusa_heads";
     if (medusa_status s = check_heads(who, dtype, h, W1, b1, W2, B, d, V, K, top_s, topk_ids,
                                       topk_logp))
@@ -172,6 +209,7 @@ medusa_status medusa_heads_lm(medusa_dtype dtype, const void *h, const void *W_l
                               const void *b1, const void *W2, int B, int d, int V, int K,
                               int top_s, int32_t *root, float *root_logp, int32_t *topk_ids,
                               float *topk_logp, void *ws, size_t ws_bytes, medusa_stream stream) {
+    const NvtxRange range("medusa_heads_lm");
     const char *who = "medusa_heads_lm";
     if (medusa_status s = check_heads(who, dtype, h, W1, b1, W2, B, d, V, K, top_s, topk_ids,
                                       topk_logp))
@@ -195,6 +233,7 @@ medusa_status medusa_heads_sample(medusa_dtype dtype, const void *h, const void 
                                   float temperature, uint64_t seed, uint64_t step,
                                   int32_t *drafts, float *draft_logits, void *ws,
                                   size_t ws_bytes, medusa_stream stream) {
+    const NvtxRange range("medusa_heads_sample");
     const char *who = "medusa_heads_sample";
     // drafts is the top-1 list of the perturbed keys; no log-probabilities
     if (medusa_status s =
@@ -268,6 +307,7 @@ medusa_status medusa_build_tree(const int32_t *root, const int32_t *topk_ids,
                                 int32_t *parent, int32_t *depth, int32_t *pos_id,
                                 uint64_t *anc_mask, int32_t *paths, int32_t *n_leaf, void *ws,
                                 size_t ws_bytes, medusa_stream stream) {
+    const NvtxRange range("medusa_build_tree");
     const char *who = "medusa_build_tree";
     if (medusa_status s = check_tree(who, root, topk_ids, topk_logp, B, K, s_host, top_s, n,
                                      tokens, parent, depth, pos_id, anc_mask, paths, n_leaf, ws,
@@ -287,6 +327,7 @@ medusa_status medusa_build_tree_static(const int32_t *root, const int32_t *topk_
                                        int32_t *pos_id, uint64_t *anc_mask, int32_t *paths,
                                        int32_t *n_leaf, void *ws, size_t ws_bytes,
                                        medusa_stream stream) {
+    const NvtxRange range("medusa_build_tree_static");
     const char *who = "medusa_build_tree_static";
     if (medusa_status s = check_tree(who, root, topk_ids, log_a, B, K, s_host, top_s, n, tokens,
                                      parent, depth, pos_id, anc_mask, paths, n_leaf, ws,
@@ -312,6 +353,7 @@ medusa_status medusa_tree_attention(medusa_dtype dtype, const void *q, const voi
                                     int P_max, const uint64_t *anc_mask, int B, int R, int H,
                                     int dh, float scale, void *out, void *ws, size_t ws_bytes,
                                     medusa_stream stream) {
+    const NvtxRange range("medusa_tree_attention");
     const char *who = "medusa_tree_attention";
     if (dtype != MEDUSA_F32 && dtype != MEDUSA_BF16)
         return fail(MEDUSA_ERR_INVALID_ARG, "%s: unknown dtype %d", who, (int)dtype);
@@ -410,6 +452,7 @@ medusa_status medusa_evaluate_posterior(medusa_dtype dtype, const void *logits,
                                         int32_t *path_tokens, int32_t *next_token,
                                         int32_t *accept, void *ws, size_t ws_bytes,
                                         medusa_stream stream) {
+    const NvtxRange range("medusa_evaluate_posterior");
     const char *who = "medusa_evaluate_posterior";
     if (medusa_status s = check_posterior(who, dtype, logits, tokens, parent, depth, B, R, V, K,
                                           mode, eps, delta, temperature, accept_len, path,
@@ -430,6 +473,7 @@ medusa_status medusa_evaluate_posterior_commit(
     int32_t *next_token, int32_t *accept, void *const *k_cache, void *const *v_cache,
     const int32_t *prefix_len, int H, int dh, int32_t *new_prefix_len, void *ws,
     size_t ws_bytes, medusa_stream stream) {
+    const NvtxRange range("medusa_evaluate_posterior_commit");
     const char *who = "medusa_evaluate_posterior_commit";
     if (medusa_status s = check_posterior(who, dtype, logits, tokens, parent, depth, B, R, V, K,
                                           mode, eps, delta, temperature, accept_len, path,
@@ -460,6 +504,7 @@ medusa_status medusa_speculative_posterior(medusa_dtype dtype, const void *logit
                                            int32_t *path_tokens, int32_t *next_token,
                                            int32_t *accept, void *ws, size_t ws_bytes,
                                            medusa_stream stream) {
+    const NvtxRange range("medusa_speculative_posterior");
     const char *who = "medusa_speculative_posterior";
     if (dtype != MEDUSA_F32 && dtype != MEDUSA_BF16)
         return fail(MEDUSA_ERR_INVALID_ARG, "%s: unknown dtype %d", who, (int)dtype);
@@ -487,6 +532,7 @@ medusa_status medusa_commit_kv(medusa_dtype dtype, void *const *k_cache, void *c
                                const int32_t *accept_len, int B, int K, int R, int H, int dh,
                                int32_t *new_prefix_len, void *ws, size_t ws_bytes,
                                medusa_stream stream) {
+    const NvtxRange range("medusa_commit_kv");
     const char *who = "medusa_commit_kv";
     if (medusa_status s = check_commit(who, dtype, k_cache, v_cache, prefix_len, new_prefix_len,
                                        H, dh))

@@ -60,6 +60,7 @@ struct AttnArgs {
     int chunk, nps;
     int row_tiles;  // 128-row tiles of the R tree rows
     float scale_log2;
+    uint32_t wait_polls;  // poll limit of the key loop's mbarrier waits
     float *part_o;
     float2 *part_ml;
     int *status;
@@ -93,7 +94,7 @@ struct AttnArgs {
 constexpr int kTcSub = 64;               // keys per pipeline stage
 constexpr int kTcStages = 3;
 constexpr float kRescaleLog2 = 8.f;      // lazy-rescale threshold (log2 units)
-constexpr uint32_t kWaitPolls = 1u << 16;
+constexpr uint32_t kWaitPolls = 1u << 16;  // the drain's limit (the key loop's: a.wait_polls)
 
 template <int DH>
 struct TcSmem {
@@ -239,7 +240,7 @@ __global__ void __launch_bounds__(256, 2) tree_attn_tc_kernel(AttnArgs a) {
         const int k0 = kbeg + j * kTcSub;
         // P V of sub-chunk j-1 done: its stage may be refilled (with j+2) and O
         // may be rescaled
-        if (j > 0 && !tc::mbar_wait_bounded(&bar_o, (j - 1) & 1, kWaitPolls)) failed = 1;
+        if (j > 0 && !tc::mbar_wait_bounded(&bar_o, (j - 1) & 1, a.wait_polls)) failed = 1;
         if (j + 2 < nsub)
             tc_load_stage<DH>(stage_k(j + 2), stage_v(j + 2), kc, vc, k0 + 2 * kTcSub, kend, H, h,
                               tid);
@@ -269,7 +270,7 @@ __global__ void __launch_bounds__(256, 2) tree_attn_tc_kernel(AttnArgs a) {
             tc::mma_commit(&bar_s);
         }
         __syncwarp();
-        if (!tc::mbar_wait_bounded(&bar_s, j & 1, kWaitPolls)) failed = 1;
+        if (!tc::mbar_wait_bounded(&bar_s, j & 1, a.wait_polls)) failed = 1;
         tc::fence_after_sync();
 
         // ---- this thread's 32 keys of the sub-chunk
@@ -601,6 +602,7 @@ cudaError_t launch_tree_attention(medusa_dtype dtype, const void *q, const void 
     a.nps = NS;
     a.row_tiles = tp.row_tiles;
     a.scale_log2 = scale * kLog2e;
+    a.wait_polls = wait_budget();
     a.part_o = part_o;
     a.part_ml = part_ml;
     a.status = status;

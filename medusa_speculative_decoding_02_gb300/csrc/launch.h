@@ -30,6 +30,20 @@ cudaError_t launch_pdl(void (*kernel)(KArgs...), dim3 grid, dim3 block, size_t s
     return cudaLaunchKernelEx(&cfg, kernel, static_cast<KArgs>(args)...);
 }
 
+// NVTX range around one public call (visible in Nsight timelines; free
+// when no tool is attached)
+struct NvtxRange {
+    explicit NvtxRange(const char *name);
+    ~NvtxRange();
+    NvtxRange(const NvtxRange &) = delete;
+    NvtxRange &operator=(const NvtxRange &) = delete;
+};
+
+// poll limit of the bounded device waits inside the main loops (see
+// medusa_set_wait_budget); the drain before a kernel frees its resources
+// keeps its own fixed limit
+uint32_t wait_budget();
+
 int device_sm_count();   // SMs of the current device (cached per device)
 void note_launch();      // count one kernel launch
 void set_last_error(const char *fmt, ...);  // message for medusa_last_error()

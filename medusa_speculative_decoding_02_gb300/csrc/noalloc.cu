@@ -58,6 +58,7 @@ extern "C" medusa_status medusa_heads_noalloc(medusa_dtype dtype, const void *h,
                                               const void *b1, const void *W2, int B, int d, int V,
                                               int K, int top_s, int32_t *topk_ids,
                                               float *topk_logp, medusa_stream stream) {
+    const NvtxRange range("medusa_heads_noalloc");
     if (B >= 1 && K >= 1 && d >= 1 && V >= 1 && top_s >= 1) {
         const size_t need = heads_workspace_bytes(B, K, d, V, top_s);
         if (need > kStaticScratchBytes) {

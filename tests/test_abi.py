@@ -39,6 +39,33 @@ def test_exports_every_declared_symbol(L):
     assert set(m.EXPORTS) <= names
 
 
+def test_wait_budget_roundtrip(L):
+    default = m.wait_budget()
+    assert default == 1 << 16 or "MEDUSA_FAULT_WAIT_BUDGET" in os.environ
+    try:
+        m.set_wait_budget(123)
+        assert m.wait_budget() == 123
+        m.set_wait_budget(0)
+        assert m.wait_budget() == 0
+    finally:
+        m.set_wait_budget(default)
+    assert m.wait_budget() == default
+
+
+@pytest.mark.parametrize("value,expect", [("7", 7), ("0", 0), ("junk", 1 << 16), ("", 1 << 16)])
+def test_wait_budget_from_environment(L, value, expect):
+    """MEDUSA_FAULT_WAIT_BUDGET sets the budget a process starts with; a value
+    that is not a whole number leaves the default."""
+    import subprocess
+    import sys
+    env = dict(os.environ, MEDUSA_FAULT_WAIT_BUDGET=value)
+    r = subprocess.run([sys.executable, "-c",
+                        "import medusa_speculative_decoding_02_gb300 as m; print(m.wait_budget())"],
+                       cwd=ROOT, env=env, capture_output=True, text=True, timeout=120)
+    assert r.returncode == 0, r.stderr
+    assert int(r.stdout.strip().splitlines()[-1]) == expect
+
+
 def test_status_strings(L):
     for code, name in m.STATUS.items():
         assert L.medusa_status_string(code).decode() == name
