@@ -670,6 +670,8 @@ def run_ours(args, cfg):
 
     stages = {k: {"us": round(float(np.mean(v)) * 1e3, 2),
                   "us_median": round(float(np.median(v)) * 1e3, 2),
+                  "us_p10": round(float(np.percentile(v, 10)) * 1e3, 2),
+                  "us_p90": round(float(np.percentile(v, 90)) * 1e3, 2),
                   "GB/s": round(nb[k] / (float(np.mean(v)) * 1e-3) / 1e9, 1),
                   "frac_hbm": round(nb[k] / (float(np.mean(v)) * 1e-3) / 1e9 / peaks["hbm_gbs"], 4)}
               for k, v in per_call.items()}
