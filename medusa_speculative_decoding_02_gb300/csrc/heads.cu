@@ -365,10 +365,14 @@ heads_w2_kernel(const float *__restrict__ z, const T *__restrict__ W2, const T *
     const int r0 = (int)(((long long)g * V) / G);
     const int r1 = (int)(((long long)(g + 1) * V) / G);
     const int nrows = r1 - r0;
-    // The weights are never written by any kernel, so this warp's first row
-    // can be pulled into L2 before the wait for phase 1's z.
+    // The weights are never written by any kernel, so this warp's first two
+    // rows can be pulled into L2 before the wait for phase 1's z (the CTA
+    // starts while phase 1's last CTAs still stream).
     if (lane == 0 && warp < nrows)
         prefetch_l2_bulk(w2_row(W2, Wlm, 0, r0 + warp, V, d), (unsigned)(d * sizeof(T)));
+    if (lane == 0 && warp + kW2Warps < nrows)
+        prefetch_l2_bulk(w2_row(W2, Wlm, 0, r0 + warp + kW2Warps, V, d),
+                         (unsigned)(d * sizeof(T)));
     pdl_enter();
 
     for (int k0 = 0; k0 < K; k0 += hpg) {
