@@ -17,7 +17,8 @@
 //   (no node outside a level's best n can be among the global first n);
 //   finally the survivors of all levels are ranked together and the first n
 //   kept.  Ranks come from counting how many candidates precede each one,
-//   which is deterministic and needs no sort.
+//   which is deterministic and needs no sort.  Full trees of at most 512
+//   nodes skip the level cut and rank all their nodes at once.
 // Node identity is (depth, rank path) with the rank path packed four bits per
 // level, level 1 in the top nibble, so equal-depth paths compare
 // lexicographically as integers.
@@ -124,6 +125,11 @@ struct TreeArgs {
     int K, S, n;
     long long full;  // nodes of the full Cartesian tree (capped)
     int s[MEDUSA_MAX_HEADS];
+    // full trees of at most kDirectMax nodes: level D (1-based) holds node
+    // indices [lvl_base[D-1], lvl_base[D]), and mdiv[j] = ceil(2^16 / s[j])
+    // divides by s[j] exactly for dividends below 4096
+    int lvl_base[MEDUSA_MAX_HEADS + 1];
+    uint32_t mdiv[MEDUSA_MAX_HEADS];
     const int32_t *prefix_len;
     int32_t *tokens, *parent, *depth, *pos_id;
     uint64_t *anc_mask;
@@ -201,26 +207,25 @@ __global__ void __launch_bounds__(kTreeThreads) build_tree_kernel(TreeArgs a) {
     __syncthreads();
 
     if (a.full <= kDirectMax) {
-        // ---- small tree: every node of the full tree, ranked once
+        // ---- small tree: every node of the full tree.  Node t of level D
+        // has local index l = t - lvl_base[D-1], whose mixed-radix digits
+        // (level 1 most significant) are its rank path; the score is summed
+        // from depth 1 down in fp64, as the frontier does.
         const int full = (int)a.full;
         for (int t = tid; t < full; t += nt) {
-            int D = 1, base = 0, width = a.s[0];
-            while (t >= base + width) {
-                base += width;
-                width *= a.s[D];
-                ++D;
-            }
-            // mixed-radix digits of the index within its depth, depth 1 first;
-            // the score is summed from depth 1 down, as the frontier does
-            const int l = t - base;
-            int div = width / a.s[0];
+            int D = 1;
+            while (t >= a.lvl_base[D]) ++D;
+            uint32_t l = (uint32_t)(t - a.lvl_base[D - 1]);
             uint32_t path = 0;
+            for (int j = D - 1; j >= 0; --j) {
+                const uint32_t q = (l * a.mdiv[j]) >> 16;  // l / s[j]
+                path |= (l - q * (uint32_t)a.s[j]) << nib_shift(j + 1);
+                l = q;
+            }
             double sc = 0.0;
             for (int j = 0; j < D; ++j) {
-                const int r = (l / div) % a.s[j];
-                sc = (j == 0) ? lp[0][r] : sc + lp[j][r];
-                path |= (uint32_t)r << nib_shift(j + 1);
-                if (j + 1 < D) div /= a.s[j + 1];
+                const double v = lp[j][(path >> nib_shift(j + 1)) & 0xFu];
+                sc = (j == 0) ? v : sc + v;
             }
             sm.cand_key[t] = score_key(sc);
             sm.cand_lo[t] = ((uint64_t)D << 32) | path;
@@ -359,7 +364,8 @@ __global__ void __launch_bounds__(kTreeThreads) build_tree_kernel(TreeArgs a) {
             mw[2] |= w == 2 ? bit : 0;
             mw[3] |= w == 3 ? bit : 0;
         }
-        for (int w = 0; w < W; ++w) a.anc_mask[o * W + w] = w == 0 ? mw[0] : w == 1 ? mw[1] : w == 2 ? mw[2] : mw[3];
+        for (int w = 0; w < W; ++w)
+            a.anc_mask[o * W + w] = w == 0 ? mw[0] : w == 1 ? mw[1] : w == 2 ? mw[2] : mw[3];
     }
     __syncthreads();
     if (tid == 0) a.n_leaf[b] = nl;
@@ -409,6 +415,18 @@ cudaError_t launch_build_tree(const int32_t *root, const int32_t *ids, const flo
     a.S = S;
     a.n = n;
     for (int k = 0; k < MEDUSA_MAX_HEADS; ++k) a.s[k] = k < K ? s_host[k] : 0;
+    {
+        long long base = 0, level = 1;
+        a.lvl_base[0] = 0;
+        for (int k = 0; k < MEDUSA_MAX_HEADS; ++k) {
+            if (k < K && a.full <= kDirectMax) {
+                level *= s_host[k];
+                base += level;
+            }
+            a.lvl_base[k + 1] = (int)std::min<long long>(base, 1 << 20);
+            a.mdiv[k] = k < K ? (65536u + (uint32_t)s_host[k] - 1u) / (uint32_t)s_host[k] : 0u;
+        }
+    }
     a.prefix_len = prefix_len;
     a.tokens = tokens;
     a.parent = parent;
