@@ -177,14 +177,32 @@ posterior_rows_kernel(const T *__restrict__ logits, int R, int V, int splits, fl
         s_A[warp] = mo.A;
     }
     __syncthreads();
-    if (threadIdx.x == 0) {
-        for (int w = 1; w < kRowThreads / kWarp; ++w) {
-            if (better(s_val[w], s_id[w], bv, bi)) {
-                bv = s_val[w];
-                bi = s_id[w];
+    if (warp == 0) {
+        // the warps' states, merged by the first warp in three shuffle rounds
+        constexpr int NW = kRowThreads / kWarp;
+        static_assert(NW == 8, "merge rounds assume eight warps");
+        const bool have = lane < NW;
+        bv = have ? s_val[lane] : -INFINITY;
+        bi = have ? s_id[lane] : INT_MAX;
+        mo = Moments{have ? s_m[lane] : -INFINITY, have ? s_S[lane] : 0.f,
+                     have ? s_A[lane] : 0.f};
+#pragma unroll
+        for (int o = NW / 2; o > 0; o >>= 1) {
+            const float ov = __shfl_xor_sync(0xffffffffu, bv, o);
+            const int oi = __shfl_xor_sync(0xffffffffu, bi, o);
+            if (better(ov, oi, bv, bi)) {
+                bv = ov;
+                bi = oi;
             }
-            if (TYPICAL) mo.merge(s_m[w], s_S[w], s_A[w]);
+            if (TYPICAL) {
+                const float om = __shfl_xor_sync(0xffffffffu, mo.m, o);
+                const float oS = __shfl_xor_sync(0xffffffffu, mo.S, o);
+                const float oA = __shfl_xor_sync(0xffffffffu, mo.A, o);
+                mo.merge(om, oS, oA);
+            }
         }
+    }
+    if (threadIdx.x == 0) {
         RowPart pt;
         pt.amax = bv;
         pt.arg = bi;
@@ -232,6 +250,7 @@ posterior_select_kernel(const T *__restrict__ logits, const int32_t *__restrict_
     __shared__ int s_par[MEDUSA_MAX_TREE_ROWS];
     __shared__ int s_dep[MEDUSA_MAX_TREE_ROWS];
     __shared__ int s_tok[MEDUSA_MAX_TREE_ROWS];
+    __shared__ int s_arg[MEDUSA_MAX_TREE_ROWS];  // argmax of each node's own row
     __shared__ int s_L, s_best;
     __shared__ int s_path[MEDUSA_MAX_HEADS + 1];
     __shared__ int s_code;
@@ -255,6 +274,14 @@ posterior_select_kernel(const T *__restrict__ logits, const int32_t *__restrict_
     }
     __syncthreads();
     if (i < R) {
+        // this node's own row argmax (the next token if the path ends here),
+        // loaded with the parent row's statistics
+        {
+            int arg;
+            float m2, log2s, H;
+            row_stats(parts + ((size_t)b * R + i) * splits, splits, false, arg, m2, log2s, H);
+            s_arg[i] = arg;
+        }
         int acc = 1;
         if (i > 0) {
             const int p = s_par[i], tok = s_tok[i], D = s_dep[i];
@@ -316,10 +343,7 @@ posterior_select_kernel(const T *__restrict__ logits, const int32_t *__restrict_
         }
         s_L = L;
         accept_len[b] = L;
-        int arg;
-        float m2, log2s, H;
-        row_stats(parts + ((size_t)b * R + best) * splits, splits, false, arg, m2, log2s, H);
-        next_token[b] = arg;
+        next_token[b] = s_arg[best];
     }
     if (!ca.k_cache) return;  // uniform over the CTA
     // commit of the accepted path into the KV cache (medusa_commit_kv)
