@@ -402,16 +402,19 @@ __global__ void __launch_bounds__(256, 2) tree_attn_tc_kernel(AttnArgs a) {
     if (warp == 0) tc::tmem_dealloc(tmem, 256);
 }
 
-// One warp per (sequence, row, head).  Lane s reads split s's (m, l), so the
-// weights come from one round of independent loads; the O partials of all
-// splits are then read with independent loads as well (no load waits on
-// another).
+// One warp per (sequence, row, head).  Lane s reads split s's (m, l), and
+// the O rows of the first kPre splits are loaded in the same round (they do
+// not depend on the weights), so the common case (NS <= kPre) costs one
+// round of independent loads; later splits' rows are read with independent
+// loads as well.  An empty split (l = 0) has weight 0 and its row, never
+// written, is never used.
 template <int DH>
 __global__ void __launch_bounds__(256)
 tree_attn_combine_kernel(const float *__restrict__ part_o, const float2 *__restrict__ part_ml,
                          int B, int R, int H, int NS, bf16 *__restrict__ out) {
     pdl_enter();
     constexpr int PER = DH / 32;
+    constexpr int kPre = 8;
     const int lane = threadIdx.x & 31;
     const long long item = (long long)blockIdx.x * (blockDim.x >> 5) + (threadIdx.x >> 5);
     if (item >= (long long)B * R * H) return;
@@ -419,8 +422,17 @@ tree_attn_combine_kernel(const float *__restrict__ part_o, const float2 *__restr
     const int row = (int)((item / H) % R);
     const int b = (int)(item / ((long long)H * R));
     const size_t base = (size_t)(b * H + h) * NS;
-    float M = -INFINITY;
-    for (int s = lane; s < NS; s += 32) {
+    const float2 ml0 =
+        lane < NS ? part_ml[(base + lane) * R + row] : make_float2(-INFINITY, 0.f);
+    float pre[kPre][PER];
+#pragma unroll
+    for (int j = 0; j < kPre; ++j)
+        if (j < NS)
+#pragma unroll
+            for (int p = 0; p < PER; ++p)
+                pre[j][p] = part_o[((base + j) * R + row) * DH + lane + 32 * p];
+    float M = ml0.y > 0.f ? ml0.x : -INFINITY;
+    for (int s = lane + 32; s < NS; s += 32) {
         const float2 ml = part_ml[(base + s) * R + row];
         if (ml.y > 0.f) M = fmaxf(M, ml.x);
     }
@@ -431,17 +443,29 @@ tree_attn_combine_kernel(const float *__restrict__ part_o, const float2 *__restr
 #pragma unroll
     for (int j = 0; j < PER; ++j) acc[j] = 0.f;
     for (int s0 = 0; s0 < NS; s0 += 32) {
+        const float2 ml = s0 == 0                 ? ml0
+                          : s0 + lane < NS ? part_ml[(base + s0 + lane) * R + row]
+                                           : make_float2(-INFINITY, 0.f);
         float w_l = 0.f;
-        if (s0 + lane < NS) {
-            const float2 ml = part_ml[(base + s0 + lane) * R + row];
-            if (ml.y > 0.f) {
-                w_l = exp2f(ml.x - M);
-                L = fmaf(w_l, ml.y, L);
-            }
+        if (ml.y > 0.f) {
+            w_l = exp2f(ml.x - M);
+            L = fmaf(w_l, ml.y, L);
         }
         const int cnt = min(32, NS - s0);
+        int j0 = 0;
+        if (s0 == 0) {
+#pragma unroll
+            for (int j = 0; j < kPre; ++j) {
+                const float w = __shfl_sync(0xffffffffu, w_l, j);
+                if (j < cnt && w != 0.f) {
+#pragma unroll
+                    for (int p = 0; p < PER; ++p) acc[p] = fmaf(w, pre[j][p], acc[p]);
+                }
+            }
+            j0 = kPre;
+        }
 #pragma unroll 4
-        for (int j = 0; j < cnt; ++j) {
+        for (int j = j0; j < cnt; ++j) {
             const float w = __shfl_sync(0xffffffffu, w_l, j);
             const float *src = part_o + ((base + s0 + j) * R + row) * DH;
             if (w != 0.f) {
