@@ -499,6 +499,13 @@ heads_reduce_kernel(const float2 *__restrict__ part_ms, const float *__restrict_
     // this warp's contiguous share of the candidates
     const int c_lo = (int)(((long long)warp * C) / NW);
     const int c_hi = (int)(((long long)(warp + 1) * C) / NW);
+    // the (max, sum) pairs load in the same round as the candidates
+    // (G <= kMaxW2Ctas = 2 * kReduceThreads)
+    const float2 ms0 = threadIdx.x < G ? part_ms[(size_t)kb * G + threadIdx.x]
+                                       : make_float2(-INFINITY, 0.f);
+    const float2 ms1 = threadIdx.x + kReduceThreads < G
+                           ? part_ms[(size_t)kb * G + threadIdx.x + kReduceThreads]
+                           : make_float2(-INFINITY, 0.f);
     float val = -INFINITY;
     int id = INT_MAX;
     for (int c0 = c_lo; c0 < c_hi; c0 += kWarp * U) {
@@ -516,10 +523,8 @@ heads_reduce_kernel(const float2 *__restrict__ part_ms, const float *__restrict_
     }
     WarpTop st;
     st.reset();
-    for (int g = threadIdx.x; g < G; g += kReduceThreads) {
-        const float2 ms = part_ms[(size_t)kb * G + g];
-        st.merge_ms(ms.x, ms.y);
-    }
+    st.merge_ms(ms0.x, ms0.y);
+    st.merge_ms(ms1.x, ms1.y);
 #pragma unroll
     for (int o = 16; o > 0; o >>= 1) {
         const float om = __shfl_xor_sync(0xffffffffu, st.m, o);
@@ -560,6 +565,7 @@ heads_reduce_kernel(const float2 *__restrict__ part_ms, const float *__restrict_
 // ---------------------------------------------------------------- host ---
 
 constexpr int kMaxW2Ctas = 1024;
+static_assert(kMaxW2Ctas <= 2 * kReduceThreads, "phase 3 loads at most two (max, sum) pairs a thread");
 // Shared memory per phase-2 CTA.  One sequence (NB = 1) runs two CTAs per SM,
 // and two CTAs must stay within the 196 KB shared-memory carveout: the
 // largest carveout (228 KB) leaves L1 so small that the weight stream runs
