@@ -403,18 +403,17 @@ __global__ void __launch_bounds__(256, 2) tree_attn_tc_kernel(AttnArgs a) {
 }
 
 // One warp per (sequence, row, head).  Lane s reads split s's (m, l), and
-// the O rows of the first kPre splits are loaded in the same round (they do
-// not depend on the weights), so the common case (NS <= kPre) costs one
-// round of independent loads; later splits' rows are read with independent
-// loads as well.  An empty split (l = 0) has weight 0 and its row, never
+// the O rows of the first PRE splits are loaded in the same round (they do
+// not depend on the weights), so NS <= PRE costs one round of independent
+// loads (PRE = 4, 8 or 16, the smallest that covers NS); later splits' rows
+// are read with independent loads as well.  An empty split (l = 0) has weight 0 and its row, never
 // written, is never used.
-template <int DH>
+template <int DH, int PRE>
 __global__ void __launch_bounds__(256)
 tree_attn_combine_kernel(const float *__restrict__ part_o, const float2 *__restrict__ part_ml,
                          int B, int R, int H, int NS, bf16 *__restrict__ out) {
     pdl_enter();
     constexpr int PER = DH / 32;
-    constexpr int kPre = 8;
     const int lane = threadIdx.x & 31;
     const long long item = (long long)blockIdx.x * (blockDim.x >> 5) + (threadIdx.x >> 5);
     if (item >= (long long)B * R * H) return;
@@ -424,9 +423,9 @@ tree_attn_combine_kernel(const float *__restrict__ part_o, const float2 *__restr
     const size_t base = (size_t)(b * H + h) * NS;
     const float2 ml0 =
         lane < NS ? part_ml[(base + lane) * R + row] : make_float2(-INFINITY, 0.f);
-    float pre[kPre][PER];
+    float pre[PRE][PER];
 #pragma unroll
-    for (int j = 0; j < kPre; ++j)
+    for (int j = 0; j < PRE; ++j)
         if (j < NS)
 #pragma unroll
             for (int p = 0; p < PER; ++p)
@@ -455,14 +454,14 @@ tree_attn_combine_kernel(const float *__restrict__ part_o, const float2 *__restr
         int j0 = 0;
         if (s0 == 0) {
 #pragma unroll
-            for (int j = 0; j < kPre; ++j) {
+            for (int j = 0; j < PRE; ++j) {
                 const float w = __shfl_sync(0xffffffffu, w_l, j);
                 if (j < cnt && w != 0.f) {
 #pragma unroll
                     for (int p = 0; p < PER; ++p) acc[p] = fmaf(w, pre[j][p], acc[p]);
                 }
             }
-            j0 = kPre;
+            j0 = PRE;
         }
 #pragma unroll 4
         for (int j = j0; j < cnt; ++j) {
@@ -641,8 +640,12 @@ cudaError_t launch_tree_attention(medusa_dtype dtype, const void *q, const void 
     if (e) return e;
     const long long items = (long long)B * R * H;
     const int cblocks = (int)((items + 7) / 8);
-    e = launch_pdl(dh == 128 ? tree_attn_combine_kernel<128> : tree_attn_combine_kernel<64>,
-                   dim3(cblocks), dim3(256), 0, stream, static_cast<const float *>(part_o),
+    auto comb = NS <= 4 ? tree_attn_combine_kernel<64, 4>
+                : NS <= 8 ? tree_attn_combine_kernel<64, 8> : tree_attn_combine_kernel<64, 16>;
+    if (dh == 128)
+        comb = NS <= 4 ? tree_attn_combine_kernel<128, 4>
+               : NS <= 8 ? tree_attn_combine_kernel<128, 8> : tree_attn_combine_kernel<128, 16>;
+    e = launch_pdl(comb, dim3(cblocks), dim3(256), 0, stream, static_cast<const float *>(part_o),
                    static_cast<const float2 *>(part_ml), B, R, H, NS, static_cast<bf16 *>(out));
     note_launch();
     return e;
