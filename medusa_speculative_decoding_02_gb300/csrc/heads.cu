@@ -138,17 +138,24 @@ heads_w1_kernel(const T *__restrict__ h, const T *__restrict__ W1, const T *__re
     const int gw = blockIdx.x * nwarps + warp;
     const int r_begin = (int)(((long long)gw * rows) / total_warps);
     const int r_end = (int)(((long long)(gw + 1) * rows) / total_warps);
+    // the biases of this warp's first 32 rows, fetched once up front (lane i
+    // holds row r_begin + i), so no row waits on a bias load
+    const float bias_l =
+        (b1 && r_begin + lane < r_end) ? Vec16<T>::load1(b1 + r_begin + lane) : 0.f;
     for (int row = r_begin; row < r_end; ++row) {
         float acc[NB];
         row_dot<T, NB, U>(reinterpret_cast<const uint4 *>(W1 + (size_t)row * d), smem4, nvec, lane,
                           acc);
+        const int ri = row - r_begin;
+        const float bias = ri < kWarp ? __shfl_sync(0xffffffffu, bias_l, ri)
+                                      : (b1 && lane < B ? Vec16<T>::load1(b1 + row) : 0.f);
         if (lane < B) {
             float a = 0.f;
 #pragma unroll
             for (int b = 0; b < NB; ++b)
                 if (b == lane) a = acc[b];
             const int k = row / d, j = row - k * d;
-            const float u = a + (b1 ? Vec16<T>::load1(b1 + row) : 0.f);
+            const float u = a + bias;
             const float silu = u / (1.f + expf(-u));
             z[((size_t)k * B + lane) * d + j] = hs[plane_index<VN>(lane, j, nvec)] + silu;
         }
@@ -565,7 +572,8 @@ heads_reduce_kernel(const float2 *__restrict__ part_ms, const float *__restrict_
 // ---------------------------------------------------------------- host ---
 
 constexpr int kMaxW2Ctas = 1024;
-static_assert(kMaxW2Ctas <= 2 * kReduceThreads, "phase 3 loads at most two (max, sum) pairs a thread");
+static_assert(kMaxW2Ctas <= 2 * kReduceThreads,
+              "phase 3 loads at most two (max, sum) pairs a thread");
 // Shared memory per phase-2 CTA.  One sequence (NB = 1) runs two CTAs per SM,
 // and two CTAs must stay within the 196 KB shared-memory carveout: the
 // largest carveout (228 KB) leaves L1 so small that the weight stream runs
