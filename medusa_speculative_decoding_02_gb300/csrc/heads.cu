@@ -75,13 +75,12 @@ __device__ __forceinline__ void fma_vec(const uint4 &w, const float4 *__restrict
 }
 
 // Dot products of one weight row (nvec 16-byte vectors) with NB activation
-// rows; result replicated in every lane.
+// rows from vector `base` on, added to acc.
 template <typename T, int NB, int U>
-__device__ __forceinline__ void row_dot(const uint4 *__restrict__ w, const float4 *__restrict__ act,
-                                        int nvec, int lane, float (&acc)[NB]) {
-#pragma unroll
-    for (int b = 0; b < NB; ++b) acc[b] = 0.f;
-    for (int base = lane; base < nvec; base += kWarp * U) {
+__device__ __forceinline__ void row_dot_tail(const uint4 *__restrict__ w,
+                                             const float4 *__restrict__ act, int nvec, int base,
+                                             float (&acc)[NB]) {
+    for (; base < nvec; base += kWarp * U) {
         uint4 v[U];
 #pragma unroll
         for (int u = 0; u < U; ++u) {
@@ -94,8 +93,49 @@ __device__ __forceinline__ void row_dot(const uint4 *__restrict__ w, const float
             if (idx < nvec) fma_vec<T, NB>(v[u], act, idx, nvec, acc);
         }
     }
+}
+
+// Dot products of one weight row with NB activation rows; result replicated
+// in every lane.
+template <typename T, int NB, int U>
+__device__ __forceinline__ void row_dot(const uint4 *__restrict__ w, const float4 *__restrict__ act,
+                                        int nvec, int lane, float (&acc)[NB]) {
+#pragma unroll
+    for (int b = 0; b < NB; ++b) acc[b] = 0.f;
+    row_dot_tail<T, NB, U>(w, act, nvec, lane, acc);
 #pragma unroll
     for (int b = 0; b < NB; ++b) acc[b] = warp_sum(acc[b]);
+}
+
+// Stage NB activation rows of d elements (src row b at src + b * stride,
+// rows >= B zero) into shared memory in the split-plane layout, one 16-byte
+// load per vector of VN elements.
+template <typename S, int VN, int NB>
+__device__ __forceinline__ void stage_planes(const S *__restrict__ src, size_t stride, int B,
+                                             int d, float4 *__restrict__ dst) {
+    constexpr int NPL = VN / 4;
+    constexpr int SN = 16 / sizeof(S);  // source elements per 16-byte load
+    const int nvec = d / VN;
+    const int nsv = d / SN;
+    for (int i = threadIdx.x; i < NB * nsv; i += blockDim.x) {
+        const int b = i / nsv, sv = i - b * nsv;
+        float f[SN];
+        if (b < B) {
+            const uint4 w = *reinterpret_cast<const uint4 *>(src + b * stride + (size_t)sv * SN);
+            Vec16<S>::widen(w, f);
+        } else {
+#pragma unroll
+            for (int e = 0; e < SN; ++e) f[e] = 0.f;
+        }
+        // elements sv*SN .. sv*SN+SN-1: SN/4 groups of four, each one float4
+#pragma unroll
+        for (int g = 0; g < SN / 4; ++g) {
+            const int c = sv * SN + 4 * g;
+            const int p = (c % VN) / 4, idx = c / VN;
+            dst[(b * NPL + p) * nvec + idx] =
+                make_float4(f[4 * g], f[4 * g + 1], f[4 * g + 2], f[4 * g + 3]);
+        }
+    }
 }
 
 // ------------------------------------------------------------- phase 1 ---
@@ -120,14 +160,6 @@ heads_w1_kernel(const T *__restrict__ h, const T *__restrict__ W1, const T *__re
     float *hs = reinterpret_cast<float *>(smem4);
     constexpr int VN = Vec16<T>::N;
     const int nvec = d / VN;
-    for (int i = threadIdx.x; i < NB * d; i += blockDim.x) {
-        const int b = i / d, c = i - b * d;
-        hs[plane_index<VN>(b, c, nvec)] = (b < B) ? Vec16<T>::load1(h + (size_t)b * d + c) : 0.f;
-    }
-    if (z_lm)  // the LM head's z is h itself (no residual block)
-        for (int i = blockIdx.x * blockDim.x + threadIdx.x; i < B * d; i += gridDim.x * blockDim.x)
-            z_lm[i] = Vec16<T>::load1(h + i);
-    __syncthreads();
     const int lane = threadIdx.x & 31;
     const int warp = threadIdx.x >> 5;
     const int nwarps = blockDim.x >> 5;
@@ -138,14 +170,19 @@ heads_w1_kernel(const T *__restrict__ h, const T *__restrict__ W1, const T *__re
     const int gw = blockIdx.x * nwarps + warp;
     const int r_begin = (int)(((long long)gw * rows) / total_warps);
     const int r_end = (int)(((long long)(gw + 1) * rows) / total_warps);
+    stage_planes<T, VN, NB>(h, (size_t)d, B, d, smem4);
+    if (z_lm)  // the LM head's z is h itself (no residual block)
+        for (int i = blockIdx.x * blockDim.x + threadIdx.x; i < B * d; i += gridDim.x * blockDim.x)
+            z_lm[i] = Vec16<T>::load1(h + i);
+    __syncthreads();
     // the biases of this warp's first 32 rows, fetched once up front (lane i
     // holds row r_begin + i), so no row waits on a bias load
     const float bias_l =
         (b1 && r_begin + lane < r_end) ? Vec16<T>::load1(b1 + r_begin + lane) : 0.f;
     for (int row = r_begin; row < r_end; ++row) {
         float acc[NB];
-        row_dot<T, NB, U>(reinterpret_cast<const uint4 *>(W1 + (size_t)row * d), smem4, nvec, lane,
-                          acc);
+        const uint4 *wrow = reinterpret_cast<const uint4 *>(W1 + (size_t)row * d);
+        row_dot<T, NB, U>(wrow, smem4, nvec, lane, acc);
         const int ri = row - r_begin;
         const float bias = ri < kWarp ? __shfl_sync(0xffffffffu, bias_l, ri)
                                       : (b1 && lane < B ? Vec16<T>::load1(b1 + row) : 0.f);
@@ -385,13 +422,9 @@ heads_w2_kernel(const float *__restrict__ z, const T *__restrict__ W2, const T *
     for (int k0 = 0; k0 < K; k0 += hpg) {
         const int hk = min(hpg, K - k0);
         // stage z for heads k0 .. k0+hk-1 (zero rows for b >= B)
-        for (int i = threadIdx.x; i < hk * NB * d; i += blockDim.x) {
-            const int kk = i / (NB * d);
-            const int rem = i - kk * NB * d;
-            const int b = rem / d, c = rem - b * d;
-            zs[(size_t)kk * NB * d + plane_index<VN>(b, c, nvec)] =
-                (b < B) ? z[((size_t)(k0 + kk) * B + b) * d + c] : 0.f;
-        }
+        for (int kk = 0; kk < hk; ++kk)
+            stage_planes<float, VN, NB>(z + (size_t)(k0 + kk) * B * d, (size_t)d, B, d,
+                                        zs4 + (size_t)kk * NB * d / 4);
         __syncthreads();
 
         WarpTop st[NB];
@@ -427,9 +460,9 @@ heads_w2_kernel(const float *__restrict__ z, const T *__restrict__ W2, const T *
                 ++cur;
             }
             float acc[NB];
-            const T *wrow = w2_row(W2, Wlm, k0 + kk, v, V, d);
-            row_dot<T, NB, U>(reinterpret_cast<const uint4 *>(wrow), zs4 + (size_t)kk * NB * d / 4,
-                              nvec, lane, acc);
+            const uint4 *wrow = reinterpret_cast<const uint4 *>(w2_row(W2, Wlm, k0 + kk, v, V, d));
+            const float4 *zk = zs4 + (size_t)kk * NB * d / 4;
+            row_dot<T, NB, U>(wrow, zk, nvec, lane, acc);
             if (!SAMPLE) {
 #pragma unroll
                 for (int b = 0; b < NB; ++b)
