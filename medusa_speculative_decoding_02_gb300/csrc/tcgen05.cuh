@@ -179,17 +179,6 @@ __host__ __device__ constexpr uint32_t idesc_bf16(int M, int N, int b_mn_major) 
            | ((uint32_t)(M >> 4) << 24);   // M / 16
 }
 
-// D[tmem] (+)= A[smem] * B[smem]; issued by one thread
-__device__ __forceinline__ void mma_bf16_ss(uint32_t tmem_d, uint64_t adesc, uint64_t bdesc,
-                                            uint32_t idesc, uint32_t accumulate) {
-    asm volatile(
-        "{\n.reg .pred p;\n"
-        "setp.ne.b32 p, %4, 0;\n"
-        "tcgen05.mma.cta_group::1.kind::f16 [%0], %1, %2, %3, p;\n}\n" ::"r"(tmem_d),
-        "l"(adesc), "l"(bdesc), "r"(idesc), "r"(accumulate)
-        : "memory");
-}
-
 // D[tmem] (+)= A[tmem] * B[smem]; issued by one thread.  A (16-bit) sits one
 // row per lane, two consecutive K elements per 32-bit column (the lower K
 // index in the low half).
