@@ -241,14 +241,9 @@ __global__ void __launch_bounds__(256, 2) tree_attn_tc_kernel(AttnArgs a) {
         // P V of sub-chunk j-1 done: its stage may be refilled (with j+2) and O
         // may be rescaled
         if (j > 0 && !tc::mbar_wait_bounded(&bar_o, (j - 1) & 1, a.wait_polls)) failed = 1;
-        if (j + 2 < nsub)
-            tc_load_stage<DH>(stage_k(j + 2), stage_v(j + 2), kc, vc, k0 + 2 * kTcSub, kend, H, h,
-                              tid);
-        // groups committed after sub-chunk j's: j+1 and j+2 where they exist
-        const int newer = min(2, nsub - 1 - j);
-        if (newer == 2)
-            cp_async_wait<2>();
-        else if (newer == 1)
+        // groups in flight: j's and j+1's where it exists (j+2's is issued
+        // below, while the S MMA of sub-chunk j runs)
+        if (j + 1 < nsub)
             cp_async_wait<1>();
         else
             cp_async_wait<0>();
@@ -269,6 +264,10 @@ __global__ void __launch_bounds__(256, 2) tree_attn_tc_kernel(AttnArgs a) {
             }
             tc::mma_commit(&bar_s);
         }
+        // ---- refill the stage of sub-chunk j-1 with j+2 while the MMA runs
+        if (j + 2 < nsub)
+            tc_load_stage<DH>(stage_k(j + 2), stage_v(j + 2), kc, vc, k0 + 2 * kTcSub, kend,
+                              H, h, tid);
         __syncwarp();
         if (!tc::mbar_wait_bounded(&bar_s, j & 1, a.wait_polls)) failed = 1;
         tc::fence_after_sync();
