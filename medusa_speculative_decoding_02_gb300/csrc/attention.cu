@@ -116,7 +116,9 @@ __device__ __forceinline__ void tc_load_stage(unsigned char *k_s, unsigned char 
                                               const bf16 *kc, const bf16 *vc, int k0, int kend,
                                               int H, int h, int tid) {
     constexpr int CPR = (DH / 64) * 8;  // 16-byte chunks per key row
-    for (int i = tid; i < kTcSub * CPR; i += 256) {
+    // warp 0 holds the thread that issues the MMAs: warps 1-7 copy, so that
+    // thread goes from its MMA issue straight to its softmax rows
+    for (int i = tid - kWarp; i >= 0 && i < kTcSub * CPR; i += 256 - kWarp) {
         const int r = i / CPR, c16 = i - r * CPR;
         const int key = k0 + r;
         const bool ok = key < kend;
