@@ -37,6 +37,14 @@ __device__ __forceinline__ void cp_async_wait() {
     asm volatile("cp.async.wait_group %0;\n" ::"n"(N));
 }
 
+// 2^x by the hardware's approximate exponential (relative error far below
+// the bf16 rounding the weights receive next; -inf gives +0)
+__device__ __forceinline__ float ex2_approx(float x) {
+    float y;
+    asm("ex2.approx.ftz.f32 %0, %1;" : "=f"(y) : "f"(x));
+    return y;
+}
+
 __device__ __forceinline__ uint32_t pack_bf16(float lo, float hi) {
     __nv_bfloat162 v = __floats2bfloat162_rn(lo, hi);
     return *reinterpret_cast<uint32_t *>(&v);
@@ -288,7 +296,6 @@ __global__ void __launch_bounds__(256, 2) tree_attn_tc_kernel(AttnArgs a) {
         if (!masked) {
 #pragma unroll
             for (int e = 0; e < HALF; ++e) {
-                x[e] *= a.scale_log2;
                 mx[e & 3] = fmaxf(mx[e & 3], x[e]);
             }
         } else {
@@ -302,14 +309,17 @@ __global__ void __launch_bounds__(256, 2) tree_attn_tc_kernel(AttnArgs a) {
                                                         : (t < 64 ? am0 : am1);
                     vis = (w >> (t & 63)) & 1u;
                 }
-                x[e] = vis ? x[e] * a.scale_log2 : -INFINITY;
+                x[e] = vis ? x[e] : -INFINITY;
                 mx[e & 3] = fmaxf(mx[e & 3], x[e]);
             }
         }
         // row max of the sub-chunk: halves exchange through the dead K_j tile
         // (it is refilled only after the barrier that ends this iteration)
         float *xch = reinterpret_cast<float *>(k_s);
-        xch[half * 128 + lrow] = fmaxf(fmaxf(mx[0], mx[1]), fmaxf(mx[2], mx[3]));
+        // (scores are scaled into log2 units here and inside the exponent:
+        // the scale is positive, so the max of the scaled scores is the
+        // scaled max)
+        xch[half * 128 + lrow] = fmaxf(fmaxf(mx[0], mx[1]), fmaxf(mx[2], mx[3])) * a.scale_log2;
         __syncthreads();
         const float cm = fmaxf(xch[lrow], xch[128 + lrow]);
         const bool raise = cm > m_run + kRescaleLog2;
@@ -323,7 +333,8 @@ __global__ void __launch_bounds__(256, 2) tree_attn_tc_kernel(AttnArgs a) {
             uint32_t pk[HALF / 2];
 #pragma unroll
             for (int e = 0; e < HALF; e += 2) {
-                const uint32_t w = pack_bf16(exp2f(x[e] - mu), exp2f(x[e + 1] - mu));
+                const uint32_t w = pack_bf16(ex2_approx(fmaf(x[e], a.scale_log2, -mu)),
+                                             ex2_approx(fmaf(x[e + 1], a.scale_log2, -mu)));
                 pk[e / 2] = w;
                 // the row sum adds the rounded weights the MMA uses, so that the
                 // output is an exact convex combination of V rows under them
@@ -510,7 +521,8 @@ tree_attn_f32_kernel(const float *__restrict__ q, const float *const *kcs, const
     }
     const int W = (R + 63) / 64;
     const uint64_t *mrow = anc_mask + ((size_t)b * R + i) * W;
-    for (int c = threadIdx.x; c < dh; c += blockDim.x) qs[c] = q[(((size_t)b * R + i) * H + h) * dh + c];
+    for (int c = threadIdx.x; c < dh; c += blockDim.x)
+        qs[c] = q[(((size_t)b * R + i) * H + h) * dh + c];
     __syncthreads();
     float lmax = -INFINITY;
     for (int j = threadIdx.x; j < n; j += blockDim.x) {
