@@ -197,6 +197,7 @@ __global__ void __launch_bounds__(kTreeThreads) build_tree_kernel(TreeArgs a) {
         s_root = a.root[b];
         s_prefix = a.prefix_len ? a.prefix_len[b] : 0;
     }
+    for (int i = tid; i < R; i += nt) sm.has_child[i] = 0;
     for (int i = tid; i < K * S; i += nt) {
         const int k = i / S, r = i - k * S;
         const float v = a.logp[(size_t)b * a.logp_bstride + (size_t)k * S + r];
@@ -279,45 +280,42 @@ __global__ void __launch_bounds__(kTreeThreads) build_tree_kernel(TreeArgs a) {
     }
     __syncthreads();
 
-    // ---- canonical order: root, then (depth, rank path) ascending (the lo
-    // words are distinct), four threads per node
+    // ---- canonical order (root, then (depth, rank path) ascending; the lo
+    // words are distinct) and parents in one pass, four threads per node: a
+    // node's place is 1 + the number of picks below its lo word, and its
+    // parent -- the node one level up with the same rank path minus the last
+    // rank, always a pick too (a child never precedes its parent) -- sits at
+    // 1 + the number of picks below the parent's lo word
     for (int base = 0; base < n; base += nt / 4) {
         const int i = base + (tid >> 2), q = tid & 3;
-        int cnt = 0;
+        int cnt = 0, pcnt = 0, D = 0;
         uint64_t li = 0;
         if (i < n) {
             li = sm.sel_lo[i];
+            D = (int)(li >> 32);
+            const uint32_t ppath = (uint32_t)li & ~((uint32_t)0xF << nib_shift(D));
+            const uint64_t want = D > 1 ? ((uint64_t)(D - 1) << 32) | ppath : 0;
 #pragma unroll 4
-            for (int j = q; j < n; j += 4) cnt += sm.sel_lo[j] < li;
+            for (int j = q; j < n; j += 4) {
+                const uint64_t lj = sm.sel_lo[j];
+                cnt += lj < li;
+                pcnt += lj < want;
+            }
         }
         cnt += __shfl_xor_sync(0xffffffffu, cnt, 1);
         cnt += __shfl_xor_sync(0xffffffffu, cnt, 2);
-        if (i < n && q == 0) sm.c_lo[1 + cnt] = li;
-    }
-    if (tid == 0) sm.c_lo[0] = 0;
-    for (int i = tid; i < R; i += nt) sm.has_child[i] = 0;
-    __syncthreads();
-    // parent = the node one level up with this node's rank path minus its
-    // last rank; c_lo is sorted, so binary search finds its index
-    for (int i = tid; i < R; i += nt) {
-        int p = -1;
-        if (i > 0) {
-            const uint64_t li = sm.c_lo[i];
-            const int D = (int)(li >> 32);
-            p = 0;
-            if (D > 1) {
-                const uint64_t want = ((uint64_t)(D - 1) << 32) |
-                                      ((uint32_t)li & ~((uint32_t)0xF << nib_shift(D)));
-                int lo = 1, hi = i;
-                while (lo < hi) {
-                    const int mid = (lo + hi) >> 1;
-                    if (sm.c_lo[mid] < want) lo = mid + 1; else hi = mid;
-                }
-                p = lo;
-            }
+        pcnt += __shfl_xor_sync(0xffffffffu, pcnt, 1);
+        pcnt += __shfl_xor_sync(0xffffffffu, pcnt, 2);
+        if (i < n && q == 0) {
+            const int p = D > 1 ? 1 + pcnt : 0;
+            sm.c_lo[1 + cnt] = li;
+            sm.c_parent[1 + cnt] = p;
             sm.has_child[p] = 1;
         }
-        sm.c_parent[i] = p;
+    }
+    if (tid == 0) {
+        sm.c_lo[0] = 0;
+        sm.c_parent[0] = -1;
     }
     __syncthreads();
 
