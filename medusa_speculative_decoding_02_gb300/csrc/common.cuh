@@ -30,6 +30,16 @@ __device__ __forceinline__ void prefetch_l2_bulk(const void *p, unsigned bytes) 
     asm volatile("cp.async.bulk.prefetch.L2.global [%0], %1;\n" ::"l"(p), "r"(bytes) : "memory");
 }
 
+// 2^x by the hardware's approximate exponential (ex2.approx.ftz: relative
+// error ~2^-22, subnormal results flushed to 0, -inf gives +0).  Used where
+// the result is rounded to bf16 next (attention weights) or only compared in
+// the log domain (posterior sums).
+__device__ __forceinline__ float ex2_approx(float x) {
+    float y;
+    asm("ex2.approx.ftz.f32 %0, %1;" : "=f"(y) : "f"(x));
+    return y;
+}
+
 // bf16 pair packed in a 32-bit word -> two floats (exact widening).
 __device__ __forceinline__ float bf_lo(uint32_t w) { return __uint_as_float(w << 16); }
 __device__ __forceinline__ float bf_hi(uint32_t w) { return __uint_as_float(w & 0xffff0000u); }

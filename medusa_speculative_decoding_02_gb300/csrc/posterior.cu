@@ -38,14 +38,6 @@ constexpr int kSelectThreads = 256;
 constexpr float kLog2e = 1.4426950408889634f;
 constexpr float kLn2 = 0.6931471805599453f;
 
-// 2^x by the hardware's approximate exponential (relative error ~2^-22; the
-// sums it feeds decide acceptance only through log-domain comparisons)
-__device__ __forceinline__ float ex2_approx(float x) {
-    float y;
-    asm("ex2.approx.ftz.f32 %0, %1;" : "=f"(y) : "f"(x));
-    return y;
-}
-
 // Statistics of one slice of a logits row (a row is split over several CTAs).
 struct RowPart {
     float amax;   // largest logit of the slice
