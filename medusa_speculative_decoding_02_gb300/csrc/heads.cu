@@ -514,9 +514,9 @@ heads_w2_kernel(const float *__restrict__ z, const T *__restrict__ W2, const T *
 
 // One CTA per (head, sequence).  The G partial top-s lists sit contiguously
 // (G*S candidates); each warp selects the top-s of its share with
-// warp_select_top (loads issued together, no load waits on another), then the
-// warps' lists are merged by parallel ranking.  Partial (max, sum) pairs merge
-// in parallel.
+// warp_select_top, the partial (max, sum) pairs loading in the same round as
+// the candidates; then one warp merges the warps' lists by warp selection
+// (warp_merge_top) while another merges their (max, sum) pairs.
 __global__ void __launch_bounds__(kReduceThreads)
 heads_reduce_kernel(const float2 *__restrict__ part_ms, const float *__restrict__ part_val,
                     const int *__restrict__ part_id, int G, int B, int K, int S, int lm,
