@@ -175,17 +175,17 @@ heads_w1_kernel(const T *__restrict__ h, const T *__restrict__ W1, const T *__re
         for (int i = blockIdx.x * blockDim.x + threadIdx.x; i < B * d; i += gridDim.x * blockDim.x)
             z_lm[i] = Vec16<T>::load1(h + i);
     __syncthreads();
-    // the biases of this warp's first 32 rows, fetched once up front (lane i
-    // holds row r_begin + i), so no row waits on a bias load
-    const float bias_l =
-        (b1 && r_begin + lane < r_end) ? Vec16<T>::load1(b1 + r_begin + lane) : 0.f;
+    // the biases of the warp's rows, 32 at a time (lane i holds the bias of
+    // the chunk's row i), fetched before the chunk's first row: no row waits
+    // on a bias load of its own
+    float bias_l = 0.f;
     for (int row = r_begin; row < r_end; ++row) {
+        const int ri = (row - r_begin) & (kWarp - 1);
+        if (ri == 0) bias_l = (b1 && row + lane < r_end) ? Vec16<T>::load1(b1 + row + lane) : 0.f;
         float acc[NB];
         const uint4 *wrow = reinterpret_cast<const uint4 *>(W1 + (size_t)row * d);
         row_dot<T, NB, U>(wrow, smem4, nvec, lane, acc);
-        const int ri = row - r_begin;
-        const float bias = ri < kWarp ? __shfl_sync(0xffffffffu, bias_l, ri)
-                                      : (b1 && lane < B ? Vec16<T>::load1(b1 + row) : 0.f);
+        const float bias = __shfl_sync(0xffffffffu, bias_l, ri);
         if (lane < B) {
             float a = 0.f;
 #pragma unroll

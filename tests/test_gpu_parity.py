@@ -174,6 +174,22 @@ def test_heads_ragged_shapes(dev, dtype, B, d, V, K, S):
     check_topk(ids, logp, o_ids, o_logits, o_logz)
 
 
+@pytest.mark.parametrize("dtype,B", [("bf16", 1), ("bf16", 2), ("f32", 1)])
+def test_heads_bias_many_rows_per_warp(dev, dtype, B):
+    """Full-width W1 (K = 5, d = 4096: about four rows per phase-1 warp) with a
+    non-zero bias, so the per-warp bias fetch is used at every row position;
+    a small vocabulary keeps the oracle quick."""
+    cfg = synth.v7b().replace(name=f"bias{dtype}{B}", dtype=dtype, B=B, V=1000, w1_std=0.02,
+                              w2_std=0.05)
+    hi = synth.heads_inputs(cfg)
+    rng = np.random.default_rng(41 + B)
+    hi.b1 = synth.cast(rng.standard_normal((cfg.K, cfg.d)).astype(np.float32) * 0.5, dtype)
+    _, ids, logp = run_heads(cfg, dev, hi)
+    o_ids, _, o_logits, o_logz = oracle.heads(hi.h, hi.W1, hi.b1, hi.W2, cfg.top_s,
+                                              want_logits=True)
+    check_topk(ids, logp, o_ids, o_logits, o_logz)
+
+
 @pytest.mark.parametrize("cfg_fn", [synth.v7b, synth.v13b, synth.batch8],
                          ids=["v7b", "v13b", "batch8"])
 def test_heads_full_size(dev, cfg_fn):
