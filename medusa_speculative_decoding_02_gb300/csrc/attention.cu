@@ -73,24 +73,29 @@ struct AttnArgs {
 // a sequence are its cache slots 0 .. P+R-1, prefix and tree alike (they are
 // contiguous); a key range is `cps` consecutive sub-chunks of 64 keys.  K and
 // V of the sub-chunks stream through a three-stage cp.async ring in shared
-// memory (two sub-chunks in flight while one computes); Q, S, P and O live
-// in tensor memory:
+// memory (two sub-chunks in flight while one computes), issued by warps 1-7
+// so that the thread issuing the MMAs goes from the S MMA to its softmax
+// rows; the next stage is issued while the S MMA runs.  Q, S, P and O live in
+// tensor memory:
 //     columns [0, 64)        S = Q K_j^T (fp32), then P over it (bf16 pairs)
 //     columns [64, 64+DH/2)  Q (bf16 pairs, one query row per lane)
 //     columns [128, 128+DH)  O += P V_j (fp32)
 // 256 threads: threads t and t+128 own query row 128*tile + t (rows >= R are
-// zero), each
-// taking half of a sub-chunk's keys and half of the output columns; one
-// thread issues the MMAs (A from tensor memory, B from shared memory).  Every
-// thread reads its S half-row, masks it (slots past the range; tree slots
-// that are not ancestors-or-self of the row) and writes P = 2^(s*scale*log2e
-// - m) back over the S columns it read.  The row reference m is raised only
-// when a sub-chunk's max exceeds it by more than 2^8; the threads then
-// rescale their O row in tensor memory.  Otherwise P may reach 2^8, harmless
-// in bf16 and fp32.  The CTA writes one unnormalised partial (O, m, l) per
-// row; tree_attn_combine_kernel merges the ranges.  Every mbarrier wait is
-// bounded; on a timeout the CTA records MEDUSA_DEV_TIMEOUT, stops, waits once
-// more (bounded) for its MMAs and frees its tensor memory before returning.
+// zero), each taking half of a sub-chunk's keys and half of the output
+// columns; one thread issues the MMAs (A from tensor memory, B from shared
+// memory).  Every thread reads its S half-row, masks it (slots past the
+// range; tree slots that are not ancestors-or-self of the row) and writes
+// P = 2^(s*scale*log2e - m) back over the S columns it read: the row max is
+// taken on the raw scores and scaled once, the scale enters the exponent
+// through one FMA, and the exponential is the hardware's ex2.approx (P is
+// rounded to bf16 next).  The row reference m is raised only when a
+// sub-chunk's max exceeds it by more than 2^8; the threads then rescale
+// their O row in tensor memory.  Otherwise P may reach 2^8, harmless in bf16
+// and fp32.  The row sum adds the bf16-rounded weights the MMA uses.  The CTA
+// writes one unnormalised partial (O, m, l) per row; tree_attn_combine_kernel
+// merges the ranges.  Every mbarrier wait is bounded; on a timeout the CTA
+// records MEDUSA_DEV_TIMEOUT, stops, waits once more (bounded) for its MMAs
+// and frees its tensor memory before returning.
 constexpr int kTcSub = 64;               // keys per pipeline stage
 constexpr int kTcStages = 3;
 constexpr float kRescaleLog2 = 8.f;      // lazy-rescale threshold (log2 units)
