@@ -498,6 +498,27 @@ def test_posterior_batch8(dev):
         check_posterior(gp, l16, ot, cfg.K, mode, cfg.eps, cfg.delta, 1.0)
 
 
+def test_posterior_many_sequences_one_workspace(dev):
+    """Batches past the heads' limit of 8 (the posterior takes any B): 53,
+    3, 49 and 53 sequences through one workspace, each checked against the
+    oracle; the status word stays 0."""
+    cfg = synth.tiny()
+    ws = m.new_workspace(m.posterior_workspace_size(53, cfg.R), dev)
+    for B in (53, 3, 49, 53):
+        c = cfg.replace(name=f"many{B}", B=B, prefix=(0,) * B)
+        rng = np.random.default_rng(B)
+        ot = oracle_tree_for(rng, c.s, c.n, B, c.prefix, c.V)
+        logits = synth.plant_bernoulli(synth.base_logits(c), ot["tokens"], ot["parent"], rng,
+                                       prob=0.8, amount=9.0)
+        for mode in (m.GREEDY, m.TYPICAL):
+            gp = m.evaluate_posterior(T(logits, dev), T(ot["tokens"], dev), T(ot["parent"], dev),
+                                      T(ot["depth"], dev), c.K, mode, c.eps, c.delta, 1.0, ws=ws)
+            torch.cuda.synchronize()
+            check_posterior(gp, logits, ot, c.K, mode, c.eps, c.delta, 1.0)
+            assert m.read_device_status(ws) == 0
+    assert (N(gp.accept_len) > 0).any()
+
+
 @pytest.mark.parametrize("dtype,V,s,n,temp", [
     ("f32", 1000, (2, 2, 2), 14, 0.7), ("bf16", 1008, (4, 3), 15, 1.0),
     ("bf16", 32000, (16, 16), 255, 0.7), ("bf16", 8, (2,), 1, 2.0), ("f32", 4, (4, 4), 20, 1.0)])
