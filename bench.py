@@ -27,6 +27,7 @@ import math
 import os
 import subprocess
 import sys
+import tempfile
 import time
 
 import numpy as np
@@ -86,16 +87,18 @@ class ClockSampler:
         self.path = None
 
     def __enter__(self):
+        fd, self.path = tempfile.mkstemp(prefix="medusa_clocks_", suffix=".csv")
+        self.f = os.fdopen(fd, "w")
         try:
-            os.makedirs(os.path.join(ROOT, "gpurun_out"), exist_ok=True)
-            self.path = os.path.join(ROOT, "gpurun_out", f"clocks_{os.getpid()}.csv")
-            self.f = open(self.path, "w")
             self.proc = subprocess.Popen(
                 ["nvidia-smi", f"--id={self.index}", f"--query-gpu={self.Q}", "--format=csv,noheader,nounits",
                  "-lms", "200"], stdout=self.f, stderr=subprocess.DEVNULL)
             time.sleep(0.3)
         except Exception:
             self.proc = None
+            self.f.close()
+            os.unlink(self.path)
+            self.path = None
         return self
 
     def __exit__(self, *exc):
@@ -112,7 +115,11 @@ class ClockSampler:
             return None
         sm, mx, reasons = [], [], set()
         names = ["hw_slowdown", "hw_thermal_slowdown", "sw_thermal_slowdown", "sw_power_cap"]
-        for line in open(self.path):
+        with open(self.path) as f:
+            lines = f.readlines()
+        os.unlink(self.path)
+        self.path = None
+        for line in lines:
             parts = [x.strip() for x in line.split(",")]
             if len(parts) < 9:
                 continue
