@@ -22,6 +22,7 @@ of this method here) on a bounded sample of the same workload.
 from __future__ import annotations
 
 import argparse
+import datetime
 import json
 import math
 import os
@@ -76,23 +77,32 @@ def measured_peaks() -> tuple[dict, str]:
 # ---------------------------------------------------------------- clocks ---
 
 class ClockSampler:
-    """nvidia-smi sampling of SM clocks and throttle reasons while running."""
-    Q = ("index,clocks.sm,clocks.max.sm,power.draw,clocks_event_reasons.active,"
+    """nvidia-smi sampling of SM clocks and throttle reasons while running.
+
+    Samples carry nvidia-smi's timestamp; `begin()` / `end()` mark the timed
+    region on the host clock (called with the device synchronised, so they
+    bracket the GPU work), and the summary keeps the samples taken inside
+    it.  A region shorter than the sampling interval may hold none: the
+    summary then falls back to every sample and says so."""
+    Q = ("timestamp,index,clocks.sm,clocks.max.sm,power.draw,clocks_event_reasons.active,"
          "clocks_event_reasons.hw_slowdown,clocks_event_reasons.hw_thermal_slowdown,"
          "clocks_event_reasons.sw_thermal_slowdown,clocks_event_reasons.sw_power_cap")
+    INTERVAL_MS = 10
 
     def __init__(self, index: int):
         self.index = index
         self.proc = None
         self.path = None
+        self.t0 = self.t1 = None
 
     def __enter__(self):
         fd, self.path = tempfile.mkstemp(prefix="medusa_clocks_", suffix=".csv")
         self.f = os.fdopen(fd, "w")
         try:
             self.proc = subprocess.Popen(
-                ["nvidia-smi", f"--id={self.index}", f"--query-gpu={self.Q}", "--format=csv,noheader,nounits",
-                 "-lms", "200"], stdout=self.f, stderr=subprocess.DEVNULL)
+                ["nvidia-smi", f"--id={self.index}", f"--query-gpu={self.Q}",
+                 "--format=csv,noheader,nounits", "-lms", str(self.INTERVAL_MS)],
+                stdout=self.f, stderr=subprocess.DEVNULL)
             time.sleep(0.3)
         except Exception:
             self.proc = None
@@ -101,8 +111,15 @@ class ClockSampler:
             self.path = None
         return self
 
+    def begin(self):
+        self.t0 = datetime.datetime.now()
+
+    def end(self):
+        self.t1 = datetime.datetime.now()
+
     def __exit__(self, *exc):
         if self.proc is not None:
+            time.sleep(2 * self.INTERVAL_MS / 1000)  # the sample after the region
             self.proc.terminate()
             try:
                 self.proc.wait(timeout=5)
@@ -113,28 +130,36 @@ class ClockSampler:
     def summary(self):
         if self.proc is None or not self.path or not os.path.exists(self.path):
             return None
-        sm, mx, reasons = [], [], set()
-        names = ["hw_slowdown", "hw_thermal_slowdown", "sw_thermal_slowdown", "sw_power_cap"]
         with open(self.path) as f:
             lines = f.readlines()
         os.unlink(self.path)
         self.path = None
+        names = ["hw_slowdown", "hw_thermal_slowdown", "sw_thermal_slowdown", "sw_power_cap"]
+        samples = []  # (time, sm MHz, max MHz, active reasons)
         for line in lines:
             parts = [x.strip() for x in line.split(",")]
-            if len(parts) < 9:
+            if len(parts) < 10:
                 continue
             try:
-                sm.append(float(parts[1]))
-                mx.append(float(parts[2]))
+                sm, mx = float(parts[2]), float(parts[3])
             except ValueError:
                 continue
-            for nm, v in zip(names, parts[5:9]):
-                if v.lower().startswith("active"):
-                    reasons.add(nm)
-        if not sm:
+            try:
+                ts = datetime.datetime.strptime(parts[0], "%Y/%m/%d %H:%M:%S.%f")
+            except ValueError:
+                ts = None  # counted only when no sample can be placed in the region
+            act = {nm for nm, v in zip(names, parts[6:10]) if v.lower().startswith("active")}
+            samples.append((ts, sm, mx, act))
+        if not samples:
             return None
-        return {"sm_mhz": float(np.median(sm)), "sm_max_mhz": float(max(mx)),
-                "reasons": sorted(reasons), "samples": len(sm)}
+        inside = [x for x in samples if x[0] is not None and self.t0 is not None
+                  and self.t1 is not None and self.t0 <= x[0] <= self.t1]
+        use = inside or samples
+        return {"sm_mhz": float(np.median([x[1] for x in use])),
+                "sm_max_mhz": float(max(x[2] for x in use)),
+                "reasons": sorted(set().union(*(x[3] for x in use))),
+                "samples": len(use), "in_timed_region": bool(inside),
+                "interval_ms": self.INTERVAL_MS}
 
 
 # ------------------------------------------------------------ CPU oracle ---
@@ -441,6 +466,7 @@ def run_ours(args, cfg):
     with ClockSampler(dev.index) as clk:
         barrier()
         torch.cuda.synchronize(dev)
+        clk.begin()
         t_start.record(stream)
         for i in range(args.steps):
             step()
@@ -451,6 +477,7 @@ def run_ours(args, cfg):
         for i in range(args.steps):
             step(recs[i])
         torch.cuda.synchronize(dev)
+        clk.end()
     total_ms = t_start.elapsed_time(t_end)
     for r in recs:
         per_call["heads"].append(r[0].elapsed_time(r[1]))
