@@ -521,9 +521,11 @@ def test_posterior_many_sequences_one_workspace(dev):
 
 @pytest.mark.parametrize("dtype,V,s,n,temp", [
     ("f32", 1000, (2, 2, 2), 14, 0.7), ("bf16", 1008, (4, 3), 15, 1.0),
-    ("bf16", 32000, (16, 16), 255, 0.7), ("bf16", 8, (2,), 1, 2.0), ("f32", 4, (4, 4), 20, 1.0)])
+    ("bf16", 32000, (16, 16), 255, 0.7), ("bf16", 8, (2,), 1, 2.0), ("f32", 4, (4, 4), 20, 1.0),
+    ("bf16", 1000, (2,) * 8, 255, 1.0), ("f32", 64, (3,) * 8, 100, 0.5)])
 def test_posterior_shapes(dev, dtype, V, s, n, temp):
-    """Small and odd vocabularies, 2..256 rows, temperature != 1."""
+    """Small and odd vocabularies, 2..256 rows, temperature != 1, and the
+    deepest trees (8 heads: paths of 9 nodes)."""
     cfg = synth.tiny().replace(name=f"post{dtype}{V}{n}", dtype=dtype, V=V, s=s, n=n, K=len(s))
     ot = oracle_tree_for(np.random.default_rng(V + n), s, n, 1, (0,))
     ot["tokens"][:, 1:] %= V
@@ -582,6 +584,34 @@ def test_full_step_v7b_chain(dev):
     gp = run_posterior(dev, l16, gt, cfg.K, m.GREEDY)
     op = check_posterior(gp, l16, ot, cfg.K, m.GREEDY, 0.09, 0.3, 1.0)
     assert int(op["accept_len"][0]) >= 4
+
+
+def test_full_step_batch8_chain(dev):
+    """The same chain on 8 independent sequences: ragged prefixes (635 to
+    3990 slots, each cache its own allocation), one planted chain per
+    sequence, typical acceptance."""
+    cfg = synth.batch8()
+    hi, ids, logp = run_heads(cfg, dev)
+    o_ids, _, o_logits, o_logz = oracle_heads_for(cfg, hi)
+    check_topk(ids, logp, o_ids, o_logits, o_logz)
+    root = synth.root_tokens(cfg)
+    gt = run_tree(dev, root, ids, logp, cfg.s, cfg.n, cfg.prefix)
+    ot = oracle.build_tree(root, ids, logp.astype(np.float64), cfg.s, cfg.n,
+                           prefix_len=np.asarray(cfg.prefix))
+    check_tree(gt, ot)
+    ai = synth.attention_inputs(cfg)
+    g = run_attention(dev, ai, gt["anc_mask"], cfg.P_max, cfg.dh)
+    o = oracle_attention_heads(ai, ot["anc_mask"], cfg.dh, [0, 31])
+    check_close(g[..., [0, 31], :], o, "batch8 step")
+    logits = synth.base_logits(cfg)
+    for b in range(cfg.B):
+        sl = slice(b, b + 1)
+        synth.plant_chain(logits[sl], gt["tokens"][sl], gt["parent"][sl], gt["depth"][sl], b % 6,
+                          synth.rng_for(cfg, "plant", b))
+    l16 = synth.cast(logits, "bf16")
+    gp = run_posterior(dev, l16, gt, cfg.K, m.TYPICAL, cfg.eps, cfg.delta)
+    op = check_posterior(gp, l16, ot, cfg.K, m.TYPICAL, cfg.eps, cfg.delta, 1.0)
+    assert (op["accept_len"] >= np.minimum(np.arange(cfg.B) % 6, gt["depth"].max(1))).all()
 
 
 # ---------------------------------------------------- device-side checks ---
