@@ -73,10 +73,10 @@ struct AttnArgs {
 // a sequence are its cache slots 0 .. P+R-1, prefix and tree alike (they are
 // contiguous); a key range is `cps` consecutive sub-chunks of 64 keys.  K and
 // V of the sub-chunks stream through a three-stage cp.async ring in shared
-// memory (two sub-chunks in flight while one computes), issued by warps 1-7
-// so that the thread issuing the MMAs goes from the S MMA to its softmax
-// rows; the next stage is issued while the S MMA runs.  Q, S, P and O live in
-// tensor memory:
+// memory (two sub-chunks in flight while one computes); every thread copies
+// four 16-byte chunks of K and of V per stage at a fixed column (constant
+// steps, no per-chunk index arithmetic), and the next stage is issued while
+// the S MMA runs.  Q, S, P and O live in tensor memory:
 //     columns [0, 64)        S = Q K_j^T (fp32), then P over it (bf16 pairs)
 //     columns [64, 64+DH/2)  Q (bf16 pairs, one query row per lane)
 //     columns [128, 128+DH)  O += P V_j (fp32)
@@ -115,20 +115,28 @@ struct TcSmem {
 };
 
 // Issue the cp.async copies of sub-chunk keys [k0, k0+kTcSub) (rows past kend
-// are zero-filled) into one stage; every thread commits one group.
+// are zero-filled) into one stage; every thread commits one group.  Thread t
+// owns 16-byte column t % CPR of key rows t / CPR + RPP * u: rows RPP apart
+// (a multiple of 8) share the 128-byte swizzle phase, so each further chunk
+// is a constant step in both shared and global memory.
 template <int DH>
 __device__ __forceinline__ void tc_load_stage(unsigned char *k_s, unsigned char *v_s,
                                               const bf16 *kc, const bf16 *vc, int k0, int kend,
                                               int H, int h, int tid) {
-    constexpr int CPR = (DH / 64) * 8;  // 16-byte chunks per key row
-    // warp 0 holds the thread that issues the MMAs: warps 1-7 copy, so that
-    // thread goes from its MMA issue straight to its softmax rows
-    for (int i = tid - kWarp; i >= 0 && i < kTcSub * CPR; i += 256 - kWarp) {
-        const int r = i / CPR, c16 = i - r * CPR;
-        const int key = k0 + r;
-        const bool ok = key < kend;
-        const size_t off = ((size_t)(ok ? key : k0) * H + h) * DH + c16 * 8;
-        const uint32_t so = (c16 >> 3) * kTcSub * 128 + tc::sw128(r, c16 & 7);
+    constexpr int CPR = (DH / 64) * 8;    // 16-byte chunks per key row
+    constexpr int RPP = 256 / CPR;        // key rows covered by one pass of the CTA
+    constexpr int PASSES = kTcSub / RPP;
+    static_assert(RPP % 8 == 0 && kTcSub % RPP == 0, "passes keep the swizzle phase");
+    const int c16 = tid % CPR, r0 = tid / CPR;
+    const uint32_t so0 = (c16 >> 3) * kTcSub * 128 + tc::sw128(r0, c16 & 7);
+    const size_t row_elems = (size_t)H * DH;
+    const size_t off0 = ((size_t)k0 * H + h) * DH + c16 * 8;  // key k0: always in range
+#pragma unroll
+    for (int u = 0; u < PASSES; ++u) {
+        const int r = r0 + u * RPP;
+        const bool ok = k0 + r < kend;
+        const size_t off = ok ? off0 + (size_t)r * row_elems : off0;
+        const uint32_t so = so0 + u * RPP * 128;
         cp_async16(tc::smem_addr(k_s + so), kc + off, ok ? 16 : 0);
         cp_async16(tc::smem_addr(v_s + so), vc + off, ok ? 16 : 0);
     }
