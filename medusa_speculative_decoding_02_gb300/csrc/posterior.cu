@@ -244,6 +244,23 @@ posterior_select_kernel(const T *__restrict__ logits, const int32_t *__restrict_
                         int32_t *__restrict__ accept_len, int32_t *__restrict__ path,
                         int32_t *__restrict__ path_tokens, int32_t *__restrict__ next_token,
                         int32_t *__restrict__ accept_out, CommitArgs ca, int *status) {
+    const int b = blockIdx.x;
+    const int i = threadIdx.x;
+    // The one predecessor of this kernel that can still be running is the
+    // rows kernel, and it writes only the row slices: the tree arrays and the
+    // logits were complete before it passed its own launch wait, so they are
+    // read before ours (the node's entries and, for typical acceptance, its
+    // token's logit in its parent's row); the slices are read after it.
+    int par = -1, dep = 0, tk = 0;
+    float y_tok = 0.f;
+    if (i < R) {
+        const size_t o = (size_t)b * R + i;
+        par = parent[o];
+        dep = depth[o];
+        tk = tokens[o];
+        if (typical && i > 0 && par >= 0 && par < i && tk >= 0 && tk < V)
+            y_tok = Vec16<T>::load1(logits + ((size_t)b * R + par) * V + tk);
+    }
     pdl_enter();
     __shared__ int s_acc[MEDUSA_MAX_TREE_ROWS];
     __shared__ int s_chain[MEDUSA_MAX_TREE_ROWS];
@@ -254,19 +271,16 @@ posterior_select_kernel(const T *__restrict__ logits, const int32_t *__restrict_
     __shared__ int s_L, s_best;
     __shared__ int s_path[MEDUSA_MAX_HEADS + 1];
     __shared__ int s_code;
-    const int b = blockIdx.x;
-    const int i = threadIdx.x;
     if (i == 0) {
         s_L = 0;
         s_best = INT_MAX;
     }
     if (i < R) {
-        const size_t o = (size_t)b * R + i;
-        s_par[i] = parent[o];
-        s_dep[i] = depth[o];
-        s_tok[i] = tokens[o];
+        s_par[i] = par;
+        s_dep[i] = dep;
+        s_tok[i] = tk;
         s_chain[i] = (i == 0);
-        if (i == 0 && (s_dep[0] != 0 || s_par[0] != -1)) {
+        if (i == 0 && (dep != 0 || par != -1)) {
             set_status(status, MEDUSA_DEV_BAD_DEPTH);
             s_dep[0] = 0;
             s_par[0] = -1;
@@ -305,7 +319,7 @@ posterior_select_kernel(const T *__restrict__ logits, const int32_t *__restrict_
                 if (!typical) {
                     acc = (tok == arg);
                 } else {
-                    const float y = Vec16<T>::load1(logits + ((size_t)b * R + p) * V + tok) * y_scale;
+                    const float y = y_tok * y_scale;  // loaded before the launch wait
                     const float lp2 = y - m2 - log2s;
                     const float thr2 = fminf(log2_eps, log2_delta - H * kLog2e);
                     acc = lp2 > thr2;
