@@ -128,6 +128,20 @@ spec_sample_kernel(const T *__restrict__ logits, const int32_t *__restrict__ tok
                    uint64_t step, const float2 *__restrict__ parts, int ns_stats,
                    SpecPick *__restrict__ picks, int32_t *__restrict__ acc_out,
                    int32_t *__restrict__ L_out, int *status) {
+    // The predecessor that can still be running, spec_stats_kernel, writes
+    // only the row normalisers: thread k's draft token, its raw p and q
+    // logits and its uniform are read before the launch wait.
+    const int tid0 = threadIdx.x, b0 = blockIdx.y;
+    int x_k = -1;
+    float lp_raw = 0.f, lq_raw = 0.f, u_k = 1.f;
+    if (tid0 >= 1 && tid0 <= K) {
+        x_k = tokens[(size_t)b0 * (K + 1) + tid0];
+        if (x_k >= 0 && x_k < V) {
+            lp_raw = load_elt(logits + ((size_t)b0 * (K + 1) + (tid0 - 1)) * V, x_k);
+            lq_raw = draft[((size_t)b0 * K + (tid0 - 1)) * V + x_k];
+            u_k = uniform_at(seed, step, kRngAccept, b0, tid0, 0);
+        }
+    }
     pdl_enter();
     __shared__ float s_lz[2 * MEDUSA_MAX_HEADS + 1];
     __shared__ int s_rej[MEDUSA_MAX_HEADS + 1];
@@ -147,16 +161,13 @@ spec_sample_kernel(const T *__restrict__ logits, const int32_t *__restrict__ tok
     // acceptance decisions: thread k (1..K) judges draft k; rejected -> 1
     if (tid >= 1 && tid <= K) {
         const int k = tid;
-        const int x = tokens[(size_t)b * (K + 1) + k];
         int rej = 1;
-        if (x < 0 || x >= V) {
+        if (x_k < 0 || x_k >= V) {
             set_status(status, MEDUSA_DEV_BAD_TOKEN);
         } else {
-            const float lp = load_elt(logits + ((size_t)b * (K + 1) + (k - 1)) * V, x) * inv_T -
-                             s_lz[k - 1];
-            const float lq = draft[((size_t)b * K + (k - 1)) * V + x] * inv_T - s_lz[K + k];
-            const float u = uniform_at(seed, step, kRngAccept, b, k, 0);
-            rej = !(lp - lq - logf(u) > 0.f);
+            const float lp = lp_raw * inv_T - s_lz[k - 1];
+            const float lq = lq_raw * inv_T - s_lz[K + k];
+            rej = !(lp - lq - logf(u_k) > 0.f);
         }
         s_rej[k] = rej;
     }
@@ -241,8 +252,12 @@ __global__ void __launch_bounds__(32)
 spec_select_kernel(const int32_t *__restrict__ tokens, const SpecPick *__restrict__ picks,
                    const int32_t *__restrict__ L_in, int K, int ns, int32_t *__restrict__ accept_len,
                    int32_t *__restrict__ path_tokens, int32_t *__restrict__ next_token) {
-    pdl_enter();
     const int b = blockIdx.x, lane = threadIdx.x;
+    // the chain's tokens come from before spec_sample_kernel (the one
+    // predecessor that can still be running), so they load before the wait;
+    // lanes 0..K hold them (K <= 8 < 32)
+    const int tok_q = lane <= K ? tokens[(size_t)b * (K + 1) + lane] : -1;
+    pdl_enter();
     float bk = -INFINITY, bkp = -INFINITY;
     int bi = INT_MAX, bip = INT_MAX;
     for (int j = lane; j < ns; j += 32) {
@@ -265,8 +280,7 @@ spec_select_kernel(const int32_t *__restrict__ tokens, const SpecPick *__restric
         const int nt = (L < K && bi != INT_MAX) ? bi : bip;
         next_token[b] = nt == INT_MAX ? 0 : nt;
     }
-    for (int q = lane; q <= K; q += 32)
-        path_tokens[(size_t)b * (K + 1) + q] = q <= L ? tokens[(size_t)b * (K + 1) + q] : -1;
+    if (lane <= K) path_tokens[(size_t)b * (K + 1) + lane] = lane <= L ? tok_q : -1;
 }
 
 size_t align256(size_t x) { return (x + 255) & ~size_t(255); }
