@@ -253,6 +253,14 @@ posterior_select_kernel(const T *__restrict__ logits, const int32_t *__restrict_
     // token's logit in its parent's row); the slices are read after it.
     int par = -1, dep = 0, tk = 0;
     float y_tok = 0.f;
+    // the commit's cache pointers and prefix length (caller inputs as well)
+    void *kc = nullptr, *vc = nullptr;
+    int P = 0;
+    if (ca.k_cache) {
+        kc = ca.k_cache[b];
+        vc = ca.v_cache[b];
+        P = ca.prefix_len[b];
+    }
     if (i < R) {
         const size_t o = (size_t)b * R + i;
         par = parent[o];
@@ -362,9 +370,6 @@ posterior_select_kernel(const T *__restrict__ logits, const int32_t *__restrict_
     if (!ca.k_cache) return;  // uniform over the CTA
     // commit of the accepted path into the KV cache (medusa_commit_kv)
     __syncthreads();
-    void *kc = ca.k_cache[b];
-    void *vc = ca.v_cache[b];
-    const int P = ca.prefix_len[b];
     if (i == 0) {
         s_code = commit_check(kc, vc, P, s_path, s_L, K, R);
         if (s_code != MEDUSA_DEV_OK) set_status(status, s_code);
