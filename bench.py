@@ -1,20 +1,23 @@
-"""Benchmark one Medusa decoding step on synthetic Vicuna-7B-shaped inputs.
+"""Benchmark one Medusa decoding step on synthetic Vicuna-7B/13B-shaped inputs.
 
     python bench.py [--gpus N] [--steps K] [--warmup W] [--impl ours|reference]
 
 A step is one pass of the whole hot path on one batch of input:
     medusa_heads -> medusa_build_tree -> medusa_tree_attention -> medusa_evaluate_posterior
-at the 7B shape, batch 1 (d=4096, V=32000, K=5 heads, s=(4,3,2,2,1) cut to 64
-nodes, 32 x 128 attention heads, prefix 1024, typical acceptance eps=0.09,
-delta=0.3).  Inputs are seeded random values of those shapes.
+The headline workload is the 7B shape at batch 1 (d=4096, V=32000, K=5 heads,
+s=(4,3,2,2,1) cut to 64 nodes, 32 x 128 attention heads, prefix 1024, typical
+acceptance eps=0.09, delta=0.3).  The same step is also timed on the 13B shape
+(d=5120, 40 attention heads, prefix 4096) and on a ragged batch of 8 sequences
+at the 7B shape (prefixes 256..4096), each reported per call beside the
+headline.  Inputs are seeded random values of those shapes.
 
 The metric is the step's achieved HBM bandwidth: algorithmic bytes of the step
 (every weight, cache and logits byte the method must read once, plus its
 outputs) divided by the device time of the step; the step time in microseconds
 is reported beside it.  One JSON line goes to stdout.
 
-Multi-GPU: the step does not shard (one sequence, one GPU); with N > 1 every
-rank runs an independent replica and rank 0 reports the aggregate.
+Multi-GPU: the step does not shard (one sequence batch, one GPU); with N > 1
+every rank runs an independent replica and rank 0 reports the aggregate.
 
 --impl reference times the float64 CPU oracle (the only other implementation
 of this method here) on a bounded sample of the same workload.
@@ -43,6 +46,7 @@ L2_BYTES = 129 * 1024 * 1024  # GB300 L2
 
 METRIC = "Medusa step µs and achieved HBM GB/s (heads+tree attn+posterior), 7B shape, bs1"
 UNIT = "GB/s"
+CLOCK_WINDOW_S = 0.6  # the headline's timed steps continue this long for the clock record
 
 
 # ------------------------------------------------------------ accounting ---
@@ -62,6 +66,11 @@ def step_bytes(cfg: synth.StepConfig, heads_frac: float = 1.0, attn_heads=None) 
     post = B * R * V * e + B * R * 12 + B * (2 + 2 * (K + 1)) * 4
     return dict(heads=heads, tree=tree, attention=attn, posterior=post,
                 total=heads + tree + attn + post)
+
+
+def heads_flops(cfg: synth.StepConfig) -> float:
+    """Multiply-adds of the heads' two GEMVs (x2 flops each)."""
+    return 2.0 * cfg.B * cfg.K * (cfg.d * cfg.d + cfg.V * cfg.d)
 
 
 def measured_peaks() -> tuple[dict, str]:
@@ -191,6 +200,50 @@ def oracle_step(cfg, inp, heads_sample=None, attn_heads=None):
     return time.perf_counter() - t0
 
 
+def host_cores() -> int:
+    try:
+        return len(os.sched_getaffinity(0))
+    except AttributeError:
+        return os.cpu_count() or 1
+
+
+def cpu_baseline(cfg, inp, nb_total: float, budget_s: float = 10.0) -> dict:
+    """The oracle on the full step: single-threaded (the parity build, as it
+    stands) and on every host core (its OpenMP build, same bits).  Each leg
+    runs whole steps until about budget_s / 2 of host time has passed."""
+    import oracle
+    oracle.build()
+
+    def leg():
+        secs = []
+        tb = time.perf_counter()
+        while True:
+            secs.append(oracle_step(cfg, inp))
+            if time.perf_counter() - tb > budget_s / 2 or len(secs) >= 5:
+                return secs
+
+    oracle.set_parallel(False)
+    one = leg()
+    out = {"value": round(nb_total / float(np.mean(one)) / 1e9, 4), "unit": UNIT, "cores": 1,
+           "kind": "oracle",
+           "sample": f"{len(one)} full oracle steps of the same workload (single-threaded "
+                     f"float64 C), mean {float(np.mean(one)):.2f} s per step"}
+    cores = host_cores()
+    if oracle.parallel_available() and cores > 1:
+        oracle.set_parallel(True)
+        try:
+            cores = oracle.threads()
+            allc = leg()
+        finally:
+            oracle.set_parallel(False)
+        out["all_cores"] = {
+            "value": round(nb_total / float(np.mean(allc)) / 1e9, 4), "unit": UNIT,
+            "cores": cores, "kind": "oracle (OpenMP build, same bits)",
+            "sample": f"{len(allc)} full oracle steps on {cores} threads, mean "
+                      f"{float(np.mean(allc)):.2f} s per step"}
+    return out
+
+
 def make_inputs(cfg):
     hi = synth.heads_inputs(cfg)
     root = synth.root_tokens(cfg)
@@ -206,13 +259,177 @@ def plant_on(inp, cfg, tree_np):
     inp["logits"] = synth.cast(lg, cfg.dtype)
 
 
-def scan_sizes(m, dev, T, timed_loop) -> dict:
-    """Tree attention and the posterior alone on larger workloads than the bs1
-    step (ragged batch of 8, prefix 8192), where their bytes, not the launch
-    latency, set the time.  Trees come from seeded random top-s tables."""
+# ------------------------------------------------------------------ step ---
+
+CALLS = ("heads", "tree", "attention", "posterior")
+
+
+class StepRunner:
+    """Device-resident inputs, outputs and workspace of one decoding step on
+    one workload, and the step itself: the four public calls on one stream.
+
+    The verification logits carry one planted accepted chain (length 3) on
+    the tree this step's heads produce."""
+
+    def __init__(self, m, cfg, dev, T):
+        import torch
+        self.m, self.cfg, self.dev = m, cfg, dev
+        self.inp = inp = make_inputs(cfg)
+        hi = inp["heads"]
+        self.W1, self.b1, self.W2 = T(hi.W1), T(hi.b1), T(hi.W2)
+        B, K, S, R, n, d = cfg.B, cfg.K, cfg.top_s, cfg.R, cfg.n, cfg.d
+        # h and the root share one device buffer, so that a step's first
+        # inputs arrive in one copy
+        h_bytes = B * d * 2
+        self.start = torch.empty(h_bytes + 16 * ((B * 4 + 15) // 16), dtype=torch.uint8,
+                                 device=dev)
+        self.h = self.start[:h_bytes].view(torch.bfloat16).view(B, d)
+        self.root = self.start[h_bytes:h_bytes + B * 4].view(torch.int32)
+        self.h.copy_(T(hi.h))
+        self.root.copy_(T(inp["root"]))
+        ai = inp["attn"]
+        self.q = T(ai.q)
+        self.kc = [T(x) for x in ai.k_cache]
+        self.vc = [T(x) for x in ai.v_cache]
+        self.kptr, self.vptr = m.cache_pointers(self.kc, dev), m.cache_pointers(self.vc, dev)
+        self.prefix = T(ai.prefix_len)
+        ws_bytes = max(m.heads_workspace_size(B, K, d, cfg.V, S),
+                       m.build_tree_workspace_size(B, K, S, n),
+                       m.tree_attention_workspace_size(m.BF16, B, R, cfg.H, cfg.dh, cfg.P_max),
+                       m.posterior_workspace_size(B, R))
+        self.ws = m.new_workspace(ws_bytes, dev)
+        self.ids = torch.empty((B, K, S), dtype=torch.int32, device=dev)
+        self.logp = torch.empty((B, K, S), dtype=torch.float32, device=dev)
+        self.tree = m.Tree.empty(B, n, K, dev)
+        self.out = torch.empty_like(self.q)
+        # the posterior's results share one device buffer (one copy back per step)
+        quad = lambda x: (x + 3) // 4 * 4  # int32 slots, 16-byte aligned pieces
+        res_sizes = (B, B * (K + 1), B * (K + 1), B)
+        self.results = torch.zeros(sum(quad(x) for x in res_sizes), dtype=torch.int32,
+                                   device=dev)
+        views, o = [], 0
+        for x in res_sizes:
+            views.append(self.results[o:o + x])
+            o += quad(x)
+        self.post = m.Posterior(views[0], views[1].view(B, K + 1), views[2].view(B, K + 1),
+                                views[3], None)
+        self.stream = torch.cuda.current_stream(dev)
+        m.heads(self.h, self.W1, self.b1, self.W2, S, ws=self.ws, out=(self.ids, self.logp))
+        m.build_tree(self.root, self.ids, self.logp, cfg.s, n, prefix_len=self.prefix,
+                     ws=self.ws, out=self.tree)
+        tnp = {k: getattr(self.tree, k).cpu().numpy() for k in ("tokens", "parent", "depth")}
+        plant_on(inp, cfg, tnp)
+        self.logits = T(inp["logits"])
+        self.mode = m.TYPICAL if cfg.mode == "typical" else m.GREEDY
+        self.nb = step_bytes(cfg)
+
+    def step(self, record=None, before_attention=None):
+        m, cfg = self.m, self.cfg
+        if record is not None:
+            record[0].record(self.stream)
+        m.heads(self.h, self.W1, self.b1, self.W2, cfg.top_s, ws=self.ws,
+                out=(self.ids, self.logp))
+        if record is not None:
+            record[1].record(self.stream)
+        m.build_tree(self.root, self.ids, self.logp, cfg.s, cfg.n, prefix_len=self.prefix,
+                     ws=self.ws, out=self.tree)
+        if record is not None:
+            record[2].record(self.stream)
+        if before_attention is not None:
+            before_attention()
+        m.tree_attention(self.q, self.kptr, self.vptr, self.prefix, cfg.P_max,
+                         self.tree.anc_mask, out=self.out, ws=self.ws)
+        if record is not None:
+            record[3].record(self.stream)
+        m.evaluate_posterior(self.logits, self.tree.tokens, self.tree.parent, self.tree.depth,
+                             cfg.K, self.mode, cfg.eps, cfg.delta, cfg.temperature, ws=self.ws,
+                             out=self.post)
+        if record is not None:
+            record[4].record(self.stream)
+
+    def check_status(self, where: str):
+        if self.m.read_device_status(self.ws) != 0:
+            raise RuntimeError(f"device status set {where} ({self.cfg.name})")
+
+    def warm(self, steps: int) -> float:
+        """Untimed warm-up steps; returns a rough device time per step (s)."""
+        import torch
+        a, z = torch.cuda.Event(enable_timing=True), torch.cuda.Event(enable_timing=True)
+        a.record(self.stream)
+        for _ in range(steps):
+            self.step()
+        z.record(self.stream)
+        torch.cuda.synchronize(self.dev)
+        self.check_status("during warm-up")
+        return a.elapsed_time(z) * 1e-3 / max(steps, 1)
+
+    def per_call(self, steps: int) -> dict:
+        """Region 2: the same steps with an event around every call (an event
+        between calls cuts the programmatic-dependent-launch overlap of
+        consecutive kernels, so the calls' sum exceeds the step)."""
+        import torch
+        recs = [[torch.cuda.Event(enable_timing=True) for _ in range(5)] for _ in range(steps)]
+        for i in range(steps):
+            self.step(recs[i])
+        torch.cuda.synchronize(self.dev)
+        return {c: [r[j].elapsed_time(r[j + 1]) for r in recs] for j, c in enumerate(CALLS)}
+
+    def stages(self, per_call: dict, peak_gbs: float) -> dict:
+        out = {}
+        for k, v in per_call.items():
+            ms = float(np.mean(v))
+            gbs = self.nb[k] / (ms * 1e-3) / 1e9
+            out[k] = {"us": round(ms * 1e3, 2), "us_median": round(float(np.median(v)) * 1e3, 2),
+                      "us_p10": round(float(np.percentile(v, 10)) * 1e3, 2),
+                      "us_p90": round(float(np.percentile(v, 90)) * 1e3, 2),
+                      "bytes": int(self.nb[k]), "GB/s": round(gbs, 1),
+                      "frac_hbm": round(gbs / peak_gbs, 4)}
+        hms = float(np.mean(per_call["heads"]))
+        out["heads"]["TFLOP/s"] = round(heads_flops(self.cfg) / (hms * 1e-3) / 1e12, 2)
+        return out
+
+
+def time_side_step(m, cfg, dev, T, steps: int, warmup: int, peak_gbs: float) -> dict:
+    """The whole step on another workload (13B shape, batch of 8), timed like
+    the headline: events at the two ends of `steps` steps, then per call."""
+    import torch
+    r = StepRunner(m, cfg, dev, T)
+    r.warm(warmup)
+    a, z = torch.cuda.Event(enable_timing=True), torch.cuda.Event(enable_timing=True)
+    a.record(r.stream)
+    for _ in range(steps):
+        r.step()
+    z.record(r.stream)
+    torch.cuda.synchronize(dev)
+    ms = a.elapsed_time(z) / steps
+    pc = r.per_call(steps)
+    r.check_status("in the timed steps")
+    gbs = r.nb["total"] / (ms * 1e-3) / 1e9
+    out = {"workload": cfg.name, "B": cfg.B, "d": cfg.d, "V": cfg.V, "K": cfg.K,
+           "attn_heads": cfg.H, "head_dim": cfg.dh, "prefix": list(cfg.prefix),
+           "tree_nodes": cfg.n, "accept": cfg.mode, "steps": steps,
+           "us_per_step": round(ms * 1e3, 2), "bytes_per_step": int(r.nb["total"]),
+           "GB/s": round(gbs, 1), "frac_hbm": round(gbs / peak_gbs, 4),
+           "stages": r.stages(pc, peak_gbs)}
+    del r
+    torch.cuda.empty_cache()
+    return out
+
+
+# ------------------------------------------------------------- size scan ---
+
+def scan_sizes(m, dev, T, timed_loop, peak_gbs: float) -> dict:
+    """Tree attention and the posterior alone over the tree-size x context
+    sweep (n in {16,32,64,128} x prefix in {512,2048,8192}, greedy and
+    typical) and on the ragged batch of 8, where their bytes, not the launch
+    latency, set the time.  Trees come from seeded random top-s tables.
+    Consecutive calls rotate through enough input copies that none finds its
+    inputs in L2."""
     import torch
     out = {"attention": [], "posterior": []}
-    for cfg in (synth.batch8(), synth.sweep(64, 8192), synth.sweep(128, 8192)):
+    cfgs = [synth.batch8()] + [synth.sweep(n, P) for n in synth.SWEEP_N for P in synth.SWEEP_P]
+    post_done = set()
+    for cfg in cfgs:
         rng = np.random.default_rng(cfg.seed)
         B, K, S = cfg.B, cfg.K, cfg.top_s
         ids = np.stack([np.stack([rng.choice(cfg.V, size=S, replace=False) for _ in range(K)])
@@ -223,12 +440,14 @@ def scan_sizes(m, dev, T, timed_loop) -> dict:
         tree = m.build_tree(T(np.arange(B, dtype=np.int32)), T(ids), T(logp), cfg.s, cfg.n,
                             prefix_len=prefix)
         nb = step_bytes(cfg)
-        # enough copies that consecutive calls never find their inputs in L2
         copies = max(2, int(np.ceil(2 * L2_BYTES / nb["attention"])))
-        sets = [synth.attention_inputs(cfg, rep=r) for r in range(copies)]
-        q = T(sets[0].q)
-        kc = [[T(x) for x in a.k_cache] for a in sets]
-        vc = [[T(x) for x in a.v_cache] for a in sets]
+        a0 = synth.attention_inputs(cfg)
+        q = T(a0.q)
+        k0 = [T(x) for x in a0.k_cache]
+        v0 = [T(x) for x in a0.v_cache]
+        # the other copies are rotations of the first (still N(0,1) values)
+        kc = [k0] + [[x.roll(r, dims=0).contiguous() for x in k0] for r in range(1, copies)]
+        vc = [v0] + [[x.roll(r, dims=0).contiguous() for x in v0] for r in range(1, copies)]
         ptrs = [(m.cache_pointers(k, dev), m.cache_pointers(v, dev)) for k, v in zip(kc, vc)]
         ws = m.new_workspace(max(
             m.tree_attention_workspace_size(m.BF16, B, cfg.R, cfg.H, cfg.dh, cfg.P_max),
@@ -246,34 +465,41 @@ def scan_sizes(m, dev, T, timed_loop) -> dict:
         # the ancestors-or-self of each node
         depth = tree.depth.cpu().numpy()
         flops = 4.0 * cfg.H * cfg.dh * (cfg.R * sum(cfg.prefix) + float((depth + 1).sum()))
-        out["attention"].append({"config": cfg.name, "B": B, "prefix": list(cfg.prefix),
-                                 "tree_rows": cfg.R, "us": round(us, 2),
-                                 "bytes": int(nb["attention"]),
-                                 "GB/s": round(nb["attention"] / (us * 1e-6) / 1e9, 1),
-                                 "TFLOP/s": round(flops / (us * 1e-6) / 1e12, 1)})
-        if B > 1:
+        gbs = nb["attention"] / (us * 1e-6) / 1e9
+        out["attention"].append({"config": cfg.name.replace("_greedy", ""), "B": B,
+                                 "prefix": list(cfg.prefix), "tree_rows": cfg.R,
+                                 "us": round(us, 2), "bytes": int(nb["attention"]),
+                                 "GB/s": round(gbs, 1), "frac_hbm": round(gbs / peak_gbs, 4),
+                                 "TFLOP/s": round(flops / (us * 1e-6) / 1e12, 1),
+                                 "input_copies": copies})
+        del kc, vc, ptrs, k0, v0
+        # the posterior depends on the tree (R, B) only, not on the prefix
+        if (B, cfg.R) not in post_done:
+            post_done.add((B, cfg.R))
             lcopies = max(2, int(np.ceil(2 * L2_BYTES / nb["posterior"])))
             lg0 = T(synth.cast(synth.base_logits(cfg), "bf16"))
             logits = [lg0] + [lg0.roll(r, dims=-1).contiguous() for r in range(1, lcopies)]
             post = m.Posterior.empty(B, cfg.R, K, dev, with_accept=False)
+            for mode, mname in ((m.GREEDY, "greedy"), (m.TYPICAL, "typical")):
+                def posterior():
+                    lg = logits[it[0] % lcopies]
+                    it[0] += 1
+                    m.evaluate_posterior(lg, tree.tokens, tree.parent, tree.depth, K, mode,
+                                         ws=ws, out=post)
 
-            def posterior():
-                lg = logits[it[0] % lcopies]
-                it[0] += 1
-                m.evaluate_posterior(lg, tree.tokens, tree.parent, tree.depth, K, m.TYPICAL,
-                                     ws=ws, out=post)
-
-            us = timed_loop(posterior)
-            out["posterior"].append({"config": cfg.name, "B": B, "tree_rows": cfg.R,
-                                     "us": round(us, 2), "bytes": int(nb["posterior"]),
-                                     "GB/s": round(nb["posterior"] / (us * 1e-6) / 1e9, 1)})
+                us = timed_loop(posterior)
+                gbs = nb["posterior"] / (us * 1e-6) / 1e9
+                out["posterior"].append({"config": ("batch8" if B > 1 else f"sweep_n{cfg.n}"),
+                                         "mode": mname, "B": B, "tree_rows": cfg.R,
+                                         "us": round(us, 2), "bytes": int(nb["posterior"]),
+                                         "GB/s": round(gbs, 1),
+                                         "frac_hbm": round(gbs / peak_gbs, 4),
+                                         "input_copies": lcopies})
+            del logits
         if m.read_device_status(ws) != 0:
             raise RuntimeError(f"device status set in the size scan ({cfg.name})")
-        out["attention"][-1]["input_copies"] = copies
-        if B > 1:
-            out["posterior"][-1]["input_copies"] = lcopies
-            del logits
-        del kc, vc, q, o, sets
+        del q, o
+        torch.cuda.empty_cache()
     return out
 
 
@@ -368,6 +594,8 @@ def run_ours(args, cfg):
     torch.cuda.set_device(dev)
     import medusa_speculative_decoding_02_gb300 as m
     m.lib()
+    peaks, peak_src = measured_peaks()
+    peak_gbs = peaks["hbm_gbs"]
 
     def T(a):
         a = np.ascontiguousarray(a)
@@ -375,122 +603,58 @@ def run_ours(args, cfg):
             return torch.from_numpy(a.view(np.int16)).view(torch.bfloat16).to(dev)
         return torch.from_numpy(a).to(dev)
 
-    inp = make_inputs(cfg)
-    hi = inp["heads"]
-    W1, b1, W2 = T(hi.W1), T(hi.b1), T(hi.W2)
-    # h and the root share one device buffer, so that a step's first inputs
-    # arrive in one copy
-    h_bytes = cfg.B * cfg.d * 2
-    start = torch.empty(h_bytes + 16 * ((cfg.B * 4 + 15) // 16), dtype=torch.uint8, device=dev)
-    h = start[:h_bytes].view(torch.bfloat16).view(cfg.B, cfg.d)
-    root = start[h_bytes:h_bytes + cfg.B * 4].view(torch.int32)
-    h.copy_(T(hi.h))
-    root.copy_(T(inp["root"]))
-    ai = inp["attn"]
-    q = T(ai.q)
-    kc = [T(x) for x in ai.k_cache]
-    vc = [T(x) for x in ai.v_cache]
-    kptr, vptr = m.cache_pointers(kc, dev), m.cache_pointers(vc, dev)
-    prefix = T(ai.prefix_len)
-    B, K, S, R, n = cfg.B, cfg.K, cfg.top_s, cfg.R, cfg.n
-    ws_bytes = max(m.heads_workspace_size(B, K, cfg.d, cfg.V, S),
-                   m.build_tree_workspace_size(B, K, S, n),
-                   m.tree_attention_workspace_size(m.BF16, B, R, cfg.H, cfg.dh, cfg.P_max),
-                   m.posterior_workspace_size(B, R))
-    ws = m.new_workspace(ws_bytes, dev)
-    ids = torch.empty((B, K, S), dtype=torch.int32, device=dev)
-    logp = torch.empty((B, K, S), dtype=torch.float32, device=dev)
-    tree = m.Tree.empty(B, n, K, dev)
-    out = torch.empty_like(q)
-    # the posterior's results share one device buffer (one copy back per step)
-    quad = lambda n: (n + 3) // 4 * 4  # int32 slots, 16-byte aligned pieces
-    res_sizes = (B, B * (K + 1), B * (K + 1), B)
-    results = torch.zeros(sum(quad(x) for x in res_sizes), dtype=torch.int32, device=dev)
-    res_views, o = [], 0
-    for x in res_sizes:
-        res_views.append(results[o:o + x])
-        o += quad(x)
-    post = m.Posterior(res_views[0], res_views[1].view(B, K + 1), res_views[2].view(B, K + 1),
-                       res_views[3], None)
-    stream = torch.cuda.current_stream(dev)
-
-    # the verification logits carry one planted chain on this step's tree
-    m.heads(h, W1, b1, W2, S, ws=ws, out=(ids, logp))
-    m.build_tree(root, ids, logp, cfg.s, n, prefix_len=prefix, ws=ws, out=tree)
-    tnp = {k: getattr(tree, k).cpu().numpy() for k in ("tokens", "parent", "depth")}
-    plant_on(inp, cfg, tnp)
-    logits = T(inp["logits"])
-    mode = m.TYPICAL if cfg.mode == "typical" else m.GREEDY
-
-    ev = [torch.cuda.Event(enable_timing=True) for _ in range(5)]
-
-    def step(record=None, before_attention=None):
-        if record is not None:
-            record[0].record(stream)
-        m.heads(h, W1, b1, W2, S, ws=ws, out=(ids, logp))
-        if record is not None:
-            record[1].record(stream)
-        m.build_tree(root, ids, logp, cfg.s, n, prefix_len=prefix, ws=ws, out=tree)
-        if record is not None:
-            record[2].record(stream)
-        if before_attention is not None:
-            before_attention()
-        m.tree_attention(q, kptr, vptr, prefix, cfg.P_max, tree.anc_mask, out=out, ws=ws)
-        if record is not None:
-            record[3].record(stream)
-        m.evaluate_posterior(logits, tree.tokens, tree.parent, tree.depth, K, mode, cfg.eps,
-                             cfg.delta, cfg.temperature, ws=ws, out=post)
-        if record is not None:
-            record[4].record(stream)
-
     def barrier():
         if world > 1:
             import torch.distributed as dist
             dist.barrier()
 
-    for _ in range(args.warmup):
-        step()
-    torch.cuda.synchronize(dev)
-    if m.read_device_status(ws) != 0:
-        raise RuntimeError("device status set during warm-up")
+    run = StepRunner(m, cfg, dev, T)
+    B, K, R = cfg.B, cfg.K, cfg.R
+    stream = run.stream
+    est = run.warm(args.warmup)
+    window_steps = max(0, int(math.ceil(CLOCK_WINDOW_S / max(est, 1e-6))) - args.steps)
 
-    # Region 1: the step as a user runs it, events only at the two ends (an
-    # event between calls would cut the programmatic-dependent-launch overlap
-    # of consecutive kernels).  Region 2: the same steps with an event around
-    # every call, for the per-call breakdown and the heads roofline.
-    per_call = {k: [] for k in ("heads", "tree", "attention", "posterior")}
-    recs = [[torch.cuda.Event(enable_timing=True) for _ in range(5)] for _ in range(args.steps)]
-    t_start = torch.cuda.Event(enable_timing=True)
-    t_end = torch.cuda.Event(enable_timing=True)
+    # Region 1: exactly `steps` steps as a user runs them, events only at the
+    # two ends; `value` and `ms_per_step` come from these.  The same loop then
+    # continues, without a break, for the clock window, so that the clock
+    # samples cover the timed steps; its own rate is reported beside them.
+    # Region 2: the same steps with an event around every call.
+    t_start, t_end, t_win = (torch.cuda.Event(enable_timing=True) for _ in range(3))
     launches0 = m.launch_count()
     with ClockSampler(dev.index) as clk:
         barrier()
         torch.cuda.synchronize(dev)
         clk.begin()
         t_start.record(stream)
-        for i in range(args.steps):
-            step()
+        for _ in range(args.steps):
+            run.step()
         t_end.record(stream)
-        torch.cuda.synchronize(dev)
-        barrier()
         launches = m.launch_count() - launches0
-        for i in range(args.steps):
-            step(recs[i])
+        for _ in range(window_steps):
+            run.step()
+        t_win.record(stream)
         torch.cuda.synchronize(dev)
         clk.end()
+        barrier()
+        per_call = run.per_call(args.steps)
+        run.check_status("in the timed steps")
+        # the same step on the 13B shape and on the ragged batch of 8
+        side = {"v13b_step": time_side_step(m, synth.v13b(), dev, T, args.steps, args.warmup,
+                                            peak_gbs),
+                "batch8_step": time_side_step(m, synth.batch8(), dev, T, args.steps,
+                                              args.warmup, peak_gbs)}
     total_ms = t_start.elapsed_time(t_end)
-    for r in recs:
-        per_call["heads"].append(r[0].elapsed_time(r[1]))
-        per_call["tree"].append(r[1].elapsed_time(r[2]))
-        per_call["attention"].append(r[2].elapsed_time(r[3]))
-        per_call["posterior"].append(r[3].elapsed_time(r[4]))
-    nb = step_bytes(cfg)
+    win_ms = t_start.elapsed_time(t_win)
+    nb = run.nb
     s_step, value = replica_throughput(total_ms / args.steps * 1e-3, nb["total"], dev)
     ms_step = s_step * 1e3
 
-    # ---- Region 3: the KV-cache commit (a row past the step proper), alone
-    # and fused into the posterior, each timed over a loop with events at the
-    # two ends.  The commit moves the accepted path's rows inside the tree
+    # ---- Region 3: rows past the step proper and the size scan, each timed
+    # over a loop with events at the two ends.
+    h, W1, b1, W2, S = run.h, run.W1, run.b1, run.W2, cfg.top_s
+    ws, post, logits, tree = run.ws, run.post, run.logits, run.tree
+    kptr, vptr, prefix, mode = run.kptr, run.vptr, run.prefix, run.mode
+    # The KV-cache commit moves the accepted path's rows inside the tree
     # slots; new_prefix_len goes to its own buffer, so every repetition sees
     # the same prefix.
     new_prefix = torch.empty_like(prefix)
@@ -551,11 +715,12 @@ def run_ours(args, cfg):
         m.heads_lm(h, w_lm, W1, b1, W2, S, ws=ws_lm, out=lm_out)
 
     def heads_only():
-        m.heads(h, W1, b1, W2, S, ws=ws, out=(ids, logp))
+        m.heads(h, W1, b1, W2, S, ws=ws, out=(run.ids, run.logp))
 
     us_heads_lm = timed_loop(heads_lm)
     us_heads = timed_loop(heads_only)
     lm_bytes = nb["heads"] + cfg.V * cfg.d * 2 + B * 8
+    del w_lm
 
     # exact speculative sampling: drafts sampled in the heads pass, then the
     # p/q posterior on a chain (verification rows: this step's first K+1 rows)
@@ -576,7 +741,7 @@ def run_ours(args, cfg):
                                 out=spec_out)
 
     heads_sample()
-    chain[:, 0] = root
+    chain[:, 0] = run.root
     chain[:, 1:] = smp_out[0]
     us_heads_sample = timed_loop(heads_sample)
     us_spec = timed_loop(spec_post)
@@ -587,7 +752,7 @@ def run_ours(args, cfg):
     us_commit = timed_loop(commit_only)
     if m.read_device_status(ws) != 0:
         raise RuntimeError("device status set by the commit")
-    size_scan = scan_sizes(m, dev, T, timed_loop)
+    size_scan = scan_sizes(m, dev, T, timed_loop, peak_gbs)
     next_rows = {"commit_kv": {
         "us": round(us_commit, 2), "rows_moved": moved, "bytes": commit_bytes,
         "GB/s": round(commit_bytes / (us_commit * 1e-6) / 1e9, 1),
@@ -603,24 +768,26 @@ def run_ours(args, cfg):
         "heads_lm": {
             "us": round(us_heads_lm, 2), "bytes": int(lm_bytes),
             "GB/s": round(lm_bytes / (us_heads_lm * 1e-6) / 1e9, 1),
-            "frac_hbm": None, "heads_alone_us": round(us_heads, 2),
+            "frac_hbm": round(lm_bytes / (us_heads_lm * 1e-6) / 1e9 / peak_gbs, 4),
+            "heads_alone_us": round(us_heads, 2),
             "note": "LM head (32000 x 4096) + 5 Medusa heads in one weight pass"}}
 
     # ---- end to end through the public API with pinned host buffers
-    host_start = torch.empty(start.numel(), dtype=torch.uint8).pin_memory()
-    host_start.copy_(start.cpu())
+    ai = run.inp["attn"]
+    host_start = torch.empty(run.start.numel(), dtype=torch.uint8).pin_memory()
+    host_start.copy_(run.start.cpu())
+    bf = lambda a: torch.from_numpy(np.ascontiguousarray(a).view(np.int16)).view(torch.bfloat16)
     host_in = {
         "start": host_start,  # h and the root
-        "q": torch.from_numpy(np.ascontiguousarray(ai.q).view(np.int16)).view(torch.bfloat16).pin_memory(),
-        "k_tree": torch.from_numpy(ai.k_cache[0][cfg.prefix[0]:].view(np.int16)).view(torch.bfloat16).pin_memory(),
-        "v_tree": torch.from_numpy(ai.v_cache[0][cfg.prefix[0]:].view(np.int16)).view(torch.bfloat16).pin_memory(),
-        "logits": torch.from_numpy(inp["logits"].view(np.int16)).view(torch.bfloat16).pin_memory(),
+        "q": bf(ai.q).pin_memory(),
+        "k_tree": bf(ai.k_cache[0][cfg.prefix[0]:]).pin_memory(),
+        "v_tree": bf(ai.v_cache[0][cfg.prefix[0]:]).pin_memory(),
+        "logits": bf(run.inp["logits"]).pin_memory(),
     }
-    host_out = {"results": torch.empty(results.shape, dtype=torch.int32).pin_memory()}
+    host_out = {"results": torch.empty(run.results.shape, dtype=torch.int32).pin_memory()}
     h2d = sum(v.numel() * v.element_size() for v in host_in.values())
     d2h = sum(v.numel() * v.element_size() for v in host_out.values())
     P0 = cfg.prefix[0]
-
     copy_stream = torch.cuda.Stream(dev)
 
     def e2e_issue():
@@ -629,14 +796,14 @@ def run_ours(args, cfg):
         # posterior, so they travel on a second stream during the heads pass
         main = torch.cuda.current_stream(dev)
         copy_stream.wait_stream(main)
-        start.copy_(host_in["start"], non_blocking=True)
+        run.start.copy_(host_in["start"], non_blocking=True)
         with torch.cuda.stream(copy_stream):
-            q.copy_(host_in["q"], non_blocking=True)
-            kc[0][P0:].copy_(host_in["k_tree"], non_blocking=True)
-            vc[0][P0:].copy_(host_in["v_tree"], non_blocking=True)
-            logits.copy_(host_in["logits"], non_blocking=True)
-        step(before_attention=lambda: main.wait_stream(copy_stream))
-        host_out["results"].copy_(results, non_blocking=True)
+            run.q.copy_(host_in["q"], non_blocking=True)
+            run.kc[0][P0:].copy_(host_in["k_tree"], non_blocking=True)
+            run.vc[0][P0:].copy_(host_in["v_tree"], non_blocking=True)
+            run.logits.copy_(host_in["logits"], non_blocking=True)
+        run.step(before_attention=lambda: main.wait_stream(copy_stream))
+        host_out["results"].copy_(run.results, non_blocking=True)
 
     def e2e_eager():
         e2e_issue()
@@ -664,6 +831,39 @@ def run_ours(args, cfg):
     eager_s, eager_value = time_e2e(e2e_eager)
     e2e_s, e2e_value = time_e2e(e2e_graph)
 
+    # where the end-to-end time goes: the host call that launches the graph,
+    # the graph's span on the GPU (events on the stream around the launch),
+    # and what is left (launch latency to the GPU plus the host's wait for
+    # the stream); the input copy that gates the first kernel is timed alone
+    ga, gz = torch.cuda.Event(enable_timing=True), torch.cuda.Event(enable_timing=True)
+    launch_us, span_us, wall_us = [], [], []
+    for _ in range(e2e_steps):
+        t0 = time.perf_counter()
+        ga.record(stream)
+        graph.replay()
+        t1 = time.perf_counter()
+        gz.record(stream)
+        stream.synchronize()
+        t2 = time.perf_counter()
+        launch_us.append((t1 - t0) * 1e6)
+        wall_us.append((t2 - t0) * 1e6)
+        span_us.append(ga.elapsed_time(gz) * 1e3)
+
+    def first_copy():
+        run.start.copy_(host_in["start"], non_blocking=True)
+
+    first_copy_us = timed_loop(first_copy)
+    e2e_breakdown = {
+        "wall_us": round(float(np.median(wall_us)), 2),
+        "graph_launch_call_us": round(float(np.median(launch_us)), 2),
+        "gpu_span_us": round(float(np.median(span_us)), 2),
+        "launch_and_sync_us": round(float(np.median(wall_us) - np.median(span_us)), 2),
+        "device_resident_step_us": round(ms_step * 1e3, 2),
+        "copies_and_graph_on_gpu_us": round(float(np.median(span_us)) - ms_step * 1e3, 2),
+        "first_input_copy_us": round(first_copy_us, 2),
+        "first_input_copy_bytes": int(host_start.numel()),
+    }
+
     if world > 1:
         import torch.distributed as dist
         dist.barrier()
@@ -671,12 +871,6 @@ def run_ours(args, cfg):
     if rank != 0:
         return 0
 
-    peaks, peak_src = measured_peaks()
-    for rows in size_scan.values():
-        for r in rows:
-            r["frac_hbm"] = round(r["GB/s"] / peaks["hbm_gbs"], 4)
-    next_rows["heads_lm"]["frac_hbm"] = round(
-        next_rows["heads_lm"]["GB/s"] / peaks["hbm_gbs"], 4)
     heads_ms = float(np.mean(per_call["heads"]))
     achieved = nb["heads"] / (heads_ms * 1e-3) / 1e9
     traffic = None
@@ -686,29 +880,20 @@ def run_ours(args, cfg):
             traffic = json.load(open(tp)).get("bytes_per_launch")
         except Exception:
             traffic = None
-    roofline = {"bound": "hbm", "achieved": round(achieved, 1), "peak": peaks["hbm_gbs"],
-                "unit": "GB/s", "frac": round(achieved / peaks["hbm_gbs"], 4), "traffic": traffic,
+    roofline = {"bound": "hbm", "achieved": round(achieved, 1), "peak": peak_gbs,
+                "unit": "GB/s", "frac": round(achieved / peak_gbs, 4), "traffic": traffic,
                 "kernel": "medusa_heads (heads_w1 + heads_w2 + heads_reduce)",
                 "peak_source": f"hbm_gbs of {peak_src}"}
 
-    # ---- CPU baseline: the oracle on the full step, ~10 s of host work
-    import oracle
-    oracle.build()
-    cpu_secs = []
-    tb = time.perf_counter()
-    while True:
-        cpu_secs.append(oracle_step(cfg, inp))
-        if time.perf_counter() - tb > 10.0 or len(cpu_secs) >= 5:
-            break
-    cpu_value = nb["total"] / float(np.mean(cpu_secs)) / 1e9
+    clocks = clk.summary()
+    if clocks is not None:
+        clocks["window"] = {"steps": args.steps + window_steps,
+                            "seconds": round(win_ms * 1e-3, 3),
+                            "us_per_step": round(win_ms / (args.steps + window_steps) * 1e3, 2),
+                            "note": "the timed steps, continued without a break while the "
+                                    "clocks are sampled"}
+        clocks["step_kcycles"] = round(ms_step * clocks["sm_mhz"], 1)  # ms x MHz = k cycles
 
-    stages = {k: {"us": round(float(np.mean(v)) * 1e3, 2),
-                  "us_median": round(float(np.median(v)) * 1e3, 2),
-                  "us_p10": round(float(np.percentile(v, 10)) * 1e3, 2),
-                  "us_p90": round(float(np.percentile(v, 90)) * 1e3, 2),
-                  "GB/s": round(nb[k] / (float(np.mean(v)) * 1e-3) / 1e9, 1),
-                  "frac_hbm": round(nb[k] / (float(np.mean(v)) * 1e-3) / 1e9 / peaks["hbm_gbs"], 4)}
-              for k, v in per_call.items()}
     line = {
         "metric": METRIC, "value": round(value, 2), "unit": UNIT, "n_gpus": world,
         "steps": args.steps, "warmup": args.warmup, "ms_per_step": round(ms_step, 5),
@@ -716,21 +901,20 @@ def run_ours(args, cfg):
         "scaling": "weak", "vs_baseline": None, "dtype": "bf16",
         "data": "synthetic (seeded, Vicuna-7B shapes: random weights, KV and logits)",
         "config": workload_config(cfg, world),
-        "stages": stages,
+        "stages": run.stages(per_call, peak_gbs),
+        **side,
         "next_rows": next_rows,
         "size_scan": size_scan,
         "roofline": roofline,
-        "cpu_baseline": {"value": round(cpu_value, 4), "unit": UNIT, "cores": 1, "kind": "oracle",
-                         "sample": f"{len(cpu_secs)} full oracle steps of the same workload "
-                                   f"(single-threaded float64 C), mean "
-                                   f"{float(np.mean(cpu_secs)):.2f} s per step"},
+        "cpu_baseline": cpu_baseline(cfg, run.inp, nb["total"]),
         "e2e": {"value": round(e2e_value, 2), "unit": UNIT, "h2d_bytes_per_step": int(h2d),
                 "d2h_bytes_per_step": int(d2h), "us_per_step": round(e2e_s * 1e6, 2),
                 "steps": e2e_steps, "api": "StepGraph.replay (copies + calls in one CUDA graph)",
                 "eager_value": round(eager_value, 2),
-                "eager_us_per_step": round(eager_s * 1e6, 2)},
+                "eager_us_per_step": round(eager_s * 1e6, 2),
+                "breakdown": e2e_breakdown},
         "gpu_launches": int(launches),
-        "clocks": clk.summary(),
+        "clocks": clocks,
     }
     print(json.dumps(line), flush=True)
     return 0

@@ -95,8 +95,14 @@ enum {
     MEDUSA_DEV_TIMEOUT = 6,        /* a bounded wait gave up                  */
     MEDUSA_DEV_BAD_PATH = 7,       /* accept_len outside 0..min(K,R-1), or a
                                       path entry outside [0, R)              */
-    MEDUSA_DEV_BAD_CACHE = 8       /* a cache pointer NULL or not 16-byte
+    MEDUSA_DEV_BAD_CACHE = 8,      /* a cache pointer NULL or not 16-byte
                                       aligned                                 */
+    MEDUSA_DEV_DRAIN_TIMEOUT = 9   /* after a timeout, the drain of the CTA's
+                                      own MMAs also gave up; the tensor memory
+                                      was freed with an MMA possibly still in
+                                      flight, so this call's outputs and later
+                                      tensor-core results on the device are
+                                      suspect.  Overrides an earlier code.    */
 };
 
 /* Limits. */
@@ -122,7 +128,9 @@ MEDUSA_API uint64_t medusa_launch_count(void);
  * polls (each poll blocks for a hardware-defined interval), sets
  * MEDUSA_DEV_TIMEOUT, stops the key loop, drains its MMAs and copies with a
  * fixed limit, frees its tensor memory and publishes an empty key range, so
- * the context stays usable.  Default 65536 polls; the environment variable
+ * the context stays usable.  Freeing assumes an issued MMA finishes within
+ * the drain's limit (2^16 polls, far beyond an MMA's latency); if the drain
+ * gives up too, the status reads MEDUSA_DEV_DRAIN_TIMEOUT instead.  Default 65536 polls; the environment variable
  * MEDUSA_FAULT_WAIT_BUDGET sets the value the library starts with.  A budget
  * of 0 makes every such wait fail at once: it exercises the timeout path
  * without a hung GPU.  Process-wide; affects launches made after the call. */
@@ -205,7 +213,10 @@ MEDUSA_API medusa_status medusa_heads_lm(medusa_dtype dtype, const void *h, cons
  * device looks up the array's device address (cudaGetSymbolAddress) with that
  * device current; make that first call before any stream capture.  All calls
  * share the one array: calls that overlap on the GPU race and must be
- * serialised by the caller.
+ * serialised by the caller.  The looked-up address is kept for the life of
+ * the process, so resetting a device (cudaDeviceReset) or otherwise
+ * re-creating its primary context after the first call is not supported: the
+ * saved address would no longer be valid.
  * ---------------------------------------------------------------------- */
 MEDUSA_API medusa_status medusa_heads_noalloc(medusa_dtype dtype, const void *h,
                                               const void *W1, const void *b1,

@@ -36,7 +36,8 @@ STATUS = {0: "MEDUSA_OK", 1: "MEDUSA_ERR_INVALID_ARG", 2: "MEDUSA_ERR_UNSUPPORTE
           3: "MEDUSA_ERR_WORKSPACE", 4: "MEDUSA_ERR_CUDA", 5: "MEDUSA_ERR_TIMEOUT",
           6: "MEDUSA_ERR_DEVICE_CHECK"}
 DEVICE_STATUS = {0: "ok", 1: "bad token", 2: "bad parent", 3: "bad prefix", 4: "bad score",
-                 5: "bad depth", 6: "timeout", 7: "bad path", 8: "bad cache"}
+                 5: "bad depth", 6: "timeout", 7: "bad path", 8: "bad cache",
+                 9: "drain timeout"}
 
 EXPORTS = ("medusa_status_string", "medusa_last_error", "medusa_launch_count",
            "medusa_wait_budget", "medusa_set_wait_budget",

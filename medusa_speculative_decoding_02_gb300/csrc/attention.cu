@@ -95,7 +95,12 @@ struct AttnArgs {
 // writes one unnormalised partial (O, m, l) per row; tree_attn_combine_kernel
 // merges the ranges.  Every mbarrier wait is bounded; on a timeout the CTA
 // records MEDUSA_DEV_TIMEOUT, stops, waits once more (bounded) for its MMAs
-// and frees its tensor memory before returning.
+// and frees its tensor memory before returning.  Freeing is safe when the
+// drain sees the last commit arrive; an issued MMA takes far less than the
+// drain's 2^16 polls.  If the drain gives up as well, the CTA still frees
+// (holding the columns would stall every later allocation on the SM) and
+// records MEDUSA_DEV_DRAIN_TIMEOUT over any earlier code, so the caller
+// knows the outputs and the tensor memory may be corrupt.
 constexpr int kTcSub = 64;               // keys per pipeline stage
 constexpr int kTcStages = 3;
 constexpr float kRescaleLog2 = 8.f;      // lazy-rescale threshold (log2 units)
@@ -383,15 +388,18 @@ __global__ void __launch_bounds__(256, 2) tree_attn_tc_kernel(AttnArgs a) {
         ++done;
     }
     // ---- wait for the last P V, then write the partial rows
+    bool drain_failed = false;
     if (done > 0 && !tc::mbar_wait_bounded(&bar_o, (done - 1) & 1, kWaitPolls)) {
         failed = 1;
-        tc::mbar_wait_bounded(&bar_o, (done - 1) & 1, kWaitPolls);  // drain before freeing TMEM
+        // drain before freeing TMEM
+        drain_failed = !tc::mbar_wait_bounded(&bar_o, (done - 1) & 1, kWaitPolls);
     }
     cp_async_wait<0>();
     tc::fence_after_sync();
     __syncthreads();
     const bool ok = !failed && done == nsub;  // uniform over the CTA
     if (failed && tid == 0) set_status(a.status, MEDUSA_DEV_TIMEOUT);
+    if (drain_failed && a.status) atomicExch(a.status, MEDUSA_DEV_DRAIN_TIMEOUT);
     if (ok) {
         // this thread's half of the row's DH output columns
         float *dst = a.part_o + (pbase + row) * DH;

@@ -101,6 +101,17 @@ __device__ __forceinline__ bool better(float va, int ia, float vb, int ib) {
 // started and passed the trigger, and it waits for this grid's completion
 // before touching memory; both instructions are no-ops for a kernel launched
 // without the attribute.
+//
+// The order -- wait, then trigger -- is relied on by the kernels that read
+// inputs before their own wait: posterior_select_kernel (tree arrays, the
+// typical-acceptance logits and, with the fused commit, the cache pointers
+// and prefix lengths), spec_sample_kernel and spec_select_kernel
+// (draft tokens, their p and q logits and uniforms; the chain's tokens), and
+// the L2 prefetches of heads_w1/heads_w2 (weights, never written).  Because
+// every kernel of the library waits before it triggers, a kernel that starts
+// early can only overlap its immediate predecessor; all older grids have
+// completed and their writes are visible.  Triggering before the wait in any
+// kernel would turn those early reads into races with the grid before it.
 __device__ __forceinline__ void pdl_enter() {
     asm volatile("griddepcontrol.wait;\n" ::: "memory");
     asm volatile("griddepcontrol.launch_dependents;\n" ::: "memory");

@@ -20,32 +20,64 @@ import numpy as np
 _HERE = os.path.dirname(os.path.abspath(__file__))
 _SRC = os.path.join(_HERE, "oracle.c")
 _LIB = os.path.join(_HERE, "liboracle.so")
+_LIB_OMP = os.path.join(_HERE, "liboracle_omp.so")
 _lock = threading.Lock()
-_lib = None
+_libs = {}
+_parallel = False
 
 F32, BF16 = 0, 1
 GREEDY, TYPICAL = 0, 1
 
+_CFLAGS = ["-O2", "-std=c11", "-ffp-contract=off", "-fno-fast-math", "-Wall",
+           "-Wno-unknown-pragmas", "-shared", "-fPIC"]
+
+
+def _compile(out: str, extra, force: bool) -> None:
+    if force or not os.path.exists(out) or os.path.getmtime(out) < os.path.getmtime(_SRC):
+        tmp = out + f".{os.getpid()}.tmp"
+        subprocess.run(["gcc", *_CFLAGS, *extra, "-o", tmp, _SRC, "-lm"], check=True)
+        os.replace(tmp, out)
+
 
 def build(force: bool = False) -> str:
-    """Compile oracle.c into liboracle.so next to it (plain gcc, no BLAS)."""
-    if force or not os.path.exists(_LIB) or os.path.getmtime(_LIB) < os.path.getmtime(_SRC):
-        tmp = _LIB + f".{os.getpid()}.tmp"
-        subprocess.run(
-            ["gcc", "-O2", "-std=c11", "-ffp-contract=off", "-fno-fast-math",
-             "-Wall", "-shared", "-fPIC", "-o", tmp, _SRC, "-lm"],
-            check=True,
-        )
-        os.replace(tmp, _LIB)
+    """Compile oracle.c into liboracle.so next to it (plain gcc, no BLAS), and
+    into liboracle_omp.so with OpenMP when the compiler supports it."""
+    _compile(_LIB, [], force)
+    try:
+        _compile(_LIB_OMP, ["-fopenmp"], force)
+    except (subprocess.CalledProcessError, OSError):
+        pass  # parallel_available() reports False
     return _LIB
 
 
+def parallel_available() -> bool:
+    """True if the OpenMP build of the oracle exists."""
+    return os.path.exists(_LIB_OMP)
+
+
+def set_parallel(on: bool) -> None:
+    """Route later calls to the OpenMP build (all host cores) or back to the
+    serial build.  The benchmark's all-core CPU baseline turns this on, and so
+    do the parity tests' full-size attention checks, which would otherwise
+    take minutes; every other test uses the serial build.  Both builds give
+    the same bits (tests/test_oracle_parallel.py)."""
+    global _parallel
+    if on and not parallel_available():
+        raise RuntimeError("the OpenMP build of the oracle is not available")
+    _parallel = bool(on)
+
+
+def threads() -> int:
+    """Threads the current build's parallel loops use (1 for the serial build)."""
+    return int(_load().oracle_threads())
+
+
 def _load():
-    global _lib
+    path = _LIB_OMP if _parallel else _LIB
     with _lock:
-        if _lib is None:
+        if path not in _libs:
             build()
-            lib = ctypes.CDLL(_LIB)
+            lib = ctypes.CDLL(path)
             P = ctypes.c_void_p
             I = ctypes.c_int
             D = ctypes.c_double
@@ -73,8 +105,10 @@ def _load():
             lib.oracle_speculative_posterior.restype = I
             lib.oracle_commit_kv.argtypes = [P, P, P, P, P, I, I, ctypes.c_size_t, P]
             lib.oracle_commit_kv.restype = I
-            _lib = lib
-    return _lib
+            lib.oracle_threads.argtypes = []
+            lib.oracle_threads.restype = I
+            _libs[path] = lib
+    return _libs[path]
 
 
 def _ptr(a):

@@ -28,6 +28,14 @@
  * as a whole.  Build with -ffp-contract=off so that x86 and Arm give the same
  * bits.
  *
+ * The file is compiled twice.  liboracle.so is the serial build every parity
+ * test uses.  liboracle_omp.so is the same source with -fopenmp, used only to
+ * time the CPU baseline on all host cores: the `omp parallel for` pragmas
+ * below spread independent output elements (heads' rows, attention heads,
+ * posterior nodes) over threads, and each element is still computed by the
+ * same sequential loop, so both builds give the same bits.  Without -fopenmp
+ * the pragmas are ignored.
+ *
  * Parity status of each function (pins live in tests/test_oracle_pins.py):
  *   oracle_heads              pinned (identity-initialised heads reproduce
  *                             the LM-head softmax; numpy float64 matmul +
@@ -57,6 +65,19 @@
 #include <stdint.h>
 #include <stdlib.h>
 #include <string.h>
+#ifdef _OPENMP
+#include <omp.h>
+#endif
+
+/* Threads the parallel loops use (1 in the serial build). */
+int oracle_threads(void)
+{
+#ifdef _OPENMP
+    return omp_get_max_threads();
+#else
+    return 1;
+#endif
+}
 
 enum { ORC_F32 = 0, ORC_BF16 = 1 };
 enum { ORC_GREEDY = 0, ORC_TYPICAL = 1 };
@@ -105,6 +126,7 @@ int oracle_heads(int dtype, const void *h, const void *W1, const void *b1,
     for (int b = 0; b < B; ++b) {
         for (int k = 0; k < K; ++k) {
             /* residual block: z = h + SiLU(W1 h + b1) */
+#pragma omp parallel for schedule(static)
             for (int j = 0; j < d; ++j) {
                 double u = 0.0;
                 for (int c = 0; c < d; ++c)
@@ -116,6 +138,7 @@ int oracle_heads(int dtype, const void *h, const void *W1, const void *b1,
                 z[j] = rd(dtype, h, (size_t)b * d + j) + silu;
             }
             /* vocabulary projection: logits = W2 z */
+#pragma omp parallel for schedule(static)
             for (int v = 0; v < V; ++v) {
                 double acc = 0.0;
                 for (int c = 0; c < d; ++c)
@@ -180,6 +203,7 @@ int oracle_lm_head(int dtype, const void *h, const void *W_lm, int B, int d,
         return 2;
     }
     for (int b = 0; b < B; ++b) {
+#pragma omp parallel for schedule(static)
         for (int v = 0; v < V; ++v) {
             double acc = 0.0;
             for (int c = 0; c < d; ++c)
@@ -423,9 +447,10 @@ int oracle_tree_attention(int dtype, const void *q, const void *const *k_cache,
     int maxslots = 0;
     for (int b = 0; b < B; ++b)
         if (prefix_len[b] + R > maxslots) maxslots = prefix_len[b] + R;
-    double *sc = (double *)malloc((size_t)maxslots * sizeof(double));
+    /* one score row per attention head, so that heads are independent */
+    double *sc_all = (double *)malloc((size_t)H * maxslots * sizeof(double));
     char *vis = (char *)malloc((size_t)maxslots);
-    if (!sc || !vis) { free(sc); free(vis); return 2; }
+    if (!sc_all || !vis) { free(sc_all); free(vis); return 2; }
     for (int b = 0; b < B; ++b) {
         const int P = prefix_len[b];
         const int nslot = P + R;
@@ -439,7 +464,9 @@ int oracle_tree_attention(int dtype, const void *q, const void *const *k_cache,
                     vis[j] = (char)((row[t / 64] >> (t % 64)) & 1u);
                 }
             }
+#pragma omp parallel for schedule(static)
             for (int hh = 0; hh < H; ++hh) {
+                double *sc = sc_all + (size_t)hh * maxslots;
                 size_t qo = (((size_t)b * R + i) * H + hh) * dh;
                 double m = -INFINITY;
                 for (int j = 0; j < nslot; ++j) {
@@ -467,7 +494,7 @@ int oracle_tree_attention(int dtype, const void *q, const void *const *k_cache,
             }
         }
     }
-    free(sc); free(vis);
+    free(sc_all); free(vis);
     return 0;
 }
 
@@ -535,22 +562,27 @@ int oracle_posterior(int dtype, const void *logits, const int32_t *tokens,
 {
     if (B < 1 || R < 1 || V < 1 || K < 0 || !(T > 0.0))
         return 1;
-    double *x = (double *)malloc((size_t)V * sizeof(double));
+    for (size_t i = 0; i < (size_t)B * R; ++i) {
+        if (i % R == 0) continue;
+        const int p = parent[i];
+        if (p < 0 || p >= (int)(i % R) || tokens[i] < 0 || tokens[i] >= V)
+            return 3;
+    }
+    /* one widened row per node, so that nodes are independent */
+    double *x_all = (double *)malloc((size_t)R * V * sizeof(double));
     int *acc = (int *)malloc((size_t)R * sizeof(int));
     int *chain = (int *)malloc((size_t)R * sizeof(int));
-    if (!x || !acc || !chain) { free(x); free(acc); free(chain); return 2; }
+    if (!x_all || !acc || !chain) { free(x_all); free(acc); free(chain); return 2; }
     for (int b = 0; b < B; ++b) {
         const int32_t *tok = tokens + (size_t)b * R;
         const int32_t *pa = parent + (size_t)b * R;
         const int32_t *de = depth + (size_t)b * R;
         acc[0] = 1;
         if (margin) margin[(size_t)b * R] = INFINITY;
+#pragma omp parallel for schedule(dynamic, 1)
         for (int i = 1; i < R; ++i) {
             const int p = pa[i];
-            if (p < 0 || p >= i || tok[i] < 0 || tok[i] >= V) {
-                free(x); free(acc); free(chain);
-                return 3;
-            }
+            double *x = x_all + (size_t)i * V;
             size_t off = ((size_t)b * R + p) * V;
             double mg = INFINITY;
             if (mode == ORC_GREEDY) {
@@ -595,7 +627,7 @@ int oracle_posterior(int dtype, const void *logits, const int32_t *tokens,
         accept_len[b] = L;
         next_token[b] = orc_argmax_row(dtype, logits, ((size_t)b * R + best) * V, V);
     }
-    free(x); free(acc); free(chain);
+    free(x_all); free(acc); free(chain);
     return 0;
 }
 
