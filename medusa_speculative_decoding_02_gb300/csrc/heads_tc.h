@@ -1,0 +1,35 @@
+// heads_tc.h -- the tensor-core heads path (heads_tc.cu), used by heads.cu
+// for batches of several bf16 sequences.
+#pragma once
+
+#include <cuda_runtime.h>
+#include <stddef.h>
+#include <stdint.h>
+
+#include "medusa.h"
+
+namespace medusa {
+
+// Smallest batch the tensor-core path takes: below it the CUDA-core GEMV's
+// shared-memory traffic per weight byte is low enough to run at HBM rate.
+constexpr int kHeadsTcMinBatch = 3;
+
+// Whether launch_heads_tc handles this call (bf16, top-s mode without the LM
+// head, B in kHeadsTcMinBatch..8, d a multiple of 64, V a multiple of 8, and
+// enough 8-row units for every CTA).
+bool heads_tc_eligible(medusa_dtype dtype, int B, int d, int V, int K, bool with_lm_head,
+                       bool sample);
+
+// CTAs per head in phase 2 (the G of its partials).
+int heads_tc_ctas_per_head(int K);
+
+// Bytes of the z operand the two phases share: [K][16][d] bf16.
+size_t heads_tc_zt_bytes(int K, int d);
+
+// Phase 1 (z into zt) and phase 2 (partials, index (k * B + b) * G + g with
+// G = heads_tc_ctas_per_head(K)); heads_reduce_kernel merges the partials.
+cudaError_t launch_heads_tc(const void *h, const void *W1, const void *b1, const void *W2, int B,
+                            int d, int V, int K, int S, void *zt, float2 *part_ms,
+                            float *part_val, int *part_id, int *status, cudaStream_t stream);
+
+}  // namespace medusa

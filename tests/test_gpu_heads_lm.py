@@ -68,14 +68,14 @@ def check_topk(g_ids, g_logp, o_ids, o_logits, o_logz):
 
 
 def run(cfg, dev, hi, w_lm):
+    """heads_lm, and the plain heads call on the same inputs.  The two may
+    take different paths (several bf16 sequences run the plain heads on the
+    tensor cores), so each is compared with the oracle, not with the other."""
     args = (T(hi.h, dev), T(w_lm, dev), T(hi.W1, dev), T(hi.b1, dev), T(hi.W2, dev))
     root, root_lp, ids, logp = m.heads_lm(*args, cfg.top_s)
     ids_ref, logp_ref = m.heads(args[0], *args[2:], cfg.top_s)
     torch.cuda.synchronize()
-    # same candidates; log Z may differ in the last bit if the grid differs
-    assert torch.equal(ids, ids_ref)
-    torch.testing.assert_close(logp, logp_ref, rtol=1e-6, atol=1e-6)
-    return N(root), N(root_lp), N(ids), N(logp)
+    return N(root), N(root_lp), N(ids), N(logp), N(ids_ref), N(logp_ref)
 
 
 CASES = [
@@ -94,11 +94,12 @@ def test_heads_lm_shapes(dev, dtype, B, d, V, K, S):
                                s=(S,) * K, w1_std=0.05, w2_std=0.05)
     hi = synth.heads_inputs(cfg)
     w_lm = synth.lm_head_weight(cfg)
-    root, root_lp, ids, logp = run(cfg, dev, hi, w_lm)
+    root, root_lp, ids, logp, ids_ref, logp_ref = run(cfg, dev, hi, w_lm)
     o_ids, _, o_logits, o_logz = oracle.lm_head(hi.h, w_lm, 1, want_logits=True)
     check_root(root, root_lp, o_ids, o_logits, o_logz)
     h_ids, _, h_logits, h_logz = oracle.heads(hi.h, hi.W1, hi.b1, hi.W2, S, want_logits=True)
     check_topk(ids, logp, h_ids, h_logits, h_logz)
+    check_topk(ids_ref, logp_ref, h_ids, h_logits, h_logz)
 
 
 @pytest.mark.parametrize("cfg_fn", [synth.v7b, synth.batch8], ids=["v7b", "batch8"])
@@ -109,13 +110,14 @@ def test_heads_lm_full_size(dev, cfg_fn):
     cfg = cfg_fn()
     hi = synth.heads_inputs(cfg)
     w_lm = synth.lm_head_weight(cfg)
-    root, root_lp, ids, logp = run(cfg, dev, hi, w_lm)
+    root, root_lp, ids, logp, ids_ref, logp_ref = run(cfg, dev, hi, w_lm)
     o_ids, _, o_logits, o_logz = oracle.lm_head(hi.h, w_lm, 1, want_logits=True)
     check_root(root, root_lp, o_ids, o_logits, o_logz)
     for k in (0, cfg.K - 1):
         h_ids, _, h_logits, h_logz = oracle.heads(hi.h, hi.W1[k:k + 1], hi.b1[k:k + 1],
                                                   hi.W2[k:k + 1], cfg.top_s, want_logits=True)
         check_topk(ids[:, k:k + 1], logp[:, k:k + 1], h_ids, h_logits, h_logz)
+        check_topk(ids_ref[:, k:k + 1], logp_ref[:, k:k + 1], h_ids, h_logits, h_logz)
 
 
 def test_heads_lm_identity_variant(dev):
@@ -124,7 +126,7 @@ def test_heads_lm_identity_variant(dev):
     cfg = synth.v7b(lm_head_variant=True)
     hi = synth.heads_inputs(cfg)
     w_lm = synth.lm_head_weight(cfg)
-    root, root_lp, ids, logp = run(cfg, dev, hi, w_lm)
+    root, root_lp, ids, logp, _, _ = run(cfg, dev, hi, w_lm)
     for k in range(cfg.K):
         assert np.array_equal(ids[:, k, 0], root)
         np.testing.assert_array_equal(logp[:, k, 0], root_lp)
@@ -138,7 +140,7 @@ def test_heads_lm_root_ties(dev):
     w_lm = np.zeros((V, d), np.float32)
     w_lm[[811, 90, 433], 0] = 3.0
     hi.h[:] = 1.0
-    root, root_lp, _, _ = run(cfg, dev, hi, w_lm)
+    root, root_lp, _, _, _, _ = run(cfg, dev, hi, w_lm)
     assert int(root[0]) == 90
     ref = 3.0 - np.log(3 * np.exp(3.0) + (V - 3))
     assert abs(float(root_lp[0]) - ref) < 1e-5
