@@ -10,12 +10,16 @@
 
 namespace medusa {
 
-// Smallest batch the tensor-core path takes: below it the CUDA-core GEMV's
-// shared-memory traffic per weight byte is low enough to run at HBM rate.
-constexpr int kHeadsTcMinBatch = 3;
+// Smallest batch the tensor-core path takes.  At one sequence the CUDA-core
+// GEMV streams the weights at the HBM rate (216 us for the 7B heads on
+// GB300) and the tensor-core path's two-phase set-up costs more (~230 us);
+// from two sequences on the CUDA-core GEMV's shared-memory loads of the
+// activations slow it (280 us at two, 860 us at eight) while the
+// tensor-core path stays at ~230-240 us.
+constexpr int kHeadsTcMinBatch = 2;
 
 // Whether launch_heads_tc handles this call (bf16, top-s mode without the LM
-// head, B in kHeadsTcMinBatch..8, d a multiple of 64, V a multiple of 8, and
+// head, B in kHeadsTcMinBatch..8, d a multiple of 256, V a multiple of 8, and
 // enough 8-row units for every CTA).
 bool heads_tc_eligible(medusa_dtype dtype, int B, int d, int V, int K, bool with_lm_head,
                        bool sample);

@@ -129,7 +129,9 @@ posterior_rows_kernel(const T *__restrict__ logits, int R, int V, int splits, fl
                     }
 #pragma unroll
                     for (int e = 0; e < VN; ++e) {
-                        const float t = fmaf(f[e], y_scale, -mo.m);
+                        // clamped: a -inf logit adds 0 to both sums (0 * -inf
+                        // would make A NaN); 2^-127 flushes to 0 all the same
+                        const float t = fmaxf(fmaf(f[e], y_scale, -mo.m), -127.f);
                         const float p = ex2_approx(t);
                         mo.S += p;
                         mo.A = fmaf(p, t, mo.A);

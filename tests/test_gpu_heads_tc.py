@@ -1,6 +1,6 @@
 """The heads on the tensor cores (several bf16 sequences), against the oracle.
 
-The path takes batches of 3..8 bf16 sequences with d a multiple of 64 and V
+The path takes batches of 2..8 bf16 sequences with d a multiple of 256 and V
 a multiple of 8: phase 1 (W1 h, bias, SiLU, residual) and phase 2 (W2 z,
 running softmax normaliser and top-s) as tcgen05 MMAs fed by TMA, then the
 same merge of the per-CTA partials as the CUDA-core path.  Shapes below
@@ -58,6 +58,7 @@ def run(dev, hi, S, ws=None):
     (5, 512, 8000, 8, 1, 0.3),      # eight heads (19 CTAs each); top-1
     (7, 4096, 1216, 4, 8, 0.5),     # d = 4096; eight 8-row units per phase-2 CTA
     (4, 1536, 32000, 3, 3, 0.2),    # the full vocabulary
+    (2, 1024, 4000, 5, 4, 0.5),     # two sequences (the smallest batch on this path)
 ])
 def test_heads_tc_shapes(dev, B, d, V, K, S, bias):
     cfg, hi = case(B, d, V, K, S, bias, seed=B * 1000 + K)

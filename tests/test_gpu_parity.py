@@ -558,6 +558,25 @@ def test_posterior_shapes(dev, dtype, V, s, n, temp):
         check_posterior(gp, lg, ot, len(s), mode, 0.09, 0.3, temp)
 
 
+@pytest.mark.parametrize("dtype", ["bf16", "f32"])
+def test_posterior_masked_vocabulary(dev, dtype):
+    """-inf logits (a masked vocabulary: every fifth token, a whole block, and
+    some of the tree's own tokens) add nothing to the softmax sums and are
+    never accepted; the entropy and decisions match the oracle."""
+    cfg = synth.v7b().replace(name=f"mask{dtype}", dtype=dtype, V=4000)
+    ot = oracle_tree_for(np.random.default_rng(5), cfg.s, cfg.n, 1, cfg.prefix, cfg.V)
+    logits = synth.base_logits(cfg)
+    synth.plant_bernoulli(logits, ot["tokens"], ot["parent"], synth.rng_for(cfg, "plant"))
+    logits[..., 3::5] = -np.inf
+    logits[..., 1200:1900] = -np.inf
+    for i in range(1, cfg.R, 9):
+        logits[0, ot["parent"][0, i], ot["tokens"][0, i]] = -np.inf
+    lg = synth.cast(logits, dtype)
+    for mode in (m.GREEDY, m.TYPICAL):
+        gp = run_posterior(dev, lg, ot, cfg.K, mode)
+        check_posterior(gp, lg, ot, cfg.K, mode, 0.09, 0.3, 1.0)
+
+
 @pytest.mark.parametrize("ties", [
     [31999, 7, 12345],       # maxima far apart (different threads and slices)
     [13, 10, 2058, 4106],    # two in one 16-byte group, more in later groups
