@@ -156,6 +156,11 @@ __device__ __forceinline__ void named_sync_epi() {
     asm volatile("bar.sync 1, %0;\n" ::"r"(kEpiWarps * kWarp) : "memory");
 }
 
+// the MMA warp and the epilogue warps (tensor-memory hand-over)
+__device__ __forceinline__ void named_sync_mma_epi() {
+    asm volatile("bar.sync 2, %0;\n" ::"r"((kEpiWarps + 1) * kWarp) : "memory");
+}
+
 __global__ void __launch_bounds__(kTcThreads, 1)
 heads_tc_kernel(const __grid_constant__ TcMaps maps, const TcArgs a) {
     extern __shared__ unsigned char smem_raw[];
@@ -192,11 +197,18 @@ heads_tc_kernel(const __grid_constant__ TcMaps maps, const TcArgs a) {
         *err = 0;
         *consumed = 0;
     }
-    if (warp == 1) tc::tmem_alloc(tmem_holder, kTmemCols);
-    tc::fence_before_sync();
     __syncthreads();
-    tc::fence_after_sync();
-    const uint32_t tmem = *tmem_holder;
+    // Tensor memory is allocated only after the wait for the previous grid
+    // (by the MMA warp, which then meets the epilogue warps), so this CTA
+    // never holds columns while an earlier grid may still need some.
+    uint32_t tmem = 0;
+    auto take_tmem = [&]() {
+        if (warp == 1) tc::tmem_alloc(tmem_holder, kTmemCols);
+        tc::fence_before_sync();
+        named_sync_mma_epi();
+        tc::fence_after_sync();
+        tmem = *tmem_holder;
+    };
 
     // stage i -> ring slot i % kRing: the rows of tile i / nkb at K-blocks
     // kKbs * (i % nkb) .. + kKbs - 1, in one copy (the number of copies, not
@@ -260,6 +272,7 @@ heads_tc_kernel(const __grid_constant__ TcMaps maps, const TcArgs a) {
         // ---------------------------------------------------- MMA issuer ---
         grid_wait();
         grid_trigger();
+        take_tmem();
         if (lane == 0) {
             constexpr uint32_t idesc = tc::idesc_bf16(kTileRows, kBRows, 0);
             int i = 0;
@@ -317,6 +330,7 @@ heads_tc_kernel(const __grid_constant__ TcMaps maps, const TcArgs a) {
         // ------------------------------------------------------ epilogue ---
         grid_wait();
         grid_trigger();
+        take_tmem();
         const int q = warp & 3;  // tensor-memory lane quarter of this warp
         const int B = a.B;
         // phase 2 running state: per sequence, this thread's (max, sum-exp)
