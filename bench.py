@@ -612,7 +612,7 @@ def run_ours(args, cfg):
     B, K, R = cfg.B, cfg.K, cfg.R
     stream = run.stream
     est = run.warm(args.warmup)
-    window_steps = max(0, int(math.ceil(CLOCK_WINDOW_S / max(est, 1e-6))) - args.steps)
+    window_steps = max(0, int(math.ceil(args.clock_window_s / max(est, 1e-6))) - args.steps)
 
     # Region 1: exactly `steps` steps as a user runs them, events only at the
     # two ends; `value` and `ms_per_step` come from these.  The same loop then
@@ -926,6 +926,9 @@ def main():
     ap.add_argument("--steps", type=int, default=50)
     ap.add_argument("--warmup", type=int, default=5)
     ap.add_argument("--impl", default="ours", choices=["ours", "reference"])
+    ap.add_argument("--clock-window-s", type=float, default=CLOCK_WINDOW_S,
+                    help="seconds the headline's timed steps continue so that the clock "
+                         "samples cover them (0: only the timed steps)")
     args = ap.parse_args()
     if args.warmup < 3 and args.impl == "ours":
         args.warmup = 3
