@@ -215,15 +215,27 @@ posterior_rows_kernel(const T *__restrict__ logits, int R, int V, int splits, fl
     }
 }
 
+// A row's slices, all loaded in one round (independent loads: the merge
+// below would otherwise wait on each in turn).
+struct RowSlices {
+    RowPart p[kMaxSplits];
+    __device__ __forceinline__ void load(const RowPart *__restrict__ parts, int splits) {
+#pragma unroll
+        for (int k = 0; k < kMaxSplits; ++k)
+            if (k < splits) p[k] = parts[k];
+    }
+};
+
 // Merge the slices of one row: argmax, and log2 S, H (nats) when typical.
-__device__ __forceinline__ void row_stats(const RowPart *__restrict__ parts, int splits,
-                                          bool typical, int &arg, float &m2, float &log2s,
-                                          float &H) {
+__device__ __forceinline__ void row_stats(const RowSlices &rs, int splits, bool typical, int &arg,
+                                          float &m2, float &log2s, float &H) {
     float bv = -INFINITY;
     int bi = INT_MAX;
     Moments mo{-INFINITY, 0.f, 0.f};
-    for (int k = 0; k < splits; ++k) {
-        const RowPart pt = parts[k];
+#pragma unroll
+    for (int k = 0; k < kMaxSplits; ++k) {
+        if (k >= splits) break;
+        const RowPart pt = rs.p[k];
         if (better(pt.amax, pt.arg, bv, bi)) {
             bv = pt.amax;
             bi = pt.arg;
@@ -296,14 +308,19 @@ posterior_select_kernel(const T *__restrict__ logits, const int32_t *__restrict_
             s_par[0] = -1;
         }
     }
+    // this node's own row (the next token if the path ends here) and its
+    // parent's row: every slice of both in one round of loads
+    RowSlices own, up;
+    if (i < R) {
+        own.load(parts + ((size_t)b * R + i) * splits, splits);
+        if (i > 0 && par >= 0 && par < i) up.load(parts + ((size_t)b * R + par) * splits, splits);
+    }
     __syncthreads();
     if (i < R) {
-        // this node's own row argmax (the next token if the path ends here),
-        // loaded with the parent row's statistics
         {
             int arg;
             float m2, log2s, H;
-            row_stats(parts + ((size_t)b * R + i) * splits, splits, false, arg, m2, log2s, H);
+            row_stats(own, splits, false, arg, m2, log2s, H);
             s_arg[i] = arg;
         }
         int acc = 1;
@@ -325,7 +342,7 @@ posterior_select_kernel(const T *__restrict__ logits, const int32_t *__restrict_
             } else {
                 int arg;
                 float m2, log2s, H;
-                row_stats(parts + ((size_t)b * R + p) * splits, splits, typical, arg, m2, log2s, H);
+                row_stats(up, splits, typical, arg, m2, log2s, H);  // p == par here
                 if (!typical) {
                     acc = (tok == arg);
                 } else {
