@@ -276,11 +276,13 @@ __global__ void __launch_bounds__(256, 2) tree_attn_tc_kernel(AttnArgs a) {
         // ---- S = Q K_j^T (A = Q in tensor memory, B = K_j in shared memory)
         if (tid == 0) {
             constexpr uint32_t idesc = tc::idesc_bf16(128, kTcSub, 0);
+            // the K-slices' descriptors differ only in the start-address
+            // field (bytes >> 4), so the base is built once per sub-chunk
+            const uint64_t bd0 = tc::sdesc_sw128(tc::smem_addr(k_s), 16, 1024);
 #pragma unroll
             for (int ks = 0; ks < DH / 16; ++ks) {
                 const uint32_t koff = (ks >> 2) * kTcSub * 128 + (ks & 3) * 32;
-                const uint64_t bd = tc::sdesc_sw128(tc::smem_addr(k_s) + koff, 16, 1024);
-                tc::mma_bf16_ts(t_s, t_q + ks * 8, bd, idesc, ks > 0);
+                tc::mma_bf16_ts(t_s, t_q + ks * 8, bd0 + (koff >> 4), idesc, ks > 0);
             }
             tc::mma_commit(&bar_s);
         }
@@ -375,12 +377,12 @@ __global__ void __launch_bounds__(256, 2) tree_attn_tc_kernel(AttnArgs a) {
         // ---- O += P_j V_j (A = P in tensor memory, B = V_j in shared memory)
         if (tid == 0) {
             constexpr uint32_t idesc = tc::idesc_bf16(128, DH, 1);
+            const uint64_t bd0 = tc::sdesc_sw128(tc::smem_addr(v_s), kTcSub * 128, 1024);
 #pragma unroll
             for (int ks = 0; ks < kTcSub / 16; ++ks) {
                 const uint32_t pa = t_s + (ks >> 1) * HALF + (ks & 1) * 8;
-                const uint64_t bd =
-                    tc::sdesc_sw128(tc::smem_addr(v_s) + ks * 16 * 128, kTcSub * 128, 1024);
-                tc::mma_bf16_ts(t_o, pa, bd, idesc, (done > 0 || ks > 0) ? 1u : 0u);
+                tc::mma_bf16_ts(t_o, pa, bd0 + ((ks * 16 * 128) >> 4), idesc,
+                                (done > 0 || ks > 0) ? 1u : 0u);
             }
             tc::mma_commit(&bar_o);
         }
