@@ -389,7 +389,52 @@ class StepRunner:
         return out
 
 
-def time_side_step(m, cfg, dev, T, steps: int, warmup: int, peak_gbs: float) -> dict:
+def time_heads_modes(m, r, dev, T, reps: int, peak_gbs: float) -> dict:
+    """The LM head joining the heads' pass and the sampled drafts, on the
+    runner's workload, each timed over a loop of `reps` calls (events at the
+    two ends; the weights exceed L2, so no call finds them there)."""
+    import torch
+    cfg = r.cfg
+    B, K, S, d, V = cfg.B, cfg.K, cfg.top_s, cfg.d, cfg.V
+    w_lm = T(synth.lm_head_weight(cfg))
+    ws_lm = m.new_workspace(m.heads_lm_workspace_size(B, K, d, V, S), dev)
+    lm_out = (torch.empty((B,), dtype=torch.int32, device=dev),
+              torch.empty((B,), dtype=torch.float32, device=dev),
+              torch.empty((B, K, S), dtype=torch.int32, device=dev),
+              torch.empty((B, K, S), dtype=torch.float32, device=dev))
+    ws_smp = m.new_workspace(m.heads_workspace_size(B, K, d, V, 1), dev)
+    smp_out = (torch.empty((B, K), dtype=torch.int32, device=dev),
+               torch.empty((B, K, V), dtype=torch.float32, device=dev))
+    calls = {
+        "heads_lm": (lambda: m.heads_lm(r.h, w_lm, r.W1, r.b1, r.W2, S, ws=ws_lm, out=lm_out),
+                     r.nb["heads"] + V * d * 2 + B * 8),
+        "heads_sample": (lambda: m.heads_sample(r.h, r.W1, r.b1, r.W2, 1.0, 11, 0, ws=ws_smp,
+                                                out=smp_out),
+                         r.nb["heads"] + B * K * V * 4),
+    }
+    out = {}
+    for name, (fn, nbytes) in calls.items():
+        for _ in range(3):
+            fn()
+        torch.cuda.synchronize(dev)
+        a, z = torch.cuda.Event(enable_timing=True), torch.cuda.Event(enable_timing=True)
+        a.record(r.stream)
+        for _ in range(reps):
+            fn()
+        z.record(r.stream)
+        torch.cuda.synchronize(dev)
+        us = a.elapsed_time(z) / reps * 1e3
+        gbs = nbytes / (us * 1e-6) / 1e9
+        out[name] = {"us": round(us, 2), "bytes": int(nbytes), "GB/s": round(gbs, 1),
+                     "frac_hbm": round(gbs / peak_gbs, 4)}
+    if m.read_device_status(ws_lm) != 0 or m.read_device_status(ws_smp) != 0:
+        raise RuntimeError(f"device status set by the heads modes ({cfg.name})")
+    del w_lm
+    return out
+
+
+def time_side_step(m, cfg, dev, T, steps: int, warmup: int, peak_gbs: float,
+                   heads_modes: bool = False) -> dict:
     """The whole step on another workload (13B shape, batch of 8), timed like
     the headline: events at the two ends of `steps` steps, then per call."""
     import torch
@@ -411,6 +456,8 @@ def time_side_step(m, cfg, dev, T, steps: int, warmup: int, peak_gbs: float) -> 
            "us_per_step": round(ms * 1e3, 2), "bytes_per_step": int(r.nb["total"]),
            "GB/s": round(gbs, 1), "frac_hbm": round(gbs / peak_gbs, 4),
            "stages": r.stages(pc, peak_gbs)}
+    if heads_modes:
+        out["heads_modes"] = time_heads_modes(m, r, dev, T, max(steps, 20), peak_gbs)
     del r
     torch.cuda.empty_cache()
     return out
@@ -642,7 +689,7 @@ def run_ours(args, cfg):
         side = {"v13b_step": time_side_step(m, synth.v13b(), dev, T, args.steps, args.warmup,
                                             peak_gbs),
                 "batch8_step": time_side_step(m, synth.batch8(), dev, T, args.steps,
-                                              args.warmup, peak_gbs)}
+                                              args.warmup, peak_gbs, heads_modes=True)}
     total_ms = t_start.elapsed_time(t_end)
     win_ms = t_start.elapsed_time(t_win)
     nb = run.nb

@@ -538,17 +538,18 @@ cudaError_t launch_heads(medusa_dtype dtype, const void *h, const void *Wlm, con
     if (heads_tc_eligible(dtype, B, d, V, K, Wlm != nullptr, sample != nullptr)) {
         // several bf16 sequences: both GEMVs on the tensor cores (heads_tc.cu),
         // then the same merge of the per-CTA partials
-        const HeadsLayout L = heads_layout(B, K, d, S);
+        const int lm = Wlm ? 1 : 0, Kt = K + lm;
+        const HeadsLayout L = heads_layout(B, Kt, d, S);
         float2 *pms = reinterpret_cast<float2 *>(w + L.ms_off);
         float *pval = reinterpret_cast<float *>(w + L.val_off);
         int *pid = reinterpret_cast<int *>(w + L.id_off);
-        cudaError_t e = launch_heads_tc(h, W1, b1, W2, B, d, V, K, S, w + L.z_off, pms, pval, pid,
-                                        reinterpret_cast<int *>(w), stream);
+        cudaError_t e = launch_heads_tc(h, Wlm, W1, b1, W2, B, d, V, K, S, sample, w + L.z_off,
+                                        pms, pval, pid, reinterpret_cast<int *>(w), stream);
         if (e) return e;
-        e = launch_pdl(heads_reduce_kernel, dim3(K * B), dim3(kReduceThreads), 0, stream,
+        e = launch_pdl(heads_reduce_kernel, dim3(Kt * B), dim3(kReduceThreads), 0, stream,
                        static_cast<const float2 *>(pms), static_cast<const float *>(pval),
-                       static_cast<const int *>(pid), heads_tc_ctas_per_head(K), B, K, S, 0, ids,
-                       logp, static_cast<int32_t *>(nullptr), static_cast<float *>(nullptr));
+                       static_cast<const int *>(pid), heads_tc_ctas_per_head(Kt), B, Kt, S, lm,
+                       ids, logp, root, root_logp);
         note_launch();
         return e;
     }

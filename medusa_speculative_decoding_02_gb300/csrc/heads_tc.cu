@@ -53,6 +53,7 @@
 #include "common.cuh"
 #include "heads_tc.h"
 #include "launch.h"
+#include "philox.cuh"
 #include "tcgen05.cuh"
 #include "topk.cuh"
 
@@ -82,8 +83,9 @@ constexpr uint32_t kDrainPolls = 1u << 16;      // the drain's own limit
 // copy brings kKbs K-blocks of a tile's rows and lands as kKbs consecutive
 // [rows][128 B] swizzled blocks, the layout the MMA reads.
 struct TcMaps {
-    CUtensorMap w[kMaxMaps];  // weight rows: box (64, height of map i, kKbs)
-    CUtensorMap b;            // B operand: box (64, 16, kKbs)
+    CUtensorMap w[kMaxMaps];    // weight rows: box (64, height of map i, kKbs)
+    CUtensorMap wlm[kMaxMaps];  // phase 2 with the LM head: W_lm's rows, same boxes
+    CUtensorMap b;              // B operand: box (64, 16, kKbs)
 };
 
 struct TcArgs {
@@ -91,6 +93,14 @@ struct TcArgs {
     int B, d, V, K, S;
     int cph;            // phase 2: CTAs per head
     int8_t map_of[17];  // tile height / 8 -> index into TcMaps::w
+    int lm;             // 1: the LM head is head 0 of phase 2 (z = h), the Medusa heads follow
+    // sampling (phase 2): one draft per head, the top-1 of logit/T + Gumbel
+    // noise (Philox stream purpose 1, row = head, key (seed, step)), raw
+    // logits to logits_out [B][K][V]
+    int sample;
+    float inv_T;
+    uint64_t seed, step;
+    float *logits_out;
     const bf16 *h;      // [B][d]
     const bf16 *b1;     // [K][d] or null
     bf16 *zt;           // [K][16][d] (phase 1 writes it, phase 2 reads it by TMA)
@@ -112,10 +122,14 @@ struct TcSmem {
     static constexpr int TOTAL = SLOTS + kEpiWarps * kMaxB * (int)sizeof(TopSlot);
     static constexpr int ALLOC = TOTAL + 1024;
 };
+// an 8-row-B stage's last K-block lets the MMA read 8 rows (1 KB) past the
+// slot; past the last slot those bytes must still lie inside the CTA's block
+static_assert(TcSmem::TOTAL - TcSmem::RING >= 1024, "guard after the ring");
 
-// This CTA's rows: [row0, row0 + 8 * units), and (phase 2) its head.
+// This CTA's rows: [row0, row0 + 8 * units) of its weight matrix, the token
+// id of its first row (phase 2) and (phase 2) its head in the pass.
 struct Span {
-    int row0, units, head;
+    int row0, units, head, tok0;
 };
 
 __device__ __forceinline__ Span cta_span(const TcArgs &a) {
@@ -126,13 +140,17 @@ __device__ __forceinline__ Span cta_span(const TcArgs &a) {
         s.row0 = u0 * 8;
         s.units = u1 - u0;
         s.head = 0;
+        s.tok0 = 0;
     } else {
         const int k = blockIdx.x / a.cph, j = blockIdx.x - k * a.cph;
         const long long U = a.V / 8;
         const int u0 = (int)(j * U / a.cph), u1 = (int)((j + 1) * U / a.cph);
-        s.row0 = k * a.V + u0 * 8;
+        // with the LM head, head 0 reads W_lm and head k >= 1 reads W2's
+        // head k - 1
+        s.row0 = (a.lm && k == 0 ? 0 : (k - a.lm) * a.V) + u0 * 8;
         s.units = u1 - u0;
         s.head = k;
+        s.tok0 = u0 * 8;
     }
     return s;
 }
@@ -218,7 +236,8 @@ heads_tc_kernel(const __grid_constant__ TcMaps maps, const TcArgs a) {
         int first, rows;
         tile_of(sp, T, t, first, rows);
         tc::mbar_arrive_expect_tx(&full[s], (uint32_t)(kKbs * (rows * 128 + kBRows * 128)));
-        tc::tma_load_3d(smem + s * kSlotBytes, &maps.w[a.map_of[rows / 8]], 0, sp.row0 + first,
+        const CUtensorMap *wm = a.lm && a.phase == 2 && sp.head == 0 ? maps.wlm : maps.w;
+        tc::tma_load_3d(smem + s * kSlotBytes, &wm[a.map_of[rows / 8]], 0, sp.row0 + first,
                         kg * kKbs, &full[s]);
     };
     auto issue_b = [&](int i) {
@@ -231,7 +250,10 @@ heads_tc_kernel(const __grid_constant__ TcMaps maps, const TcArgs a) {
         // ------------------------------------------------ TMA producer ---
         int issued = 0;
         if (lane == 0) {
-            for (int mi = 0; mi < kMaxMaps; ++mi) tc::prefetch_tmap(&maps.w[mi]);
+            for (int mi = 0; mi < kMaxMaps; ++mi) {
+                tc::prefetch_tmap(&maps.w[mi]);
+                if (a.lm) tc::prefetch_tmap(&maps.wlm[mi]);
+            }
             tc::prefetch_tmap(&maps.b);
             // The weights are never written by any kernel: the first stages'
             // weight boxes go out before the wait for the previous grid; their
@@ -333,6 +355,16 @@ heads_tc_kernel(const __grid_constant__ TcMaps maps, const TcArgs a) {
         take_tmem();
         const int q = warp & 3;  // tensor-memory lane quarter of this warp
         const int B = a.B;
+        if (a.phase == 1 && a.lm) {
+            // the LM head multiplies h itself: its B-operand rows are h (value
+            // rows) and zero (remainder rows); every CTA copies a share
+            const int n = kBRows * a.d, e0 = (int)((long long)blockIdx.x * n / gridDim.x),
+                      e1 = (int)((long long)(blockIdx.x + 1) * n / gridDim.x);
+            for (int e = e0 + threadIdx.x - 64; e < e1; e += kEpiWarps * kWarp) {
+                const int r = e / a.d, j = e - r * a.d;
+                a.zt[e] = r < B ? a.h[(size_t)r * a.d + j] : __float2bfloat16_rn(0.f);
+            }
+        }
         // phase 2 running state: per sequence, this thread's (max, sum-exp)
         // and the warp's top-s list (entry i in lane i)
         float m_run[kMaxB], s_run[kMaxB], l_val[kMaxB];
@@ -378,7 +410,7 @@ heads_tc_kernel(const __grid_constant__ TcMaps maps, const TcArgs a) {
                 if (valid) {
                     const int k = r / a.d, j = r - k * a.d;
                     const float bias = a.b1 ? Vec16<bf16>::load1(a.b1 + r) : 0.f;
-                    bf16 *zk = a.zt + (size_t)k * kBRows * a.d + j;
+                    bf16 *zk = a.zt + (size_t)(k + a.lm) * kBRows * a.d + j;
 #pragma unroll
                     for (int b = 0; b < kMaxB; ++b) {
                         bf16 hi = __float2bfloat16_rn(0.f), lo = hi;
@@ -394,17 +426,26 @@ heads_tc_kernel(const __grid_constant__ TcMaps maps, const TcArgs a) {
                     }
                 }
             } else {
-                const int v = r - sp.head * a.V;  // token id
+                const int v = sp.tok0 + first + row;  // token id
 #pragma unroll
                 for (int b = 0; b < kMaxB; ++b) {
                     if (b >= B) break;
-                    const float x = D[b] + D[kMaxB + b];
+                    const float logit = D[b] + D[kMaxB + b];
+                    // sampling ranks y + Gumbel noise and normalises y = logit / T
+                    float x = logit, y = logit;
+                    if (a.sample) {
+                        y = logit * a.inv_T;
+                        x = valid ? y + gumbel_at(a.seed, a.step, kRngDraft, b, sp.head, v)
+                                  : -INFINITY;
+                        if (valid && a.logits_out)
+                            a.logits_out[((size_t)b * a.K + sp.head) * a.V + v] = logit;
+                    }
                     if (valid) {
-                        if (x > m_run[b]) {
-                            s_run[b] = s_run[b] * expf(m_run[b] - x) + 1.f;
-                            m_run[b] = x;
+                        if (y > m_run[b]) {
+                            s_run[b] = s_run[b] * expf(m_run[b] - y) + 1.f;
+                            m_run[b] = y;
                         } else {
-                            s_run[b] += expf(x - m_run[b]);
+                            s_run[b] += expf(y - m_run[b]);
                         }
                     }
                     // top-s: lanes whose candidate beats the list's last entry
@@ -556,12 +597,13 @@ cudaError_t launch_phase(const TcMaps &maps, const TcArgs &a, int grid, cudaStre
 
 bool heads_tc_eligible(medusa_dtype dtype, int B, int d, int V, int K, bool with_lm_head,
                        bool sample) {
-    if (dtype != MEDUSA_BF16 || with_lm_head || sample) return false;
+    if (dtype != MEDUSA_BF16 || (with_lm_head && sample)) return false;
     if (B < kHeadsTcMinBatch || B > kMaxB) return false;
     if (d % (kKb * kKbs) || d > 16384 || V % 8 || V < 8) return false;
     const int sms = device_sm_count();
+    const int Kt = K + (with_lm_head ? 1 : 0);
     // every CTA needs at least one 8-row unit in both phases
-    return (long long)K * d / 8 >= sms && V / 8 >= std::max(1, sms / K);
+    return (long long)K * d / 8 >= sms && V / 8 >= std::max(1, sms / Kt);
 }
 
 int heads_tc_ctas_per_head(int K) { return std::max(1, device_sm_count() / K); }
@@ -596,11 +638,15 @@ bool plan_maps(TcMaps &m, TcArgs &a, const void *W, uint64_t rows, int d, long l
     return true;
 }
 
-cudaError_t launch_heads_tc(const void *h, const void *W1, const void *b1, const void *W2, int B,
-                            int d, int V, int K, int S, void *zt, float2 *part_ms,
-                            float *part_val, int *part_id, int *status, cudaStream_t stream) {
+cudaError_t launch_heads_tc(const void *h, const void *Wlm, const void *W1, const void *b1,
+                            const void *W2, int B, int d, int V, int K, int S,
+                            const SampleArgs *sample, void *zt, float2 *part_ms, float *part_val,
+                            int *part_id, int *status, cudaStream_t stream) {
     const int sms = device_sm_count();
-    const int cph = heads_tc_ctas_per_head(K);
+    const int lm = Wlm ? 1 : 0;
+    const int Kt = K + lm;  // heads of phase 2
+    const int cph = heads_tc_ctas_per_head(Kt);
+    // phase 1: 8 K-blocks a stage (tiles of up to 64 rows) where d allows
     TcMaps m1, m2;
     TcArgs a1 = {}, a2 = {};
     if (!plan_maps(m1, a1, W1, (uint64_t)K * d, d, (long long)K * d / 8, sms) ||
@@ -609,8 +655,21 @@ cudaError_t launch_heads_tc(const void *h, const void *W1, const void *b1, const
                        "(cuTensorMapEncodeTiled failed or too many tile heights)");
         return cudaErrorInvalidValue;
     }
+    // phase 1 has no LM-head rows; phase 2's W_lm maps share W2's tile heights
+    for (int i = 0; i < kMaxMaps; ++i) m1.wlm[i] = m1.w[i];
+    if (lm) {  // the same partition of V rows per head: the same tile heights, in order
+        TcArgs alm = {};
+        TcMaps tmp;
+        if (!plan_maps(tmp, alm, Wlm, (uint64_t)V, d, V / 8, cph)) {
+            set_last_error("tensor maps for the LM head could not be made");
+            return cudaErrorInvalidValue;
+        }
+        for (int i = 0; i < kMaxMaps; ++i) m2.wlm[i] = tmp.w[i];
+    } else {
+        for (int i = 0; i < kMaxMaps; ++i) m2.wlm[i] = m2.w[i];
+    }
     if (!encode_rows(&m1.b, h, (uint64_t)B, (uint64_t)d, kBRows) ||
-        !encode_rows(&m2.b, zt, (uint64_t)K * kBRows, (uint64_t)d, kBRows)) {
+        !encode_rows(&m2.b, zt, (uint64_t)Kt * kBRows, (uint64_t)d, kBRows)) {
         set_last_error("cuTensorMapEncodeTiled failed for the heads' activations");
         return cudaErrorInvalidValue;
     }
@@ -628,6 +687,14 @@ cudaError_t launch_heads_tc(const void *h, const void *W1, const void *b1, const
     a.part_id = part_id;
     a.status = status;
     a.wait_polls = wait_budget();
+    a.lm = lm;
+    if (sample && sample->on) {
+        a.sample = 1;
+        a.inv_T = sample->inv_T;
+        a.seed = sample->seed;
+        a.step = sample->step;
+        a.logits_out = sample->logits_out;
+    }
     a.phase = 1;
     a.cph = 1;
     std::copy(a1.map_of, a1.map_of + 17, a.map_of);
@@ -635,8 +702,9 @@ cudaError_t launch_heads_tc(const void *h, const void *W1, const void *b1, const
     if (e) return e;
     a.phase = 2;
     a.cph = cph;
+    a.K = Kt;
     std::copy(a2.map_of, a2.map_of + 17, a.map_of);
-    return launch_phase(m2, a, cph * K, stream);
+    return launch_phase(m2, a, cph * Kt, stream);
 }
 
 }  // namespace medusa

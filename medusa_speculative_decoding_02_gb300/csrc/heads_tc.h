@@ -6,6 +6,7 @@
 #include <stddef.h>
 #include <stdint.h>
 
+#include "launch.h"
 #include "medusa.h"
 
 namespace medusa {
@@ -18,9 +19,9 @@ namespace medusa {
 // tensor-core path stays at ~230-240 us.
 constexpr int kHeadsTcMinBatch = 2;
 
-// Whether launch_heads_tc handles this call (bf16, top-s mode without the LM
-// head, B in kHeadsTcMinBatch..8, d a multiple of 256, V a multiple of 8, and
-// enough 8-row units for every CTA).
+// Whether launch_heads_tc handles this call (bf16, B in kHeadsTcMinBatch..8,
+// d a multiple of 256, V a multiple of 8, enough 8-row units for every CTA;
+// top-s mode with or without the LM head, or sampling mode).
 bool heads_tc_eligible(medusa_dtype dtype, int B, int d, int V, int K, bool with_lm_head,
                        bool sample);
 
@@ -31,9 +32,12 @@ int heads_tc_ctas_per_head(int K);
 size_t heads_tc_zt_bytes(int K, int d);
 
 // Phase 1 (z into zt) and phase 2 (partials, index (k * B + b) * G + g with
-// G = heads_tc_ctas_per_head(K)); heads_reduce_kernel merges the partials.
-cudaError_t launch_heads_tc(const void *h, const void *W1, const void *b1, const void *W2, int B,
-                            int d, int V, int K, int S, void *zt, float2 *part_ms,
-                            float *part_val, int *part_id, int *status, cudaStream_t stream);
+// G = heads_tc_ctas_per_head(Kt), Kt = K + 1 with the LM head as head 0);
+// heads_reduce_kernel merges the partials.  sample (or null): draft mode.
+// zt holds heads_tc_zt_bytes(Kt, d).
+cudaError_t launch_heads_tc(const void *h, const void *Wlm, const void *W1, const void *b1,
+                            const void *W2, int B, int d, int V, int K, int S,
+                            const SampleArgs *sample, void *zt, float2 *part_ms, float *part_val,
+                            int *part_id, int *status, cudaStream_t stream);
 
 }  // namespace medusa

@@ -109,3 +109,44 @@ def test_heads_tc_wait_timeout_sets_status_and_context_survives(dev):
     assert m.read_device_status(ws) == 0
     o_ids, _, o_logits, o_logz = oracle.heads(hi.h, hi.W1, hi.b1, hi.W2, 4, want_logits=True)
     check_topk(ids, logp, o_ids, o_logits, o_logz)
+
+
+@pytest.mark.parametrize("B", [2, 8])
+def test_heads_tc_lm_head(dev, B):
+    """The LM head in the same tensor-core pass (head 0 multiplies h itself,
+    from its own weight matrix): the root and its log-probability against
+    the oracle's LM head, the Medusa heads' top-s against the oracle."""
+    from test_gpu_heads_lm import check_root
+    K, d, V, S = 5, 1024, 4000, 4
+    cfg, hi = case(B, d, V, K, S, 0.5, seed=50 + B)
+    w_lm = synth.lm_head_weight(cfg)
+    root, root_lp, ids, logp = m.heads_lm(T(hi.h, dev), T(w_lm, dev), T(hi.W1, dev),
+                                          T(hi.b1, dev), T(hi.W2, dev), S)
+    torch.cuda.synchronize()
+    o_ids, _, o_logits, o_logz = oracle.lm_head(hi.h, w_lm, 1, want_logits=True)
+    check_root(N(root), N(root_lp), o_ids, o_logits, o_logz)
+    h_ids, _, h_logits, h_logz = oracle.heads(hi.h, hi.W1, hi.b1, hi.W2, S, want_logits=True)
+    check_topk(N(ids), N(logp), h_ids, h_logits, h_logz)
+
+
+@pytest.mark.parametrize("B,temp", [(2, 0.7), (8, 1.0)])
+def test_heads_tc_sampling(dev, B, temp):
+    """Drafts sampled in the tensor-core pass (top-1 of logit / T plus the
+    Gumbel noise of the library's Philox streams): ids equal the oracle's
+    outside a key gap of 1e-3, and the raw logits written out match."""
+    K, d, V = 5, 1024, 4000
+    cfg, hi = case(B, d, V, K, 1, 0.5, seed=70 + B)
+    seed, step = 99 + B, 5
+    drafts, dl = m.heads_sample(T(hi.h, dev), T(hi.W1, dev), T(hi.b1, dev), T(hi.W2, dev), temp,
+                                seed, step)
+    torch.cuda.synchronize()
+    g_dr, g_dl = N(drafts), N(dl)
+    o_dr, o_lg, o_keys = oracle.draft_sample(hi.h, hi.W1, hi.b1, hi.W2, temp, seed, step,
+                                             want_keys=True)
+    err = np.abs(g_dl - o_lg)
+    assert err.max() <= 1e-2, err.max()
+    for b in range(B):
+        for k in range(K):
+            a, o = int(g_dr[b, k]), int(o_dr[b, k])
+            if a != o:
+                assert o_keys[b, k, o] - o_keys[b, k, a] < 1e-3, (b, k, a, o)
