@@ -362,6 +362,12 @@ MEDUSA_API medusa_status medusa_tree_attention(medusa_dtype dtype, const void *q
  *   path_tokens [B,K+1]    their tokens (-1 padded)
  *   next_token [B]         argmax of the best node's row (ties -> smaller id)
  *   accept [B,R] or NULL   per-node decision (root = 1)
+ * The outputs may be device memory or page-locked host memory that the
+ * device addresses at the same pointer (cudaHostAlloc, or cudaHostRegister
+ * with mapping, under unified addressing): the kernel then writes the
+ * results straight to the host, readable once the stream has synchronised,
+ * with no copy back.  Pageable host memory is rejected
+ * (MEDUSA_ERR_INVALID_ARG).
  * Requirements: R <= 256, K <= 8, V % 8 == 0 (bf16) or V % 4 == 0 (f32),
  * temperature > 0, eps > 0, delta > 0.
  * ---------------------------------------------------------------------- */

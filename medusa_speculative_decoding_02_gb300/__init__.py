@@ -137,6 +137,18 @@ def _need(t: torch.Tensor, name: str):
         raise ValueError(f"{name} must be contiguous")
 
 
+def _result_ptr(t: Optional[torch.Tensor], name: str):
+    """Pointer of a posterior output: a CUDA tensor, or a pinned CPU tensor
+    that the kernel writes directly (no copy back)."""
+    if t is None:
+        return None
+    if not (t.is_cuda or t.is_pinned()):
+        raise ValueError(f"{name} must be a CUDA tensor or pinned host memory")
+    if not t.is_contiguous():
+        raise ValueError(f"{name} must be contiguous")
+    return _ptr(t)
+
+
 def launch_count() -> int:
     return int(lib().medusa_launch_count())
 
@@ -354,6 +366,15 @@ class Posterior:
                          torch.empty((B, K + 1), **i32), torch.empty((B,), **i32),
                          torch.empty((B, R), **i32) if with_accept else None)
 
+    @staticmethod
+    def pinned(B: int, R: int, K: int, with_accept: bool = True) -> "Posterior":
+        """Results in page-locked host memory: the posterior kernel writes
+        them there directly; read them after the stream has synchronised."""
+        i32 = dict(dtype=torch.int32)
+        mk = lambda shape: torch.empty(shape, **i32).pin_memory()
+        return Posterior(mk((B,)), mk((B, K + 1)), mk((B, K + 1)), mk((B,)),
+                         mk((B, R)) if with_accept else None)
+
 
 def posterior_workspace_size(B: int, R: int) -> int:
     return int(lib().medusa_posterior_workspace_size(B, R))
@@ -370,9 +391,13 @@ def evaluate_posterior(logits, tokens, parent, depth, K: int, mode: int = GREEDY
     o = out or Posterior.empty(B, R, K, logits.device, with_accept)
     _check(lib().medusa_evaluate_posterior(_dtype(logits), _ptr(logits), _ptr(tokens), _ptr(parent),
                                            _ptr(depth), B, R, V, K, int(mode), float(eps),
-                                           float(delta), float(temperature), _ptr(o.accept_len),
-                                           _ptr(o.path), _ptr(o.path_tokens), _ptr(o.next_token),
-                                           _ptr(o.accept), _ptr(ws), ws.numel(), _stream(stream)))
+                                           float(delta), float(temperature),
+                                           _result_ptr(o.accept_len, "accept_len"),
+                                           _result_ptr(o.path, "path"),
+                                           _result_ptr(o.path_tokens, "path_tokens"),
+                                           _result_ptr(o.next_token, "next_token"),
+                                           _result_ptr(o.accept, "accept"), _ptr(ws), ws.numel(),
+                                           _stream(stream)))
     return o
 
 
@@ -392,8 +417,10 @@ def evaluate_posterior_commit(logits, tokens, parent, depth, K: int, k_ptrs, v_p
         new_prefix_len = torch.empty((B,), dtype=torch.int32, device=logits.device)
     _check(lib().medusa_evaluate_posterior_commit(
         _dtype(logits), _ptr(logits), _ptr(tokens), _ptr(parent), _ptr(depth), B, R, V, K,
-        int(mode), float(eps), float(delta), float(temperature), _ptr(o.accept_len), _ptr(o.path),
-        _ptr(o.path_tokens), _ptr(o.next_token), _ptr(o.accept), _ptr(k_ptrs), _ptr(v_ptrs),
+        int(mode), float(eps), float(delta), float(temperature),
+        _result_ptr(o.accept_len, "accept_len"), _result_ptr(o.path, "path"),
+        _result_ptr(o.path_tokens, "path_tokens"), _result_ptr(o.next_token, "next_token"),
+        _result_ptr(o.accept, "accept"), _ptr(k_ptrs), _ptr(v_ptrs),
         _ptr(prefix_len), int(H), int(dh), _ptr(new_prefix_len), _ptr(ws), ws.numel(),
         _stream(stream)))
     return o, new_prefix_len
@@ -483,8 +510,9 @@ class StepGraph:
 
     ``fn`` issues the step on the current stream: copies of the step's
     inputs from pinned host buffers, the library calls (heads, tree,
-    attention, posterior, ...), and copies of the results back to pinned
-    host buffers.  Every buffer it touches must stay allocated and at the
+    attention, posterior, ...), and the results' way back to the host: copies
+    into pinned buffers, or a posterior whose outputs are pinned host memory
+    (``Posterior.pinned``), which its kernel writes directly.  Every buffer it touches must stay allocated and at the
     same address while the graph lives; new inputs are written into the same
     pinned host buffers before each ``replay``.  The launches keep their
     programmatic-dependent-launch edges inside the graph.

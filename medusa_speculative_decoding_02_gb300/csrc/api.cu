@@ -391,6 +391,30 @@ size_t medusa_posterior_workspace_size(int B, int R) {
 
 namespace {
 
+// The posterior's results may go to device memory or straight to page-locked
+// host memory that the device addresses at the same pointer (cudaHostAlloc,
+// or cudaHostRegister with mapping, under unified addressing): the select
+// kernel writes them there, and the host reads them after the stream syncs.
+// Pageable host memory is refused.  If the runtime cannot answer (no device)
+// the check is left to the launch.
+medusa_status check_result_pointer(const void *p, const char *who) {
+    if (!p) return MEDUSA_OK;
+    cudaPointerAttributes at;
+    if (cudaPointerGetAttributes(&at, p) != cudaSuccess) {
+        (void)cudaGetLastError();
+        return MEDUSA_OK;
+    }
+    if (at.type == cudaMemoryTypeUnregistered)
+        return fail(MEDUSA_ERR_INVALID_ARG,
+                    "%s: a result pointer is pageable host memory (device or pinned host memory)",
+                    who);
+    if (at.type == cudaMemoryTypeHost && at.devicePointer != p)
+        return fail(MEDUSA_ERR_INVALID_ARG,
+                    "%s: a pinned host result buffer is not mapped at the same device address",
+                    who);
+    return MEDUSA_OK;
+}
+
 medusa_status check_posterior(const char *who, medusa_dtype dtype, const void *logits,
                               const int32_t *tokens, const int32_t *parent, const int32_t *depth,
                               int B, int R, int V, int K, medusa_accept_mode mode, float eps,
@@ -416,7 +440,11 @@ medusa_status check_posterior(const char *who, medusa_dtype dtype, const void *l
         return fail(MEDUSA_ERR_INVALID_ARG, "%s: eps, delta and temperature must be > 0", who);
     if (!aligned16(logits))
         return fail(MEDUSA_ERR_INVALID_ARG, "%s: logits must be 16-byte aligned", who);
-    return check_ws(ws, ws_bytes, posterior_workspace_bytes(B, R), who);
+    if (medusa_status s = check_ws(ws, ws_bytes, posterior_workspace_bytes(B, R), who)) return s;
+    const void *outs[4] = {accept_len, path, path_tokens, next_token};
+    for (const void *o : outs)
+        if (medusa_status s = check_result_pointer(o, who)) return s;
+    return MEDUSA_OK;
 }
 
 // Host checks of the commit arguments shared by both commit entry points.
@@ -458,6 +486,7 @@ medusa_status medusa_evaluate_posterior(medusa_dtype dtype, const void *logits,
                                           mode, eps, delta, temperature, accept_len, path,
                                           path_tokens, next_token, ws, ws_bytes))
         return s;
+    if (medusa_status s = check_result_pointer(accept, who)) return s;
     cudaError_t e = launch_posterior(dtype, logits, tokens, parent, depth, B, R, V, K, mode, eps,
                                      delta, temperature, accept_len, path, path_tokens, next_token,
                                      accept, nullptr, nullptr, nullptr, 0, 0, nullptr, ws,
@@ -479,6 +508,7 @@ medusa_status medusa_evaluate_posterior_commit(
                                           mode, eps, delta, temperature, accept_len, path,
                                           path_tokens, next_token, ws, ws_bytes))
         return s;
+    if (medusa_status s = check_result_pointer(accept, who)) return s;
     if (medusa_status s = check_commit(who, dtype, k_cache, v_cache, prefix_len, new_prefix_len,
                                        H, dh))
         return s;

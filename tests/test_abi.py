@@ -233,3 +233,12 @@ def test_workspace_sizes(L):
 def test_device_status_helpers_reject_null(L):
     assert L.medusa_read_device_status(None, None, None) == 1
     assert L.medusa_clear_device_status(None, None) == 1
+
+
+def test_binding_refuses_pageable_result_buffers():
+    """The binding passes a posterior result as a CUDA tensor or pinned host
+    memory only; an ordinary CPU tensor is refused before any call."""
+    import torch
+    with pytest.raises(ValueError):
+        m._result_ptr(torch.zeros(3, dtype=torch.int32), "accept_len")
+    assert m._result_ptr(None, "accept") is None
