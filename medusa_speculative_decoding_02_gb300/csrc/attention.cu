@@ -86,12 +86,13 @@ struct AttnArgs {
 // memory).  Every thread reads its S half-row, masks it (slots past the
 // range; tree slots that are not ancestors-or-self of the row) and writes
 // P = 2^(s*scale*log2e - m) back over the S columns it read: the row max is
-// taken on the raw scores and scaled once, the scale enters the exponent
-// through one FMA, and the exponential is the hardware's ex2.approx (P is
-// rounded to bf16 next).  The row reference m is raised only when a
-// sub-chunk's max exceeds it by more than 2^8; the threads then rescale
-// their O row in tensor memory.  Otherwise P may reach 2^8, harmless in bf16
-// and fp32.  The row sum adds the bf16-rounded weights the MMA uses.  The CTA
+// taken on the raw scores (three-input maxima) and scaled once, the scale
+// enters the exponent through a packed two-score FMA, and the exponential is
+// the hardware's ex2.approx (P is rounded to bf16 next).  The row reference
+// m is raised only when a sub-chunk's max exceeds it by more than 2^8; the
+// threads then rescale their O row in tensor memory.  Otherwise P may reach
+// 2^8, harmless in bf16 and fp32.  The row sum adds the fp32 weights (packed
+// adds) while the MMA uses their bf16 rounding, as flash attention does.  The CTA
 // writes one unnormalised partial (O, m, l) per row; tree_attn_combine_kernel
 // merges the ranges.  Every mbarrier wait is bounded; on a timeout the CTA
 // records MEDUSA_DEV_TIMEOUT, stops, waits once more (bounded) for its MMAs
@@ -304,13 +305,7 @@ __global__ void __launch_bounds__(256, 2) tree_attn_tc_kernel(AttnArgs a) {
         }
         const int kc0 = k0 + half * HALF;
         const bool masked = (k0 + kTcSub > P || k0 + kTcSub > kend) && rows_live;
-        float mx[4] = {-INFINITY, -INFINITY, -INFINITY, -INFINITY};
-        if (!masked) {
-#pragma unroll
-            for (int e = 0; e < HALF; ++e) {
-                mx[e & 3] = fmaxf(mx[e & 3], x[e]);
-            }
-        } else {
+        if (masked) {
 #pragma unroll
             for (int e = 0; e < HALF; ++e) {
                 const int key = kc0 + e;
@@ -322,16 +317,24 @@ __global__ void __launch_bounds__(256, 2) tree_attn_tc_kernel(AttnArgs a) {
                     vis = (w >> (t & 63)) & 1u;
                 }
                 x[e] = vis ? x[e] : -INFINITY;
-                mx[e & 3] = fmaxf(mx[e & 3], x[e]);
             }
         }
+        // the half-row's max with three-input maxima (two accumulators)
+        float mxa = max3f(x[0], x[1], x[2]), mxb = max3f(x[3], x[4], x[5]);
+#pragma unroll
+        for (int e = 6; e + 3 < HALF; e += 4) {
+            mxa = max3f(mxa, x[e], x[e + 1]);
+            mxb = max3f(mxb, x[e + 2], x[e + 3]);
+        }
+        static_assert(HALF % 4 == 0, "the max loop leaves the last two scores");
+        mxa = max3f(mxa, x[HALF - 2], x[HALF - 1]);
         // row max of the sub-chunk: halves exchange through the dead K_j tile
         // (it is refilled only after the barrier that ends this iteration)
         float *xch = reinterpret_cast<float *>(k_s);
         // (scores are scaled into log2 units here and inside the exponent:
         // the scale is positive, so the max of the scaled scores is the
         // scaled max)
-        xch[half * 128 + lrow] = fmaxf(fmaxf(mx[0], mx[1]), fmaxf(mx[2], mx[3])) * a.scale_log2;
+        xch[half * 128 + lrow] = fmaxf(mxa, mxb) * a.scale_log2;
         __syncthreads();
         const float cm = fmaxf(xch[lrow], xch[128 + lrow]);
         const bool raise = cm > m_run + kRescaleLog2;
@@ -341,18 +344,21 @@ __global__ void __launch_bounds__(256, 2) tree_attn_tc_kernel(AttnArgs a) {
         m_run = m_new;
         const float mu = (m_run == -INFINITY) ? 0.f : m_run;
         if (rows_live) {
-            float ls[4] = {0.f, 0.f, 0.f, 0.f};
+            // two scores per packed FMA and per packed add
+            const float2 sc2 = make_float2(a.scale_log2, a.scale_log2);
+            const float2 nm2 = make_float2(-mu, -mu);
+            float2 ls[2] = {make_float2(0.f, 0.f), make_float2(0.f, 0.f)};
             uint32_t pk[HALF / 2];
 #pragma unroll
             for (int e = 0; e < HALF; e += 2) {
-                const uint32_t w = pack_bf16(ex2_approx(fmaf(x[e], a.scale_log2, -mu)),
-                                             ex2_approx(fmaf(x[e + 1], a.scale_log2, -mu)));
-                pk[e / 2] = w;
-                // the row sum adds the rounded weights the MMA uses, so that the
-                // output is an exact convex combination of V rows under them
-                ls[(e / 2) & 3] += bf_lo(w) + bf_hi(w);
+                const float2 t = __ffma2_rn(make_float2(x[e], x[e + 1]), sc2, nm2);
+                const float p0 = ex2_approx(t.x), p1 = ex2_approx(t.y);
+                pk[e / 2] = pack_bf16(p0, p1);
+                // the row sum adds the fp32 weights; the MMA uses their bf16
+                // rounding (relative difference <= 2^-9 per weight)
+                ls[(e / 2) & 1] = __fadd2_rn(ls[(e / 2) & 1], make_float2(p0, p1));
             }
-            l_run += (ls[0] + ls[1]) + (ls[2] + ls[3]);
+            l_run += (ls[0].x + ls[0].y) + (ls[1].x + ls[1].y);
             // P over the S columns this thread read: keys half*32.. -> columns
             // half*32 .. half*32+15
             tc::tmem_st16(t_s + lane_base + half * HALF, pk);

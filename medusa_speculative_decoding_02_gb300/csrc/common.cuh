@@ -40,6 +40,14 @@ __device__ __forceinline__ float ex2_approx(float x) {
     return y;
 }
 
+// Three-input maximum, one instruction on this architecture; like fmaxf, a
+// NaN operand is ignored unless all three are NaN.
+__device__ __forceinline__ float max3f(float a, float b, float c) {
+    float d;
+    asm("max.f32 %0, %1, %2, %3;" : "=f"(d) : "f"(a), "f"(b), "f"(c));
+    return d;
+}
+
 // bf16 pair packed in a 32-bit word -> two floats (exact widening).
 __device__ __forceinline__ float bf_lo(uint32_t w) { return __uint_as_float(w << 16); }
 __device__ __forceinline__ float bf_hi(uint32_t w) { return __uint_as_float(w & 0xffff0000u); }
