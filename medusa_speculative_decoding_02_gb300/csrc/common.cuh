@@ -115,7 +115,9 @@ __device__ __forceinline__ bool better(float va, int ia, float vb, int ib) {
 // typical-acceptance logits and, with the fused commit, the cache pointers
 // and prefix lengths), spec_sample_kernel and spec_select_kernel
 // (draft tokens, their p and q logits and uniforms; the chain's tokens), and
-// the L2 prefetches of heads_w1/heads_w2 (weights, never written).  Because
+// the L2 prefetches of heads_w1/heads_w2 (weights, never written) and of
+// posterior_rows_kernel (its slice of the logits: a prefetch consumes no
+// data, so it would be safe even if an earlier grid were writing them).  Because
 // every kernel of the library waits before it triggers, a kernel that starts
 // early can only overlap its immediate predecessor; all older grids have
 // completed and their writes are visible.  Triggering before the wait in any

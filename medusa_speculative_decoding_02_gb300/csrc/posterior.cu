@@ -68,7 +68,6 @@ template <typename T, bool TYPICAL>
 __global__ void __launch_bounds__(kRowThreads)
 posterior_rows_kernel(const T *__restrict__ logits, int R, int V, int splits, float y_scale,
                       RowPart *__restrict__ parts) {
-    pdl_enter();
     constexpr int VN = Vec16<T>::N;
     constexpr int U = 4;
     __shared__ float s_val[kRowThreads / kWarp];
@@ -79,6 +78,17 @@ posterior_rows_kernel(const T *__restrict__ logits, int R, int V, int splits, fl
     const int nvec = V / VN;
     const int v_lo = (int)(((long long)sp * nvec) / splits);
     const int v_hi = (int)(((long long)(sp + 1) * nvec) / splits);
+    // This CTA's slice of the logits is pulled into L2 while the previous
+    // kernel finishes: a prefetch stays inside the logits tensor and reads
+    // nothing into the kernel, and L2 stays coherent with any writer, so it
+    // may precede the wait.  Four threads split the slice.
+    if (threadIdx.x < 4) {
+        const int n = v_hi - v_lo;
+        const int q0 = v_lo + (int)((long long)threadIdx.x * n / 4);
+        const int q1 = v_lo + (int)((long long)(threadIdx.x + 1) * n / 4);
+        if (q1 > q0) prefetch_l2_bulk(x + q0, (unsigned)(q1 - q0) * 16u);
+    }
+    pdl_enter();
     // argmax by 16-byte group: the running best group (its max, index and
     // raw words) moves only on a strictly larger group max, so the earliest
     // group holding the thread's max wins; its first element equal to that
