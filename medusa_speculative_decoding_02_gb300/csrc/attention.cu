@@ -103,6 +103,7 @@ struct AttnArgs {
 // records MEDUSA_DEV_DRAIN_TIMEOUT over any earlier code, so the caller
 // knows the outputs and the tensor memory may be corrupt.
 constexpr int kTcSub = 64;               // keys per pipeline stage
+constexpr int kTailMax = 1;              // tree rows past a full 128-row tile on CUDA cores
 constexpr int kTcStages = 3;
 constexpr float kRescaleLog2 = 8.f;      // lazy-rescale threshold (log2 units)
 constexpr uint32_t kWaitPolls = 1u << 16;  // the drain's limit (the key loop's: a.wait_polls)
@@ -118,6 +119,17 @@ struct TcSmem {
     static constexpr int BAR_OFF = kTcStages * STAGE_BYTES;  // mbarriers, TMEM holder, flag
     // 2 x (TOTAL + 1 KB reserved per CTA) must stay within a 196 KB carveout
     static constexpr int TOTAL = BAR_OFF + 64;
+    // the tail variant adds the tail row's q in fp32, its weights, the warp
+    // maxima and its mask words, within the same carveout (a larger one
+    // costs the tile ~10 % at 128 live rows)
+    static constexpr int TQ_OFF = TOTAL;
+    static constexpr int TP_OFF = TQ_OFF + kTailMax * DH * 4;
+    static constexpr int TMX_OFF = TP_OFF + kTailMax * kTcSub * 4;
+    static constexpr int TAM_OFF = TMX_OFF + kTailMax * 4 * 4;
+    static constexpr int TOTAL_TAIL = TAM_OFF + kTailMax * 3 * 8;
+    static_assert(TQ_OFF % 16 == 0 && TMX_OFF % 16 == 0 && TAM_OFF % 8 == 0,
+                  "tail areas aligned");
+    static_assert(2 * (TOTAL_TAIL + 1024) <= 196 * 1024, "two tail-variant CTAs per SM");
 };
 
 // Issue the cp.async copies of sub-chunk keys [k0, k0+kTcSub) (rows past kend
@@ -149,9 +161,24 @@ __device__ __forceinline__ void tc_load_stage(unsigned char *k_s, unsigned char 
     cp_async_commit();
 }
 
-// WIDE: trees of more than 128 rows (row tiles, four mask words per row)
-template <int DH, bool WIDE>
+// WIDE: trees of more than 128 rows (row tiles, four mask words per row).
+// TAIL (dh 128): trees of 129 .. 128 + kTailMax rows in one 128-row tile; the
+// rows past the tile are computed on the CUDA cores by the tile's own threads
+// in the windows where they wait for the tensor cores: warps 4-7 score the
+// sub-chunk's 64 keys against the tail rows while the S MMA runs (key
+// (warp-4)*16 + lane/2, dh half lane%2); the tail rows' max rides on the
+// tile's row-max barrier and their reference moves by the same lazy rule;
+// the weights go to shared memory, and after the P barrier, while thread 0
+// issues the P V MMA, warp w adds keys 8w..8w+7 into its own partial of the
+// tail rows' O (four columns per lane).  The eight partials are summed once,
+// after the key loop.  The row-max exchange of the tile moves out of the K
+// tile, which warps 4-7 read while other warps are already past the S wait,
+// into tensor memory: each thread writes its half-row max into a column of
+// its own lane that its S read has freed (16 or 48; P takes 0-15 and 32-47).
+template <int DH, bool WIDE, bool TAIL>
 __global__ void __launch_bounds__(256, 2) tree_attn_tc_kernel(AttnArgs a) {
+    static_assert(!TAIL || (WIDE && DH == 128), "the tail variant: dh 128, mask words past 128");
+    static_assert(kTailMax == 1, "the tail bookkeeping below holds one row");
     pdl_enter();
     using L = TcSmem<DH>;
     constexpr int HALF = kTcSub / 2;  // keys per thread per sub-chunk
@@ -169,7 +196,8 @@ __global__ void __launch_bounds__(256, 2) tree_attn_tc_kernel(AttnArgs a) {
     const int rt = WIDE ? blockIdx.x - h * a.row_tiles : 0;
     const int split = blockIdx.y, b = blockIdx.z;
     const int R = a.R, H = a.H;
-    const int tid = threadIdx.x, warp = tid >> 5;
+    const int tid = threadIdx.x, warp = tid >> 5, lane = tid & 31;
+    const int T = TAIL ? R - 128 : 0;  // tail rows
     // warp w reads TMEM lanes 32*(w%4)..: lane = tid % 128 holds tree row
     // row0 + lane; half = column half
     const int lrow = tid & 127, half = tid >> 7;
@@ -189,6 +217,7 @@ __global__ void __launch_bounds__(256, 2) tree_attn_tc_kernel(AttnArgs a) {
     if (bad_cache) set_status(a.status, MEDUSA_DEV_BAD_CACHE);
     if (kend <= kbeg || bad_cache) {
         if (row < R && half == 0) a.part_ml[pbase + row] = make_float2(-INFINITY, 0.f);
+        if (TAIL && tid < T) a.part_ml[pbase + 128 + tid] = make_float2(-INFINITY, 0.f);
         return;
     }
     const int nsub = (kend - kbeg + kTcSub - 1) / kTcSub;
@@ -221,13 +250,38 @@ __global__ void __launch_bounds__(256, 2) tree_attn_tc_kernel(AttnArgs a) {
     if (nsub > 1) tc_load_stage<DH>(stage_k(1), stage_v(1), kc, vc, kbeg + kTcSub, kend, H, h, tid);
     // this row's ancestor-mask words (R <= 256: up to four)
     uint64_t am0 = 0, am1 = 0, am2 = 0, am3 = 0;
+    const int W = (R + 63) / 64;
     if (kend > P && row < R) {
-        const int W = (R + 63) / 64;
         const uint64_t *mr = a.anc_mask + ((size_t)b * R + row) * W;
         am0 = mr[0];
         if (W > 1) am1 = mr[1];
         if (WIDE && W > 2) am2 = mr[2];
         if (WIDE && W > 3) am3 = mr[3];
+    }
+    // ---- tail rows: q in fp32 and mask words in shared memory, and the
+    // per-thread state (references identical in every thread)
+    float *tq = reinterpret_cast<float *>(tc_raw + L::TQ_OFF);     // [kTailMax][DH]
+    float *tp = reinterpret_cast<float *>(tc_raw + L::TP_OFF);     // [kTailMax][64] weights
+    float *tmx = reinterpret_cast<float *>(tc_raw + L::TMX_OFF);   // [kTailMax][4] warp maxima
+    uint64_t *tam = reinterpret_cast<uint64_t *>(tc_raw + L::TAM_OFF);  // [kTailMax][3]
+    float tm[kTailMax], tl[kTailMax], tx[kTailMax], to[kTailMax][4];
+#pragma unroll
+    for (int t = 0; t < kTailMax; ++t) {
+        tm[t] = -INFINITY;
+        tl[t] = 0.f;
+        tx[t] = -INFINITY;
+#pragma unroll
+        for (int c = 0; c < 4; ++c) to[t][c] = 0.f;
+    }
+    if constexpr (TAIL) {
+        for (int e = tid; e < T * DH; e += 256) {
+            const int t = e / DH, c = e - t * DH;
+            tq[e] = __bfloat162float(a.q[(((size_t)b * R + 128 + t) * H + h) * DH + c]);
+        }
+        if (tid < T * 3) {
+            const int t = tid / 3, w = tid - t * 3;
+            tam[tid] = w < W ? a.anc_mask[((size_t)b * R + 128 + t) * W + w] : 0ull;
+        }
     }
     if (tid == 0) {
         tc::mbar_init(&bar_s, 1);
@@ -292,6 +346,50 @@ __global__ void __launch_bounds__(256, 2) tree_attn_tc_kernel(AttnArgs a) {
             tc_load_stage<DH>(stage_k(j + 2), stage_v(j + 2), kc, vc, k0 + 2 * kTcSub, kend,
                               H, h, tid);
         __syncwarp();
+        if constexpr (TAIL) {
+            if (warp >= 4) {
+                // ---- tail scores: key kk against each tail row, dh half hd
+                // (column block hd of the K tile), halves summed by a shuffle
+                const int kk = (warp - 4) * 16 + (lane >> 1), hd = lane & 1;
+                const unsigned char *kb = k_s + hd * kTcSub * 128;
+#pragma unroll
+                for (int t = 0; t < kTailMax; ++t) {
+                    if (t >= T) break;
+                    const float *q = tq + t * DH + hd * 64;
+                    float acc[4] = {0.f, 0.f, 0.f, 0.f};
+#pragma unroll
+                    for (int c = 0; c < 8; ++c) {
+                        const float4 qa = *reinterpret_cast<const float4 *>(q + c * 8);
+                        const float4 qb = *reinterpret_cast<const float4 *>(q + c * 8 + 4);
+                        const uint4 kv = *reinterpret_cast<const uint4 *>(kb + tc::sw128(kk, c));
+                        acc[0] = fmaf(qa.x, bf_lo(kv.x), acc[0]);
+                        acc[1] = fmaf(qa.y, bf_hi(kv.x), acc[1]);
+                        acc[2] = fmaf(qa.z, bf_lo(kv.y), acc[2]);
+                        acc[3] = fmaf(qa.w, bf_hi(kv.y), acc[3]);
+                        acc[0] = fmaf(qb.x, bf_lo(kv.z), acc[0]);
+                        acc[1] = fmaf(qb.y, bf_hi(kv.z), acc[1]);
+                        acc[2] = fmaf(qb.z, bf_lo(kv.w), acc[2]);
+                        acc[3] = fmaf(qb.w, bf_hi(kv.w), acc[3]);
+                    }
+                    float sc = (acc[0] + acc[1]) + (acc[2] + acc[3]);
+                    sc += __shfl_xor_sync(0xffffffffu, sc, 1);
+                    const int key = k0 + kk;
+                    bool vis = key < kend;
+                    if (vis && key >= P) {
+                        const int tt = key - P;
+                        const uint64_t w = tt < 64 ? tam[t * 3] : tt < 128 ? tam[t * 3 + 1]
+                                                                           : tam[t * 3 + 2];
+                        vis = (w >> (tt & 63)) & 1u;
+                    }
+                    tx[t] = vis ? sc : -INFINITY;
+                    float mx = tx[t];
+#pragma unroll
+                    for (int o = 2; o < kWarp; o <<= 1)
+                        mx = fmaxf(mx, __shfl_xor_sync(0xffffffffu, mx, o));
+                    if (lane == 0) tmx[t * 4 + warp - 4] = mx;
+                }
+            }
+        }
         if (!tc::mbar_wait_bounded(&bar_s, j & 1, a.wait_polls)) failed = 1;
         tc::fence_after_sync();
 
@@ -329,20 +427,55 @@ __global__ void __launch_bounds__(256, 2) tree_attn_tc_kernel(AttnArgs a) {
         static_assert(HALF % 4 == 0, "the max loop leaves the last two scores");
         mxa = max3f(mxa, x[HALF - 2], x[HALF - 1]);
         // row max of the sub-chunk: halves exchange through the dead K_j tile
-        // (it is refilled only after the barrier that ends this iteration)
-        float *xch = reinterpret_cast<float *>(k_s);
+        // (it is refilled only after the barrier that ends this iteration) or,
+        // in the tail variant, through tensor memory
         // (scores are scaled into log2 units here and inside the exponent:
         // the scale is positive, so the max of the scaled scores is the
         // scaled max)
-        xch[half * 128 + lrow] = fmaxf(mxa, mxb) * a.scale_log2;
-        __syncthreads();
-        const float cm = fmaxf(xch[lrow], xch[128 + lrow]);
+        const float hmx = fmaxf(mxa, mxb) * a.scale_log2;
+        float cm;
+        if constexpr (TAIL) {
+            tc::tmem_st1(t_s + lane_base + half * HALF + 16, hmx);
+            tc::tmem_wait_st();
+            tc::fence_before_sync();
+            __syncthreads();
+            tc::fence_after_sync();
+            cm = fmaxf(hmx, tc::tmem_ld1(t_s + lane_base + (1 - half) * HALF + 16));
+        } else {
+            float *xch = reinterpret_cast<float *>(k_s);
+            xch[half * 128 + lrow] = hmx;
+            __syncthreads();
+            cm = fmaxf(xch[lrow], xch[128 + lrow]);
+        }
         const bool raise = cm > m_run + kRescaleLog2;
         const float m_new = raise ? cm : m_run;
         const float alpha = raise ? exp2f(m_run - m_new) : 1.f;  // 0 when m_run = -inf
         l_run *= alpha;
         m_run = m_new;
         const float mu = (m_run == -INFINITY) ? 0.f : m_run;
+        if constexpr (TAIL) {
+            // ---- tail rows: reference (every thread alike), then the
+            // weights of warps 4-7's keys into shared memory
+#pragma unroll
+            for (int t = 0; t < kTailMax; ++t) {
+                if (t >= T) break;
+                const float4 w4 = *reinterpret_cast<const float4 *>(tmx + t * 4);
+                const float tcm = fmaxf(fmaxf(w4.x, w4.y), fmaxf(w4.z, w4.w)) * a.scale_log2;
+                if (tcm > tm[t] + kRescaleLog2) {
+                    const float al = exp2f(tm[t] - tcm);  // 0 when the reference was -inf
+                    tl[t] *= al;
+#pragma unroll
+                    for (int c = 0; c < 4; ++c) to[t][c] *= al;
+                    tm[t] = tcm;
+                }
+                if (warp >= 4 && (lane & 1) == 0) {
+                    const float tmu = tm[t] == -INFINITY ? 0.f : tm[t];
+                    const float p = ex2_approx(fmaf(tx[t], a.scale_log2, -tmu));
+                    tp[t * kTcSub + (warp - 4) * 16 + (lane >> 1)] = p;
+                    tl[t] += p;
+                }
+            }
+        }
         if (rows_live) {
             // two scores per packed FMA and per packed add
             const float2 sc2 = make_float2(a.scale_log2, a.scale_log2);
@@ -393,6 +526,27 @@ __global__ void __launch_bounds__(256, 2) tree_attn_tc_kernel(AttnArgs a) {
             tc::mma_commit(&bar_o);
         }
         __syncwarp();
+        if constexpr (TAIL) {
+            // ---- tail P V: keys 8w..8w+7 into this warp's partial, four
+            // columns per lane (V_j stays until the next iteration's barrier)
+            const int col0 = lane * 4;
+            const unsigned char *vb = v_s + (col0 / 64) * kTcSub * 128 + (col0 % 8) * 2;
+            const int vch = (col0 % 64) / 8;
+#pragma unroll
+            for (int t = 0; t < kTailMax; ++t) {
+                if (t >= T) break;
+#pragma unroll
+                for (int i = 0; i < 8; ++i) {
+                    const int kk = warp * 8 + i;
+                    const float p = tp[t * kTcSub + kk];
+                    const uint2 wv = *reinterpret_cast<const uint2 *>(vb + tc::sw128(kk, vch));
+                    to[t][0] = fmaf(p, bf_lo(wv.x), to[t][0]);
+                    to[t][1] = fmaf(p, bf_hi(wv.x), to[t][1]);
+                    to[t][2] = fmaf(p, bf_lo(wv.y), to[t][2]);
+                    to[t][3] = fmaf(p, bf_hi(wv.y), to[t][3]);
+                }
+            }
+        }
         ++done;
     }
     // ---- wait for the last P V, then write the partial rows
@@ -422,13 +576,41 @@ __global__ void __launch_bounds__(256, 2) tree_attn_tc_kernel(AttnArgs a) {
             }
         }
     }
-    // row sums: halves exchange through stage 0 (no copy is in flight now)
+    // row sums: halves exchange through stage 0 (no copy is in flight now);
+    // the tail rows' per-warp partials go there as well, past the first 4 KB
     float *xs = reinterpret_cast<float *>(tc_raw);
+    float *tob = reinterpret_cast<float *>(tc_raw + 4096);  // [8 warps][kTailMax][DH]
+    float *tlb = tob + 8 * kTailMax * DH;                    // [4 warps][kTailMax]
     xs[half * 128 + lrow] = l_run;
+    if constexpr (TAIL) {
+#pragma unroll
+        for (int t = 0; t < kTailMax; ++t) {
+            if (t >= T) break;
+            *reinterpret_cast<float4 *>(tob + (warp * kTailMax + t) * DH + lane * 4) =
+                make_float4(to[t][0], to[t][1], to[t][2], to[t][3]);
+            const float ls = warp_sum(tl[t]);
+            if (warp >= 4 && lane == 0) tlb[(warp - 4) * kTailMax + t] = ls;
+        }
+    }
     __syncthreads();
     if (half == 0 && row < R) {
         const float l = xs[lrow] + xs[128 + lrow];
         a.part_ml[pbase + row] = ok ? make_float2(m_run, l) : make_float2(-INFINITY, 0.f);
+    }
+    if constexpr (TAIL) {
+        for (int e = tid; e < T * DH; e += 256) {
+            const int t = e / DH, c = e - t * DH;
+            float o = 0.f;
+#pragma unroll
+            for (int w = 0; w < 8; ++w) o += tob[(w * kTailMax + t) * DH + c];
+            if (ok) a.part_o[(pbase + 128 + t) * DH + c] = o;
+        }
+        if (tid < T) {
+            float l = 0.f;
+#pragma unroll
+            for (int w = 0; w < 4; ++w) l += tlb[w * kTailMax + tid];
+            a.part_ml[pbase + 128 + tid] = ok ? make_float2(tm[0], l) : make_float2(-INFINITY, 0.f);
+        }
     }
     tc::fence_before_sync();
     __syncthreads();
@@ -596,11 +778,14 @@ size_t align256(size_t x) { return (x + 255) & ~size_t(255); }
 // two CTAs per SM over the whole grid at P_max.
 struct TcPlan {
     int ns, chunk, row_tiles;
+    bool tail;  // 129 .. 128 + kTailMax rows: one tile, the rest on CUDA cores
 };
 
-TcPlan tc_plan(int B, int H, int R, int P_max) {
+TcPlan tc_plan(int B, int H, int R, int P_max, int dh) {
     TcPlan p;
-    p.row_tiles = (R + 127) / 128;
+    // (the tail code reads dh as two 64-column blocks: dh 64 keeps two tiles)
+    p.tail = dh == 128 && R > 128 && R - 128 <= kTailMax;
+    p.row_tiles = p.tail ? 1 : (R + 127) / 128;
     const int nsub = (P_max + R + kTcSub - 1) / kTcSub;
     const int waves = B == 1 ? 1 : 2;
     const int per_head =
@@ -615,7 +800,7 @@ TcPlan tc_plan(int B, int H, int R, int P_max) {
 
 size_t attention_workspace_bytes(medusa_dtype dtype, int B, int R, int H, int dh, int P_max) {
     if (dtype == MEDUSA_F32) return MEDUSA_WS_HEADER;
-    const TcPlan tp = tc_plan(B, H, R, P_max);
+    const TcPlan tp = tc_plan(B, H, R, P_max, dh);
     const size_t rows = (size_t)B * H * tp.ns * R;
     return MEDUSA_WS_HEADER + align256(rows * dh * sizeof(float)) + align256(rows * sizeof(float2));
 }
@@ -639,7 +824,7 @@ cudaError_t launch_tree_attention(medusa_dtype dtype, const void *q, const void 
         note_launch();
         return e;
     }
-    const TcPlan tp = tc_plan(B, H, R, P_max);
+    const TcPlan tp = tc_plan(B, H, R, P_max, dh);
     const int NS = tp.ns;
     const size_t rows = (size_t)B * H * NS * R;
     char *w = static_cast<char *>(ws) + MEDUSA_WS_HEADER;
@@ -664,9 +849,13 @@ cudaError_t launch_tree_attention(medusa_dtype dtype, const void *q, const void 
     a.part_ml = part_ml;
     a.status = status;
     const bool wide = tp.row_tiles > 1;
-    auto kern = wide ? tree_attn_tc_kernel<64, true> : tree_attn_tc_kernel<64, false>;
-    if (dh == 128) kern = wide ? tree_attn_tc_kernel<128, true> : tree_attn_tc_kernel<128, false>;
-    const int smem = dh == 128 ? TcSmem<128>::TOTAL : TcSmem<64>::TOTAL;
+    auto kern = wide ? tree_attn_tc_kernel<64, true, false> : tree_attn_tc_kernel<64, false, false>;
+    if (dh == 128)
+        kern = tp.tail ? tree_attn_tc_kernel<128, true, true>
+               : wide  ? tree_attn_tc_kernel<128, true, false>
+                       : tree_attn_tc_kernel<128, false, false>;
+    int smem = dh == 128 ? TcSmem<128>::TOTAL : TcSmem<64>::TOTAL;
+    if (tp.tail) smem = TcSmem<128>::TOTAL_TAIL;
     if ((e = cudaFuncSetAttribute(kern, cudaFuncAttributeMaxDynamicSharedMemorySize, smem)))
         return e;
     e = launch_pdl(kern, dim3(H * tp.row_tiles, NS, B), dim3(256), (size_t)smem, stream, a);

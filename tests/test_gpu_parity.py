@@ -399,10 +399,14 @@ def test_attention_tiny_f32(dev):
     (1, (4, 3, 2, 2, 1), 64, 4, 128, (1023,)), (3, (8, 4, 4), 128, 2, 128, (5, 300, 64)),
     (1, (16, 16), 255, 1, 128, (100,)), (2, (4, 4, 2), 32, 2, 64, (128, 0)),
     (1, (1,), 1, 2, 128, (10,)), (2, (8, 4, 4, 2, 2), 200, 1, 64, (65, 1)),
-    (1, (4, 3, 2, 2, 1), 64, 2, 64, (3000,)), (3, (4, 4, 2), 32, 3, 128, (2500, 40, 1700))])
+    (1, (4, 3, 2, 2, 1), 64, 2, 64, (3000,)), (3, (4, 4, 2), 32, 3, 128, (2500, 40, 1700)),
+    (2, (8, 4, 4, 2, 2), 129, 3, 128, (77, 1)), (1, (8, 4, 4, 2, 2), 130, 2, 128, (200,)),
+    (2, (8, 4, 4), 128, 2, 64, (90, 3))])
 def test_attention_shapes(dev, B, s, n, H, dh, prefix):
     """Ragged prefixes (0, 1, non-multiples of the 64-key tile), tree sizes
-    from 2 to 256 rows (both warp-count instantiations), dh 64 and 128."""
+    from 2 to 256 rows (both warp-count instantiations), dh 64 and 128.  A
+    tree of 129 rows at dh 128 takes one tile and computes its last row on the
+    CUDA cores; 130 and 131 rows, and 129 rows at dh 64, take two tiles."""
     cfg = synth.v7b().replace(name=f"att{B}{n}{H}{dh}{prefix}", B=B, s=s, n=n, H=H, dh=dh,
                               prefix=prefix)
     ot = oracle_tree_for(np.random.default_rng(n + dh), s, n, B, prefix)
@@ -439,14 +443,17 @@ def test_attention_sweep(dev, n, P):
     check_close(g, o, cfg.name)
 
 
-@pytest.mark.parametrize("P,growth", [(1024, 0.02), (8192, 0.004), (700, -0.03)])
-def test_attention_growing_scores(dev, P, growth):
+@pytest.mark.parametrize("P,growth,n", [(1024, 0.02, 64), (8192, 0.004, 64), (700, -0.03, 64),
+                                         (2048, 0.01, 128), (900, -0.03, 128)])
+def test_attention_growing_scores(dev, P, growth, n):
     """Key rows scaled by exp(growth * slot): the scores' row maxima grow (or
     shrink) steadily along the prefix, so later 64-key sub-chunks raise the
     softmax reference by more than 2^8 many times and the O accumulator is
     rescaled in tensor memory (growth > 0), or the first sub-chunk dominates
-    (growth < 0)."""
-    cfg = synth.v7b().replace(name=f"grow{P}{growth}", H=4, prefix=(P,))
+    (growth < 0).  With n = 128 (129 rows) the row past the tensor-core tile
+    moves its own reference by the same rule."""
+    s = (4, 3, 2, 2, 1) if n == 64 else (8, 4, 4, 2, 2)
+    cfg = synth.v7b().replace(name=f"grow{P}{growth}{n}", H=4, prefix=(P,), s=s, n=n)
     ot = oracle_tree_for(np.random.default_rng(P), cfg.s, cfg.n, 1, cfg.prefix)
     ai = synth.attention_inputs(cfg)
     k = synth.bf16_bits_to_f32(ai.k_cache[0])
