@@ -104,6 +104,7 @@ struct AttnArgs {
 // knows the outputs and the tensor memory may be corrupt.
 constexpr int kTcSub = 64;               // keys per pipeline stage
 constexpr int kTailMax = 1;              // tree rows past a full 128-row tile on CUDA cores
+constexpr int kTailMinSubs = 8;          // sub-chunks per CTA that make the tail path pay
 constexpr int kTcStages = 3;
 constexpr float kRescaleLog2 = 8.f;      // lazy-rescale threshold (log2 units)
 constexpr uint32_t kWaitPolls = 1u << 16;  // the drain's limit (the key loop's: a.wait_polls)
@@ -782,18 +783,30 @@ struct TcPlan {
 };
 
 TcPlan tc_plan(int B, int H, int R, int P_max, int dh) {
-    TcPlan p;
-    // (the tail code reads dh as two 64-column blocks: dh 64 keeps two tiles)
-    p.tail = dh == 128 && R > 128 && R - 128 <= kTailMax;
-    p.row_tiles = p.tail ? 1 : (R + 127) / 128;
     const int nsub = (P_max + R + kTcSub - 1) / kTcSub;
     const int waves = B == 1 ? 1 : 2;
-    const int per_head =
-        std::max(1, 2 * waves * device_sm_count() / std::max(1, B * H * p.row_tiles));
-    const int cps = std::max(2, (nsub + per_head - 1) / per_head);
-    p.ns = (nsub + cps - 1) / cps;
-    p.chunk = cps * kTcSub;
-    return p;
+    auto plan = [&](int row_tiles, bool tail) {
+        TcPlan p;
+        p.tail = tail;
+        p.row_tiles = row_tiles;
+        const int per_head =
+            std::max(1, 2 * waves * device_sm_count() / std::max(1, B * H * row_tiles));
+        const int cps = std::max(2, (nsub + per_head - 1) / per_head);
+        p.ns = (nsub + cps - 1) / cps;
+        p.chunk = cps * kTcSub;
+        return p;
+    };
+    // A tree one row past the tile (dh 128: the tail code reads dh as two
+    // 64-column blocks) takes one tile and the tail row when every CTA then
+    // runs at least kTailMinSubs sub-chunks: with fewer, the halved grid and
+    // the tail's own set-up and merge cost more than the second tile saves
+    // (129 rows, one sequence: prefix 512 23.0 against 18.2 us, 2048 30.3
+    // against 28.4 us, 8192 49.6 against 60.2 us).
+    if (dh == 128 && R > 128 && R - 128 <= kTailMax) {
+        const TcPlan t = plan(1, true);
+        if (t.chunk / kTcSub >= kTailMinSubs) return t;
+    }
+    return plan((R + 127) / 128, false);
 }
 
 }  // namespace

@@ -404,9 +404,8 @@ def test_attention_tiny_f32(dev):
     (2, (8, 4, 4), 128, 2, 64, (90, 3))])
 def test_attention_shapes(dev, B, s, n, H, dh, prefix):
     """Ragged prefixes (0, 1, non-multiples of the 64-key tile), tree sizes
-    from 2 to 256 rows (both warp-count instantiations), dh 64 and 128.  A
-    tree of 129 rows at dh 128 takes one tile and computes its last row on the
-    CUDA cores; 130 and 131 rows, and 129 rows at dh 64, take two tiles."""
+    from 2 to 256 rows (both warp-count instantiations), dh 64 and 128;
+    129, 130 and 131 rows here take two 128-row tiles (short key ranges)."""
     cfg = synth.v7b().replace(name=f"att{B}{n}{H}{dh}{prefix}", B=B, s=s, n=n, H=H, dh=dh,
                               prefix=prefix)
     ot = oracle_tree_for(np.random.default_rng(n + dh), s, n, B, prefix)
@@ -443,17 +442,19 @@ def test_attention_sweep(dev, n, P):
     check_close(g, o, cfg.name)
 
 
-@pytest.mark.parametrize("P,growth,n", [(1024, 0.02, 64), (8192, 0.004, 64), (700, -0.03, 64),
-                                         (2048, 0.01, 128), (900, -0.03, 128)])
-def test_attention_growing_scores(dev, P, growth, n):
+@pytest.mark.parametrize("P,growth,n,H", [(1024, 0.02, 64, 4), (8192, 0.004, 64, 4),
+                                           (700, -0.03, 64, 4), (8192, 0.004, 128, 32),
+                                           (900, -0.03, 128, 4)])
+def test_attention_growing_scores(dev, P, growth, n, H):
     """Key rows scaled by exp(growth * slot): the scores' row maxima grow (or
     shrink) steadily along the prefix, so later 64-key sub-chunks raise the
     softmax reference by more than 2^8 many times and the O accumulator is
     rescaled in tensor memory (growth > 0), or the first sub-chunk dominates
-    (growth < 0).  With n = 128 (129 rows) the row past the tensor-core tile
-    moves its own reference by the same rule."""
+    (growth < 0).  With n = 128 (129 rows) at prefix 8192 and 32 heads the
+    row past the tensor-core tile is computed on the CUDA cores and moves its
+    own reference by the same rule; at prefix 900 the tree takes two tiles."""
     s = (4, 3, 2, 2, 1) if n == 64 else (8, 4, 4, 2, 2)
-    cfg = synth.v7b().replace(name=f"grow{P}{growth}{n}", H=4, prefix=(P,), s=s, n=n)
+    cfg = synth.v7b().replace(name=f"grow{P}{growth}{n}", H=H, prefix=(P,), s=s, n=n)
     ot = oracle_tree_for(np.random.default_rng(P), cfg.s, cfg.n, 1, cfg.prefix)
     ai = synth.attention_inputs(cfg)
     k = synth.bf16_bits_to_f32(ai.k_cache[0])
@@ -461,8 +462,23 @@ def test_attention_growing_scores(dev, P, growth, n):
     f = np.exp(np.clip(growth * slot, -4.0, 4.0)).astype(np.float32)
     ai.k_cache[0] = synth.cast(k * f[:, None, None], "bf16")
     g = run_attention(dev, ai, ot["anc_mask"], cfg.P_max, cfg.dh)
-    o = oracle.tree_attention(ai.q, ai.k_cache, ai.v_cache, ai.prefix_len, ot["anc_mask"],
-                              1.0 / math.sqrt(cfg.dh))
+    o = oracle_attention_heads(ai, ot["anc_mask"], cfg.dh, list(range(cfg.H)))
+    check_close(g, o, cfg.name)
+
+
+@pytest.mark.parametrize("prefix", [(8192,), (4100, 8192), (8192, 5, 6000)],
+                         ids=["one", "two", "three"])
+def test_attention_tail_row(dev, prefix):
+    """Trees of 129 rows over long prefixes (32 heads of 128): one 128-row
+    tensor-core tile per key range, the last row on the CUDA cores of the
+    same CTAs.  Every head of every sequence against the oracle; ragged
+    prefixes, and a 5-slot prefix whose later key ranges are empty."""
+    cfg = synth.v7b().replace(name=f"tail{len(prefix)}", B=len(prefix), s=(8, 4, 4, 2, 2), n=128,
+                              prefix=prefix)
+    ot = oracle_tree_for(np.random.default_rng(len(prefix)), cfg.s, cfg.n, cfg.B, cfg.prefix)
+    ai = synth.attention_inputs(cfg)
+    g = run_attention(dev, ai, ot["anc_mask"], cfg.P_max, cfg.dh)
+    o = oracle_attention_heads(ai, ot["anc_mask"], cfg.dh, list(range(cfg.H)))
     check_close(g, o, cfg.name)
 
 
