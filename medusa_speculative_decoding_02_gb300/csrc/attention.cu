@@ -69,7 +69,9 @@ struct AttnArgs {
 // ------------------------------------------------------- tensor-core path ---
 //
 // tree_attn_tc_kernel: one CTA per (key range, head, 128-row tile of the
-// tree, sequence); trees of more than 128 rows take two tiles.  The keys of
+// tree, sequence); trees of more than 128 rows take two tiles, except a tree
+// of 129 rows over long key ranges, whose last row the tile's own threads
+// compute on the CUDA cores (the TAIL variant, below).  The keys of
 // a sequence are its cache slots 0 .. P+R-1, prefix and tree alike (they are
 // contiguous); a key range is `cps` consecutive sub-chunks of 64 keys.  K and
 // V of the sub-chunks stream through a three-stage cp.async ring in shared
