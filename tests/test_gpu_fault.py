@@ -8,7 +8,6 @@ copies with its fixed limit, free its tensor memory and return.  The context
 must stay usable: after the budget is restored and the status cleared, the
 same call on the same buffers matches the oracle again.
 """
-import math
 
 import numpy as np
 import pytest
@@ -41,8 +40,8 @@ def T(a, dev):
     return torch.from_numpy(a).to(dev)
 
 
-def attention_case(dev, n, prefix):
-    cfg = synth.v7b().replace(name=f"fault{n}_{prefix}", H=2, n=n,
+def attention_case(dev, n, prefix, H=2):
+    cfg = synth.v7b().replace(name=f"fault{n}_{prefix}_{H}", H=H, n=n,
                               s=(8, 4, 4, 2, 2) if n > 64 else (4, 3, 2, 2, 1), prefix=(prefix,))
     rng = np.random.default_rng(n + prefix)
     S = max(cfg.s)
@@ -59,8 +58,8 @@ def attention_case(dev, n, prefix):
                 anc_mask=T(ot["anc_mask"].view(np.int64), dev))
     ws = m.new_workspace(m.tree_attention_workspace_size(m.BF16, 1, cfg.R, cfg.H, cfg.dh,
                                                          cfg.P_max), dev)
-    ref = oracle.tree_attention(ai.q, ai.k_cache, ai.v_cache, ai.prefix_len, ot["anc_mask"],
-                                1.0 / math.sqrt(cfg.dh))
+    from test_gpu_parity import oracle_attention_heads
+    ref = oracle_attention_heads(ai, ot["anc_mask"], cfg.dh, list(range(cfg.H)))
     return args, ws, ref, (kc, vc)
 
 
@@ -71,12 +70,15 @@ def run(args, ws):
     return out.float().cpu().numpy()
 
 
-@pytest.mark.parametrize("n,prefix", [(64, 1024), (64, 0), (128, 3000), (200, 700)])
-def test_attention_wait_timeout_sets_status_and_context_survives(dev, n, prefix):
+@pytest.mark.parametrize("n,prefix,H", [(64, 1024, 2), (64, 0, 2), (128, 3000, 2), (200, 700, 2),
+                                         (128, 8192, 32)])
+def test_attention_wait_timeout_sets_status_and_context_survives(dev, n, prefix, H):
     """Every (head, key range) CTA times out: the status word reads "timeout"
     and every output row is zero (no key range survives the merge); then,
-    with the default budget back, the same buffers give the oracle's result."""
-    args, ws, ref, _keep = attention_case(dev, n, prefix)
+    with the default budget back, the same buffers give the oracle's result.
+    The last case (129 rows over prefix 8192, 32 heads) runs the one-tile
+    variant whose last row is computed on the CUDA cores."""
+    args, ws, ref, _keep = attention_case(dev, n, prefix, H)
     default = m.wait_budget()
     assert default > 0
     m.set_wait_budget(0)
