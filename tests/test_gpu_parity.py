@@ -466,13 +466,14 @@ def test_attention_growing_scores(dev, P, growth, n, H):
     check_close(g, o, cfg.name)
 
 
-@pytest.mark.parametrize("prefix", [(8192,), (4100, 8192), (8192, 5, 6000)],
-                         ids=["one", "two", "three"])
+@pytest.mark.parametrize("prefix", [(8192,), (4100, 8192), (8192, 5, 6000), (0, 8192)],
+                         ids=["one", "two", "three", "empty_prefix"])
 def test_attention_tail_row(dev, prefix):
     """Trees of 129 rows over long prefixes (32 heads of 128): one 128-row
     tensor-core tile per key range, the last row on the CUDA cores of the
     same CTAs.  Every head of every sequence against the oracle; ragged
-    prefixes, and a 5-slot prefix whose later key ranges are empty."""
+    prefixes, a 5-slot prefix whose later key ranges are empty, and an empty
+    prefix (the tree's own slots are the only keys)."""
     cfg = synth.v7b().replace(name=f"tail{len(prefix)}", B=len(prefix), s=(8, 4, 4, 2, 2), n=128,
                               prefix=prefix)
     ot = oracle_tree_for(np.random.default_rng(len(prefix)), cfg.s, cfg.n, cfg.B, cfg.prefix)
