@@ -631,8 +631,20 @@ __global__ void __launch_bounds__(256)
 tree_attn_combine_kernel(const float *__restrict__ part_o, const float2 *__restrict__ part_ml,
                          int B, int R, int H, int NS, bf16 *__restrict__ out) {
     pdl_enter();
-    constexpr int PER = DH / 32;
+    constexpr int PER = DH / 32;  // contiguous output columns per lane: one 8- or 16-byte load
+    static_assert(PER == 2 || PER == 4, "dh 64 or 128");
     const int lane = threadIdx.x & 31;
+    const int c0 = lane * PER;
+    // this lane's PER columns of one partial row
+    auto load_cols = [&](const float *row_base, float (&v)[PER]) {
+        if constexpr (PER == 4) {
+            const float4 t = *reinterpret_cast<const float4 *>(row_base + c0);
+            v[0] = t.x; v[1] = t.y; v[2] = t.z; v[3] = t.w;
+        } else {
+            const float2 t = *reinterpret_cast<const float2 *>(row_base + c0);
+            v[0] = t.x; v[1] = t.y;
+        }
+    };
     const long long item = (long long)blockIdx.x * (blockDim.x >> 5) + (threadIdx.x >> 5);
     if (item >= (long long)B * R * H) return;
     const int h = (int)(item % H);
@@ -644,10 +656,7 @@ tree_attn_combine_kernel(const float *__restrict__ part_o, const float2 *__restr
     float pre[PRE][PER];
 #pragma unroll
     for (int j = 0; j < PRE; ++j)
-        if (j < NS)
-#pragma unroll
-            for (int p = 0; p < PER; ++p)
-                pre[j][p] = part_o[((base + j) * R + row) * DH + lane + 32 * p];
+        if (j < NS) load_cols(part_o + ((base + j) * R + row) * DH, pre[j]);
     float M = ml0.y > 0.f ? ml0.x : -INFINITY;
     for (int s = lane + 32; s < NS; s += 32) {
         const float2 ml = part_ml[(base + s) * R + row];
@@ -684,18 +693,22 @@ tree_attn_combine_kernel(const float *__restrict__ part_o, const float2 *__restr
 #pragma unroll 4
         for (int j = j0; j < cnt; ++j) {
             const float w = __shfl_sync(0xffffffffu, w_l, j);
-            const float *src = part_o + ((base + s0 + j) * R + row) * DH;
             if (w != 0.f) {
+                float v[PER];
+                load_cols(part_o + ((base + s0 + j) * R + row) * DH, v);
 #pragma unroll
-                for (int p = 0; p < PER; ++p) acc[p] = fmaf(w, src[lane + 32 * p], acc[p]);
+                for (int p = 0; p < PER; ++p) acc[p] = fmaf(w, v[p], acc[p]);
             }
         }
     }
     L = warp_sum(L);
     const float inv = L > 0.f ? 1.f / L : 0.f;
-    bf16 *dst = out + (((size_t)b * R + row) * H + h) * DH;
-#pragma unroll
-    for (int p = 0; p < PER; ++p) dst[lane + 32 * p] = __float2bfloat16_rn(acc[p] * inv);
+    bf16 *dst = out + (((size_t)b * R + row) * H + h) * DH + c0;
+    if constexpr (PER == 4)
+        *reinterpret_cast<uint2 *>(dst) =
+            make_uint2(pack_bf16(acc[0] * inv, acc[1] * inv), pack_bf16(acc[2] * inv, acc[3] * inv));
+    else
+        *reinterpret_cast<uint32_t *>(dst) = pack_bf16(acc[0] * inv, acc[1] * inv);
 }
 
 // ------------------------------------------------------------ f32 path ---
