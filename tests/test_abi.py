@@ -242,3 +242,34 @@ def test_binding_refuses_pageable_result_buffers():
     with pytest.raises(ValueError):
         m._result_ptr(torch.zeros(3, dtype=torch.int32), "accept_len")
     assert m._result_ptr(None, "accept") is None
+
+
+def test_attention_plan_tail_rule():
+    """The attention's workspace follows its plan: one partial row (dh
+    floats and an (m, l) pair) per (sequence, head, key range, tree row), so
+    its size shows how many key ranges the plan took.  A 129-row tree at dh 128
+    takes one 128-row tile when every CTA then runs at least 8 sub-chunks of
+    64 keys (long prefixes), two tiles otherwise; 130 rows and dh 64 always
+    take two.  Checked with the 152-SM plan the library uses without a
+    device."""
+    def ws(R, dh, P, ns):
+        rows = 32 * ns * R
+        a256 = lambda x: (x + 255) // 256 * 256
+        return m.WS_HEADER + a256(rows * dh * 4) + a256(rows * 8)
+
+    def ns_for(R, P, tiles):
+        nsub = (P + R + 63) // 64
+        per_head = max(1, 2 * 152 // (32 * tiles))
+        cps = max(2, -(-nsub // per_head))
+        return -(-nsub // cps), cps
+
+    for P in (512, 2048, 4096, 8192):
+        ns1, cps1 = ns_for(129, P, 1)
+        ns2, _ = ns_for(129, P, 2)
+        expect = ws(129, 128, P, ns1 if cps1 >= 8 else ns2)
+        assert m.tree_attention_workspace_size(m.BF16, 1, 129, 32, 128, P) == expect, P
+        assert m.tree_attention_workspace_size(m.BF16, 1, 129, 32, 64, P) == ws(129, 64, P, ns2), P
+        assert m.tree_attention_workspace_size(m.BF16, 1, 130, 32, 128, P) == \
+            ws(130, 128, P, ns_for(130, P, 2)[0]), P
+    # the switch point: one tile from prefix 4096 on, two below
+    assert ns_for(129, 2048, 1)[1] < 8 <= ns_for(129, 4096, 1)[1]
