@@ -17,6 +17,8 @@
  *                                 consecutive cache slots and the prefix
  *                                 grows (also fused into the posterior as
  *                                 medusa_evaluate_posterior_commit).
+ *   medusa_step_run               1-4 (and 5) with the step's input copies
+ *                                 from page-locked host memory, in one call.
  * Page citations are by title and section:
  *   [P1] "Medusa: Faster LLM text generation" (nazmi.tech)
  *   [P2] "Medusa 深读：解码慢不是算力问题，是搬运问题" (jokeuncle.pages.dev)
@@ -26,10 +28,11 @@
  * Conventions shared by every call
  *   - All tensor pointers are DEVICE pointers unless the name ends in _host.
  *     The caller allocates and owns every buffer; the library allocates
- *     nothing and keeps no per-call state between calls.
+ *     nothing and keeps no per-call state between calls, except the step
+ *     executor (section 7), which owns a side stream and two events.
  *   - Every call is asynchronous on `stream` (a cudaStream_t passed as void*;
  *     NULL = legacy default stream).  No call synchronises the host, except
- *     medusa_read_device_status.
+ *     medusa_read_device_status and medusa_step_run when asked to.
  *   - Arguments are validated on the host before any launch.  A bad argument
  *     returns MEDUSA_ERR_INVALID_ARG (or MEDUSA_ERR_UNSUPPORTED for a legal
  *     but unimplemented shape) and launches nothing; medusa_last_error()
@@ -464,6 +467,115 @@ MEDUSA_API medusa_status medusa_evaluate_posterior_commit(
     int32_t *next_token, int32_t *accept, void *const *k_cache, void *const *v_cache,
     const int32_t *prefix_len, int H, int dh, int32_t *new_prefix_len, void *ws,
     size_t ws_bytes, medusa_stream stream);
+
+/* ------------------------------------------------------------------------
+ * 7. The decoding step as one call: a step executor.
+ *
+ * [P1] Introduction and [P2] §3-§6: one Medusa step is heads -> candidate
+ * tree -> tree attention -> posterior (and, optionally, the commit).  The
+ * executor issues that sequence with the step's input copies in one host
+ * call, so that a caller whose inputs sit in page-locked host memory pays
+ * no per-call overhead of its own between them:
+ *   1. `early` copies on `stream` (the inputs of the heads and the tree:
+ *      the hidden state, the root token),
+ *   2. medusa_heads,
+ *   3. `late` copies on the executor's own side stream, which first waits
+ *      for everything issued to `stream` before this run (the inputs of the
+ *      attention and the posterior: q, the tree's K/V rows, the
+ *      verification logits); they travel during the heads pass,
+ *   4. medusa_build_tree, then `stream` waits for the side stream,
+ *   5. medusa_tree_attention,
+ *   6. medusa_evaluate_posterior, or medusa_evaluate_posterior_commit when
+ *      new_prefix_len is not NULL.
+ * Every kernel is stream-launched with programmatic dependent launch, as
+ * the separate calls are.  The results equal those of the separate calls
+ * on the same inputs.
+ *
+ * The descriptor names every buffer of the step; each field has the meaning
+ * it has in the call it is passed to (R = n + 1; the tree's outputs are
+ * the attention's and the posterior's inputs).  Copies: `dst` device
+ * memory, `src` page-locked host memory or device memory, `bytes` > 0;
+ * at most MEDUSA_STEP_MAX_COPIES in each list.  One workspace serves all
+ * four calls (at least the largest of their *_workspace_size values).
+ *
+ * medusa_step_create validates the descriptor's structure (NULL
+ * pointers, counts, sizes) before touching CUDA, copies the descriptor, the
+ * copy lists and s_host, and creates a non-blocking side stream and two
+ * events on the current device (and, in graph mode, a capture stream and
+ * the graph): the only CUDA objects the library owns.  It allocates no
+ * device memory of its own.  The buffers the descriptor names must stay
+ * allocated, at the same addresses, while the executor lives; new inputs
+ * are written into the same host buffers before each run.
+ * With flags = MEDUSA_STEP_GRAPH, create also runs the sequence once under
+ * stream capture (on a capture stream of its own; nothing executes) and
+ * instantiates it as a CUDA graph, so that each run is one graph launch:
+ * the launches keep their programmatic-dependent-launch edges, and the
+ * wait budget (medusa_set_wait_budget) in force at create is the one the
+ * graph's attention uses.  A call's validation failure then surfaces at
+ * create.
+ * medusa_step_run issues one step on `stream`; with `synchronize` != 0 it
+ * also waits for the step to complete (results written to page-locked host
+ * memory are then readable).  A call's own validation or launch failure
+ * stops the run there and returns that call's status.  One executor serves
+ * one host thread at a time.  medusa_step_destroy releases the side stream,
+ * events and graph (after the work they carry has completed); NULL is a
+ * no-op.
+ * medusa_step_desc_size returns sizeof(medusa_step_desc), so that a binding
+ * can check its mirror of the struct.
+ * ---------------------------------------------------------------------- */
+#define MEDUSA_STEP_MAX_COPIES 64
+#define MEDUSA_STEP_GRAPH 1       /* capture the sequence once as a CUDA graph */
+
+typedef struct medusa_copy {
+    void *dst;
+    const void *src;
+    size_t bytes;
+} medusa_copy;
+
+typedef struct medusa_step_desc {
+    const medusa_copy *early;   /* copies before the heads, on `stream`     */
+    int32_t n_early;
+    const medusa_copy *late;    /* copies during the heads, on the side     */
+    int32_t n_late;
+    medusa_dtype dtype;         /* of h, W1, b1, W2, q, caches, logits      */
+    /* heads */
+    const void *h, *W1, *b1, *W2;
+    int32_t B, d, V, K, top_s;
+    int32_t *topk_ids;
+    float *topk_logp;
+    /* tree */
+    const int32_t *root;
+    const int32_t *s_host;      /* [K] host; copied at create               */
+    int32_t n;
+    const int32_t *prefix_len;
+    int32_t *tokens, *parent, *depth, *pos_id;
+    uint64_t *anc_mask;
+    int32_t *paths, *n_leaf;
+    /* attention */
+    const void *q;
+    const void *const *k_cache, *const *v_cache;
+    int32_t P_max, H, dh;
+    float scale;
+    void *attn_out;
+    /* posterior (and commit) */
+    const void *logits;
+    medusa_accept_mode mode;
+    float eps, delta, temperature;
+    int32_t *accept_len, *path, *path_tokens, *next_token, *accept;
+    int32_t *new_prefix_len;    /* non-NULL: fused commit into the caches   */
+    void *ws;
+    size_t ws_bytes;
+    int32_t flags;              /* MEDUSA_STEP_GRAPH or 0                   */
+} medusa_step_desc;
+
+typedef struct medusa_step_exec medusa_step_exec;
+
+MEDUSA_API size_t medusa_step_desc_size(void);
+MEDUSA_API medusa_status medusa_step_create(const medusa_step_desc *desc,
+                                            medusa_step_exec **exec_out);
+MEDUSA_API medusa_status medusa_step_run(medusa_step_exec *exec, medusa_stream stream,
+                                         int synchronize);
+MEDUSA_API void medusa_step_destroy(medusa_step_exec *exec);
 
 #ifdef __cplusplus
 }

@@ -9,9 +9,11 @@ the compiled library is missing, importing the calls fails loudly.
 Public calls (same names as the C ABI in include/medusa.h):
     heads, heads_lm, heads_sample, heads_noalloc, build_tree, build_tree_static, tree_attention, evaluate_posterior,
     speculative_posterior, commit_kv, evaluate_posterior_commit
-plus workspace-size queries, device-status helpers, launch_count, and
-``StepGraph``, which captures a whole decoding step (copies and calls) into a
-CUDA graph once and replays it per step.
+plus workspace-size queries, device-status helpers, launch_count,
+``StepExecutor`` (medusa_step_create / medusa_step_run: the whole step, input
+copies included, issued by one native call), and ``StepGraph``, which
+captures a whole decoding step (copies and calls) into a CUDA graph once and
+replays it per step.
 """
 from __future__ import annotations
 
@@ -29,6 +31,7 @@ LIB_PATH = os.path.join(_HERE, "libmedusa_gb300.so")
 F32, BF16 = 0, 1
 GREEDY, TYPICAL = 0, 1
 WS_HEADER = 256
+STEP_GRAPH = 1
 MAX_TOP_S = 16
 MAX_TREE_ROWS = 256
 
@@ -48,7 +51,32 @@ EXPORTS = ("medusa_status_string", "medusa_last_error", "medusa_launch_count",
            "medusa_tree_attention_workspace_size", "medusa_tree_attention",
            "medusa_posterior_workspace_size", "medusa_evaluate_posterior",
            "medusa_evaluate_posterior_commit", "medusa_commit_kv", "medusa_heads_sample",
-           "medusa_speculative_workspace_size", "medusa_speculative_posterior")
+           "medusa_speculative_workspace_size", "medusa_speculative_posterior",
+           "medusa_step_desc_size", "medusa_step_create", "medusa_step_run",
+           "medusa_step_destroy")
+
+
+class _Copy(ctypes.Structure):
+    """medusa_copy"""
+    _fields_ = [("dst", ctypes.c_void_p), ("src", ctypes.c_void_p), ("bytes", ctypes.c_size_t)]
+
+
+class _StepDesc(ctypes.Structure):
+    """medusa_step_desc, field for field (checked against medusa_step_desc_size)."""
+    _P, _I, _F = ctypes.c_void_p, ctypes.c_int32, ctypes.c_float
+    _fields_ = [("early", _P), ("n_early", _I), ("late", _P), ("n_late", _I), ("dtype", _I),
+                ("h", _P), ("W1", _P), ("b1", _P), ("W2", _P),
+                ("B", _I), ("d", _I), ("V", _I), ("K", _I), ("top_s", _I),
+                ("topk_ids", _P), ("topk_logp", _P),
+                ("root", _P), ("s_host", _P), ("n", _I), ("prefix_len", _P),
+                ("tokens", _P), ("parent", _P), ("depth", _P), ("pos_id", _P), ("anc_mask", _P),
+                ("paths", _P), ("n_leaf", _P),
+                ("q", _P), ("k_cache", _P), ("v_cache", _P), ("P_max", _I), ("H", _I), ("dh", _I),
+                ("scale", _F), ("attn_out", _P),
+                ("logits", _P), ("mode", _I), ("eps", _F), ("delta", _F), ("temperature", _F),
+                ("accept_len", _P), ("path", _P), ("path_tokens", _P), ("next_token", _P),
+                ("accept", _P), ("new_prefix_len", _P), ("ws", _P), ("ws_bytes", ctypes.c_size_t),
+                ("flags", _I)]
 
 
 class MedusaError(RuntimeError):
@@ -98,6 +126,10 @@ def lib() -> ctypes.CDLL:
         "medusa_speculative_workspace_size": ([I, I], S),
         "medusa_speculative_posterior": ([I, P, P, P, I, I, I, F, U64, U64, P, P, P, P, P, S, P],
                                          I),
+        "medusa_step_desc_size": ([], S),
+        "medusa_step_create": ([ctypes.POINTER(_StepDesc), ctypes.POINTER(P)], I),
+        "medusa_step_run": ([P, P, I], I),
+        "medusa_step_destroy": ([P], None),
     }
     for name, (args, res) in sig.items():
         fn = getattr(L, name)
@@ -533,3 +565,108 @@ class StepGraph:
 
     def replay(self):
         self.graph.replay()
+
+
+# ---------------------------------------------------------- step executor ---
+
+def _copy_pair(dst: torch.Tensor, src: torch.Tensor, name: str):
+    _need(dst, f"{name} destination")
+    if not (src.is_cuda or src.is_pinned()):
+        raise ValueError(f"{name} source must be pinned host memory or a CUDA tensor")
+    if not src.is_contiguous():
+        raise ValueError(f"{name} source must be contiguous")
+    nb = dst.numel() * dst.element_size()
+    if src.numel() * src.element_size() != nb or nb == 0:
+        raise ValueError(f"{name}: source and destination sizes differ or are empty")
+    return _Copy(dst.data_ptr(), src.data_ptr(), nb)
+
+
+class StepExecutor:
+    """One decoding step issued by one native call (medusa_step_run).
+
+    The executor holds the step's buffers (the descriptor of
+    medusa_step_create): ``early`` and ``late`` are lists of (device
+    destination, pinned-host or device source) tensor pairs copied at the
+    start of every run -- early ones before the heads on the caller's stream,
+    late ones on the executor's side stream during the heads pass.  Then
+    heads, tree, attention and posterior (with the fused commit when
+    ``new_prefix_len`` is given) run as the separate calls do.  Every tensor
+    must keep its address while the executor lives; write new inputs into
+    the same host buffers before each ``run``.  With ``graph=True`` the
+    sequence is captured once at construction as a CUDA graph and each run
+    is one graph launch.
+    """
+
+    def __init__(self, *, h, W1, b1, W2, top_s: int, topk: tuple, root, s: Sequence[int], n: int,
+                 prefix_len, tree: "Tree", q, k_ptrs, v_ptrs, P_max: int, attn_out, logits,
+                 post: "Posterior", K: int, mode: int = GREEDY, eps=0.09, delta=0.3,
+                 temperature=1.0, ws=None, early=(), late=(), new_prefix_len=None, scale=None,
+                 graph: bool = False):
+        L = lib()
+        if ctypes.sizeof(_StepDesc) != L.medusa_step_desc_size():
+            raise MedusaError(1, "medusa_step_desc layout differs from the binding's")
+        for t, nm in ((h, "h"), (W1, "W1"), (W2, "W2"), (root, "root"), (prefix_len, "prefix_len"),
+                      (q, "q"), (attn_out, "attn_out"), (logits, "logits"), (k_ptrs, "k_ptrs"),
+                      (v_ptrs, "v_ptrs")):
+            _need(t, nm)
+        B, d = h.shape
+        V = W2.shape[1]
+        H, dh = q.shape[2], q.shape[3]
+        ids, logp = topk
+        if ws is None:
+            R = n + 1
+            need = max(heads_workspace_size(B, K, d, V, top_s),
+                       build_tree_workspace_size(B, K, top_s, n),
+                       tree_attention_workspace_size(_dtype(q), B, R, H, dh, P_max),
+                       posterior_workspace_size(B, R))
+            ws = new_workspace(need, h.device)
+        self._early = (_Copy * max(1, len(early)))(
+            *[_copy_pair(a, b, f"early[{i}]") for i, (a, b) in enumerate(early)])
+        self._late = (_Copy * max(1, len(late)))(
+            *[_copy_pair(a, b, f"late[{i}]") for i, (a, b) in enumerate(late)])
+        self._s = (ctypes.c_int32 * K)(*[int(x) for x in s])
+        pv = lambda t: None if t is None else t.data_ptr()
+        res = lambda t, nm: None if t is None else _result_ptr(t, nm).value
+        desc = _StepDesc(
+            early=ctypes.addressof(self._early), n_early=len(early),
+            late=ctypes.addressof(self._late), n_late=len(late), dtype=_dtype(h),
+            h=pv(h), W1=pv(W1), b1=pv(b1), W2=pv(W2), B=B, d=d, V=V, K=K, top_s=int(top_s),
+            topk_ids=pv(ids), topk_logp=pv(logp), root=pv(root),
+            s_host=ctypes.addressof(self._s), n=int(n), prefix_len=pv(prefix_len),
+            tokens=pv(tree.tokens), parent=pv(tree.parent), depth=pv(tree.depth),
+            pos_id=pv(tree.pos_id), anc_mask=pv(tree.anc_mask), paths=pv(tree.paths),
+            n_leaf=pv(tree.n_leaf), q=pv(q), k_cache=pv(k_ptrs), v_cache=pv(v_ptrs),
+            P_max=int(P_max), H=H, dh=dh,
+            scale=float(1.0 / math.sqrt(dh) if scale is None else scale), attn_out=pv(attn_out),
+            logits=pv(logits), mode=int(mode), eps=float(eps), delta=float(delta),
+            temperature=float(temperature),
+            accept_len=res(post.accept_len, "accept_len"), path=res(post.path, "path"),
+            path_tokens=res(post.path_tokens, "path_tokens"),
+            next_token=res(post.next_token, "next_token"), accept=res(post.accept, "accept"),
+            new_prefix_len=pv(new_prefix_len), ws=pv(ws), ws_bytes=ws.numel(),
+            flags=STEP_GRAPH if graph else 0)
+        # every buffer the descriptor names stays referenced while the executor lives
+        self._keep = (h, W1, b1, W2, ids, logp, root, prefix_len, tree, q, k_ptrs, v_ptrs,
+                      attn_out, logits, post, new_prefix_len, ws, tuple(early), tuple(late))
+        self.ws = ws
+        handle = ctypes.c_void_p()
+        _check(L.medusa_step_create(ctypes.byref(desc), ctypes.byref(handle)))
+        self._handle = handle
+
+    def run(self, stream=None, synchronize: bool = True):
+        """Issue one step on ``stream`` (the current stream by default); with
+        ``synchronize`` wait for it, so results in pinned memory are ready."""
+        if self._handle is None:
+            raise MedusaError(1, "StepExecutor is closed")
+        _check(lib().medusa_step_run(self._handle, _stream(stream), int(bool(synchronize))))
+
+    def close(self):
+        if getattr(self, "_handle", None) is not None:
+            lib().medusa_step_destroy(self._handle)
+            self._handle = None
+
+    def __del__(self):
+        try:
+            self.close()
+        except Exception:
+            pass

@@ -1,0 +1,242 @@
+// step.cu -- the step executor: one host call issues a whole decoding step.
+//
+// "Medusa: Faster LLM text generation", Introduction, and "Medusa 深读" §3-§6:
+// a step is heads -> candidate tree -> tree attention -> posterior (and the
+// commit).  The executor issues that sequence through the public calls of
+// this library, together with the step's input copies from page-locked host
+// memory: the heads' inputs first on the caller's stream, the attention's and
+// the posterior's on a side stream while the heads stream the weights,
+// joined before the attention.  Issued from here, the step's launches leave
+// the host a few microseconds apart, far ahead of the GPU, and each kernel
+// keeps its programmatic-dependent-launch overlap with the one before it.
+#include <cstring>
+#include <new>
+
+#include "launch.h"
+
+struct medusa_step_exec {
+    medusa_step_desc desc;
+    medusa_copy early[MEDUSA_STEP_MAX_COPIES];
+    medusa_copy late[MEDUSA_STEP_MAX_COPIES];
+    int32_t s_host[MEDUSA_MAX_HEADS];
+    cudaStream_t side;
+    cudaEvent_t fork, join;
+    // graph mode: the sequence captured once, and the kernels it launches
+    cudaGraphExec_t graph;
+    uint64_t graph_launches;
+};
+
+namespace {
+
+using medusa::set_last_error;
+
+medusa_status invalid(const char *what) {
+    set_last_error("medusa_step_create: %s", what);
+    return MEDUSA_ERR_INVALID_ARG;
+}
+
+medusa_status cuda_error(cudaError_t e, const char *where) {
+    set_last_error("%s: %s", where, cudaGetErrorString(e));
+    return MEDUSA_ERR_CUDA;
+}
+
+medusa_status check_copies(const medusa_copy *c, int32_t n, const char *which) {
+    if (n < 0 || n > MEDUSA_STEP_MAX_COPIES) {
+        set_last_error("medusa_step_create: %s copy count %d outside 0..%d", which, n,
+                       MEDUSA_STEP_MAX_COPIES);
+        return MEDUSA_ERR_INVALID_ARG;
+    }
+    if (n > 0 && !c) return invalid(which[0] == 'e' ? "early copy list is NULL"
+                                                    : "late copy list is NULL");
+    for (int32_t i = 0; i < n; ++i)
+        if (!c[i].dst || !c[i].src || c[i].bytes == 0) {
+            set_last_error("medusa_step_create: %s copy %d has a NULL pointer or no bytes", which,
+                           i);
+            return MEDUSA_ERR_INVALID_ARG;
+        }
+    return MEDUSA_OK;
+}
+
+// The descriptor's structure; shapes, alignments and workspace sizes are
+// checked by each call when the step runs.
+medusa_status check_desc(const medusa_step_desc &d) {
+    if (medusa_status s = check_copies(d.early, d.n_early, "early")) return s;
+    if (medusa_status s = check_copies(d.late, d.n_late, "late")) return s;
+    if (d.dtype != MEDUSA_F32 && d.dtype != MEDUSA_BF16) return invalid("unknown dtype");
+    if (d.B < 1 || d.B > MEDUSA_MAX_BATCH) return invalid("B outside 1..8");
+    if (d.K < 1 || d.K > MEDUSA_MAX_HEADS) return invalid("K outside 1..8");
+    if (d.top_s < 1 || d.top_s > MEDUSA_MAX_TOP_S) return invalid("top_s outside 1..16");
+    if (d.n < 1 || d.n + 1 > MEDUSA_MAX_TREE_ROWS) return invalid("n + 1 outside 2..256");
+    if (d.d < 1 || d.V < 1 || d.H < 1 || d.dh < 1 || d.P_max < 0)
+        return invalid("d, V, H, dh must be positive and P_max non-negative");
+    if (d.flags & ~MEDUSA_STEP_GRAPH) return invalid("unknown flags");
+    if (!d.s_host) return invalid("s_host is NULL");
+    for (int k = 0; k < d.K; ++k)
+        if (d.s_host[k] < 1 || d.s_host[k] > d.top_s) return invalid("s_host[k] outside 1..top_s");
+    const void *need[] = {d.h, d.W1, d.W2, d.topk_ids, d.topk_logp, d.root, d.prefix_len,
+                          d.tokens, d.parent, d.depth, d.pos_id, d.anc_mask, d.paths, d.n_leaf,
+                          d.q, d.k_cache, d.v_cache, d.attn_out, d.logits, d.accept_len, d.path,
+                          d.path_tokens, d.next_token, d.ws};
+    for (const void *p : need)
+        if (!p) return invalid("a required buffer is NULL (only b1, accept, new_prefix_len "
+                               "may be)");
+    return MEDUSA_OK;
+}
+
+// The step's sequence on `st` (the caller's stream, or the capture stream).
+medusa_status issue_step(medusa_step_exec *ex, cudaStream_t st) {
+    const medusa_step_desc &d = ex->desc;
+    const int R = d.n + 1;
+    cudaError_t e;
+    // the side stream's copies overwrite buffers that earlier work on
+    // `stream` (the previous step's attention and posterior) reads
+    if (d.n_late > 0 && (e = cudaEventRecord(ex->fork, st)))
+        return cuda_error(e, "medusa_step (fork)");
+    for (int i = 0; i < d.n_early; ++i)
+        if ((e = cudaMemcpyAsync(d.early[i].dst, d.early[i].src, d.early[i].bytes,
+                                 cudaMemcpyDefault, st)))
+            return cuda_error(e, "medusa_step (early copy)");
+    if (medusa_status s = medusa_heads(d.dtype, d.h, d.W1, d.b1, d.W2, d.B, d.d, d.V, d.K,
+                                       d.top_s, d.topk_ids, d.topk_logp, d.ws, d.ws_bytes, st))
+        return s;
+    if (d.n_late > 0) {
+        if ((e = cudaStreamWaitEvent(ex->side, ex->fork, 0)))
+            return cuda_error(e, "medusa_step (side wait)");
+        for (int i = 0; i < d.n_late; ++i)
+            if ((e = cudaMemcpyAsync(d.late[i].dst, d.late[i].src, d.late[i].bytes,
+                                     cudaMemcpyDefault, ex->side)))
+                return cuda_error(e, "medusa_step (late copy)");
+        if ((e = cudaEventRecord(ex->join, ex->side)))
+            return cuda_error(e, "medusa_step (join)");
+    }
+    if (medusa_status s = medusa_build_tree(d.root, d.topk_ids, d.topk_logp, d.B, d.K, d.s_host,
+                                            d.top_s, d.n, d.prefix_len, d.tokens, d.parent,
+                                            d.depth, d.pos_id, d.anc_mask, d.paths, d.n_leaf,
+                                            d.ws, d.ws_bytes, st))
+        return s;
+    if (d.n_late > 0 && (e = cudaStreamWaitEvent(st, ex->join, 0)))
+        return cuda_error(e, "medusa_step (join wait)");
+    if (medusa_status s = medusa_tree_attention(d.dtype, d.q, d.k_cache, d.v_cache, d.prefix_len,
+                                                d.P_max, d.anc_mask, d.B, R, d.H, d.dh, d.scale,
+                                                d.attn_out, d.ws, d.ws_bytes, st))
+        return s;
+    medusa_status s;
+    if (d.new_prefix_len)
+        s = medusa_evaluate_posterior_commit(
+            d.dtype, d.logits, d.tokens, d.parent, d.depth, d.B, R, d.V, d.K, d.mode, d.eps,
+            d.delta, d.temperature, d.accept_len, d.path, d.path_tokens, d.next_token, d.accept,
+            const_cast<void *const *>(d.k_cache), const_cast<void *const *>(d.v_cache),
+            d.prefix_len, d.H, d.dh, d.new_prefix_len, d.ws, d.ws_bytes, st);
+    else
+        s = medusa_evaluate_posterior(d.dtype, d.logits, d.tokens, d.parent, d.depth, d.B, R, d.V,
+                                      d.K, d.mode, d.eps, d.delta, d.temperature, d.accept_len,
+                                      d.path, d.path_tokens, d.next_token, d.accept, d.ws,
+                                      d.ws_bytes, st);
+    if (s) return s;
+    return MEDUSA_OK;
+}
+
+// Graph mode: the sequence issued once on a capture stream of its own (the
+// side stream joins the capture through the fork event and leaves it through
+// the join), then instantiated.  Relaxed capture, so that the calls' host
+// checks (pointer attributes) are allowed while capturing.
+medusa_status capture_step(medusa_step_exec *ex) {
+    cudaStream_t cap;
+    cudaError_t e = cudaStreamCreateWithFlags(&cap, cudaStreamNonBlocking);
+    if (e) return cuda_error(e, "medusa_step_create (capture stream)");
+    const uint64_t launches0 = medusa_launch_count();
+    if ((e = cudaStreamBeginCapture(cap, cudaStreamCaptureModeRelaxed))) {
+        cudaStreamDestroy(cap);
+        return cuda_error(e, "medusa_step_create (begin capture)");
+    }
+    medusa_status s = issue_step(ex, cap);
+    cudaGraph_t graph = nullptr;
+    e = cudaStreamEndCapture(cap, &graph);  // always leaves capture mode
+    if (!s && e) s = cuda_error(e, "medusa_step_create (end capture)");
+    if (!s && (e = cudaGraphInstantiate(&ex->graph, graph, 0))) {
+        ex->graph = nullptr;
+        s = cuda_error(e, "medusa_step_create (instantiate)");
+    }
+    if (graph) cudaGraphDestroy(graph);
+    cudaStreamDestroy(cap);
+    ex->graph_launches = medusa_launch_count() - launches0;
+    return s;
+}
+
+}  // namespace
+
+extern "C" {
+
+size_t medusa_step_desc_size(void) { return sizeof(medusa_step_desc); }
+
+medusa_status medusa_step_create(const medusa_step_desc *desc, medusa_step_exec **exec_out) {
+    if (!desc || !exec_out) return invalid("NULL descriptor or output pointer");
+    *exec_out = nullptr;
+    if (medusa_status s = check_desc(*desc)) return s;
+    medusa_step_exec *ex = new (std::nothrow) medusa_step_exec();
+    if (!ex) {
+        set_last_error("medusa_step_create: out of host memory");
+        return MEDUSA_ERR_INVALID_ARG;
+    }
+    ex->desc = *desc;
+    if (desc->n_early) std::memcpy(ex->early, desc->early, sizeof(medusa_copy) * desc->n_early);
+    if (desc->n_late) std::memcpy(ex->late, desc->late, sizeof(medusa_copy) * desc->n_late);
+    std::memcpy(ex->s_host, desc->s_host, sizeof(int32_t) * desc->K);
+    ex->desc.early = ex->early;
+    ex->desc.late = ex->late;
+    ex->desc.s_host = ex->s_host;
+    cudaError_t e = cudaStreamCreateWithFlags(&ex->side, cudaStreamNonBlocking);
+    if (e) {
+        delete ex;
+        return cuda_error(e, "medusa_step_create (side stream)");
+    }
+    e = cudaEventCreateWithFlags(&ex->fork, cudaEventDisableTiming);
+    if (!e) {
+        e = cudaEventCreateWithFlags(&ex->join, cudaEventDisableTiming);
+        if (e) cudaEventDestroy(ex->fork);
+    }
+    if (e) {
+        cudaStreamDestroy(ex->side);
+        delete ex;
+        return cuda_error(e, "medusa_step_create (events)");
+    }
+    if (desc->flags & MEDUSA_STEP_GRAPH) {
+        if (medusa_status s = capture_step(ex)) {
+            medusa_step_destroy(ex);
+            return s;
+        }
+    }
+    *exec_out = ex;
+    return MEDUSA_OK;
+}
+
+medusa_status medusa_step_run(medusa_step_exec *ex, medusa_stream stream, int synchronize) {
+    const medusa::NvtxRange range("medusa_step_run");
+    if (!ex) {
+        set_last_error("medusa_step_run: NULL executor");
+        return MEDUSA_ERR_INVALID_ARG;
+    }
+    cudaStream_t st = static_cast<cudaStream_t>(stream);
+    cudaError_t e;
+    if (ex->graph) {
+        if ((e = cudaGraphLaunch(ex->graph, st))) return cuda_error(e, "medusa_step_run (graph)");
+        for (uint64_t i = 0; i < ex->graph_launches; ++i) medusa::note_launch();
+    } else if (medusa_status s = issue_step(ex, st)) {
+        return s;
+    }
+    if (synchronize && (e = cudaStreamSynchronize(st)))
+        return cuda_error(e, "medusa_step_run (synchronize)");
+    return MEDUSA_OK;
+}
+
+void medusa_step_destroy(medusa_step_exec *ex) {
+    if (!ex) return;
+    // each releases its resources once the work it carries has completed
+    if (ex->graph) cudaGraphExecDestroy(ex->graph);
+    cudaEventDestroy(ex->join);
+    cudaEventDestroy(ex->fork);
+    cudaStreamDestroy(ex->side);
+    delete ex;
+}
+
+}  // extern "C"

@@ -195,7 +195,7 @@ def heads_inputs(cfg: StepConfig, rep: int = 0) -> HeadsInputs:
     """h ~ N(0, h_std); W1 ~ N(0, w1_std); b1 = 0; W2 ~ N(0, w2_std).  The
     LM-head variant sets W1 = 0, b1 = 0 and every head's W2 to one shared
     LM-head matrix W_lm ~ N(0, w2_std)."""
-    h = _normal(cfg, "h", rep, (cfg.B, cfg.d), cfg.h_std, cfg.dtype)
+    h = hidden_states(cfg, rep)
     b1 = _zeros((cfg.K, cfg.d), cfg.dtype)
     if cfg.lm_head_variant:
         W1 = _zeros((cfg.K, cfg.d, cfg.d), cfg.dtype)
@@ -206,6 +206,11 @@ def heads_inputs(cfg: StepConfig, rep: int = 0) -> HeadsInputs:
         W1 = _normal(cfg, "w1", rep, (cfg.K, cfg.d, cfg.d), cfg.w1_std, cfg.dtype)
         W2 = _normal(cfg, "w2", rep, (cfg.K, cfg.V, cfg.d), cfg.w2_std, cfg.dtype)
     return HeadsInputs(h=h, W1=W1, b1=b1, W2=W2)
+
+
+def hidden_states(cfg: StepConfig, rep: int = 0) -> np.ndarray:
+    """h [B,d] ~ N(0, h_std) alone (the same values heads_inputs returns)."""
+    return _normal(cfg, "h", rep, (cfg.B, cfg.d), cfg.h_std, cfg.dtype)
 
 
 def lm_head_weight(cfg: StepConfig, rep: int = 0) -> np.ndarray:

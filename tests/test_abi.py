@@ -273,3 +273,96 @@ def test_attention_plan_tail_rule():
             ws(130, 128, P, ns_for(130, P, 2)[0]), P
     # the switch point: one tile from prefix 4096 on, two below
     assert ns_for(129, 2048, 1)[1] < 8 <= ns_for(129, 4096, 1)[1]
+
+
+def test_step_desc_layout_matches_header(tmp_path):
+    """The binding's mirror of medusa_step_desc has every field at the offset
+    the C compiler gives it (gcc on include/medusa.h), and the same size."""
+    import shutil
+    import subprocess
+    gcc = shutil.which("gcc") or shutil.which("cc")
+    if gcc is None:
+        pytest.skip("no C compiler")
+    names = [f[0] for f in m._StepDesc._fields_]
+    src = tmp_path / "layout.c"
+    src.write_text(
+        '#include <stddef.h>\n#include <stdio.h>\n#include "medusa.h"\nint main(void) {\n'
+        + "".join(f'  printf("{n} %zu\\n", offsetof(medusa_step_desc, {n}));\n' for n in names)
+        + '  printf("sizeof %zu\\n", sizeof(medusa_step_desc));\n'
+        + '  printf("copy %zu\\n", sizeof(medusa_copy));\n  return 0;\n}\n')
+    exe = tmp_path / "layout"
+    subprocess.run([gcc, "-I", os.path.join(ROOT, "include"), str(src), "-o", str(exe)],
+                   check=True)
+    got = dict(line.split() for line in subprocess.run(
+        [str(exe)], check=True, capture_output=True, text=True).stdout.splitlines())
+    for n in names:
+        assert int(got[n]) == getattr(m._StepDesc, n).offset, n
+    assert int(got["sizeof"]) == ctypes.sizeof(m._StepDesc)
+    assert int(got["copy"]) == ctypes.sizeof(m._Copy)
+
+
+def _step_desc(**kw):
+    """A structurally valid descriptor with fake device addresses."""
+    d = m._StepDesc()
+    for name, typ in m._StepDesc._fields_:
+        if typ is ctypes.c_void_p:
+            setattr(d, name, 4096)
+    s = (ctypes.c_int32 * 5)(4, 3, 2, 2, 1)
+    d.s_host = ctypes.addressof(s)
+    d.b1 = d.accept = d.new_prefix_len = None
+    d.dtype, d.B, d.d, d.V, d.K, d.top_s, d.n = m.BF16, 1, 4096, 32000, 5, 4, 64
+    d.P_max, d.H, d.dh, d.scale = 1024, 32, 128, 0.088
+    d.mode, d.eps, d.delta, d.temperature = m.TYPICAL, 0.09, 0.3, 1.0
+    d.ws_bytes = 1 << 24
+    d.early = d.late = None
+    for k, v in kw.items():
+        setattr(d, k, v)
+    return d, s
+
+
+@pytest.mark.parametrize("kw,msg", [
+    (dict(B=0), "B outside"), (dict(B=9), "B outside"), (dict(K=9), "K outside"),
+    (dict(top_s=17), "top_s"), (dict(n=256), "n + 1"), (dict(n=0), "n + 1"),
+    (dict(dtype=7), "dtype"), (dict(s_host=None), "s_host"), (dict(q=None), "required"),
+    (dict(logits=None), "required"), (dict(ws=None), "required"),
+    (dict(n_early=1), "early copy list"), (dict(n_late=65), "late copy count"),
+    (dict(P_max=-1), "P_max"), (dict(flags=2), "unknown flags"),
+])
+def test_step_create_rejects_before_cuda(L, kw, msg):
+    d, _s = _step_desc(**kw)
+    ex = ctypes.c_void_p(1234)
+    rc = L.medusa_step_create(ctypes.byref(d), ctypes.byref(ex))
+    assert rc == 1, m.STATUS.get(rc)
+    assert msg in L.medusa_last_error().decode()
+    assert ex.value is None  # the output is cleared on failure
+
+
+def test_step_create_rejects_bad_copies_and_s(L):
+    bad = (m._Copy * 2)(m._Copy(4096, 8192, 64), m._Copy(4096, None, 64))
+    d, _s = _step_desc(early=ctypes.addressof(bad), n_early=2)
+    ex = ctypes.c_void_p()
+    assert L.medusa_step_create(ctypes.byref(d), ctypes.byref(ex)) == 1
+    assert "early copy 1" in L.medusa_last_error().decode()
+    zero = (m._Copy * 1)(m._Copy(4096, 8192, 0))
+    d, _s = _step_desc(late=ctypes.addressof(zero), n_late=1)
+    assert L.medusa_step_create(ctypes.byref(d), ctypes.byref(ex)) == 1
+    assert "late copy 0" in L.medusa_last_error().decode()
+    s = (ctypes.c_int32 * 5)(4, 3, 5, 2, 1)  # s_k > top_s
+    d, _ = _step_desc(s_host=ctypes.addressof(s))
+    assert L.medusa_step_create(ctypes.byref(d), ctypes.byref(ex)) == 1
+    assert "s_host[k]" in L.medusa_last_error().decode()
+    assert L.medusa_step_create(None, ctypes.byref(ex)) == 1
+    assert L.medusa_step_run(None, None, 1) == 1
+    L.medusa_step_destroy(None)  # a no-op
+
+
+def test_step_create_without_a_device_fails_cleanly(L):
+    """A valid descriptor on a machine without a GPU fails at the side
+    stream's creation with MEDUSA_ERR_CUDA and returns no executor."""
+    import torch
+    if torch.cuda.is_available():
+        pytest.skip("a device is present")
+    d, _s = _step_desc()
+    ex = ctypes.c_void_p(1234)
+    assert L.medusa_step_create(ctypes.byref(d), ctypes.byref(ex)) == 4
+    assert ex.value is None
