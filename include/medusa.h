@@ -494,8 +494,10 @@ MEDUSA_API medusa_status medusa_evaluate_posterior_commit(
  * The descriptor names every buffer of the step; each field has the meaning
  * it has in the call it is passed to (R = n + 1; the tree's outputs are
  * the attention's and the posterior's inputs).  Copies: `dst` device
- * memory, `src` page-locked host memory or device memory, `bytes` > 0;
- * at most MEDUSA_STEP_MAX_COPIES in each list.  One workspace serves all
+ * memory, `src` page-locked host memory or device memory (each copy's
+ * direction is resolved at create, which refuses any other memory with
+ * MEDUSA_ERR_INVALID_ARG), `bytes` > 0; at most MEDUSA_STEP_MAX_COPIES in
+ * each list.  One workspace serves all
  * four calls (at least the largest of their *_workspace_size values).
  *
  * medusa_step_create validates the descriptor's structure (NULL

@@ -18,6 +18,10 @@ struct medusa_step_exec {
     medusa_step_desc desc;
     medusa_copy early[MEDUSA_STEP_MAX_COPIES];
     medusa_copy late[MEDUSA_STEP_MAX_COPIES];
+    // each copy's direction, resolved once at create (a copy of kind
+    // cudaMemcpyDefault would have its pointers looked up at every issue)
+    cudaMemcpyKind early_kind[MEDUSA_STEP_MAX_COPIES];
+    cudaMemcpyKind late_kind[MEDUSA_STEP_MAX_COPIES];
     int32_t s_host[MEDUSA_MAX_HEADS];
     cudaStream_t side;
     cudaEvent_t fork, join;
@@ -83,6 +87,37 @@ medusa_status check_desc(const medusa_step_desc &d) {
     return MEDUSA_OK;
 }
 
+// The direction of each copy: the destination must be device memory, the
+// source page-locked host memory or device memory.
+medusa_status resolve_kinds(const medusa_copy *c, int32_t n, cudaMemcpyKind *kind,
+                            const char *which) {
+    for (int32_t i = 0; i < n; ++i) {
+        cudaPointerAttributes a{}, b{};
+        cudaError_t e = cudaPointerGetAttributes(&a, c[i].dst);
+        if (!e) e = cudaPointerGetAttributes(&b, c[i].src);
+        if (e) {
+            cudaGetLastError();
+            set_last_error("medusa_step_create: %s copy %d: %s", which, i, cudaGetErrorString(e));
+            return MEDUSA_ERR_INVALID_ARG;
+        }
+        if (a.type != cudaMemoryTypeDevice && a.type != cudaMemoryTypeManaged) {
+            set_last_error("medusa_step_create: %s copy %d: destination is not device memory",
+                           which, i);
+            return MEDUSA_ERR_INVALID_ARG;
+        }
+        if (b.type == cudaMemoryTypeHost) {
+            kind[i] = cudaMemcpyHostToDevice;
+        } else if (b.type == cudaMemoryTypeDevice || b.type == cudaMemoryTypeManaged) {
+            kind[i] = cudaMemcpyDeviceToDevice;
+        } else {
+            set_last_error("medusa_step_create: %s copy %d: source is neither page-locked host "
+                           "memory nor device memory", which, i);
+            return MEDUSA_ERR_INVALID_ARG;
+        }
+    }
+    return MEDUSA_OK;
+}
+
 // The step's sequence on `st` (the caller's stream, or the capture stream).
 medusa_status issue_step(medusa_step_exec *ex, cudaStream_t st) {
     const medusa_step_desc &d = ex->desc;
@@ -94,7 +129,7 @@ medusa_status issue_step(medusa_step_exec *ex, cudaStream_t st) {
         return cuda_error(e, "medusa_step (fork)");
     for (int i = 0; i < d.n_early; ++i)
         if ((e = cudaMemcpyAsync(d.early[i].dst, d.early[i].src, d.early[i].bytes,
-                                 cudaMemcpyDefault, st)))
+                                 ex->early_kind[i], st)))
             return cuda_error(e, "medusa_step (early copy)");
     if (medusa_status s = medusa_heads(d.dtype, d.h, d.W1, d.b1, d.W2, d.B, d.d, d.V, d.K,
                                        d.top_s, d.topk_ids, d.topk_logp, d.ws, d.ws_bytes, st))
@@ -104,7 +139,7 @@ medusa_status issue_step(medusa_step_exec *ex, cudaStream_t st) {
             return cuda_error(e, "medusa_step (side wait)");
         for (int i = 0; i < d.n_late; ++i)
             if ((e = cudaMemcpyAsync(d.late[i].dst, d.late[i].src, d.late[i].bytes,
-                                     cudaMemcpyDefault, ex->side)))
+                                     ex->late_kind[i], ex->side)))
                 return cuda_error(e, "medusa_step (late copy)");
         if ((e = cudaEventRecord(ex->join, ex->side)))
             return cuda_error(e, "medusa_step (join)");
@@ -185,6 +220,12 @@ medusa_status medusa_step_create(const medusa_step_desc *desc, medusa_step_exec 
     ex->desc.early = ex->early;
     ex->desc.late = ex->late;
     ex->desc.s_host = ex->s_host;
+    medusa_status sk = resolve_kinds(ex->early, desc->n_early, ex->early_kind, "early");
+    if (!sk) sk = resolve_kinds(ex->late, desc->n_late, ex->late_kind, "late");
+    if (sk) {
+        delete ex;
+        return sk;
+    }
     cudaError_t e = cudaStreamCreateWithFlags(&ex->side, cudaStreamNonBlocking);
     if (e) {
         delete ex;

@@ -247,3 +247,43 @@ def test_step_executor_graph_mode_reports_a_call_error_at_create(dev):
     got = st.results()
     st.separate_calls()
     _same(got, st.results())
+
+
+def test_step_executor_refuses_pageable_sources(dev):
+    """The executor resolves each copy's direction at create: a pageable
+    host source, or a host destination, is refused before any work (the
+    binding refuses pageable tensors itself, so the descriptor is built
+    here by hand)."""
+    import ctypes
+    cfg = synth.tiny()
+    st = Step(cfg, dev)
+    nb = st.h.numel() * st.h.element_size()
+    pageable = torch.empty(st.h.shape, dtype=st.h.dtype)
+    copies = (m._Copy * 1)(m._Copy(st.h.data_ptr(), pageable.data_ptr(), nb))
+    s_host = (ctypes.c_int32 * cfg.K)(*cfg.s)
+    t, p = st.tree, st.post
+    fields = dict(early=ctypes.addressof(copies), n_early=1, dtype=m.F32, h=st.h, W1=st.W1,
+                  b1=st.b1, W2=st.W2, B=cfg.B, d=cfg.d, V=cfg.V, K=cfg.K, top_s=cfg.top_s,
+                  topk_ids=st.ids, topk_logp=st.logp, root=st.root,
+                  s_host=ctypes.addressof(s_host), n=cfg.n, prefix_len=st.prefix,
+                  tokens=t.tokens, parent=t.parent, depth=t.depth, pos_id=t.pos_id,
+                  anc_mask=t.anc_mask, paths=t.paths, n_leaf=t.n_leaf, q=st.q, k_cache=st.kp,
+                  v_cache=st.vp, P_max=cfg.P_max, H=cfg.H, dh=cfg.dh, scale=0.125,
+                  attn_out=st.out, logits=st.logits, mode=m.GREEDY, eps=0.09, delta=0.3,
+                  temperature=1.0, accept_len=p.accept_len, path=p.path,
+                  path_tokens=p.path_tokens, next_token=p.next_token, ws=st.ws,
+                  ws_bytes=st.ws.numel())
+    d = m._StepDesc()
+    for k, v in fields.items():
+        setattr(d, k, v.data_ptr() if isinstance(v, torch.Tensor) else v)
+    lib = m.lib()
+    h = ctypes.c_void_p()
+    assert lib.medusa_step_create(ctypes.byref(d), ctypes.byref(h)) == 1
+    assert "source is neither" in lib.medusa_last_error().decode()
+    assert h.value is None
+    copies[0] = m._Copy(st.host["h"].data_ptr(), st.h.data_ptr(), nb)  # host destination
+    assert lib.medusa_step_create(ctypes.byref(d), ctypes.byref(h)) == 1
+    assert "destination is not device memory" in lib.medusa_last_error().decode()
+    copies[0] = m._Copy(st.h.data_ptr(), st.host["h"].data_ptr(), nb)  # pinned source
+    assert lib.medusa_step_create(ctypes.byref(d), ctypes.byref(h)) == 0
+    lib.medusa_step_destroy(h)
