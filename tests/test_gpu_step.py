@@ -187,6 +187,23 @@ def test_step_executor_v7b_commit_matches_calls(dev, graph):
 
 
 @pytest.mark.parametrize("graph", [False, True])
+def test_step_executor_batch8_matches_calls(dev, graph):
+    """Eight ragged 7B sequences: the heads run on the tensor cores (tensor
+    maps built on the host at issue, or once at capture in graph mode); the
+    executor equals the separate calls bit for bit over two steps."""
+    cfg = synth.batch8()
+    st = Step(cfg, dev, graph=graph)
+    for rep in (0, 1):
+        st.fill(rep)
+        st.ex.run()
+        got = st.results()
+        assert torch.equal(got["tokens"][:, 0], torch.from_numpy(synth.root_tokens(cfg, rep=rep)))
+        st.separate_calls()
+        _same(got, st.results())
+    assert m.read_device_status(st.ws) == 0
+
+
+@pytest.mark.parametrize("graph", [False, True])
 def test_step_executor_on_a_side_stream_with_device_results(dev, graph):
     """Issued on a non-default stream without waiting, with device-resident
     results, the step completes in stream order like the separate calls."""
