@@ -194,6 +194,9 @@ medusa_status capture_step(medusa_step_exec *ex) {
     }
     if (graph) cudaGraphDestroy(graph);
     cudaStreamDestroy(cap);
+    if (s) cudaGetLastError();  // a failed capture leaves no error for later calls
+    // the kernels one replay launches (the process-wide counter: launches
+    // by other threads during the capture would be counted too)
     ex->graph_launches = medusa_launch_count() - launches0;
     return s;
 }
