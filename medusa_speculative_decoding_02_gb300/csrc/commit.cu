@@ -2,7 +2,7 @@
 //
 // commit_kv_kernel: grid (column blocks, B), 128 threads.  Every CTA of
 // sequence b reads the accepted path once into shared memory, applies the
-// device checks (each CTA reaches the same verdict; the first error code
+// device checks (each CTA reaches the same decision; the first error code
 // wins in the status word), and moves its share of the 16-byte columns with
 // commit_columns.  Column block 0 writes new_prefix_len[b].
 #include <algorithm>
