@@ -72,17 +72,21 @@ class Step:
         self.post = m.Posterior.pinned(B, R, K) if pinned_results else \
             m.Posterior.empty(B, R, K, dev)
         self.new_prefix = torch.empty((B,), dtype=torch.int32, device=dev) if commit else None
+        self.ex = self.make_executor(graph)
+
+    def make_executor(self, graph):
+        cfg = self.cfg
         late = [(self.q, self.host["q"]), (self.logits, self.host["logits"])]
         for (k, v), (hk, hv) in zip(self.kv_rows, self.host_kv):
             late += [(k, hk), (v, hv)]
-        self.ex = m.StepExecutor(
-            h=self.h, W1=self.W1, b1=self.b1, W2=self.W2, top_s=S, topk=(self.ids, self.logp),
-            root=self.root, s=cfg.s, n=n, prefix_len=self.prefix, tree=self.tree, q=self.q,
-            k_ptrs=self.kp, v_ptrs=self.vp, P_max=cfg.P_max, attn_out=self.out,
-            logits=self.logits, post=self.post, K=K, mode=self.mode, eps=cfg.eps,
-            delta=cfg.delta, temperature=cfg.temperature, ws=self.ws,
-            early=[(self.h, self.host["h"]), (self.root, self.host["root"])], late=late,
-            new_prefix_len=self.new_prefix, graph=graph)
+        return m.StepExecutor(
+            h=self.h, W1=self.W1, b1=self.b1, W2=self.W2, top_s=cfg.top_s,
+            topk=(self.ids, self.logp), root=self.root, s=cfg.s, n=cfg.n,
+            prefix_len=self.prefix, tree=self.tree, q=self.q, k_ptrs=self.kp, v_ptrs=self.vp,
+            P_max=cfg.P_max, attn_out=self.out, logits=self.logits, post=self.post, K=cfg.K,
+            mode=self.mode, eps=cfg.eps, delta=cfg.delta, temperature=cfg.temperature,
+            ws=self.ws, early=[(self.h, self.host["h"]), (self.root, self.host["root"])],
+            late=late, new_prefix_len=self.new_prefix, graph=graph)
 
     def fill(self, rep):
         cfg = self.cfg
@@ -304,3 +308,34 @@ def test_step_executor_refuses_pageable_sources(dev):
     copies[0] = m._Copy(st.h.data_ptr(), st.host["h"].data_ptr(), nb)  # pinned source
     assert lib.medusa_step_create(ctypes.byref(d), ctypes.byref(h)) == 0
     lib.medusa_step_destroy(h)
+
+
+def test_step_executor_graph_keeps_the_wait_budget_of_create(dev):
+    """In graph mode the attention's wait budget is the one in force at
+    create.  Captured with a budget of 0 (fault injection: every mbarrier
+    wait of the tensor-core attention gives up at once), each replay reports
+    "timeout" with zero attention rows even after the budget is restored; a
+    stream-mode executor made afterwards uses the restored budget and equals
+    the separate calls, so the context stays usable."""
+    cfg = synth.v7b().replace(mode="typical")
+    default = m.wait_budget()
+    assert default > 0
+    m.set_wait_budget(0)
+    try:
+        st = Step(cfg, dev, graph=True)
+    finally:
+        m.set_wait_budget(default)
+    st.fill(0)
+    for _ in range(2):
+        st.ex.run()
+        assert m.read_device_status(st.ws) == 6  # MEDUSA_DEV_TIMEOUT
+        assert torch.count_nonzero(st.out) == 0
+        m.clear_device_status(st.ws)
+    st.ex.close()
+    ex = st.make_executor(graph=False)
+    ex.run()
+    assert m.read_device_status(st.ws) == 0
+    got = st.results()
+    assert torch.count_nonzero(got["out"]) > 0
+    st.separate_calls()
+    _same(got, st.results())
