@@ -22,19 +22,23 @@
 // would move logits by ~1e-3.
 //
 // Work split.  A CTA per SM (192 threads): warp 0 issues the TMA copies,
-// warp 1 the MMAs, warps 2-5 read the accumulators.  A ring of 10 stages
-// (weight rows x 64 columns plus the matching 16 x 64 B tile, 18 KB each)
-// runs ahead of the MMAs across tile boundaries.  Rows are handed out in
-// 8-row units: phase 1 spreads the K*d rows of W1 evenly over every CTA
-// (h is shared by all heads); phase 2 gives each head the same number of
-// CTAs and spreads the head's V rows over them, so a CTA's z never changes.
-// A CTA's rows form tiles of at most 128 rows; a tile's rows load as boxes of
-// 128, 64, 32, 16 and 8 rows.  Each of a stage's four K-slices (K = 16 per
-// MMA) accumulates into its own 128-lane x 16-column accumulator, since an
-// N = 16 MMA is too short to hide the wait on the previous one into the same
-// accumulator; the epilogue adds the four.  Two tiles' accumulators sit in
-// tensor memory, so the epilogue of one overlaps the MMAs of the next.  Phase 1's epilogue applies bias, SiLU and the residual and writes
-// zt; phase 2's keeps, per sequence, each thread's running (max, sum-exp) and
+// warp 1 the MMAs, warps 2-5 read the accumulators.  A ring of 3 stages
+// runs ahead of the MMAs across tile boundaries; a stage holds 4 K-blocks
+// (4 x 64 columns) of a tile's weight rows and the matching 16-row B tile
+// (at most 64 + 8 KB), each brought by one 3-D copy (the number of copies,
+// not their bytes, bounded the stream when a stage took one copy per box).
+// Rows are handed out in 8-row units: phase 1 spreads the K*d rows of W1
+// evenly over every CTA (h is shared by all heads); phase 2 gives each head
+// the same number of CTAs and spreads the head's V rows over them, so a
+// CTA's z never changes.  A CTA's rows form tiles of at most 128 rows (near-
+// equal multiples of 8, one tensor map per tile height).  Each of a stage's
+// four K-slices (K = 16 per MMA) accumulates into its own 128-lane x
+// 16-column accumulator, since an N = 16 MMA is too short to hide the wait
+// on the previous one into the same accumulator; the epilogue adds the
+// four.  Two tiles' accumulators sit in tensor memory, so the epilogue of
+// one overlaps the MMAs of the next.  Phase 1's epilogue applies bias, SiLU
+// and the residual and writes zt; phase 2's keeps, per sequence, each
+// thread's running (max, sum-exp) and
 // a per-warp top-s list (candidates pass a threshold test by ballot; the few
 // that pass are inserted one by one), then merges the warps and writes one
 // partial per (head, sequence, CTA) for heads_reduce_kernel.
