@@ -504,7 +504,8 @@ MEDUSA_API medusa_status medusa_evaluate_posterior_commit(
  * pointers, counts, sizes) before touching CUDA, copies the descriptor, the
  * copy lists and s_host, and creates a non-blocking side stream and two
  * events on the current device (and, in graph mode, a capture stream and
- * the graph): the only CUDA objects the library owns.  It allocates no
+ * the graph; with page-locked results, B completion words of page-locked
+ * host memory): the only CUDA objects the library owns.  It allocates no
  * device memory of its own.  The buffers the descriptor names must stay
  * allocated, at the same addresses, while the executor lives; new inputs
  * are written into the same host buffers before each run.
@@ -516,12 +517,18 @@ MEDUSA_API medusa_status medusa_evaluate_posterior_commit(
  * graph's attention uses.  A call's validation failure then surfaces at
  * create.
  * medusa_step_run issues one step on `stream`; with `synchronize` != 0 it
- * also waits for the step to complete (results written to page-locked host
- * memory are then readable).  A call's own validation or launch failure
+ * also waits for the step: when the posterior's results are page-locked host
+ * memory, until every sequence's results (and the fused commit) are written
+ * -- the posterior's last kernel raises a completion word in page-locked
+ * memory that the executor owns, and the host polls it (the stream may
+ * still be retiring that kernel; work issued later is ordered after it) --
+ * and otherwise, or if the word has not come after 20 ms, until the stream
+ * is idle.  Runs of one executor go to one stream (or are ordered by the
+ * caller).  A call's own validation or launch failure
  * stops the run there and returns that call's status.  One executor serves
  * one host thread at a time.  medusa_step_destroy releases the side stream,
- * events and graph (after the work they carry has completed); NULL is a
- * no-op.
+ * events and graph (after the work they carry has completed; freeing the
+ * completion words waits for the device); NULL is a no-op.
  * medusa_step_desc_size returns sizeof(medusa_step_desc), so that a binding
  * can check its mirror of the struct.
  * ---------------------------------------------------------------------- */

@@ -470,6 +470,34 @@ medusa_status check_commit(const char *who, medusa_dtype dtype, const void *cons
 
 }  // namespace
 
+// The posterior with or without the commit (k_cache non-null) and with an
+// optional completion word per sequence (the step executor's).
+medusa_status medusa::evaluate_posterior_signalled(
+    medusa_dtype dtype, const void *logits, const int32_t *tokens, const int32_t *parent,
+    const int32_t *depth, int B, int R, int V, int K, medusa_accept_mode mode, float eps,
+    float delta, float temperature, int32_t *accept_len, int32_t *path, int32_t *path_tokens,
+    int32_t *next_token, int32_t *accept, void *const *k_cache, void *const *v_cache,
+    const int32_t *prefix_len, int H, int dh, int32_t *new_prefix_len, void *ws,
+    size_t ws_bytes, cudaStream_t stream, uint32_t *done) {
+    const char *who = k_cache ? "medusa_evaluate_posterior_commit" : "medusa_evaluate_posterior";
+    if (medusa_status s = check_posterior(who, dtype, logits, tokens, parent, depth, B, R, V, K,
+                                          mode, eps, delta, temperature, accept_len, path,
+                                          path_tokens, next_token, ws, ws_bytes))
+        return s;
+    if (medusa_status s = check_result_pointer(accept, who)) return s;
+    if (k_cache) {
+        if (medusa_status s = check_commit(who, dtype, k_cache, v_cache, prefix_len,
+                                           new_prefix_len, H, dh))
+            return s;
+    }
+    cudaError_t e = launch_posterior(dtype, logits, tokens, parent, depth, B, R, V, K, mode, eps,
+                                     delta, temperature, accept_len, path, path_tokens, next_token,
+                                     accept, k_cache, v_cache, prefix_len, H, dh, new_prefix_len,
+                                     ws, stream, done);
+    if (e) return cuda_fail(e, who);
+    return MEDUSA_OK;
+}
+
 extern "C" {
 
 medusa_status medusa_evaluate_posterior(medusa_dtype dtype, const void *logits,
@@ -481,18 +509,11 @@ medusa_status medusa_evaluate_posterior(medusa_dtype dtype, const void *logits,
                                         int32_t *accept, void *ws, size_t ws_bytes,
                                         medusa_stream stream) {
     const NvtxRange range("medusa_evaluate_posterior");
-    const char *who = "medusa_evaluate_posterior";
-    if (medusa_status s = check_posterior(who, dtype, logits, tokens, parent, depth, B, R, V, K,
-                                          mode, eps, delta, temperature, accept_len, path,
-                                          path_tokens, next_token, ws, ws_bytes))
-        return s;
-    if (medusa_status s = check_result_pointer(accept, who)) return s;
-    cudaError_t e = launch_posterior(dtype, logits, tokens, parent, depth, B, R, V, K, mode, eps,
-                                     delta, temperature, accept_len, path, path_tokens, next_token,
-                                     accept, nullptr, nullptr, nullptr, 0, 0, nullptr, ws,
-                                     static_cast<cudaStream_t>(stream));
-    if (e) return cuda_fail(e, who);
-    return MEDUSA_OK;
+    return evaluate_posterior_signalled(dtype, logits, tokens, parent, depth, B, R, V, K, mode,
+                                        eps, delta, temperature, accept_len, path, path_tokens,
+                                        next_token, accept, nullptr, nullptr, nullptr, 0, 0,
+                                        nullptr, ws, ws_bytes, static_cast<cudaStream_t>(stream),
+                                        nullptr);
 }
 
 medusa_status medusa_evaluate_posterior_commit(
@@ -503,21 +524,13 @@ medusa_status medusa_evaluate_posterior_commit(
     const int32_t *prefix_len, int H, int dh, int32_t *new_prefix_len, void *ws,
     size_t ws_bytes, medusa_stream stream) {
     const NvtxRange range("medusa_evaluate_posterior_commit");
-    const char *who = "medusa_evaluate_posterior_commit";
-    if (medusa_status s = check_posterior(who, dtype, logits, tokens, parent, depth, B, R, V, K,
-                                          mode, eps, delta, temperature, accept_len, path,
-                                          path_tokens, next_token, ws, ws_bytes))
-        return s;
-    if (medusa_status s = check_result_pointer(accept, who)) return s;
-    if (medusa_status s = check_commit(who, dtype, k_cache, v_cache, prefix_len, new_prefix_len,
-                                       H, dh))
-        return s;
-    cudaError_t e = launch_posterior(dtype, logits, tokens, parent, depth, B, R, V, K, mode, eps,
-                                     delta, temperature, accept_len, path, path_tokens, next_token,
-                                     accept, k_cache, v_cache, prefix_len, H, dh, new_prefix_len,
-                                     ws, static_cast<cudaStream_t>(stream));
-    if (e) return cuda_fail(e, who);
-    return MEDUSA_OK;
+    if (!k_cache)
+        return fail(MEDUSA_ERR_INVALID_ARG, "medusa_evaluate_posterior_commit: NULL pointer");
+    return evaluate_posterior_signalled(dtype, logits, tokens, parent, depth, B, R, V, K, mode,
+                                        eps, delta, temperature, accept_len, path, path_tokens,
+                                        next_token, accept, k_cache, v_cache, prefix_len, H, dh,
+                                        new_prefix_len, ws, ws_bytes,
+                                        static_cast<cudaStream_t>(stream), nullptr);
 }
 
 // ----------------------------------------------------------- speculative ---

@@ -97,7 +97,19 @@ cudaError_t launch_posterior(medusa_dtype dtype, const void *logits, const int32
                              int32_t *path_tokens, int32_t *next_token, int32_t *accept,
                              void *const *k_cache, void *const *v_cache,
                              const int32_t *prefix_len, int H, int dh, int32_t *new_prefix_len,
-                             void *ws, cudaStream_t stream);
+                             void *ws, cudaStream_t stream, uint32_t *done = nullptr);
+
+// The posterior entry of the step executor: the checks of
+// medusa_evaluate_posterior (and, with k_cache, of the commit), then the
+// launch with `done` (page-locked host memory, [B] words, or null): each
+// sequence's word gains one when its results (and commit) are written.
+medusa_status evaluate_posterior_signalled(
+    medusa_dtype dtype, const void *logits, const int32_t *tokens, const int32_t *parent,
+    const int32_t *depth, int B, int R, int V, int K, medusa_accept_mode mode, float eps,
+    float delta, float temperature, int32_t *accept_len, int32_t *path, int32_t *path_tokens,
+    int32_t *next_token, int32_t *accept, void *const *k_cache, void *const *v_cache,
+    const int32_t *prefix_len, int H, int dh, int32_t *new_prefix_len, void *ws,
+    size_t ws_bytes, cudaStream_t stream, uint32_t *done);
 
 // k_cache == nullptr in launch_posterior: no commit.  elt = bytes per element.
 cudaError_t launch_commit_kv(size_t elt, void *const *k_cache, void *const *v_cache,

@@ -267,9 +267,17 @@ posterior_select_kernel(const T *__restrict__ logits, const int32_t *__restrict_
                         float y_scale, float log2_eps, float log2_delta,
                         int32_t *__restrict__ accept_len, int32_t *__restrict__ path,
                         int32_t *__restrict__ path_tokens, int32_t *__restrict__ next_token,
-                        int32_t *__restrict__ accept_out, CommitArgs ca, int *status) {
+                        int32_t *__restrict__ accept_out, CommitArgs ca, int *status,
+                        uint32_t *done) {
     const int b = blockIdx.x;
     const int i = threadIdx.x;
+    // Completion word of this sequence (page-locked host memory of a step
+    // executor, or null): each run of the step adds one once every result
+    // of the CTA is written.  Its previous value was written by the previous
+    // run's copy of this kernel, long complete, so it is read before the
+    // launch wait.
+    uint32_t seq = 0;
+    if (done && i == 0) seq = *reinterpret_cast<volatile uint32_t *>(done + b) + 1u;
     // The one predecessor of this kernel that can still be running is the
     // rows kernel, and it writes only the row slices: the tree arrays and the
     // logits were complete before it passed its own launch wait, so they are
@@ -396,17 +404,24 @@ posterior_select_kernel(const T *__restrict__ logits, const int32_t *__restrict_
         accept_len[b] = L;
         next_token[b] = s_arg[best];
     }
-    if (!ca.k_cache) return;  // uniform over the CTA
-    // commit of the accepted path into the KV cache (medusa_commit_kv)
-    __syncthreads();
-    if (i == 0) {
-        s_code = commit_check(kc, vc, P, s_path, s_L, K, R);
-        if (s_code != MEDUSA_DEV_OK) set_status(status, s_code);
-        ca.new_prefix_len[b] = s_code == MEDUSA_DEV_OK ? P + s_L + 1 : P;
+    if (ca.k_cache) {  // uniform over the CTA
+        // commit of the accepted path into the KV cache (medusa_commit_kv)
+        __syncthreads();
+        if (i == 0) {
+            s_code = commit_check(kc, vc, P, s_path, s_L, K, R);
+            if (s_code != MEDUSA_DEV_OK) set_status(status, s_code);
+            ca.new_prefix_len[b] = s_code == MEDUSA_DEV_OK ? P + s_L + 1 : P;
+        }
+        __syncthreads();
+        if (s_code == MEDUSA_DEV_OK)
+            commit_columns(kc, vc, P, s_path, s_L, ca.row_vecs, i, blockDim.x);
     }
-    __syncthreads();
-    if (s_code != MEDUSA_DEV_OK) return;
-    commit_columns(kc, vc, P, s_path, s_L, ca.row_vecs, i, blockDim.x);
+    if (done) {  // uniform over the CTA
+        // every thread's writes reach the system before the completion word
+        __threadfence_system();
+        __syncthreads();
+        if (i == 0) *reinterpret_cast<volatile uint32_t *>(done + b) = seq;
+    }
 }
 
 // Slices per logits row: enough CTAs for two per SM on 152 SMs, at most 8.
@@ -421,7 +436,7 @@ cudaError_t run_posterior(const void *logits, const int32_t *tokens, const int32
                           float eps, float delta, float temperature, int32_t *accept_len,
                           int32_t *path, int32_t *path_tokens, int32_t *next_token,
                           int32_t *accept, const CommitArgs &commit, void *ws,
-                          cudaStream_t stream) {
+                          cudaStream_t stream, uint32_t *done) {
     int *status = static_cast<int *>(ws);
     RowPart *parts = reinterpret_cast<RowPart *>(static_cast<char *>(ws) + MEDUSA_WS_HEADER);
     const T *lg = static_cast<const T *>(logits);
@@ -435,7 +450,7 @@ cudaError_t run_posterior(const void *logits, const int32_t *tokens, const int32
     e = launch_pdl(posterior_select_kernel<T>, dim3(B), dim3(kSelectThreads), 0, stream, lg, tokens,
                    parent, depth, static_cast<const RowPart *>(parts), splits, R, V, K,
                    typical ? 1 : 0, y_scale, log2f(eps), log2f(delta), accept_len, path,
-                   path_tokens, next_token, accept, commit, status);
+                   path_tokens, next_token, accept, commit, status, done);
     note_launch();
     return e;
 }
@@ -453,7 +468,7 @@ cudaError_t launch_posterior(medusa_dtype dtype, const void *logits, const int32
                              int32_t *path_tokens, int32_t *next_token, int32_t *accept,
                              void *const *k_cache, void *const *v_cache,
                              const int32_t *prefix_len, int H, int dh, int32_t *new_prefix_len,
-                             void *ws, cudaStream_t stream) {
+                             void *ws, cudaStream_t stream, uint32_t *done) {
     const bool typical = mode == MEDUSA_TYPICAL;
     const size_t elt = dtype == MEDUSA_BF16 ? 2 : 4;
     CommitArgs commit;
@@ -465,10 +480,10 @@ cudaError_t launch_posterior(medusa_dtype dtype, const void *logits, const int32
     if (dtype == MEDUSA_BF16)
         return run_posterior<bf16>(logits, tokens, parent, depth, B, R, V, K, typical, eps, delta,
                                    temperature, accept_len, path, path_tokens, next_token, accept,
-                                   commit, ws, stream);
+                                   commit, ws, stream, done);
     return run_posterior<float>(logits, tokens, parent, depth, B, R, V, K, typical, eps, delta,
                                 temperature, accept_len, path, path_tokens, next_token, accept,
-                                commit, ws, stream);
+                                commit, ws, stream, done);
 }
 
 }  // namespace medusa

@@ -9,6 +9,7 @@
 // joined before the attention.  Issued from here, the step's launches leave
 // the host a few microseconds apart, far ahead of the GPU, and each kernel
 // keeps its programmatic-dependent-launch overlap with the one before it.
+#include <chrono>
 #include <cstring>
 #include <new>
 
@@ -28,6 +29,10 @@ struct medusa_step_exec {
     // graph mode: the sequence captured once, and the kernels it launches
     cudaGraphExec_t graph;
     uint64_t graph_launches;
+    // with page-locked results: one completion word per sequence, raised by
+    // the posterior's last kernel once per run, and the runs issued
+    uint32_t *done;
+    uint32_t runs;
 };
 
 namespace {
@@ -155,19 +160,36 @@ medusa_status issue_step(medusa_step_exec *ex, cudaStream_t st) {
                                                 d.P_max, d.anc_mask, d.B, R, d.H, d.dh, d.scale,
                                                 d.attn_out, d.ws, d.ws_bytes, st))
         return s;
-    medusa_status s;
-    if (d.new_prefix_len)
-        s = medusa_evaluate_posterior_commit(
-            d.dtype, d.logits, d.tokens, d.parent, d.depth, d.B, R, d.V, d.K, d.mode, d.eps,
-            d.delta, d.temperature, d.accept_len, d.path, d.path_tokens, d.next_token, d.accept,
-            const_cast<void *const *>(d.k_cache), const_cast<void *const *>(d.v_cache),
-            d.prefix_len, d.H, d.dh, d.new_prefix_len, d.ws, d.ws_bytes, st);
-    else
-        s = medusa_evaluate_posterior(d.dtype, d.logits, d.tokens, d.parent, d.depth, d.B, R, d.V,
-                                      d.K, d.mode, d.eps, d.delta, d.temperature, d.accept_len,
-                                      d.path, d.path_tokens, d.next_token, d.accept, d.ws,
-                                      d.ws_bytes, st);
-    if (s) return s;
+    const bool commit = d.new_prefix_len != nullptr;
+    return medusa::evaluate_posterior_signalled(
+        d.dtype, d.logits, d.tokens, d.parent, d.depth, d.B, R, d.V, d.K, d.mode, d.eps, d.delta,
+        d.temperature, d.accept_len, d.path, d.path_tokens, d.next_token, d.accept,
+        commit ? const_cast<void *const *>(d.k_cache) : nullptr,
+        commit ? const_cast<void *const *>(d.v_cache) : nullptr, commit ? d.prefix_len : nullptr,
+        d.H, d.dh, d.new_prefix_len, d.ws, d.ws_bytes, st, ex->done);
+}
+
+// Wait for run number `runs`: with completion words, until every sequence's
+// word has reached it (the results are then in host memory), with a time
+// limit after which the stream is synchronised instead; otherwise the
+// stream.
+medusa_status wait_step(medusa_step_exec *ex, cudaStream_t st) {
+    if (ex->done) {
+        const volatile uint32_t *w = ex->done;
+        const auto t0 = std::chrono::steady_clock::now();
+        for (uint32_t polls = 1;; ++polls) {
+            bool all = true;
+            for (int b = 0; b < ex->desc.B && all; ++b)
+                all = static_cast<int32_t>(w[b] - ex->runs) >= 0;
+            if (all) return MEDUSA_OK;
+            if ((polls & 1023u) == 0 &&
+                std::chrono::steady_clock::now() - t0 > std::chrono::milliseconds(20))
+                break;
+        }
+    }
+    cudaError_t e = cudaStreamSynchronize(st);
+    if (e) return cuda_error(e, "medusa_step_run (synchronize)");
+    if (ex->done) ex->runs = ex->done[0];  // realign after the fallback
     return MEDUSA_OK;
 }
 
@@ -234,6 +256,22 @@ medusa_status medusa_step_create(const medusa_step_desc *desc, medusa_step_exec 
         delete ex;
         return cuda_error(e, "medusa_step_create (side stream)");
     }
+    // results in page-locked host memory: completion words beside them
+    cudaPointerAttributes at{};
+    if (cudaPointerGetAttributes(&at, desc->accept_len) == cudaSuccess &&
+        at.type == cudaMemoryTypeHost) {
+        void *p = nullptr;
+        void *dp = nullptr;
+        if (cudaHostAlloc(&p, sizeof(uint32_t) * desc->B, cudaHostAllocMapped) == cudaSuccess) {
+            if (cudaHostGetDevicePointer(&dp, p, 0) == cudaSuccess && dp == p) {
+                std::memset(p, 0, sizeof(uint32_t) * desc->B);
+                ex->done = static_cast<uint32_t *>(p);
+            } else {
+                cudaFreeHost(p);
+            }
+        }
+    }
+    cudaGetLastError();  // the probes above leave no error behind
     e = cudaEventCreateWithFlags(&ex->fork, cudaEventDisableTiming);
     if (!e) {
         e = cudaEventCreateWithFlags(&ex->join, cudaEventDisableTiming);
@@ -241,6 +279,7 @@ medusa_status medusa_step_create(const medusa_step_desc *desc, medusa_step_exec 
     }
     if (e) {
         cudaStreamDestroy(ex->side);
+        if (ex->done) cudaFreeHost(ex->done);
         delete ex;
         return cuda_error(e, "medusa_step_create (events)");
     }
@@ -268,15 +307,18 @@ medusa_status medusa_step_run(medusa_step_exec *ex, medusa_stream stream, int sy
     } else if (medusa_status s = issue_step(ex, st)) {
         return s;
     }
-    if (synchronize && (e = cudaStreamSynchronize(st)))
-        return cuda_error(e, "medusa_step_run (synchronize)");
-    return MEDUSA_OK;
+    ++ex->runs;  // the posterior was issued: its words will reach this count
+    return synchronize ? wait_step(ex, st) : MEDUSA_OK;
 }
 
 void medusa_step_destroy(medusa_step_exec *ex) {
     if (!ex) return;
     // each releases its resources once the work it carries has completed
     if (ex->graph) cudaGraphExecDestroy(ex->graph);
+    if (ex->done) {
+        cudaStreamSynchronize(ex->side);
+        cudaFreeHost(ex->done);  // synchronises the device first
+    }
     cudaEventDestroy(ex->join);
     cudaEventDestroy(ex->fork);
     cudaStreamDestroy(ex->side);

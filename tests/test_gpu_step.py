@@ -191,6 +191,23 @@ def test_step_executor_v7b_commit_matches_calls(dev, graph):
 
 
 @pytest.mark.parametrize("graph", [False, True])
+def test_step_executor_runs_without_waiting_then_waits(dev, graph):
+    """Steps issued without waiting, then one waited for: the wait covers
+    the last step (the completion words count every run issued), and the
+    results equal the separate calls'."""
+    cfg = synth.v7b().replace(mode="typical")
+    st = Step(cfg, dev, graph=graph)
+    st.fill(4)
+    for _ in range(3):
+        st.ex.run(synchronize=False)
+    st.ex.run()
+    got = st.results()
+    st.separate_calls()
+    _same(got, st.results())
+    assert m.read_device_status(st.ws) == 0
+
+
+@pytest.mark.parametrize("graph", [False, True])
 def test_step_executor_batch8_matches_calls(dev, graph):
     """Eight ragged 7B sequences: the heads run on the tensor cores (tensor
     maps built on the host at issue, or once at capture in graph mode); the
