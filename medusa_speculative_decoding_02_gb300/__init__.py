@@ -652,18 +652,24 @@ class StepExecutor:
         handle = ctypes.c_void_p()
         _check(L.medusa_step_create(ctypes.byref(desc), ctypes.byref(handle)))
         self._handle = handle
+        self._h = handle.value  # plain integers keep the per-step call short
+        self._run = L.medusa_step_run
 
     def run(self, stream=None, synchronize: bool = True):
         """Issue one step on ``stream`` (the current stream by default); with
         ``synchronize`` wait for it, so results in pinned memory are ready."""
         if self._handle is None:
             raise MedusaError(1, "StepExecutor is closed")
-        _check(lib().medusa_step_run(self._handle, _stream(stream), int(bool(synchronize))))
+        s = (torch.cuda.current_stream() if stream is None else stream).cuda_stream
+        rc = self._run(self._h, s, 1 if synchronize else 0)
+        if rc:
+            _check(rc)
 
     def close(self):
         if getattr(self, "_handle", None) is not None:
             lib().medusa_step_destroy(self._handle)
             self._handle = None
+            self._h = None
 
     def __del__(self):
         try:
