@@ -916,7 +916,7 @@ def run_ours(args, cfg):
     # where the end-to-end time goes: the native call that issues the step,
     # the step's span on the GPU (events on the stream around the call), and
     # what is left (launch latency to the GPU plus the host's wait for the
-    # stream); the input copy that gates the first kernel is timed alone
+    # results); the input copy that gates the first kernel is timed alone
     ga, gz = torch.cuda.Event(enable_timing=True), torch.cuda.Event(enable_timing=True)
     launch_us, span_us, wall_us = [], [], []
     for _ in range(e2e_steps):
@@ -925,8 +925,9 @@ def run_ours(args, cfg):
         executor.run(synchronize=False)
         t1 = time.perf_counter()
         gz.record(stream)
-        stream.synchronize()
+        executor.wait()
         t2 = time.perf_counter()
+        gz.synchronize()
         launch_us.append((t1 - t0) * 1e6)
         wall_us.append((t2 - t0) * 1e6)
         span_us.append(ga.elapsed_time(gz) * 1e3)

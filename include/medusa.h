@@ -584,6 +584,9 @@ MEDUSA_API medusa_status medusa_step_create(const medusa_step_desc *desc,
                                             medusa_step_exec **exec_out);
 MEDUSA_API medusa_status medusa_step_run(medusa_step_exec *exec, medusa_stream stream,
                                          int synchronize);
+/* The wait of medusa_step_run(..., synchronize = 1) on its own: for every run
+ * issued so far on `stream` (the host may work between the issue and it). */
+MEDUSA_API medusa_status medusa_step_wait(medusa_step_exec *exec, medusa_stream stream);
 MEDUSA_API void medusa_step_destroy(medusa_step_exec *exec);
 
 #ifdef __cplusplus

@@ -53,7 +53,7 @@ EXPORTS = ("medusa_status_string", "medusa_last_error", "medusa_launch_count",
            "medusa_evaluate_posterior_commit", "medusa_commit_kv", "medusa_heads_sample",
            "medusa_speculative_workspace_size", "medusa_speculative_posterior",
            "medusa_step_desc_size", "medusa_step_create", "medusa_step_run",
-           "medusa_step_destroy")
+           "medusa_step_wait", "medusa_step_destroy")
 
 
 class _Copy(ctypes.Structure):
@@ -129,6 +129,7 @@ def lib() -> ctypes.CDLL:
         "medusa_step_desc_size": ([], S),
         "medusa_step_create": ([ctypes.POINTER(_StepDesc), ctypes.POINTER(P)], I),
         "medusa_step_run": ([P, P, I], I),
+        "medusa_step_wait": ([P, P], I),
         "medusa_step_destroy": ([P], None),
     }
     for name, (args, res) in sig.items():
@@ -664,6 +665,13 @@ class StepExecutor:
         rc = self._run(self._h, s, 1 if synchronize else 0)
         if rc:
             _check(rc)
+
+    def wait(self, stream=None):
+        """Wait for every step issued so far (the wait of ``run``)."""
+        if self._handle is None:
+            raise MedusaError(1, "StepExecutor is closed")
+        s = (torch.cuda.current_stream() if stream is None else stream).cuda_stream
+        _check(lib().medusa_step_wait(self._h, s))
 
     def close(self):
         if getattr(self, "_handle", None) is not None:

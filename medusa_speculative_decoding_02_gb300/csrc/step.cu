@@ -311,6 +311,14 @@ medusa_status medusa_step_run(medusa_step_exec *ex, medusa_stream stream, int sy
     return synchronize ? wait_step(ex, st) : MEDUSA_OK;
 }
 
+medusa_status medusa_step_wait(medusa_step_exec *ex, medusa_stream stream) {
+    if (!ex) {
+        set_last_error("medusa_step_wait: NULL executor");
+        return MEDUSA_ERR_INVALID_ARG;
+    }
+    return wait_step(ex, static_cast<cudaStream_t>(stream));
+}
+
 void medusa_step_destroy(medusa_step_exec *ex) {
     if (!ex) return;
     // each releases its resources once the work it carries has completed

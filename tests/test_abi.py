@@ -353,6 +353,7 @@ def test_step_create_rejects_bad_copies_and_s(L):
     assert "s_host[k]" in L.medusa_last_error().decode()
     assert L.medusa_step_create(None, ctypes.byref(ex)) == 1
     assert L.medusa_step_run(None, None, 1) == 1
+    assert L.medusa_step_wait(None, None) == 1
     L.medusa_step_destroy(None)  # a no-op
 
 

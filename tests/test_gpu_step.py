@@ -202,6 +202,9 @@ def test_step_executor_runs_without_waiting_then_waits(dev, graph):
         st.ex.run(synchronize=False)
     st.ex.run()
     got = st.results()
+    st.ex.run(synchronize=False)
+    st.ex.wait()  # the wait of run() on its own
+    _same(got, st.results())
     st.separate_calls()
     _same(got, st.results())
     assert m.read_device_status(st.ws) == 0
