@@ -8,9 +8,10 @@
 //
 // At batch 1 this is a pair of GEMVs: every weight byte is used once, so the
 // kernels are HBM-bound and run on CUDA cores.  Design:
-//   phase 1  heads_w1_kernel   one warp per output row of W1 (all heads),
-//                              16-byte streaming loads, fp32 accumulation,
-//                              residual SiLU fused; z kept in fp32 scratch.
+//   phase 1  heads_w1_kernel   one full wave of warps, each streaming a
+//                              contiguous share of W1's rows (all heads) with
+//                              16-byte loads, fp32 accumulation, residual
+//                              SiLU fused; z kept in fp32 scratch.
 //   phase 2  heads_w2_kernel   persistent grid; each CTA streams an equal
 //                              slice of every head's W2 rows.  Per row a warp
 //                              forms the logit(s), then folds it into a running
