@@ -20,7 +20,9 @@
 //                            merged, they give H = ln S - ln2 * A / S.
 //   posterior_select_kernel  one CTA per sequence, one thread per node:
 //                            per-node decision, prefix-AND down the tree
-//                            level by level, longest path, next token.
+//                            level by level, longest path, next token (and,
+//                            for a step executor, a completion word raised
+//                            in page-locked memory once all is written).
 #include <algorithm>
 #include <climits>
 

@@ -8,7 +8,12 @@
 // the posterior's on a side stream while the heads stream the weights,
 // joined before the attention.  Issued from here, the step's launches leave
 // the host a few microseconds apart, far ahead of the GPU, and each kernel
-// keeps its programmatic-dependent-launch overlap with the one before it.
+// keeps its programmatic-dependent-launch overlap with the one before it;
+// in graph mode the sequence is captured once and each run is one graph
+// launch.  When the results are page-locked host memory, the wait for a
+// step polls completion words that the posterior's last kernel raises after
+// its writes, which land a few microseconds before the stream would report
+// the step complete.
 #include <chrono>
 #include <cstring>
 #include <new>
