@@ -341,6 +341,54 @@ def test_greedy_stops_at_first_mismatch(L_true):
     assert int(o["next_token"][0]) == exp_next
 
 
+@pytest.mark.parametrize("seed", range(8))
+def test_longest_path_brute_force_on_random_trees(seed):
+    """[P3] Part 2 and [P2] §5: a node counts only if every node of its
+    branch is accepted; the deepest such node (the smallest canonical index
+    among equals) ends the path, and the next token is the argmax of its
+    row.  On random trees with random per-node decisions (given to the
+    oracle as forced decisions, so that only its path logic is under test),
+    every root-to-node branch is enumerated, and the oracle's accept_len,
+    path, path_tokens and next_token must equal the enumeration's."""
+    rng = np.random.default_rng(100 + seed)
+    K = int(rng.integers(1, 6))
+    s = tuple(int(x) for x in rng.integers(1, 4, size=K))
+    full = sum(math.prod(s[:k + 1]) for k in range(K))
+    n = int(rng.integers(1, full + 1))
+    B, V, S = 2, 500, max(s)
+    ids = np.stack([np.stack([rng.choice(V, size=S, replace=False) for _ in range(K)])
+                    for _ in range(B)]).astype(np.int32)
+    p = rng.dirichlet(np.ones(S + 1), size=(B, K))[..., :S]
+    t = oracle.build_tree(np.array([7, 9], np.int32), ids, np.log(-np.sort(-p, axis=-1)), s, n)
+    R = n + 1
+    logits = rng.standard_normal((B, R, V)).astype(np.float32)
+    acc = (rng.random((B, R)) < 0.7).astype(np.int32)
+    acc[:, 0] = 1
+    o = oracle.posterior(logits, t["tokens"], t["parent"], t["depth"], K, oracle.GREEDY,
+                         forced_accept=acc)
+    assert np.array_equal(o["accept"], acc)
+    for b in range(B):
+        best, L = 0, 0
+        for i in range(1, R):  # ascending: the first node of a depth wins ties
+            branch, x = [], i
+            while x > 0:
+                branch.append(x)
+                x = int(t["parent"][b, x])
+            assert len(branch) == int(t["depth"][b, i])
+            if all(acc[b, y] for y in branch) and len(branch) > L:
+                best, L = i, len(branch)
+        path, x = [], best
+        while x > 0:
+            path.append(x)
+            x = int(t["parent"][b, x])
+        path = [0] + path[::-1]
+        pad = [-1] * (K + 1 - len(path))
+        assert int(o["accept_len"][b]) == L
+        assert list(o["path"][b]) == path + pad
+        assert list(o["path_tokens"][b]) == [int(t["tokens"][b, x]) for x in path] + pad
+        assert int(o["next_token"][b]) == int(np.argmax(logits[b, best]))
+
+
 def test_progress_guarantee_all_rejected():
     """[P3] Part 2 / [P2] §5: with every candidate wrong the step still commits
     the root and yields the next greedy token (L = 0, path = [root])."""
