@@ -423,6 +423,21 @@ def test_entropy_closed_forms():
     assert oracle.softmax_entropy(x, 2.5) == pytest.approx(oracle.softmax_entropy(x / 2.5), abs=1e-12)
 
 
+@pytest.mark.parametrize("V,scale,T", [(8, 1.0, 1.0), (1000, 3.0, 0.7), (32000, 3.0, 1.0),
+                                        (32000, 30.0, 1.0), (4096, 0.01, 2.0)])
+def test_entropy_random_rows_against_scipy(V, scale, T):
+    """[P2] §5 uses H(p) = -sum p ln p of p = softmax(logits / T): on random
+    rows, from nearly uniform to nearly one-hot, the oracle's entropy equals
+    SciPy's softmax and entropy routines (an independent implementation)."""
+    from scipy.special import softmax
+    from scipy.stats import entropy
+    rng = np.random.default_rng(V + int(scale * 10))
+    for _ in range(3):
+        x = rng.standard_normal(V) * scale
+        assert oracle.softmax_entropy(x, T) == pytest.approx(entropy(softmax(x / T)), rel=1e-10,
+                                                             abs=1e-12)
+
+
 @pytest.mark.parametrize("m,a", [(1, 12.0), (2, 6.0), (20, 4.0), (300, 1.0), (900, 2.0)])
 def test_typical_threshold_closed_form(m, a):
     """[P2] §5: accept x iff p(x) > min(eps, delta * exp(-H)).  Rows with two
