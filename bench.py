@@ -435,6 +435,48 @@ def time_heads_modes(m, r, dev, T, reps: int, peak_gbs: float) -> dict:
     return out
 
 
+def executor_e2e(m, r, cfg, steps: int, peak_gbs: float) -> dict:
+    """The workload's step end to end through the step executor in graph
+    mode: every step copies its inputs from pinned host memory (h and the
+    root first; q, every sequence's tree K/V rows and the logits on the side
+    stream) and the posterior writes its results into pinned host memory;
+    one native call issues the step and waits for the results."""
+    import torch
+    B, K, R = cfg.B, cfg.K, cfg.R
+    ai = r.inp["attn"]
+    bf = lambda a: torch.from_numpy(np.ascontiguousarray(a).view(np.int16)).view(torch.bfloat16)
+    host_start = torch.empty(r.start.numel(), dtype=torch.uint8).pin_memory()
+    host_start.copy_(r.start.cpu())
+    late = [(r.q, bf(ai.q).pin_memory()), (r.logits, bf(r.inp["logits"]).pin_memory())]
+    for b in range(B):
+        P = cfg.prefix[b]
+        late.append((r.kc[b][P:P + R], bf(ai.k_cache[b][P:P + R]).pin_memory()))
+        late.append((r.vc[b][P:P + R], bf(ai.v_cache[b][P:P + R]).pin_memory()))
+    post = m.Posterior.pinned(B, R, K, with_accept=False)
+    ex = m.StepExecutor(
+        h=r.h, W1=r.W1, b1=r.b1, W2=r.W2, top_s=cfg.top_s, topk=(r.ids, r.logp), root=r.root,
+        s=cfg.s, n=cfg.n, prefix_len=r.prefix, tree=r.tree, q=r.q, k_ptrs=r.kptr,
+        v_ptrs=r.vptr, P_max=cfg.P_max, attn_out=r.out, logits=r.logits, post=post, K=K,
+        mode=r.mode, eps=cfg.eps, delta=cfg.delta, temperature=cfg.temperature, ws=r.ws,
+        early=[(r.start, host_start)], late=late, graph=True)
+    for _ in range(3):
+        ex.run()
+    t0 = time.perf_counter()
+    for _ in range(steps):
+        ex.run()
+    sec = (time.perf_counter() - t0) / steps
+    ex.close()
+    r.check_status("in the end-to-end steps")
+    gbs = r.nb["total"] / sec / 1e9
+    h2d = host_start.numel() + sum(h.numel() * h.element_size() for _, h in late)
+    d2h = sum(t.numel() * t.element_size()
+              for t in (post.accept_len, post.path, post.path_tokens, post.next_token))
+    return {"us_per_step": round(sec * 1e6, 2), "GB/s": round(gbs, 1),
+            "frac_hbm": round(gbs / peak_gbs, 4), "h2d_bytes_per_step": int(h2d),
+            "d2h_bytes_per_step": int(d2h), "steps": steps,
+            "api": "StepExecutor(graph=True).run"}
+
+
 def time_side_step(m, cfg, dev, T, steps: int, warmup: int, peak_gbs: float,
                    heads_modes: bool = False) -> dict:
     """The whole step on another workload (13B shape, batch of 8), timed like
@@ -457,7 +499,8 @@ def time_side_step(m, cfg, dev, T, steps: int, warmup: int, peak_gbs: float,
            "tree_nodes": cfg.n, "accept": cfg.mode, "steps": steps,
            "us_per_step": round(ms * 1e3, 2), "bytes_per_step": int(r.nb["total"]),
            "GB/s": round(gbs, 1), "frac_hbm": round(gbs / peak_gbs, 4),
-           "stages": r.stages(pc, peak_gbs)}
+           "stages": r.stages(pc, peak_gbs),
+           "e2e": executor_e2e(m, r, cfg, steps, peak_gbs)}
     if heads_modes:
         out["heads_modes"] = time_heads_modes(m, r, dev, T, max(steps, 20), peak_gbs)
     del r
